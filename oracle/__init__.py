@@ -1,0 +1,125 @@
+"""fp64 CPU oracle for the FlashAttention-2 forward pass (test infrastructure).
+
+Only the tests, the package's ``smoke()`` check and the benchmark's CPU
+baseline may import this module. The GPU library and its Python binding never
+do. The arithmetic lives in ``oracle.c`` (the plain definition of attention in
+double precision, the full score row materialised); this wrapper only builds
+that file with gcc and marshals numpy arrays to it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+BF16 = 0
+FP16 = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, OpenMP) if it is missing or stale."""
+    with _lock:
+        stale = (not os.path.exists(_LIB)
+                 or os.path.getmtime(_LIB) < os.path.getmtime(_SRC))
+        if force or stale:
+            tmp = _LIB + f".tmp{os.getpid()}"
+            cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11",
+                   "-o", tmp, _SRC, "-lm"]
+            subprocess.run(cmd, check=True)
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        i64 = ctypes.c_int64
+        p = ctypes.c_void_p
+        lib.oracle_attention_rows.argtypes = [p, p, p, ctypes.c_int, i64, i64, i64, i64, i64,
+                                              ctypes.c_double, p, i64, p, p, ctypes.c_int]
+        lib.oracle_attention_rows.restype = ctypes.c_int
+        lib.oracle_softmax_row.argtypes = [p, p, ctypes.c_int, i64, i64, i64, i64, i64,
+                                           ctypes.c_double, i64, p]
+        lib.oracle_softmax_row.restype = ctypes.c_int
+        lib.oracle_decode16.argtypes = [p, i64, ctypes.c_int, p]
+        lib.oracle_decode16.restype = None
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_max_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _u16(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("oracle inputs are 16-bit bit patterns (uint16)")
+    return a
+
+
+def decode16(bits, dtype: int) -> np.ndarray:
+    """Exact double values of bf16 (dtype 0) or fp16 (dtype 1) bit patterns."""
+    bits = _u16(bits)
+    out = np.empty(bits.shape, dtype=np.float64)
+    _load().oracle_decode16(bits.ctypes.data, bits.size, dtype, out.ctypes.data)
+    return out
+
+
+def attention(q, k, v, scale: float, dtype: int, rows=None, threads: int = 0):
+    """Exact attention forward in fp64.
+
+    q: uint16 [B, Hq, N, d]; k, v: uint16 [B, Hkv, N, d].
+    rows: optional flat query-row indices (b*Hq + h)*N + i.
+    Returns (o, lse): o float64 [B, Hq, N, d] (or [len(rows), d]) and
+    lse float64 [B, Hq, N] (or [len(rows)]).
+    """
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    B, Hq, N, d = q.shape
+    Bk, Hkv, Nk, dk = k.shape
+    if (Bk, Nk, dk) != (B, N, d) or v.shape != k.shape:
+        raise ValueError("shape mismatch between q, k and v")
+    if rows is None:
+        nrows = B * Hq * N
+        rows_arr = None
+        rptr = None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        nrows = rows_arr.size
+        rptr = rows_arr.ctypes.data
+    o = np.empty((nrows, d), dtype=np.float64)
+    lse = np.empty(nrows, dtype=np.float64)
+    rc = _load().oracle_attention_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, dtype,
+                                       B, Hq, Hkv, N, d, float(scale), rptr, nrows,
+                                       o.ctypes.data, lse.ctypes.data, int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the sizes")
+    if rows is None:
+        return o.reshape(B, Hq, N, d), lse.reshape(B, Hq, N)
+    return o, lse
+
+
+def softmax_row(q, k, scale: float, dtype: int, row: int) -> np.ndarray:
+    """The normalised softmax weights of one query row (flat index), fp64 [N]."""
+    q, k = _u16(q), _u16(k)
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    p = np.empty(N, dtype=np.float64)
+    rc = _load().oracle_softmax_row(q.ctypes.data, k.ctypes.data, dtype, B, Hq, Hkv, N, d,
+                                    float(scale), int(row), p.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle rejected the sizes")
+    return p
+
+
+def max_threads() -> int:
+    return _load().oracle_max_threads()

@@ -1,0 +1,185 @@
+/*
+ * fp64 CPU oracle for the FlashAttention-2 forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is compiled into oracle/liboracle.so and
+ * is called by the tests, by the package's smoke check and by the benchmark's
+ * CPU-baseline leg. The GPU library never links, loads or calls it, and it
+ * shares no code, header or table with the GPU path.
+ *
+ * What it computes. The forward pass of FlashAttention-2 is exact
+ * scaled-dot-product attention ("A Case Study in CUDA Kernel Fusion:
+ * Implementing FlashAttention-2 on NVIDIA Hopper Architecture using the
+ * CUTLASS Library", abstract: a "memory-aware scaled dot-product attention"
+ * whose forward pass fuses an online softmax with two back-to-back GEMMs).
+ * Tiling and the online softmax change only the rounding order, so the oracle
+ * is the plain definition, with the full score row materialised:
+ *
+ *     s_j    = scale * sum_t q_t k_{j,t}          (j = 0 .. N-1)
+ *     m      = max_j s_j
+ *     p_j    = exp(s_j - m)
+ *     l      = sum_j p_j
+ *     o      = (sum_j p_j v_j) / l
+ *     lse    = m + ln(l)
+ *
+ * Scope follows "FlashAttention-2 from scratch on Ampere, Part 1"
+ * (lubitschian.com/flash/Part-1), section "Kernel Specification": forward
+ * only, non-causal, equal query/key/value lengths, 16-bit (bf16/fp16) inputs,
+ * softmax in fp32 on the GPU (fp64 here). The logsumexp output is the natural
+ * log of sum_j exp(s_j) with the scale included. Grouped KV heads follow the
+ * query-head packing of "FlashAttention-3 for Inference: INT8 Quantization and
+ * Query Head Packing for MQA/GQA" (Colfax Research author page): query head h
+ * reads KV head h / (Hq / Hkv).
+ *
+ * Every function here is pinned by tests/test_oracle.py against closed forms,
+ * invariants, a hand-computed case and an independent library computation.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_BF16 0
+#define ORACLE_FP16 1
+
+/* Exact value of a bf16 bit pattern: the top half of an IEEE binary32. */
+static double decode_bf16(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Exact value of an IEEE binary16 bit pattern (sign, 5-bit exponent with bias
+ * 15, 10-bit fraction; exponent 0 encodes subnormals, 31 encodes inf/NaN). */
+static double decode_fp16(uint16_t b) {
+    int sign = (b >> 15) & 1;
+    int e = (b >> 10) & 0x1F;
+    int f = b & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25);
+    return sign ? -v : v;
+}
+
+static double decode16(uint16_t b, int dtype) {
+    return dtype == ORACLE_FP16 ? decode_fp16(b) : decode_bf16(b);
+}
+
+/* Widen n 16-bit patterns to double (exact). */
+void oracle_decode16(const uint16_t* bits, int64_t n, int dtype, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = decode16(bits[i], dtype);
+}
+
+/*
+ * Attention forward for a list of query rows.
+ *
+ * q:   [B, Hq, N, d]   16-bit patterns, contiguous
+ * k,v: [B, Hkv, N, d]  16-bit patterns, contiguous
+ * rows: flat indices r = (b*Hq + h)*N + i of the query rows to compute, or
+ *       NULL for all B*Hq*N rows in order (then nrows must equal B*Hq*N)
+ * o_out:   [nrows, d] doubles, the unrounded output rows
+ * lse_out: [nrows]    doubles, natural-log logsumexp of the scaled scores
+ * nthreads: OpenMP threads (<= 0: library default)
+ *
+ * Returns 0, or -1 on invalid sizes.
+ */
+int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                          int dtype, int64_t B, int64_t Hq, int64_t Hkv, int64_t N,
+                          int64_t d, double scale, const int64_t* rows, int64_t nrows,
+                          double* o_out, double* lse_out, int nthreads) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || Hq % Hkv) return -1;
+    if (!rows && nrows != B * Hq * N) return -1;
+    const int64_t G = Hq / Hkv;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+
+#pragma omp parallel
+    {
+        double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+        double* s = (double*)malloc(sizeof(double) * (size_t)N);
+        double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < nrows; ++r) {
+            const int64_t flat = rows ? rows[r] : r;
+            const int64_t i = flat % N;
+            const int64_t h = (flat / N) % Hq;
+            const int64_t b = flat / (N * Hq);
+            const int64_t hk = h / G;
+            const uint16_t* qp = q + ((b * Hq + h) * N + i) * d;
+            const uint16_t* kp = k + (b * Hkv + hk) * N * d;
+            const uint16_t* vp = v + (b * Hkv + hk) * N * d;
+
+            for (int64_t t = 0; t < d; ++t) qrow[t] = decode16(qp[t], dtype);
+
+            /* scores s_j = scale * <q, k_j> over the whole key sequence */
+            double m = -INFINITY;
+            for (int64_t j = 0; j < N; ++j) {
+                double dot = 0.0;
+                for (int64_t t = 0; t < d; ++t) dot += qrow[t] * decode16(kp[j * d + t], dtype);
+                s[j] = scale * dot;
+                if (s[j] > m) m = s[j];
+            }
+            /* max-subtracted softmax weights, their sum, and the weighted sum of V */
+            double l = 0.0;
+            for (int64_t t = 0; t < d; ++t) acc[t] = 0.0;
+            for (int64_t j = 0; j < N; ++j) {
+                const double p = exp(s[j] - m);
+                l += p;
+                for (int64_t t = 0; t < d; ++t) acc[t] += p * decode16(vp[j * d + t], dtype);
+            }
+            for (int64_t t = 0; t < d; ++t) o_out[r * d + t] = acc[t] / l;
+            lse_out[r] = m + log(l);
+        }
+        free(qrow);
+        free(s);
+        free(acc);
+    }
+    return 0;
+}
+
+/*
+ * The normalised softmax row P_i = exp(s - lse) of one query row, for the
+ * oracle's own invariant checks (rows of P sum to one). p_out: [N] doubles.
+ */
+int oracle_softmax_row(const uint16_t* q, const uint16_t* k, int dtype, int64_t B,
+                       int64_t Hq, int64_t Hkv, int64_t N, int64_t d, double scale,
+                       int64_t row, double* p_out) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || Hq % Hkv) return -1;
+    if (row < 0 || row >= B * Hq * N) return -1;
+    const int64_t G = Hq / Hkv;
+    const int64_t i = row % N, h = (row / N) % Hq, b = row / (N * Hq), hk = h / G;
+    const uint16_t* qp = q + ((b * Hq + h) * N + i) * d;
+    const uint16_t* kp = k + (b * Hkv + hk) * N * d;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < N; ++j) {
+        double dot = 0.0;
+        for (int64_t t = 0; t < d; ++t) dot += decode16(qp[t], dtype) * decode16(kp[j * d + t], dtype);
+        p_out[j] = scale * dot;
+        if (p_out[j] > m) m = p_out[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+        p_out[j] = exp(p_out[j] - m);
+        l += p_out[j];
+    }
+    for (int64_t j = 0; j < N; ++j) p_out[j] /= l;
+    return 0;
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,267 @@
+"""Pins for the fp64 oracle and the seeded input generator (CPU only).
+
+Each check ties the oracle to something other than itself: values worked by
+hand (tests/golden), closed forms of attention (zero queries, constant values,
+one key), exact invariances (joint key/value permutation, key shift, batch and
+head independence, grouped heads as repeated heads), the logsumexp identity,
+and an independent library computation (torch CPU softmax in float64).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16_bits(values):
+    return gen.round_to_16bit(np.asarray(values, dtype=np.float64), gen.BF16)
+
+
+def exact_bf16(values):
+    bits = bf16_bits(values)
+    assert np.array_equal(oracle.decode16(bits, gen.BF16), np.asarray(values, dtype=np.float64))
+    return bits
+
+
+def rand_inputs(seed, B, Hq, Hkv, N, d, dtype=gen.BF16, amp=1.0):
+    return gen.make_qkv(seed, B, Hq, Hkv, N, d, dtype, amp)
+
+
+# ---------------------------------------------------------------- generator
+
+def test_splitmix64_published_vectors():
+    # Reference outputs of SplitMix64 for seed 1234567 (Vigna's reference
+    # implementation) and the first output for seed 0.
+    z = gen.splitmix64(1234567, 0, 3)
+    assert [int(x) for x in z] == [6457827717110365317, 3203168211198807973,
+                                   9817491932198370423]
+    assert int(gen.splitmix64(0, 0, 1)[0]) == 0xE220A8397B1DCDAF
+
+
+def test_generator_is_deterministic_and_chunk_free():
+    a = gen.normals(7, 0, 10)
+    b = gen.normals(7, 4, 6)
+    assert np.array_equal(a[4:], b)
+    q1, k1, v1 = rand_inputs(11, 1, 2, 1, 128, 64)
+    q2, k2, v2 = rand_inputs(11, 1, 2, 1, 128, 64)
+    assert np.array_equal(q1, q2) and np.array_equal(k1, k2) and np.array_equal(v1, v2)
+    assert q1.shape == (1, 2, 128, 64) and k1.shape == (1, 1, 128, 64)
+
+
+def test_generator_moments():
+    x = gen.normals(99, 0, 1 << 20)
+    assert abs(x.mean()) < 5e-3
+    assert abs(x.std() - 1.0) < 5e-3
+    # fraction within one standard deviation of a normal: erf(1/sqrt 2)
+    assert abs(np.mean(np.abs(x) < 1.0) - math.erf(1 / math.sqrt(2))) < 3e-3
+
+
+def test_bf16_rounding_nearest_even():
+    one = 1.0
+    cases = {
+        one + 2.0 ** -8: 0x3F80,             # halfway, ties to even (1.0)
+        one + 3 * 2.0 ** -8: 0x3F82,         # halfway, ties to even (1 + 2^-6)
+        one + 2.0 ** -8 + 2.0 ** -30: 0x3F81,  # just above halfway rounds up
+        -2.0: 0xC000,
+        0.0: 0x0000,
+        3.0e38: 0x7F62,
+    }
+    for x, bits in cases.items():
+        assert int(bf16_bits([x])[0]) == bits, (x, hex(int(bf16_bits([x])[0])))
+
+
+def test_fp16_rounding_nearest_even():
+    got = gen.round_to_16bit(np.array([1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, 65504.0, 2.0 ** -24]),
+                             gen.FP16)
+    assert [int(b) for b in got] == [0x3C00, 0x3C02, 0x7BFF, 0x0001]
+
+
+# ---------------------------------------------------------------- decoding
+
+def test_decode_fixed_patterns():
+    bf = oracle.decode16(np.array([0x3F80, 0xC000, 0x0001, 0x7F80, 0x4049], np.uint16), gen.BF16)
+    assert bf[0] == 1.0 and bf[1] == -2.0 and bf[2] == 2.0 ** -133 and math.isinf(bf[3])
+    assert bf[4] == 3.140625
+    hf = oracle.decode16(np.array([0x3C00, 0x0001, 0x7BFF, 0xFC00, 0x3555], np.uint16), gen.FP16)
+    assert hf[0] == 1.0 and hf[1] == 2.0 ** -24 and hf[2] == 65504.0 and hf[3] == -math.inf
+    assert hf[4] == 0.333251953125
+
+
+def test_decode_fp16_all_patterns_match_numpy():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.decode16(bits, gen.FP16)
+    ref = bits.view(np.float16).astype(np.float64)
+    finite = np.isfinite(ref)
+    assert np.array_equal(ours[finite], ref[finite])
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+
+
+# ---------------------------------------------------------------- hand-worked cases
+
+def test_hand_case_n2_d1():
+    g = json.load(open(os.path.join(GOLDEN, "hand_n2_d1.json")))
+    q = exact_bf16(g["q"]).reshape(1, 1, 1, 1)
+    q = np.repeat(q, 2, axis=2)  # N = 2 query rows, both q = 1
+    k = exact_bf16(g["k"]).reshape(1, 1, 2, 1)
+    v = exact_bf16(g["v"]).reshape(1, 1, 2, 1)
+    o, lse = oracle.attention(q, k, v, math.log(3) / 2, gen.BF16)
+    assert abs(o[0, 0, 0, 0] - g["o"][0]) < 1e-13
+    assert abs(lse[0, 0, 0] - math.log(4)) < 1e-13
+
+
+def test_hand_case_n3_d2():
+    g = json.load(open(os.path.join(GOLDEN, "hand_n3_d2.json")))
+    q = exact_bf16(g["q"]).reshape(1, 1, 3, 2)
+    k = exact_bf16(g["k"]).reshape(1, 1, 3, 2)
+    v = exact_bf16(g["v"]).reshape(1, 1, 3, 2)
+    o, lse = oracle.attention(q, k, v, math.log(2), gen.BF16)
+    np.testing.assert_allclose(o[0, 0, :2], np.array(g["o_rows_0_1"]), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse[0, 0, :2], [math.log(7), math.log(4.5)], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(o[0, 0, 2], [7 / 3, -7 / 3], rtol=0, atol=1e-13)
+    assert abs(lse[0, 0, 2] - math.log(3)) < 1e-13
+
+
+# ---------------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("dtype", [gen.BF16, gen.FP16])
+def test_zero_queries_give_column_mean(dtype):
+    _, k, v = rand_inputs(3, 2, 2, 2, 96, 32, dtype)
+    q = np.zeros((2, 2, 96, 32), np.uint16)
+    o, lse = oracle.attention(q, k, v, 1 / math.sqrt(32), dtype)
+    vd = oracle.decode16(v, dtype)
+    np.testing.assert_allclose(o, np.broadcast_to(vd.mean(axis=2, keepdims=True), o.shape),
+                               rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, math.log(96), rtol=0, atol=1e-13)
+
+
+def test_constant_values_give_constant_output():
+    q, k, _ = rand_inputs(5, 1, 3, 3, 80, 16, amp=3.0)
+    v = np.full(k.shape, 0x3F80, np.uint16)  # bf16 1.0
+    o, _ = oracle.attention(q, k, v, 0.25, gen.BF16)
+    np.testing.assert_allclose(o, 1.0, rtol=0, atol=1e-12)
+
+
+def test_single_key():
+    q, k, v = rand_inputs(6, 2, 2, 2, 1, 8)
+    o, lse = oracle.attention(q, k, v, 0.3, gen.BF16)
+    qd, kd, vd = (oracle.decode16(x, gen.BF16) for x in (q, k, v))
+    np.testing.assert_array_equal(o, vd)
+    np.testing.assert_allclose(lse[..., 0], 0.3 * np.sum(qd[:, :, 0] * kd[:, :, 0], -1),
+                               rtol=0, atol=1e-12)
+
+
+def test_rows_of_p_sum_to_one():
+    q, k, _ = rand_inputs(8, 1, 2, 1, 200, 64, amp=3.0)
+    for row in (0, 57, 399):
+        p = oracle.softmax_row(q, k, 0.125, gen.BF16, row)
+        assert abs(p.sum() - 1.0) <= 1e-12
+        assert np.all(p > 0)
+
+
+def test_dominant_key():
+    rng = np.random.default_rng(0)
+    N, d = 64, 16
+    q = exact_bf16(np.ones(d))
+    k = bf16_bits(rng.integers(-1, 2, size=(N, d)).astype(np.float64))
+    k[17] = bf16_bits(np.full(d, 8.0))   # score gap at least 8*16*0.5 - 16*0.5 = 56
+    v = bf16_bits(rng.standard_normal((N, d)))
+    o, _ = oracle.attention(q.reshape(1, 1, 1, d).repeat(N, 2), k.reshape(1, 1, N, d),
+                            v.reshape(1, 1, N, d), 0.5, gen.BF16)
+    vd = oracle.decode16(v, gen.BF16)
+    np.testing.assert_allclose(o[0, 0, 0], vd[17], rtol=0, atol=1e-20 + N * math.exp(-50) * 5)
+
+
+# ---------------------------------------------------------------- invariances
+
+def test_joint_permutation_of_keys_and_values():
+    q, k, v = rand_inputs(9, 1, 2, 2, 160, 32)
+    perm = np.random.default_rng(1).permutation(160)
+    o1, l1 = oracle.attention(q, k, v, 0.2, gen.BF16)
+    o2, l2 = oracle.attention(q, k[:, :, perm], v[:, :, perm], 0.2, gen.BF16)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-12)
+    # permuting keys without the values must change the output
+    o3, _ = oracle.attention(q, k[:, :, perm], v, 0.2, gen.BF16)
+    assert np.max(np.abs(o3 - o1)) > 1e-3
+
+
+def test_key_shift_invariance():
+    rng = np.random.default_rng(2)
+    N, d = 48, 8
+    qv = rng.integers(-3, 4, size=(1, 1, N, d)).astype(np.float64)
+    kv = rng.integers(-3, 4, size=(1, 1, N, d)).astype(np.float64)
+    c = rng.integers(-2, 3, size=d).astype(np.float64)
+    q, k = exact_bf16(qv), exact_bf16(kv)
+    k2 = exact_bf16(kv + c)
+    v = bf16_bits(rng.standard_normal((1, 1, N, d)))
+    o1, l1 = oracle.attention(q, k, v, 0.15, gen.BF16)
+    o2, l2 = oracle.attention(q, k2, v, 0.15, gen.BF16)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2 - l1, 0.15 * (qv @ c), rtol=0, atol=1e-12)
+
+
+def test_batch_and_head_independence():
+    q, k, v = rand_inputs(10, 2, 3, 3, 64, 16)
+    o, lse = oracle.attention(q, k, v, 0.25, gen.BF16)
+    for b in range(2):
+        for h in range(3):
+            o1, l1 = oracle.attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1],
+                                      v[b:b + 1, h:h + 1], 0.25, gen.BF16)
+            np.testing.assert_array_equal(o1[0, 0], o[b, h])
+            np.testing.assert_array_equal(l1[0, 0], lse[b, h])
+
+
+def test_grouped_heads_equal_repeated_heads():
+    q, k, v = rand_inputs(12, 2, 8, 2, 64, 16)
+    o, lse = oracle.attention(q, k, v, 0.25, gen.BF16)
+    kr, vr = np.repeat(k, 4, axis=1), np.repeat(v, 4, axis=1)
+    o2, l2 = oracle.attention(q, kr, vr, 0.25, gen.BF16)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, l2)
+    # a wrong head mapping (h % Hkv) must give a different result
+    wrong_k = np.tile(k, (1, 4, 1, 1))
+    wrong_v = np.tile(v, (1, 4, 1, 1))
+    o3, _ = oracle.attention(q, wrong_k, wrong_v, 0.25, gen.BF16)
+    assert np.max(np.abs(o3 - o)) > 1e-3
+
+
+def test_row_subset_matches_full():
+    q, k, v = rand_inputs(13, 2, 2, 1, 96, 32)
+    o, lse = oracle.attention(q, k, v, 0.2, gen.BF16)
+    rows = np.array([0, 5, 95, 96, 250, 383])
+    os_, ls_ = oracle.attention(q, k, v, 0.2, gen.BF16, rows=rows)
+    np.testing.assert_array_equal(os_, o.reshape(-1, 32)[rows])
+    np.testing.assert_array_equal(ls_, lse.reshape(-1)[rows])
+
+
+# ---------------------------------------------------------------- identities and library
+
+@pytest.mark.parametrize("dtype,amp", [(gen.BF16, 1.0), (gen.FP16, 1.0), (gen.BF16, 3.0)])
+def test_lse_identity_and_library_crosscheck(dtype, amp):
+    torch = pytest.importorskip("torch")
+    q, k, v = rand_inputs(14, 1, 2, 1, 192, 64, dtype, amp)
+    scale = 1 / 8
+    o, lse = oracle.attention(q, k, v, scale, dtype)
+    qd, kd, vd = (torch.from_numpy(oracle.decode16(x, dtype)) for x in (q, k, v))
+    kd = kd.repeat_interleave(2, dim=1)
+    vd = vd.repeat_interleave(2, dim=1)
+    s = scale * torch.einsum("bhid,bhjd->bhij", qd, kd)
+    ref_o = torch.softmax(s, dim=-1) @ vd
+    ref_lse = torch.logsumexp(s, dim=-1)
+    np.testing.assert_allclose(o, ref_o.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=0, atol=1e-12)
+    # O = sum_j exp(s_j - LSE) v_j
+    o_from_lse = torch.exp(s - torch.from_numpy(lse)[..., None]) @ vd
+    np.testing.assert_allclose(o, o_from_lse.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_oracle_rejects_bad_sizes():
+    q, k, v = rand_inputs(15, 1, 3, 2, 16, 8)
+    with pytest.raises(ValueError):
+        oracle.attention(q, k, v, 0.1, gen.BF16)  # 3 query heads over 2 KV heads
