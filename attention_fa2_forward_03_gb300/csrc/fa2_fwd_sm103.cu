@@ -1,0 +1,612 @@
+// FlashAttention-2 forward pass for GB300 (sm_103a): kernel and C ABI.
+//
+// What is computed: exact attention O = softmax(scale * Q K^T) V plus the
+// per-row logsumexp, tile by tile with an online softmax so the N x N scores
+// never reach HBM ("A Case Study in CUDA Kernel Fusion: Implementing
+// FlashAttention-2 on NVIDIA Hopper Architecture using the CUTLASS Library",
+// abstract), for the slice under "Kernel Specification" in "FlashAttention-2
+// from scratch on Ampere, Part 1": forward only, non-causal, equal lengths,
+// lengths divisible by the block size, 16-bit I/O, fp32 softmax.
+//
+// How (one CTA = two 128-row query tiles of one KV head, 320 threads):
+//   warps 0-3   softmax for query tile 0 (thread = query row = TMEM lane)
+//   warps 4-7   softmax for query tile 1
+//   warp  8     TMA producer: Q tiles once, then K_0, V_0, K_1, V_1 ... through
+//               a ring of shared-memory stages (128-byte swizzle)
+//   warp  9     TMEM allocator and the single thread that issues tcgen05.mma
+// TMEM (512 columns x 128 lanes, fp32): S_0 | S_1 | O_0 | O_1. The softmax
+// writes P (16-bit, two per column) over the first half of its S columns and
+// the MMA warp consumes it from TMEM as the A operand of O += P V.
+// Issue order per KV tile j: PV(0,j), QK(0,j+1), PV(1,j), QK(1,j+1), so the
+// exponentials of one query tile overlap the tensor-core work of the other
+// (the "overlapping copy and GEMM operations" of the Hopper case study and
+// the interleaving of on-chip work with computation of the Ampere series,
+// done here with warp specialisation). The running max is exact (FA2's
+// online softmax): the largest weight of every row is exactly 1 in 16 bits,
+// and O and l are rescaled whenever a row's max grows; a warp skips the O
+// rescale when none of its 32 rows needs it.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa2.h"
+#include "ptx_sm103.cuh"
+
+namespace fa2 {
+
+constexpr int kBM = 128;           // query rows per tile (= TMEM lanes)
+constexpr int kBN = 128;           // keys per K/V tile
+constexpr int kNQ = 2;             // query tiles per CTA
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+
+// Where a watchdog gave up (bits 8..15 of the status word).
+enum WaitSite : int {
+    kSiteQFull = 1,
+    kSiteKvEmpty = 2,
+    kSiteKvFull = 3,
+    kSiteSFull = 4,
+    kSitePFull = 5,
+    kSiteOFull = 6,
+    kSiteDrain = 7,
+};
+
+struct Params {
+    void* o;             // [rows_q, D] 16-bit
+    float* lse;          // [rows_q]
+    long long wait_limit_ns;
+    int n_kv_tiles;      // N / 128
+    int q_tiles;         // (Hq / Hkv) * N / 128: packed query tiles per KV head
+    int kv_rows;         // N
+    int debug_flags;
+    float scale_log2;    // scale * log2(e)
+};
+
+template <int D>
+struct Layout {
+    static constexpr int kBlkBytes = kBM * 128;        // 128 rows x 64 elements
+    static constexpr int kTileBytes = kBM * D * 2;     // one Q, K or V tile
+    static constexpr int kStages = D == 128 ? 4 : 8;   // K/V ring stages
+    static constexpr int kQOff = 0;
+    static constexpr int kRingOff = kNQ * kTileBytes;
+    static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
+    // q_full[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] mma_done
+    static constexpr int kNumBars = 2 + 2 * kStages + 7;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + 1024-byte alignment slack
+    // TMEM columns: S_0 | S_1 | O_0 | O_1
+    static __device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
+    static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + D * t; }
+    static constexpr uint32_t kTmemCols = 512;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+__device__ int g_fa2_status;  // per device; 0 = OK
+
+struct Waiter {
+    volatile int* abort_flag;
+    long long limit_ns;
+
+    // Waits for the phase `parity` of `bar`. Returns false if the CTA is
+    // aborting (another wait ran out) or this wait ran out, in which case it
+    // records the site in the status word and raises the CTA's abort flag.
+    __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, int site) const {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (true) {
+            if (ptx::mbar_try_wait(bar, parity)) return true;
+            if (*abort_flag) return false;
+            if (static_cast<long long>(ptx::globaltimer_ns() - t0) > limit_ns) {
+                *abort_flag = 1;
+                atomicCAS(&g_fa2_status, 0, FA2_ERR_TIMEOUT | (site << 8));
+                return false;
+            }
+        }
+    }
+
+    // Same, ignoring the abort flag: used to let in-flight copies land
+    // before an aborting CTA exits.
+    __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait(bar, parity)) {
+            if (static_cast<long long>(ptx::globaltimer_ns() - t0) > limit_ns) {
+                atomicCAS(&g_fa2_status, 0, FA2_ERR_TIMEOUT | (kSiteDrain << 8));
+                return false;
+            }
+        }
+        return true;
+    }
+};
+
+template <int D>
+struct Bars {
+    uint32_t base;
+    __device__ uint32_t q_full(int t) const { return base + 8 * t; }
+    __device__ uint32_t kv_full(int s) const { return base + 8 * (2 + s); }
+    __device__ uint32_t kv_empty(int s) const { return base + 8 * (2 + Layout<D>::kStages + s); }
+    __device__ uint32_t s_full(int t) const { return base + 8 * (2 + 2 * Layout<D>::kStages + t); }
+    __device__ uint32_t p_full(int t) const { return base + 8 * (4 + 2 * Layout<D>::kStages + t); }
+    __device__ uint32_t o_full(int t) const { return base + 8 * (6 + 2 * Layout<D>::kStages + t); }
+    __device__ uint32_t mma_done() const { return base + 8 * (8 + 2 * Layout<D>::kStages); }
+};
+
+// ---------------------------------------------------------------- producer
+
+template <int D>
+__device__ __forceinline__ void producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                         const Params& p, uint32_t sbase, const Bars<D>& bars, const Waiter& w,
+                         int n_tiles, int q_row0, int kv_row0) {
+    using L = Layout<D>;
+    constexpr int S = L::kStages;
+    const bool load_q = (p.debug_flags & 1) == 0;
+    if (load_q) {
+        for (int t = 0; t < n_tiles; ++t) {
+            const uint32_t dst = sbase + L::kQOff + t * L::kTileBytes;
+            ptx::mbar_arrive_expect_tx(bars.q_full(t), L::kTileBytes);
+#pragma unroll
+            for (int blk = 0; blk < D / 64; ++blk)
+                ptx::tma_load_2d(dst + blk * L::kBlkBytes, tmQ, blk * 64, q_row0 + t * kBM,
+                                 bars.q_full(t));
+        }
+    }
+    const int n_items = 2 * p.n_kv_tiles;  // K_0, V_0, K_1, V_1, ...
+    int issued = 0;
+    for (int item = 0; item < n_items; ++item) {
+        const int s = item % S;
+        const uint32_t ph = (item / S) & 1;
+        if (!w.wait(bars.kv_empty(s), ph ^ 1, kSiteKvEmpty)) break;
+        const uint32_t dst = sbase + L::kRingOff + s * L::kTileBytes;
+        const CUtensorMap* tm = (item & 1) ? tmV : tmK;
+        const int row = kv_row0 + (item >> 1) * kBN;
+        ptx::mbar_arrive_expect_tx(bars.kv_full(s), L::kTileBytes);
+#pragma unroll
+        for (int blk = 0; blk < D / 64; ++blk)
+            ptx::tma_load_2d(dst + blk * L::kBlkBytes, tm, blk * 64, row, bars.kv_full(s));
+        ++issued;
+    }
+    if (issued < n_items || *w.abort_flag) {
+        // Aborting: let every copy this CTA started land before it exits.
+        const int first = issued > S ? issued - S : 0;
+        for (int item = first; item < issued; ++item)
+            w.drain(bars.kv_full(item % S), (item / S) & 1);
+        if (load_q)
+            for (int t = 0; t < n_tiles; ++t) w.drain(bars.q_full(t), 0);
+    }
+}
+
+// ---------------------------------------------------------------- MMA issuer
+
+template <int D, bool kBf16>
+__device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint32_t tmem, const Bars<D>& bars,
+                           const Waiter& w, int n_tiles) {
+    using L = Layout<D>;
+    constexpr int S = L::kStages;
+    constexpr uint32_t kAB = kBf16 ? 1u : 0u;
+    constexpr uint32_t kIdS = ptx::idesc_f16(kAB, 0, 0, kBM, kBN);  // S = Q K^T, both K-major
+    constexpr uint32_t kIdO = ptx::idesc_f16(kAB, 0, 1, kBM, D);    // O += P V, V MN-major
+
+    auto stage_addr = [&](int item) { return sbase + L::kRingOff + (item % S) * L::kTileBytes; };
+    auto issue_qk = [&](int t, uint32_t kaddr) {
+        const uint32_t qaddr = sbase + L::kQOff + t * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * L::kBlkBytes + (kk % 4) * 32;
+            ptx::mma_ss(tmem + L::col_s(t), ptx::desc_sw128(qaddr + off, 16, 1024),
+                        ptx::desc_sw128(kaddr + off, 16, 1024), kIdS, kk > 0);
+        }
+    };
+    auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+            ptx::mma_ts(tmem + L::col_o(t), tmem + L::col_s(t) + kk * 8,
+                        ptx::desc_sw128(vaddr + kk * 16 * 128, L::kBlkBytes, 1024), kIdO,
+                        (acc || kk > 0) ? 1u : 0u);
+        }
+    };
+
+    bool ok = true;
+    for (int t = 0; t < n_tiles && ok; ++t) ok = w.wait(bars.q_full(t), 0, kSiteQFull);
+    if (ok) ok = w.wait(bars.kv_full(0), 0, kSiteKvFull);  // K_0 is ring item 0
+    if (ok) {
+        ptx::tc_fence_after();
+        issue_qk(0, stage_addr(0));
+        ptx::tc_commit(bars.s_full(0));
+        if (n_tiles > 1) {
+            issue_qk(1, stage_addr(0));
+            ptx::tc_commit(bars.s_full(1));
+        }
+        ptx::tc_commit(bars.kv_empty(0));
+    }
+    const int nkv = p.n_kv_tiles;
+    for (int j = 0; j < nkv && ok; ++j) {
+        const int v_item = 2 * j + 1, k_item = 2 * j + 2;
+        const bool more = j + 1 < nkv;
+        if (!(ok = w.wait(bars.kv_full(v_item % S), (v_item / S) & 1, kSiteKvFull))) break;
+        if (!(ok = w.wait(bars.p_full(0), j & 1, kSitePFull))) break;
+        ptx::tc_fence_after();
+        issue_pv(0, stage_addr(v_item), j > 0);
+        if (n_tiles == 1) ptx::tc_commit(bars.kv_empty(v_item % S));
+        if (more) {
+            if (!(ok = w.wait(bars.kv_full(k_item % S), (k_item / S) & 1, kSiteKvFull))) break;
+            ptx::tc_fence_after();
+            issue_qk(0, stage_addr(k_item));
+            ptx::tc_commit(bars.s_full(0));
+            if (n_tiles == 1) ptx::tc_commit(bars.kv_empty(k_item % S));
+        } else {
+            ptx::tc_commit(bars.o_full(0));
+        }
+        if (n_tiles > 1) {
+            if (!(ok = w.wait(bars.p_full(1), j & 1, kSitePFull))) break;
+            ptx::tc_fence_after();
+            issue_pv(1, stage_addr(v_item), j > 0);
+            ptx::tc_commit(bars.kv_empty(v_item % S));
+            if (more) {
+                issue_qk(1, stage_addr(k_item));
+                ptx::tc_commit(bars.s_full(1));
+                ptx::tc_commit(bars.kv_empty(k_item % S));
+            } else {
+                ptx::tc_commit(bars.o_full(1));
+            }
+        }
+    }
+    // Every MMA issued above must finish before the CTA frees its TMEM.
+    ptx::tc_commit(bars.mma_done());
+    w.drain(bars.mma_done(), 0);
+}
+
+// ---------------------------------------------------------------- softmax + epilogue
+
+template <int D, bool kBf16>
+__device__ __forceinline__ void softmax_tile(const Params& p, uint32_t tmem, const Bars<D>& bars, const Waiter& w,
+                             int t, int q_row0) {
+    using L = Layout<D>;
+    const int wq = (threadIdx.x / 32) & 3;  // TMEM lane quarter of this warp
+    const int lane = threadIdx.x & 31;
+    const uint32_t row_addr = tmem + (static_cast<uint32_t>(32 * wq) << 16);
+    const uint32_t colS = L::col_s(t), colO = L::col_o(t);
+    const float c = p.scale_log2;
+
+    float m = -INFINITY;  // running row max of the scaled scores, log2 units
+    float l = 0.0f;       // running sum of exp2(s*c - m)
+    bool ok = true;
+    for (int j = 0; j < p.n_kv_tiles; ++j) {
+        ok = w.wait(bars.s_full(t), j & 1, kSiteSFull);
+        if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+        }
+        ptx::tc_fence_after();
+        uint32_t s[kBN];
+        ptx::tmem_ld32_at<0>(row_addr + colS + 0, s);
+        ptx::tmem_ld32_at<32>(row_addr + colS + 32, s);
+        ptx::tmem_ld32_at<64>(row_addr + colS + 64, s);
+        ptx::tmem_ld32_at<96>(row_addr + colS + 96, s);
+        ptx::tmem_wait_ld();
+
+        float mx0 = __uint_as_float(s[0]), mx1 = __uint_as_float(s[1]);
+#pragma unroll
+        for (int i = 2; i < kBN; i += 2) {
+            mx0 = fmaxf(mx0, __uint_as_float(s[i]));
+            mx1 = fmaxf(mx1, __uint_as_float(s[i + 1]));
+        }
+        const float m_tile = fmaxf(mx0, mx1) * c;
+        bool rescale = false;
+        float alpha = 1.0f;
+        if (j == 0) {
+            m = m_tile;
+        } else {
+            const bool need = m_tile > m;
+            rescale = __any_sync(0xffffffffu, need);
+            if (need) {
+                alpha = ptx::ex2_approx(m - m_tile);
+                l *= alpha;
+                m = m_tile;
+            }
+        }
+        const float neg_m = -m;
+        float rs0 = 0.0f, rs1 = 0.0f;
+        uint32_t pk[kBN / 2];
+#pragma unroll
+        for (int i = 0; i < kBN / 2; ++i) {
+            const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(s[2 * i]), c, neg_m));
+            const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(s[2 * i + 1]), c, neg_m));
+            rs0 += p0;
+            rs1 += p1;
+            pk[i] = ptx::pack2<kBf16>(p0, p1);
+        }
+        l += rs0 + rs1;
+        ptx::tmem_st32_at<0>(row_addr + colS, pk);
+        ptx::tmem_st32_at<32>(row_addr + colS + 32, pk);
+        if (rescale) {
+            // O += P V of the previous KV tile has completed (its commit
+            // precedes this tile's S), and the next one waits for p_full, so
+            // O can be rescaled in place here.
+#pragma unroll
+            for (int cc = 0; cc < D; cc += 32) {
+                uint32_t o[32];
+                ptx::tmem_ld32(row_addr + colO + cc, o);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                ptx::tmem_st32(row_addr + colO + cc, o);
+            }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bars.p_full(t));
+    }
+    if (ok) ok = w.wait(bars.o_full(t), 0, kSiteOFull);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    ptx::tc_fence_after();
+
+    // Epilogue: O / l rounded to 16 bits, one 2*D-byte row per thread, and
+    // LSE = (m + log2 l) * ln 2.
+    const int row = q_row0 + t * kBM + 32 * wq + lane;
+    const float inv_l = ptx::rcp_approx(l);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + static_cast<size_t>(row) * D);
+#pragma unroll
+    for (int cc = 0; cc < D; cc += 32) {
+        uint32_t o[32];
+        ptx::tmem_ld32(row_addr + colO + cc, o);
+        ptx::tmem_wait_ld();
+        uint32_t h[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            h[i] = ptx::pack2<kBf16>(__uint_as_float(o[2 * i]) * inv_l,
+                                     __uint_as_float(o[2 * i + 1]) * inv_l);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+            dst[cc / 8 + v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+    }
+    p.lse[row] = (m + ptx::lg2_approx(l)) * 0.69314718055994530942f;
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa2_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const Params p) {
+    using L = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = ptx::smem_addr(smem);
+    const Bars<D> bars{sbase + L::kBarOff};
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    const int group = blockIdx.y;  // b * Hkv + kv head
+    const int qt0 = kNQ * blockIdx.x;
+    const int n_tiles = min(kNQ, p.q_tiles - qt0);
+    const int q_row0 = (group * p.q_tiles + qt0) * kBM;
+    const int kv_row0 = group * p.kv_rows;
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(bars.q_full(t), 1);
+            ptx::mbar_init(bars.s_full(t), 1);
+            ptx::mbar_init(bars.p_full(t), kBM);
+            ptx::mbar_init(bars.o_full(t), 1);
+        }
+        for (int s = 0; s < L::kStages; ++s) {
+            ptx::mbar_init(bars.kv_full(s), 1);
+            ptx::mbar_init(bars.kv_empty(s), 1);
+        }
+        ptx::mbar_init(bars.mma_done(), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == kLoadWarp && lane == 0) {
+        ptx::tma_prefetch_desc(&tmQ);
+        ptx::tma_prefetch_desc(&tmK);
+        ptx::tma_prefetch_desc(&tmV);
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), L::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Waiter w{abort_flag, p.wait_limit_ns};
+
+    if (warp == kLoadWarp) {
+        if (lane == 0) producer<D>(&tmQ, &tmK, &tmV, p, sbase, bars, w, n_tiles, q_row0, kv_row0);
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) mma_issuer<D, kBf16>(p, sbase, tmem, bars, w, n_tiles);
+        __syncwarp();
+    } else {
+        const int t = warp / 4;
+        if (t < n_tiles) softmax_tile<D, kBf16>(p, tmem, bars, w, t, q_row0);
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+}  // namespace fa2
+
+// ==================================================================== host
+
+namespace {
+
+using fa2::Layout;
+using fa2::Params;
+
+std::atomic<long long> g_wait_limit_ns{2000000000LL};
+std::atomic<int> g_debug_flags{0};
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+    bool probed = false;
+    bool supported = false;
+    bool smem_set[4] = {false, false, false, false};
+};
+DeviceState g_dev[kMaxDevices];
+
+fa2_status get_encoder() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode) return FA2_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+        return FA2_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return FA2_OK;
+}
+
+fa2_status check_device(int* dev_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA2_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FA2_ERR_UNSUPPORTED;
+    DeviceState& st = g_dev[dev];
+    if (!st.probed) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return FA2_ERR_CUDA;
+        std::lock_guard<std::mutex> lk(g_mu);
+        st.supported = (major == 10 && minor == 3);
+        st.probed = true;
+    }
+    *dev_out = dev;
+    return st.supported ? FA2_OK : FA2_ERR_UNSUPPORTED;
+}
+
+// 2-D view [rows, d] of a 16-bit tensor, boxes of 128 rows x 64 elements
+// (128 bytes, the widest box the 128-byte swizzle allows).
+fa2_status encode_map(CUtensorMap* m, const void* ptr, uint64_t rows, int d) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), rows};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                          es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
+}
+
+template <int D, bool kBf16>
+fa2_status launch(int dev, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                  const Params& p, dim3 grid, cudaStream_t stream) {
+    constexpr int kSmem = Layout<D>::kSmemBytes;
+    auto kern = fa2::fa2_fwd_kernel<D, kBf16>;
+    const int slot = (D == 128 ? 0 : 2) + (kBf16 ? 0 : 1);
+    if (!g_dev[dev].smem_set[slot]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
+            return FA2_ERR_CUDA;
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_dev[dev].smem_set[slot] = true;
+    }
+    kern<<<grid, fa2::kThreads, kSmem, stream>>>(mq, mk, mv, p);
+    return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+fa2_status fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
+                       int H_kv, int N, int d, float scale, fa2_dtype dtype, cudaStream_t stream) {
+    if (!q || !k || !v || !o || !lse) return FA2_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA2_ERR_INVALID_ARG;
+    if (B <= 0 || H_q <= 0 || H_kv <= 0 || N <= 0 || d <= 0) return FA2_ERR_INVALID_ARG;
+    if (H_q % H_kv != 0) return FA2_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.0f)) return FA2_ERR_INVALID_ARG;
+    if (dtype != FA2_BF16 && dtype != FA2_FP16) return FA2_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA2_ERR_UNSUPPORTED;
+    if (N % fa2::kBM != 0) return FA2_ERR_UNSUPPORTED;
+    // TMA coordinates and row indices are 32-bit; the grid's y extent is 65535.
+    const long long rows_q = static_cast<long long>(B) * H_q * N;
+    const long long groups = static_cast<long long>(B) * H_kv;
+    if (rows_q > 0x7FFFFFFFLL || groups > 65535) return FA2_ERR_UNSUPPORTED;
+
+    int dev = 0;
+    fa2_status st = check_device(&dev);
+    if (st != FA2_OK) return st;
+    if ((st = get_encoder()) != FA2_OK) return st;
+
+    CUtensorMap mq, mk, mv;
+    const uint64_t rows_kv = static_cast<uint64_t>(B) * H_kv * N;
+    if (encode_map(&mq, q, static_cast<uint64_t>(rows_q), d) != FA2_OK ||
+        encode_map(&mk, k, rows_kv, d) != FA2_OK || encode_map(&mv, v, rows_kv, d) != FA2_OK)
+        return FA2_ERR_CUDA;
+
+    Params p{};
+    p.o = o;
+    p.lse = lse;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    p.n_kv_tiles = N / fa2::kBN;
+    p.q_tiles = (H_q / H_kv) * (N / fa2::kBM);
+    p.kv_rows = N;
+    p.debug_flags = g_debug_flags.load();
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    const dim3 grid((p.q_tiles + fa2::kNQ - 1) / fa2::kNQ, static_cast<unsigned>(groups));
+
+    const bool bf = dtype == FA2_BF16;
+    if (d == 128)
+        return bf ? launch<128, true>(dev, mq, mk, mv, p, grid, stream)
+                  : launch<128, false>(dev, mq, mk, mv, p, grid, stream);
+    return bf ? launch<64, true>(dev, mq, mk, mv, p, grid, stream)
+              : launch<64, false>(dev, mq, mk, mv, p, grid, stream);
+}
+
+fa2_status fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                   int d, float scale, fa2_dtype dtype, cudaStream_t stream) {
+    return fa2_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, scale, dtype, stream);
+}
+
+fa2_status fa2_check_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FA2_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, fa2::g_fa2_status, sizeof(int)) != cudaSuccess) return FA2_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(fa2::g_fa2_status, &zero, sizeof(int)) != cudaSuccess) return FA2_ERR_CUDA;
+        return (v & 0xFF) == FA2_ERR_TIMEOUT ? FA2_ERR_TIMEOUT : FA2_ERR_CUDA;
+    }
+    return FA2_OK;
+}
+
+const char* fa2_status_string(fa2_status s) {
+    switch (s) {
+        case FA2_OK: return "FA2_OK";
+        case FA2_ERR_INVALID_ARG: return "FA2_ERR_INVALID_ARG";
+        case FA2_ERR_UNSUPPORTED: return "FA2_ERR_UNSUPPORTED";
+        case FA2_ERR_CUDA: return "FA2_ERR_CUDA";
+        case FA2_ERR_TIMEOUT: return "FA2_ERR_TIMEOUT";
+    }
+    return "FA2_ERR_UNKNOWN";
+}
+
+int64_t fa2_set_wait_limit_ns(int64_t limit_ns) {
+    if (limit_ns <= 0) limit_ns = 2000000000LL;
+    return g_wait_limit_ns.exchange(limit_ns);
+}
+
+int fa2_set_debug_flags(int flags) { return g_debug_flags.exchange(flags); }
+
+const char* fa2_version(void) { return "fa2-sm103a 0.1.0"; }
+
+}  // extern "C"

@@ -1,0 +1,158 @@
+"""Python binding of the C ABI in include/fa2.h (argument marshalling only).
+
+Every entry point forwards raw device pointers, sizes and the CUDA stream
+handle to ``libfa2.so``; all compute runs in the library's sm_103a kernel.
+If the library cannot be loaded the call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfa2.so")
+
+FA2_BF16 = 0
+FA2_FP16 = 1
+
+FA2_OK = 0
+FA2_ERR_INVALID_ARG = 1
+FA2_ERR_UNSUPPORTED = 2
+FA2_ERR_CUDA = 3
+FA2_ERR_TIMEOUT = 4
+
+# symbols declared in include/fa2.h
+EXPORTS = ("fa2_fwd", "fa2_fwd_gqa", "fa2_check_status", "fa2_status_string",
+           "fa2_set_wait_limit_ns", "fa2_set_debug_flags", "fa2_version")
+
+_lib = None
+
+
+class FA2Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where} failed: {status_string(status)}")
+
+
+def load(path: str = LIB_PATH):
+    """Load libfa2.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"CUDA library {path} is missing: run __graft_entry__.build() "
+                          "(python -m attention_fa2_forward_03_gb300.build)")
+    lib = ctypes.CDLL(path)
+    p, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa2_fwd.argtypes = [p, p, p, p, p, i, i, i, i, f, i, p]
+    lib.fa2_fwd.restype = i
+    lib.fa2_fwd_gqa.argtypes = [p, p, p, p, p, i, i, i, i, i, f, i, p]
+    lib.fa2_fwd_gqa.restype = i
+    lib.fa2_check_status.argtypes = [p]
+    lib.fa2_check_status.restype = i
+    lib.fa2_status_string.argtypes = [i]
+    lib.fa2_status_string.restype = ctypes.c_char_p
+    lib.fa2_set_wait_limit_ns.argtypes = [ctypes.c_int64]
+    lib.fa2_set_wait_limit_ns.restype = ctypes.c_int64
+    lib.fa2_set_debug_flags.argtypes = [i]
+    lib.fa2_set_debug_flags.restype = i
+    lib.fa2_version.argtypes = []
+    lib.fa2_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().fa2_status_string(int(status)).decode()
+
+
+# ------------------------------------------------------------------ raw pointer API
+
+def fa2_fwd_gqa_ptr(q, k, v, o, lse, B, H_q, H_kv, N, d, scale, dtype, stream=0) -> int:
+    """fa2_fwd_gqa on raw device addresses (ints); returns the status code."""
+    return load().fa2_fwd_gqa(q, k, v, o, lse, B, H_q, H_kv, N, d, float(scale), int(dtype),
+                              stream or None)
+
+
+def fa2_fwd_ptr(q, k, v, o, lse, B, H, N, d, scale, dtype, stream=0) -> int:
+    """fa2_fwd on raw device addresses (ints); returns the status code."""
+    return load().fa2_fwd(q, k, v, o, lse, B, H, N, d, float(scale), int(dtype), stream or None)
+
+
+def fa2_check_status(stream=0) -> int:
+    return load().fa2_check_status(stream or None)
+
+
+def fa2_set_wait_limit_ns(limit_ns: int) -> int:
+    return load().fa2_set_wait_limit_ns(int(limit_ns))
+
+
+def fa2_set_debug_flags(flags: int) -> int:
+    return load().fa2_set_debug_flags(int(flags))
+
+
+def fa2_version() -> str:
+    return load().fa2_version().decode()
+
+
+# ------------------------------------------------------------------ torch tensors
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return FA2_BF16
+    if t.dtype == torch.float16:
+        return FA2_FP16
+    raise TypeError(f"q/k/v must be bf16 or fp16, got {t.dtype}")
+
+
+def _stream_handle(stream, device) -> int:
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def fa2_fwd_gqa(q, k, v, o=None, lse=None, scale=None, stream=None):
+    """Attention forward on CUDA tensors q [B,Hq,N,d], k/v [B,Hkv,N,d].
+
+    Allocates o / lse with torch when they are not given (that is device-memory
+    plumbing; the library itself allocates nothing). Returns (o, lse).
+    """
+    import torch
+
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, H, N, d]")
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, N, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, Hkv, N, d] with q's B, N and d")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k and v must be contiguous CUDA tensors")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    if o.shape != q.shape or o.dtype != q.dtype or not o.is_contiguous():
+        raise ValueError("o must be a contiguous tensor like q")
+    if tuple(lse.shape) != (B, Hq, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, Hq, N]")
+    if scale is None:
+        scale = d ** -0.5
+    rc = fa2_fwd_gqa_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                         B, Hq, Hkv, N, d, scale, _dtype_code(q), _stream_handle(stream, q.device))
+    if rc != FA2_OK:
+        raise FA2Error(rc, "fa2_fwd_gqa")
+    return o, lse
+
+
+def fa2_fwd(q, k, v, o=None, lse=None, scale=None, stream=None):
+    """Multi-head attention forward: q, k, v all [B, H, N, d]. Returns (o, lse)."""
+    if q.shape[1] != k.shape[1]:
+        raise ValueError("fa2_fwd needs equal head counts; use fa2_fwd_gqa")
+    return fa2_fwd_gqa(q, k, v, o, lse, scale, stream)

@@ -1,0 +1,127 @@
+/*
+ * fa2.h - C ABI of the GB300 (sm_103a) FlashAttention-2 forward library.
+ *
+ * The operation. Exact scaled-dot-product attention, forward pass only, as
+ * defined for FlashAttention-2 in "A Case Study in CUDA Kernel Fusion:
+ * Implementing FlashAttention-2 on NVIDIA Hopper Architecture using the
+ * CUTLASS Library" (abstract: online softmax fused with two back-to-back
+ * GEMMs), restricted to the slice listed under "Kernel Specification" in
+ * "FlashAttention-2 from scratch on Ampere, Part 1" (lubitschian.com/flash/
+ * Part-1): non-causal, equal query/key/value sequence lengths, sequence
+ * lengths divisible by the block size, 16-bit (bf16 or fp16) inputs and
+ * outputs, softmax in fp32. For every batch b, query head h and query row i:
+ *
+ *     S[j]   = scale * <Q[b,h,i,:], K[b,g(h),j,:]>        j = 0 .. N-1
+ *     O[b,h,i,:] = sum_j softmax(S)[j] * V[b,g(h),j,:]
+ *     LSE[b,h,i] = ln sum_j exp(S[j])                     (natural log)
+ *
+ * with g(h) = h / (Hq / Hkv). Grouped KV heads (Hq > Hkv) use the query-head
+ * packing named in "FlashAttention-3 for Inference: INT8 Quantization and
+ * Query Head Packing for MQA/GQA" (Colfax Research author page): the Hq/Hkv
+ * query heads that share a KV head are consecutive, so their rows form one
+ * contiguous block of Hq/Hkv * N query rows that is processed against a
+ * single stream of K/V tiles. The N x N score matrix never reaches memory.
+ *
+ * Data layout. All tensors are dense, row-major, caller-owned device memory:
+ *     q, o : [B, Hq,  N, d]   16-bit elements (bf16 or fp16, same for all)
+ *     k, v : [B, Hkv, N, d]   16-bit elements
+ *     lse  : [B, Hq,  N]      fp32
+ * Every pointer must be 16-byte aligned. Outputs are fully overwritten.
+ *
+ * Execution. Calls are asynchronous on `stream` (0 = legacy default stream)
+ * and launch exactly one kernel. The library allocates no memory per call;
+ * it owns one status word per device (a __device__ variable), which the
+ * kernel sets if one of its bounded waits gives up.
+ *
+ * Errors. Argument errors are detected on the host before anything is
+ * launched; no entry point exits the process or throws.
+ */
+#ifndef FA2_H_
+#define FA2_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA2_BF16 = 0,
+    FA2_FP16 = 1
+} fa2_dtype;
+
+typedef enum {
+    FA2_OK = 0,
+    FA2_ERR_INVALID_ARG = 1,  /* NULL/misaligned pointer, non-positive size,
+                                 Hq % Hkv != 0, scale not finite and > 0 */
+    FA2_ERR_UNSUPPORTED = 2,  /* d not in {64, 128}, N % 128 != 0, sizes past
+                                 32-bit coordinates, or a device that is not
+                                 compute capability 10.3 */
+    FA2_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+    FA2_ERR_TIMEOUT = 4       /* the kernel's watchdog gave up on a wait */
+} fa2_status;
+
+/*
+ * Multi-head attention forward (Hq == Hkv == H).
+ *   q, k, v : [B, H, N, d] 16-bit, device, 16-byte aligned (inputs, read only)
+ *   o       : [B, H, N, d] 16-bit, device (output)
+ *   lse     : [B, H, N] fp32, device (output, natural-log logsumexp of the
+ *             scaled scores)
+ *   B, H, N : positive; N a multiple of 128
+ *   d       : 64 or 128
+ *   scale   : finite, > 0 (usually 1/sqrt(d))
+ *   dtype   : element type of q, k, v and o
+ *   stream  : CUDA stream the kernel is queued on
+ * Returns FA2_OK once the kernel is queued; FA2_ERR_* otherwise, and then
+ * nothing was launched.
+ */
+fa2_status fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int N, int d, float scale, fa2_dtype dtype,
+                   cudaStream_t stream);
+
+/*
+ * Grouped-KV (GQA/MQA) attention forward. Same contract as fa2_fwd, with
+ * q, o : [B, H_q, N, d], k, v : [B, H_kv, N, d], lse : [B, H_q, N] and
+ * H_q a multiple of H_kv; query head h reads KV head h / (H_q / H_kv).
+ * fa2_fwd(..., H, ...) is fa2_fwd_gqa(..., H, H, ...).
+ */
+fa2_status fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int H_q, int H_kv, int N, int d, float scale,
+                       fa2_dtype dtype, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word. Returns FA2_ERR_TIMEOUT if a kernel since the last check abandoned a
+ * wait (its outputs are then undefined), FA2_ERR_CUDA if the stream reported
+ * an error, FA2_OK otherwise.
+ */
+fa2_status fa2_check_status(cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* fa2_status_string(fa2_status status);
+
+/*
+ * Watchdog limit for each in-kernel wait, in nanoseconds, for kernels
+ * launched after the call on any device of this process (default 2e9, i.e.
+ * two seconds; values <= 0 restore the default). Returns the previous value.
+ */
+int64_t fa2_set_wait_limit_ns(int64_t limit_ns);
+
+/*
+ * Test hook for the watchdog. With flags = 1 the next kernels skip the load
+ * of their query tiles, so their waits run out and the status word reports
+ * FA2_ERR_TIMEOUT; the kernel still frees its tensor memory, waits for its
+ * own copies and returns normally. 0 (the default) restores normal
+ * operation. Returns the previous flags.
+ */
+int fa2_set_debug_flags(int flags);
+
+/* Library version string, e.g. "fa2-sm103a 0.1.0". */
+const char* fa2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA2_H_ */

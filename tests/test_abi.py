@@ -1,0 +1,96 @@
+"""The C-ABI library loads, exports every symbol include/fa2.h declares, and
+rejects invalid arguments on the host before touching a device (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_fa2_forward_03_gb300 import build, fa2
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa2.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return fa2.load()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa2_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_expected_api():
+    assert set(header_functions()) == set(fa2.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    names = {0: "FA2_OK", 1: "FA2_ERR_INVALID_ARG", 2: "FA2_ERR_UNSUPPORTED",
+             3: "FA2_ERR_CUDA", 4: "FA2_ERR_TIMEOUT"}
+    for code, name in names.items():
+        assert fa2.status_string(code) == name
+    assert fa2.status_string(99) == "FA2_ERR_UNKNOWN"
+    assert fa2.fa2_version().startswith("fa2-sm103a")
+
+
+A = 1 << 20  # a 16-byte aligned fake address: never dereferenced on these paths
+
+
+@pytest.mark.parametrize("args,expected", [
+    # (q, k, v, o, lse, B, Hq, Hkv, N, d, scale, dtype)
+    ((0, A, A, A, A, 1, 1, 1, 128, 128, 0.1, 0), fa2.FA2_ERR_INVALID_ARG),   # NULL q
+    ((A, A, A, A, 0, 1, 1, 1, 128, 128, 0.1, 0), fa2.FA2_ERR_INVALID_ARG),   # NULL lse
+    ((A + 8, A, A, A, A, 1, 1, 1, 128, 128, 0.1, 0), fa2.FA2_ERR_INVALID_ARG),  # misaligned
+    ((A, A, A, A, A + 4, 1, 1, 1, 128, 128, 0.1, 0), fa2.FA2_ERR_INVALID_ARG),  # misaligned lse
+    ((A, A, A, A, A, 0, 1, 1, 128, 128, 0.1, 0), fa2.FA2_ERR_INVALID_ARG),   # B = 0
+    ((A, A, A, A, A, 1, -2, 1, 128, 128, 0.1, 0), fa2.FA2_ERR_INVALID_ARG),  # Hq < 0
+    ((A, A, A, A, A, 1, 1, 1, 0, 128, 0.1, 0), fa2.FA2_ERR_INVALID_ARG),     # N = 0
+    ((A, A, A, A, A, 1, 6, 4, 128, 128, 0.1, 0), fa2.FA2_ERR_INVALID_ARG),   # Hq % Hkv
+    ((A, A, A, A, A, 1, 1, 1, 128, 128, 0.0, 0), fa2.FA2_ERR_INVALID_ARG),   # scale = 0
+    ((A, A, A, A, A, 1, 1, 1, 128, 128, -1.0, 0), fa2.FA2_ERR_INVALID_ARG),  # scale < 0
+    ((A, A, A, A, A, 1, 1, 1, 128, 128, float("nan"), 0), fa2.FA2_ERR_INVALID_ARG),
+    ((A, A, A, A, A, 1, 1, 1, 128, 128, float("inf"), 0), fa2.FA2_ERR_INVALID_ARG),
+    ((A, A, A, A, A, 1, 1, 1, 128, 128, 0.1, 7), fa2.FA2_ERR_INVALID_ARG),   # dtype
+    ((A, A, A, A, A, 1, 1, 1, 128, 96, 0.1, 0), fa2.FA2_ERR_UNSUPPORTED),    # d = 96
+    ((A, A, A, A, A, 1, 1, 1, 128, 256, 0.1, 0), fa2.FA2_ERR_UNSUPPORTED),   # d = 256
+    ((A, A, A, A, A, 1, 1, 1, 200, 128, 0.1, 0), fa2.FA2_ERR_UNSUPPORTED),   # N % 128
+    ((A, A, A, A, A, 1, 1, 1, 64, 64, 0.1, 1), fa2.FA2_ERR_UNSUPPORTED),     # N < block
+    ((A, A, A, A, A, 2048, 8, 8, 131072, 128, 0.1, 0), fa2.FA2_ERR_UNSUPPORTED),  # rows >= 2^31
+    ((A, A, A, A, A, 65536, 1, 1, 128, 64, 0.1, 0), fa2.FA2_ERR_UNSUPPORTED),  # grid y > 65535
+])
+def test_host_validation(lib, args, expected):
+    assert fa2.fa2_fwd_gqa_ptr(*args) == expected
+
+
+def test_mha_entry_forwards_to_gqa(lib):
+    assert fa2.fa2_fwd_ptr(0, A, A, A, A, 1, 1, 128, 128, 0.1, 0) == fa2.FA2_ERR_INVALID_ARG
+    assert fa2.fa2_fwd_ptr(A, A, A, A, A, 1, 1, 128, 80, 0.1, 0) == fa2.FA2_ERR_UNSUPPORTED
+
+
+def test_wait_limit_and_debug_flags_round_trip(lib):
+    prev = fa2.fa2_set_wait_limit_ns(12345)
+    assert fa2.fa2_set_wait_limit_ns(prev) == 12345
+    assert fa2.fa2_set_wait_limit_ns(0) == prev  # <= 0 restores the default
+    fa2.fa2_set_wait_limit_ns(prev)
+    old = fa2.fa2_set_debug_flags(1)
+    assert fa2.fa2_set_debug_flags(old) == 1
+
+
+def test_binding_refuses_missing_library(tmp_path):
+    saved = fa2._lib
+    fa2._lib = None
+    try:
+        with pytest.raises(ImportError):
+            fa2.load(str(tmp_path / "absent.so"))
+    finally:
+        fa2._lib = saved
