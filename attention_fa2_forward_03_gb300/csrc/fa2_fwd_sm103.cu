@@ -262,6 +262,24 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint
 
 // ---------------------------------------------------------------- softmax + epilogue
 
+// 32-column TMEM load/store into slice [off, off+32) of a register array;
+// `off` is a compile-time constant after unrolling.
+template <int N>
+__device__ __forceinline__ void ld_slice(uint32_t taddr, uint32_t (&r)[N], int off) {
+    if (off == 0) ptx::tmem_ld32_at<0>(taddr, r);
+    if constexpr (N > 32) if (off == 32) ptx::tmem_ld32_at<32 % N>(taddr, r);
+    if constexpr (N > 64) if (off == 64) ptx::tmem_ld32_at<64 % N>(taddr, r);
+    if constexpr (N > 96) if (off == 96) ptx::tmem_ld32_at<96 % N>(taddr, r);
+}
+
+template <int N>
+__device__ __forceinline__ void st_slice(uint32_t taddr, const uint32_t (&r)[N], int off) {
+    if (off == 0) ptx::tmem_st32_at<0>(taddr, r);
+    if constexpr (N > 32) if (off == 32) ptx::tmem_st32_at<32 % N>(taddr, r);
+    if constexpr (N > 64) if (off == 64) ptx::tmem_st32_at<64 % N>(taddr, r);
+    if constexpr (N > 96) if (off == 96) ptx::tmem_st32_at<96 % N>(taddr, r);
+}
+
 template <int D, bool kBf16>
 __device__ __forceinline__ void softmax_tile(const Params& p, uint32_t tmem, const Bars<D>& bars, const Waiter& w,
                              int t, int q_row0) {
@@ -289,13 +307,18 @@ __device__ __forceinline__ void softmax_tile(const Params& p, uint32_t tmem, con
         ptx::tmem_ld32_at<96>(row_addr + colS + 96, s);
         ptx::tmem_wait_ld();
 
-        float mx0 = __uint_as_float(s[0]), mx1 = __uint_as_float(s[1]);
+        // Row max: eight independent chains of 3-input max, then combine.
+        float mx[8];
 #pragma unroll
-        for (int i = 2; i < kBN; i += 2) {
-            mx0 = fmaxf(mx0, __uint_as_float(s[i]));
-            mx1 = fmaxf(mx1, __uint_as_float(s[i + 1]));
+        for (int k = 0; k < 8; ++k) {
+            float a = __uint_as_float(s[k]);
+#pragma unroll
+            for (int i = 1; i < 15; i += 2)
+                a = ptx::max3(a, __uint_as_float(s[k + 8 * i]), __uint_as_float(s[k + 8 * (i + 1)]));
+            mx[k] = fmaxf(a, __uint_as_float(s[k + 120]));
         }
-        const float m_tile = fmaxf(mx0, mx1) * c;
+        const float m_tile =
+            fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7]))) * c;
         bool rescale = false;
         float alpha = 1.0f;
         if (j == 0) {
@@ -309,33 +332,52 @@ __device__ __forceinline__ void softmax_tile(const Params& p, uint32_t tmem, con
                 m = m_tile;
             }
         }
-        const float neg_m = -m;
-        float rs0 = 0.0f, rs1 = 0.0f;
+        // P = exp2(S*c - m) on pairs: one packed FMA, two MUFU ex2, one packed
+        // add into four partial row sums, one 16-bit pack.
+        const uint64_t c2 = ptx::f2_pack(c, c);
+        const uint64_t nm2 = ptx::f2_pack(-m, -m);
+        uint64_t acc[4] = {0, 0, 0, 0};
         uint32_t pk[kBN / 2];
 #pragma unroll
         for (int i = 0; i < kBN / 2; ++i) {
-            const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(s[2 * i]), c, neg_m));
-            const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(s[2 * i + 1]), c, neg_m));
-            rs0 += p0;
-            rs1 += p1;
+            const uint64_t x = ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                                           c2, nm2);
+            float x0, x1;
+            ptx::f2_unpack(x, x0, x1);
+            const float p0 = ptx::ex2_approx(x0);
+            const float p1 = ptx::ex2_approx(x1);
+            acc[i & 3] = ptx::f2_add(acc[i & 3], ptx::f2_pack(p0, p1));
             pk[i] = ptx::pack2<kBf16>(p0, p1);
         }
-        l += rs0 + rs1;
+        {
+            float a0, a1, b0, b1;
+            ptx::f2_unpack(ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3])), a0, a1);
+            (void)b0;
+            (void)b1;
+            l += a0 + a1;
+        }
         ptx::tmem_st32_at<0>(row_addr + colS, pk);
         ptx::tmem_st32_at<32>(row_addr + colS + 32, pk);
         if (rescale) {
             // O += P V of the previous KV tile has completed (its commit
             // precedes this tile's S), and the next one waits for p_full, so
-            // O can be rescaled in place here.
+            // O can be rescaled in place here: load the whole row, one wait,
+            // packed multiplies, store.
+            uint32_t o[D];
 #pragma unroll
-            for (int cc = 0; cc < D; cc += 32) {
-                uint32_t o[32];
-                ptx::tmem_ld32(row_addr + colO + cc, o);
-                ptx::tmem_wait_ld();
+            for (int cc = 0; cc < D; cc += 32) ld_slice(row_addr + colO + cc, o, cc);
+            ptx::tmem_wait_ld();
+            const uint64_t a2 = ptx::f2_pack(alpha, alpha);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                ptx::tmem_st32(row_addr + colO + cc, o);
+            for (int i = 0; i < D / 2; ++i) {
+                float o0, o1;
+                ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2),
+                               o0, o1);
+                o[2 * i] = __float_as_uint(o0);
+                o[2 * i + 1] = __float_as_uint(o1);
             }
+#pragma unroll
+            for (int cc = 0; cc < D; cc += 32) st_slice(row_addr + colO + cc, o, cc);
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
