@@ -8,31 +8,38 @@
 // from scratch on Ampere, Part 1": forward only, non-causal, equal lengths,
 // lengths divisible by the block size, 16-bit I/O, fp32 softmax.
 //
-// How (one CTA = two 128-row query tiles of one KV head, 320 threads):
-//   warps 0-3   softmax for query tile 0 (thread = query row = TMEM lane)
-//   warps 4-7   softmax for query tile 1
-//   warp  8     TMA producer: Q tiles once, then K_0, V_0, K_1, V_1 ... through
-//               a ring of shared-memory stages (128-byte swizzle)
-//   warp  9     TMEM allocator and the single thread that issues tcgen05.mma
+// How. A persistent grid (one CTA per SM) walks work items; an item is two
+// 128-row query tiles of one KV head (query heads that share a KV head are
+// packed into one contiguous block of rows). 512 threads in four warpgroups:
+//   WG0, WG1  softmax for query tile 0 / 1: thread = query row = TMEM lane
+//   WG2       correction: rescales O in TMEM when a row's max grows, and the
+//             epilogue (O / l -> 16 bit, LSE) for both tiles
+//   WG3       warp 12: TMA producer (Q tiles, then K_0, V_0, K_1, V_1, ...
+//             through a ring of 128-byte-swizzled shared-memory stages);
+//             warp 13: TMEM allocator and the one thread that issues every
+//             tcgen05.mma / tcgen05.commit; warps 14-15 idle
+// Registers are moved between warpgroups with setmaxnreg (softmax 176,
+// correction 104, producer/MMA 56 per thread).
 // TMEM (512 columns x 128 lanes, fp32): S_0 | S_1 | O_0 | O_1. The softmax
 // writes P (16-bit, two per column) over the first half of its S columns and
-// the MMA warp consumes it from TMEM as the A operand of O += P V.
+// the MMA thread consumes it from TMEM as the A operand of O += P V.
 // Issue order per KV tile j: PV(0,j), QK(0,j+1), PV(1,j), QK(1,j+1), so the
 // exponentials of one query tile overlap the tensor-core work of the other
 // (the "overlapping copy and GEMM operations" of the Hopper case study and
 // the interleaving of on-chip work with computation of the Ampere series,
 // done here with warp specialisation). The running max is exact (FA2's
-// online softmax): the largest weight of every row is exactly 1 in 16 bits,
-// and O and l are rescaled whenever a row's max grows; a warp skips the O
-// rescale when none of its 32 rows needs it.
+// online softmax): the largest weight of every row is exactly 1 in 16 bits;
+// O and l are rescaled whenever a row's max grows.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <utility>
 
 #include "fa2.h"
 #include "ptx_sm103.cuh"
@@ -41,10 +48,14 @@ namespace fa2 {
 
 constexpr int kBM = 128;           // query rows per tile (= TMEM lanes)
 constexpr int kBN = 128;           // keys per K/V tile
-constexpr int kNQ = 2;             // query tiles per CTA
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kNQ = 2;             // query tiles per work item
+constexpr int kThreads = 512;
+constexpr int kCorrWarp0 = 8;      // warps 8..11
+constexpr int kLoadWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr uint32_t kRegSoftmax = 176;  // 2 x 176 + 104 + 56 = 512 = 65536 / 128
+constexpr uint32_t kRegCorr = 104;
+constexpr uint32_t kRegOther = 56;
 
 // Where a watchdog gave up (bits 8..15 of the status word).
 enum WaitSite : int {
@@ -55,6 +66,9 @@ enum WaitSite : int {
     kSitePFull = 5,
     kSiteOFull = 6,
     kSiteDrain = 7,
+    kSiteQEmpty = 8,
+    kSiteAlpha = 9,
+    kSiteStats = 10,
 };
 
 struct Params {
@@ -63,6 +77,8 @@ struct Params {
     long long wait_limit_ns;
     int n_kv_tiles;      // N / 128
     int q_tiles;         // (Hq / Hkv) * N / 128: packed query tiles per KV head
+    int pairs;           // ceil(q_tiles / 2): work items per KV head
+    int total_items;     // pairs * B * Hkv
     int kv_rows;         // N
     int debug_flags;
     float scale_log2;    // scale * log2(e)
@@ -76,9 +92,12 @@ struct Layout {
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = kNQ * kTileBytes;
     static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
-    // q_full[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] mma_done
-    static constexpr int kNumBars = 2 + 2 * kStages + 7;
-    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    // q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] alpha[2] stats[2]
+    // p_full[2] o_full[2] mma_done
+    static constexpr int kNumBars = 2 * kStages + 15;
+    static constexpr int kRowOff = kBarOff + kNumBars * 8;   // per-row floats
+    // alpha[2][128], m[2][128], l[2][128]
+    static constexpr int kMiscOff = kRowOff + 3 * kNQ * kBM * 4;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + 1024-byte alignment slack
     // TMEM columns: S_0 | S_1 | O_0 | O_1
     static __device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
@@ -127,140 +146,193 @@ struct Waiter {
 template <int D>
 struct Bars {
     uint32_t base;
+    static constexpr int S = Layout<D>::kStages;
     __device__ uint32_t q_full(int t) const { return base + 8 * t; }
-    __device__ uint32_t kv_full(int s) const { return base + 8 * (2 + s); }
-    __device__ uint32_t kv_empty(int s) const { return base + 8 * (2 + Layout<D>::kStages + s); }
-    __device__ uint32_t s_full(int t) const { return base + 8 * (2 + 2 * Layout<D>::kStages + t); }
-    __device__ uint32_t p_full(int t) const { return base + 8 * (4 + 2 * Layout<D>::kStages + t); }
-    __device__ uint32_t o_full(int t) const { return base + 8 * (6 + 2 * Layout<D>::kStages + t); }
-    __device__ uint32_t mma_done() const { return base + 8 * (8 + 2 * Layout<D>::kStages); }
+    __device__ uint32_t q_empty(int t) const { return base + 8 * (2 + t); }
+    __device__ uint32_t kv_full(int s) const { return base + 8 * (4 + s); }
+    __device__ uint32_t kv_empty(int s) const { return base + 8 * (4 + S + s); }
+    __device__ uint32_t s_full(int t) const { return base + 8 * (4 + 2 * S + t); }
+    __device__ uint32_t alpha_ready(int t) const { return base + 8 * (6 + 2 * S + t); }
+    __device__ uint32_t stats_ready(int t) const { return base + 8 * (8 + 2 * S + t); }
+    __device__ uint32_t p_full(int t) const { return base + 8 * (10 + 2 * S + t); }
+    __device__ uint32_t o_full(int t) const { return base + 8 * (12 + 2 * S + t); }
+    __device__ uint32_t mma_done() const { return base + 8 * (14 + 2 * S); }
 };
+
+// One work item: two packed query tiles of one KV head.
+struct Item {
+    int n_tiles;   // 1 or 2
+    int q_row0;    // first query row of tile 0 in the [rows_q, D] view
+    int kv_row0;   // first K/V row of the KV head
+};
+
+__device__ __forceinline__ Item make_item(const Params& p, int item) {
+    const int group = item / p.pairs;
+    const int qt0 = kNQ * (item - group * p.pairs);
+    return Item{min(kNQ, p.q_tiles - qt0), (group * p.q_tiles + qt0) * kBM, group * p.kv_rows};
+}
 
 // ---------------------------------------------------------------- producer
 
 template <int D>
 __device__ __forceinline__ void producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
-                         const Params& p, uint32_t sbase, const Bars<D>& bars, const Waiter& w,
-                         int n_tiles, int q_row0, int kv_row0) {
+                                         const Params& p, uint32_t sbase, const Bars<D>& bars, const Waiter& w) {
     using L = Layout<D>;
     constexpr int S = L::kStages;
     const bool load_q = (p.debug_flags & 1) == 0;
-    if (load_q) {
-        for (int t = 0; t < n_tiles; ++t) {
-            const uint32_t dst = sbase + L::kQOff + t * L::kTileBytes;
-            ptx::mbar_arrive_expect_tx(bars.q_full(t), L::kTileBytes);
+    int ring = 0;           // K/V ring items issued
+    int nq[2] = {0, 0};     // Q loads issued per tile slot
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+        const Item item = make_item(p, it);
+        for (int t = 0; t < item.n_tiles && ok; ++t) {
+            if (!(ok = w.wait(bars.q_empty(t), (nq[t] & 1) ^ 1, kSiteQEmpty))) break;
+            if (load_q) {
+                const uint32_t dst = sbase + L::kQOff + t * L::kTileBytes;
+                ptx::mbar_arrive_expect_tx(bars.q_full(t), L::kTileBytes);
+#pragma unroll
+                for (int blk = 0; blk < D / 64; ++blk)
+                    ptx::tma_load_2d(dst + blk * L::kBlkBytes, tmQ, blk * 64, item.q_row0 + t * kBM,
+                                     bars.q_full(t));
+            }
+            ++nq[t];
+        }
+        // Warm L2 with the query tiles this CTA takes next.
+        const int nxt = it + gridDim.x;
+        if (ok && nxt < p.total_items) {
+            const Item ni = make_item(p, nxt);
+            for (int t = 0; t < ni.n_tiles; ++t)
+#pragma unroll
+                for (int blk = 0; blk < D / 64; ++blk)
+                    ptx::tma_prefetch_l2_2d(tmQ, blk * 64, ni.q_row0 + t * kBM);
+        }
+        for (int k = 0; k < 2 * p.n_kv_tiles && ok; ++k) {
+            const int s = ring % S;
+            if (!(ok = w.wait(bars.kv_empty(s), ((ring / S) & 1) ^ 1, kSiteKvEmpty))) break;
+            const uint32_t dst = sbase + L::kRingOff + s * L::kTileBytes;
+            const CUtensorMap* tm = (k & 1) ? tmV : tmK;
+            const int row = item.kv_row0 + (k >> 1) * kBN;
+            ptx::mbar_arrive_expect_tx(bars.kv_full(s), L::kTileBytes);
 #pragma unroll
             for (int blk = 0; blk < D / 64; ++blk)
-                ptx::tma_load_2d(dst + blk * L::kBlkBytes, tmQ, blk * 64, q_row0 + t * kBM,
-                                 bars.q_full(t));
+                ptx::tma_load_2d(dst + blk * L::kBlkBytes, tm, blk * 64, row, bars.kv_full(s));
+            ++ring;
         }
     }
-    const int n_items = 2 * p.n_kv_tiles;  // K_0, V_0, K_1, V_1, ...
-    int issued = 0;
-    for (int item = 0; item < n_items; ++item) {
-        const int s = item % S;
-        const uint32_t ph = (item / S) & 1;
-        if (!w.wait(bars.kv_empty(s), ph ^ 1, kSiteKvEmpty)) break;
-        const uint32_t dst = sbase + L::kRingOff + s * L::kTileBytes;
-        const CUtensorMap* tm = (item & 1) ? tmV : tmK;
-        const int row = kv_row0 + (item >> 1) * kBN;
-        ptx::mbar_arrive_expect_tx(bars.kv_full(s), L::kTileBytes);
-#pragma unroll
-        for (int blk = 0; blk < D / 64; ++blk)
-            ptx::tma_load_2d(dst + blk * L::kBlkBytes, tm, blk * 64, row, bars.kv_full(s));
-        ++issued;
-    }
-    if (issued < n_items || *w.abort_flag) {
+    if (!ok) {
         // Aborting: let every copy this CTA started land before it exits.
-        const int first = issued > S ? issued - S : 0;
-        for (int item = first; item < issued; ++item)
-            w.drain(bars.kv_full(item % S), (item / S) & 1);
+        const int first = ring > S ? ring - S : 0;
+        for (int r = first; r < ring; ++r) w.drain(bars.kv_full(r % S), (r / S) & 1);
         if (load_q)
-            for (int t = 0; t < n_tiles; ++t) w.drain(bars.q_full(t), 0);
+            for (int t = 0; t < 2; ++t)
+                if (nq[t] > 0) w.drain(bars.q_full(t), (nq[t] - 1) & 1);
     }
 }
 
 // ---------------------------------------------------------------- MMA issuer
 
+// S = Q K^T over d in steps of K = 16: both operands K-major, 128-byte
+// swizzle; step kk reads 64-column block kk/4 at byte offset 32*(kk%4).
+template <int D, int KK>
+__device__ __forceinline__ void qk_step(uint32_t dst, uint64_t qd, uint64_t kd, uint32_t idesc) {
+    constexpr uint32_t off = ((KK / 4) * Layout<D>::kBlkBytes + (KK % 4) * 32) >> 4;
+    ptx::mma_ss_off<off, off>(dst, qd, kd, idesc, KK > 0 ? 1u : 0u);
+}
+
+template <int D, int... KK>
+__device__ __forceinline__ void qk_steps(uint32_t dst, uint64_t qd, uint64_t kd, uint32_t idesc,
+                                         std::integer_sequence<int, KK...>) {
+    (qk_step<D, KK>(dst, qd, kd, idesc), ...);
+}
+
+// O (+)= P V over the 128 keys of a tile in steps of K = 16: P from TMEM
+// (8 columns of packed pairs per step), V MN-major (16 rows of 128 B).
+template <int KK>
+__device__ __forceinline__ void pv_step(uint32_t dst, uint32_t pa, uint64_t vd, uint32_t idesc, uint32_t acc) {
+    constexpr uint32_t voff = (KK * 16 * 128) >> 4;
+    ptx::mma_ts_off<KK * 8, voff>(dst, pa, vd, idesc, KK > 0 ? 1u : acc);
+}
+
+template <int... KK>
+__device__ __forceinline__ void pv_steps(uint32_t dst, uint32_t pa, uint64_t vd, uint32_t idesc, uint32_t acc,
+                                         std::integer_sequence<int, KK...>) {
+    (pv_step<KK>(dst, pa, vd, idesc, acc), ...);
+}
+
 template <int D, bool kBf16>
 __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint32_t tmem, const Bars<D>& bars,
-                           const Waiter& w, int n_tiles) {
+                                           const Waiter& w) {
     using L = Layout<D>;
     constexpr int S = L::kStages;
     constexpr uint32_t kAB = kBf16 ? 1u : 0u;
     constexpr uint32_t kIdS = ptx::idesc_f16(kAB, 0, 0, kBM, kBN);  // S = Q K^T, both K-major
     constexpr uint32_t kIdO = ptx::idesc_f16(kAB, 0, 1, kBM, D);    // O += P V, V MN-major
 
-    auto stage_addr = [&](int item) { return sbase + L::kRingOff + (item % S) * L::kTileBytes; };
+    auto stage_addr = [&](int r) { return sbase + L::kRingOff + (r % S) * L::kTileBytes; };
+    // A descriptor's start-address field is addr >> 4 in its low 14 bits;
+    // every tile lies below 256 KB, so base + (offset >> 4) never carries out.
     auto issue_qk = [&](int t, uint32_t kaddr) {
-        const uint32_t qaddr = sbase + L::kQOff + t * L::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * L::kBlkBytes + (kk % 4) * 32;
-            ptx::mma_ss(tmem + L::col_s(t), ptx::desc_sw128(qaddr + off, 16, 1024),
-                        ptx::desc_sw128(kaddr + off, 16, 1024), kIdS, kk > 0);
-        }
+        const uint64_t qd = ptx::desc_sw128(sbase + L::kQOff + t * L::kTileBytes, 16, 1024);
+        const uint64_t kd = ptx::desc_sw128(kaddr, 16, 1024);
+        qk_steps<D>(tmem + L::col_s(t), qd, kd, kIdS, std::make_integer_sequence<int, D / 16>{});
     };
     auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-            ptx::mma_ts(tmem + L::col_o(t), tmem + L::col_s(t) + kk * 8,
-                        ptx::desc_sw128(vaddr + kk * 16 * 128, L::kBlkBytes, 1024), kIdO,
-                        (acc || kk > 0) ? 1u : 0u);
-        }
+        const uint64_t vd = ptx::desc_sw128(vaddr, L::kBlkBytes, 1024);
+        pv_steps(tmem + L::col_o(t), tmem + L::col_s(t), vd, kIdO, acc ? 1u : 0u,
+                 std::make_integer_sequence<int, kBN / 16>{});
     };
+    auto wait_ring = [&](int r) { return w.wait(bars.kv_full(r % S), (r / S) & 1, kSiteKvFull); };
 
-    bool ok = true;
-    for (int t = 0; t < n_tiles && ok; ++t) ok = w.wait(bars.q_full(t), 0, kSiteQFull);
-    if (ok) ok = w.wait(bars.kv_full(0), 0, kSiteKvFull);  // K_0 is ring item 0
-    if (ok) {
-        ptx::tc_fence_after();
-        issue_qk(0, stage_addr(0));
-        ptx::tc_commit(bars.s_full(0));
-        if (n_tiles > 1) {
-            issue_qk(1, stage_addr(0));
-            ptx::tc_commit(bars.s_full(1));
-        }
-        ptx::tc_commit(bars.kv_empty(0));
-    }
     const int nkv = p.n_kv_tiles;
-    for (int j = 0; j < nkv && ok; ++j) {
-        const int v_item = 2 * j + 1, k_item = 2 * j + 2;
-        const bool more = j + 1 < nkv;
-        if (!(ok = w.wait(bars.kv_full(v_item % S), (v_item / S) & 1, kSiteKvFull))) break;
-        if (!(ok = w.wait(bars.p_full(0), j & 1, kSitePFull))) break;
+    int ring = 0;                 // K/V ring items consumed
+    int nq[2] = {0, 0};           // items seen per tile slot (q_full phases)
+    int np[2] = {0, 0};           // P tiles consumed per tile slot (p_full phases)
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+        const int nt = make_item(p, it).n_tiles;
+        for (int t = 0; t < nt && ok; ++t) ok = w.wait(bars.q_full(t), nq[t] & 1, kSiteQFull);
+        if (!ok || !(ok = wait_ring(ring))) break;
         ptx::tc_fence_after();
-        issue_pv(0, stage_addr(v_item), j > 0);
-        if (n_tiles == 1) ptx::tc_commit(bars.kv_empty(v_item % S));
-        if (more) {
-            if (!(ok = w.wait(bars.kv_full(k_item % S), (k_item / S) & 1, kSiteKvFull))) break;
-            ptx::tc_fence_after();
-            issue_qk(0, stage_addr(k_item));
-            ptx::tc_commit(bars.s_full(0));
-            if (n_tiles == 1) ptx::tc_commit(bars.kv_empty(k_item % S));
-        } else {
-            ptx::tc_commit(bars.o_full(0));
+        for (int t = 0; t < nt; ++t) {
+            issue_qk(t, stage_addr(ring));
+            ptx::tc_commit(bars.s_full(t));
+            if (nkv == 1) ptx::tc_commit(bars.q_empty(t));
         }
-        if (n_tiles > 1) {
-            if (!(ok = w.wait(bars.p_full(1), j & 1, kSitePFull))) break;
-            ptx::tc_fence_after();
-            issue_pv(1, stage_addr(v_item), j > 0);
-            ptx::tc_commit(bars.kv_empty(v_item % S));
-            if (more) {
-                issue_qk(1, stage_addr(k_item));
-                ptx::tc_commit(bars.s_full(1));
-                ptx::tc_commit(bars.kv_empty(k_item % S));
-            } else {
-                ptx::tc_commit(bars.o_full(1));
+        ptx::tc_commit(bars.kv_empty(ring % S));
+        int k_ring = ring;
+        ++ring;
+        for (int j = 0; j < nkv; ++j) {
+            const bool more = j + 1 < nkv;
+            const int v_ring = ring++;
+            if (!(ok = wait_ring(v_ring))) break;
+            if (more) k_ring = ring++;
+            for (int t = 0; t < nt; ++t) {
+                if (!(ok = w.wait(bars.p_full(t), np[t] & 1, kSitePFull))) break;
+                ++np[t];
+                ptx::tc_fence_after();
+                issue_pv(t, stage_addr(v_ring), j > 0);
+                if (t == nt - 1) ptx::tc_commit(bars.kv_empty(v_ring % S));
+                if (more) {
+                    if (t == 0 && !(ok = wait_ring(k_ring))) break;
+                    ptx::tc_fence_after();
+                    issue_qk(t, stage_addr(k_ring));
+                    ptx::tc_commit(bars.s_full(t));
+                    if (j + 2 == nkv) ptx::tc_commit(bars.q_empty(t));
+                    if (t == nt - 1) ptx::tc_commit(bars.kv_empty(k_ring % S));
+                } else {
+                    ptx::tc_commit(bars.o_full(t));
+                }
             }
+            if (!ok) break;
         }
+        for (int t = 0; t < nt; ++t) ++nq[t];
     }
     // Every MMA issued above must finish before the CTA frees its TMEM.
     ptx::tc_commit(bars.mma_done());
     w.drain(bars.mma_done(), 0);
 }
 
-// ---------------------------------------------------------------- softmax + epilogue
+// ---------------------------------------------------------------- softmax
 
 // 32-column TMEM load/store into slice [off, off+32) of a register array;
 // `off` is a compile-time constant after unrolling.
@@ -281,132 +353,184 @@ __device__ __forceinline__ void st_slice(uint32_t taddr, const uint32_t (&r)[N],
 }
 
 template <int D, bool kBf16>
-__device__ __forceinline__ void softmax_tile(const Params& p, uint32_t tmem, const Bars<D>& bars, const Waiter& w,
-                             int t, int q_row0) {
+__device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uint8_t* smem, const Bars<D>& bars,
+                                             const Waiter& w, int t) {
     using L = Layout<D>;
-    const int wq = (threadIdx.x / 32) & 3;  // TMEM lane quarter of this warp
-    const int lane = threadIdx.x & 31;
-    const uint32_t row_addr = tmem + (static_cast<uint32_t>(32 * wq) << 16);
-    const uint32_t colS = L::col_s(t), colO = L::col_o(t);
+    const int row = threadIdx.x & 127;          // row within the query tile = TMEM lane
+    const uint32_t row_addr = tmem + (static_cast<uint32_t>(row & ~31) << 16);
+    const uint32_t colS = L::col_s(t);
+    float* alpha_buf = reinterpret_cast<float*>(smem + L::kRowOff) + t * kBM;
+    float* m_buf = alpha_buf + kNQ * kBM;
+    float* l_buf = m_buf + kNQ * kBM;
     const float c = p.scale_log2;
+    const uint64_t c2 = ptx::f2_pack(c, c);
 
-    float m = -INFINITY;  // running row max of the scaled scores, log2 units
-    float l = 0.0f;       // running sum of exp2(s*c - m)
+    int n_s = 0;       // S tiles consumed (s_full / alpha / p_full phases)
     bool ok = true;
-    for (int j = 0; j < p.n_kv_tiles; ++j) {
-        ok = w.wait(bars.s_full(t), j & 1, kSiteSFull);
-        if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
-        }
-        ptx::tc_fence_after();
-        uint32_t s[kBN];
-        ptx::tmem_ld32_at<0>(row_addr + colS + 0, s);
-        ptx::tmem_ld32_at<32>(row_addr + colS + 32, s);
-        ptx::tmem_ld32_at<64>(row_addr + colS + 64, s);
-        ptx::tmem_ld32_at<96>(row_addr + colS + 96, s);
-        ptx::tmem_wait_ld();
-
-        // Row max: eight independent chains of 3-input max, then combine.
-        float mx[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            float a = __uint_as_float(s[k]);
-#pragma unroll
-            for (int i = 1; i < 15; i += 2)
-                a = ptx::max3(a, __uint_as_float(s[k + 8 * i]), __uint_as_float(s[k + 8 * (i + 1)]));
-            mx[k] = fmaxf(a, __uint_as_float(s[k + 120]));
-        }
-        const float m_tile =
-            fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7]))) * c;
-        bool rescale = false;
-        float alpha = 1.0f;
-        if (j == 0) {
-            m = m_tile;
-        } else {
-            const bool need = m_tile > m;
-            rescale = __any_sync(0xffffffffu, need);
-            if (need) {
-                alpha = ptx::ex2_approx(m - m_tile);
-                l *= alpha;
-                m = m_tile;
+    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+        if (t >= make_item(p, it).n_tiles) continue;
+        float m = -INFINITY;  // running row max of the scaled scores, log2 units
+        float l = 0.0f;       // running sum of exp2(s*c - m)
+        for (int j = 0; j < p.n_kv_tiles; ++j, ++n_s) {
+            ok = w.wait(bars.s_full(t), n_s & 1, kSiteSFull);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
             }
-        }
-        // P = exp2(S*c - m) on pairs: one packed FMA, two MUFU ex2, one packed
-        // add into four partial row sums, one 16-bit pack.
-        const uint64_t c2 = ptx::f2_pack(c, c);
-        const uint64_t nm2 = ptx::f2_pack(-m, -m);
-        uint64_t acc[4] = {0, 0, 0, 0};
-        uint32_t pk[kBN / 2];
-#pragma unroll
-        for (int i = 0; i < kBN / 2; ++i) {
-            const uint64_t x = ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
-                                           c2, nm2);
-            float x0, x1;
-            ptx::f2_unpack(x, x0, x1);
-            const float p0 = ptx::ex2_approx(x0);
-            const float p1 = ptx::ex2_approx(x1);
-            acc[i & 3] = ptx::f2_add(acc[i & 3], ptx::f2_pack(p0, p1));
-            pk[i] = ptx::pack2<kBf16>(p0, p1);
-        }
-        {
-            float a0, a1, b0, b1;
-            ptx::f2_unpack(ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3])), a0, a1);
-            (void)b0;
-            (void)b1;
-            l += a0 + a1;
-        }
-        ptx::tmem_st32_at<0>(row_addr + colS, pk);
-        ptx::tmem_st32_at<32>(row_addr + colS + 32, pk);
-        if (rescale) {
-            // O += P V of the previous KV tile has completed (its commit
-            // precedes this tile's S), and the next one waits for p_full, so
-            // O can be rescaled in place here: load the whole row, one wait,
-            // packed multiplies, store.
-            uint32_t o[D];
-#pragma unroll
-            for (int cc = 0; cc < D; cc += 32) ld_slice(row_addr + colO + cc, o, cc);
+            ptx::tc_fence_after();
+            uint32_t s[kBN];
+            ptx::tmem_ld32_at<0>(row_addr + colS + 0, s);
+            ptx::tmem_ld32_at<32>(row_addr + colS + 32, s);
+            ptx::tmem_ld32_at<64>(row_addr + colS + 64, s);
+            ptx::tmem_ld32_at<96>(row_addr + colS + 96, s);
             ptx::tmem_wait_ld();
-            const uint64_t a2 = ptx::f2_pack(alpha, alpha);
-#pragma unroll
-            for (int i = 0; i < D / 2; ++i) {
-                float o0, o1;
-                ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2),
-                               o0, o1);
-                o[2 * i] = __float_as_uint(o0);
-                o[2 * i + 1] = __float_as_uint(o1);
-            }
-#pragma unroll
-            for (int cc = 0; cc < D; cc += 32) st_slice(row_addr + colO + cc, o, cc);
-        }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bars.p_full(t));
-    }
-    if (ok) ok = w.wait(bars.o_full(t), 0, kSiteOFull);
-    if (!__all_sync(0xffffffffu, ok)) return;
-    ptx::tc_fence_after();
 
-    // Epilogue: O / l rounded to 16 bits, one 2*D-byte row per thread, and
-    // LSE = (m + log2 l) * ln 2.
-    const int row = q_row0 + t * kBM + 32 * wq + lane;
-    const float inv_l = ptx::rcp_approx(l);
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + static_cast<size_t>(row) * D);
+            // Row max: eight independent chains of 3-input max, then combine.
+            float mx[8];
 #pragma unroll
-    for (int cc = 0; cc < D; cc += 32) {
-        uint32_t o[32];
-        ptx::tmem_ld32(row_addr + colO + cc, o);
-        ptx::tmem_wait_ld();
-        uint32_t h[16];
+            for (int k = 0; k < 8; ++k) {
+                float a = __uint_as_float(s[k]);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            h[i] = ptx::pack2<kBf16>(__uint_as_float(o[2 * i]) * inv_l,
-                                     __uint_as_float(o[2 * i + 1]) * inv_l);
+                for (int i = 1; i < 15; i += 2)
+                    a = ptx::max3(a, __uint_as_float(s[k + 8 * i]), __uint_as_float(s[k + 8 * (i + 1)]));
+                mx[k] = fmaxf(a, __uint_as_float(s[k + 120]));
+            }
+            const float m_tile =
+                fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7]))) * c;
+            // Hand the correction warpgroup this row's rescale factor
+            // (exactly 1 when the max does not move).
+            const float m_new = fmaxf(m, m_tile);
+            const float alpha = (j == 0 || m_new == m) ? 1.0f : ptx::ex2_approx(m - m_new);
+            alpha_buf[row] = alpha;
+            ptx::mbar_arrive(bars.alpha_ready(t));
+            l *= alpha;
+            m = m_new;
+
+            // P = exp2(S*c - m) on pairs: one packed FMA, two MUFU ex2, one
+            // packed add into four partial row sums, one 16-bit pack.
+            const uint64_t nm2 = ptx::f2_pack(-m, -m);
+            uint64_t acc[4] = {0, 0, 0, 0};
+            uint32_t pk[kBN / 2];
 #pragma unroll
-        for (int v = 0; v < 4; ++v)
-            dst[cc / 8 + v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+            for (int i = 0; i < kBN / 2; ++i) {
+                const uint64_t x =
+                    ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, nm2);
+                float x0, x1;
+                ptx::f2_unpack(x, x0, x1);
+                const float p0 = ptx::ex2_approx(x0);
+                const float p1 = ptx::ex2_approx(x1);
+                acc[i & 3] = ptx::f2_add(acc[i & 3], ptx::f2_pack(p0, p1));
+                pk[i] = ptx::pack2<kBf16>(p0, p1);
+            }
+            float a0, a1;
+            ptx::f2_unpack(ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3])), a0, a1);
+            l += a0 + a1;
+            ptx::tmem_st32_at<0>(row_addr + colS, pk);
+            ptx::tmem_st32_at<32>(row_addr + colS + 32, pk);
+            if (j + 1 == p.n_kv_tiles) {
+                m_buf[row] = m;
+                l_buf[row] = l;
+                ptx::mbar_arrive(bars.stats_ready(t));
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bars.p_full(t));
+        }
     }
-    p.lse[row] = (m + ptx::lg2_approx(l)) * 0.69314718055994530942f;
+}
+
+// ---------------------------------------------------------------- correction + epilogue
+
+template <int D, bool kBf16>
+__device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, uint8_t* smem, const Bars<D>& bars,
+                                                const Waiter& w) {
+    using L = Layout<D>;
+    constexpr int kChunk = 32;  // O is rescaled / stored 32 columns at a time
+    const int q = (threadIdx.x / 32) & 3;      // TMEM lane quarter
+    const int lane = threadIdx.x & 31;
+    const int row = 32 * q + lane;
+    const uint32_t row_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    const float* rowbuf = reinterpret_cast<const float*>(smem + L::kRowOff);  // alpha | m | l
+
+    int n_s[2] = {0, 0};
+    int n_items[2] = {0, 0};
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+        const Item item = make_item(p, it);
+        for (int j = 0; j < p.n_kv_tiles && ok; ++j) {
+            for (int t = 0; t < item.n_tiles; ++t) {
+                ok = w.wait(bars.alpha_ready(t), n_s[t] & 1, kSiteAlpha);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                ++n_s[t];
+                const float alpha = rowbuf[t * kBM + row];
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+                    // PV(t, j-1) has completed: the softmax saw S(t, j), whose
+                    // commit follows it; PV(t, j) waits for this warpgroup's
+                    // p_full arrival below.
+                    ptx::tc_fence_after();
+                    const uint32_t colO = L::col_o(t);
+                    const uint64_t a2 = ptx::f2_pack(alpha, alpha);
+#pragma unroll
+                    for (int h = 0; h < D; h += kChunk) {
+                        uint32_t o[kChunk];
+                        ptx::tmem_ld32_at<0>(row_addr + colO + h, o);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < kChunk / 2; ++i) {
+                            float o0, o1;
+                            ptx::f2_unpack(
+                                ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
+                                            a2),
+                                o0, o1);
+                            o[2 * i] = __float_as_uint(o0);
+                            o[2 * i + 1] = __float_as_uint(o1);
+                        }
+                        ptx::tmem_st32_at<0>(row_addr + colO + h, o);
+                    }
+                    ptx::tmem_wait_st();
+                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bars.p_full(t));
+            }
+        }
+        // Epilogue for each tile of the item: O / l -> 16 bit, LSE. The next
+        // item's first PV overwrites O only after this warpgroup's next
+        // p_full arrival, which comes after these loads.
+        for (int t = 0; t < item.n_tiles && ok; ++t) {
+            ok = w.wait(bars.stats_ready(t), n_items[t] & 1, kSiteStats);
+            if (ok) ok = w.wait(bars.o_full(t), n_items[t] & 1, kSiteOFull);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            ++n_items[t];
+            ptx::tc_fence_after();
+            const float m = rowbuf[(2 + t) * kBM + row];
+            const float l = rowbuf[(4 + t) * kBM + row];
+            const int grow = item.q_row0 + t * kBM + row;
+            const float inv_l = ptx::rcp_approx(l);
+            const uint32_t colO = L::col_o(t);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + static_cast<size_t>(grow) * D);
+#pragma unroll
+            for (int h = 0; h < D; h += kChunk) {
+                uint32_t o[kChunk];
+                ptx::tmem_ld32_at<0>(row_addr + colO + h, o);
+                ptx::tmem_wait_ld();
+                uint32_t hv[kChunk / 2];
+#pragma unroll
+                for (int i = 0; i < kChunk / 2; ++i)
+                    hv[i] = ptx::pack2<kBf16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+#pragma unroll
+                for (int v = 0; v < kChunk / 8; ++v)
+                    dst[h / 8 + v] = make_uint4(hv[4 * v], hv[4 * v + 1], hv[4 * v + 2], hv[4 * v + 3]);
+            }
+            p.lse[grow] = (m + ptx::lg2_approx(l)) * 0.69314718055994530942f;
+        }
+        ptx::tc_fence_before();
+    }
 }
 
 // ---------------------------------------------------------------- kernel
@@ -426,17 +550,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
-    const int group = blockIdx.y;  // b * Hkv + kv head
-    const int qt0 = kNQ * blockIdx.x;
-    const int n_tiles = min(kNQ, p.q_tiles - qt0);
-    const int q_row0 = (group * p.q_tiles + qt0) * kBM;
-    const int kv_row0 = group * p.kv_rows;
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(bars.q_full(t), 1);
+            ptx::mbar_init(bars.q_empty(t), 1);
             ptx::mbar_init(bars.s_full(t), 1);
-            ptx::mbar_init(bars.p_full(t), kBM);
+            ptx::mbar_init(bars.alpha_ready(t), kBM);
+            ptx::mbar_init(bars.stats_ready(t), kBM);
+            ptx::mbar_init(bars.p_full(t), 2 * kBM);  // softmax + correction warpgroups
             ptx::mbar_init(bars.o_full(t), 1);
         }
         for (int s = 0; s < L::kStages; ++s) {
@@ -462,14 +584,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const Waiter w{abort_flag, p.wait_limit_ns};
 
-    if (warp == kLoadWarp) {
-        if (lane == 0) producer<D>(&tmQ, &tmK, &tmV, p, sbase, bars, w, n_tiles, q_row0, kv_row0);
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) mma_issuer<D, kBf16>(p, sbase, tmem, bars, w, n_tiles);
-        __syncwarp();
+    if (warp < kCorrWarp0) {
+        ptx::setmaxnreg_inc<kRegSoftmax>();
+        softmax_role<D, kBf16>(p, tmem, smem, bars, w, warp / 4);
+    } else if (warp < kLoadWarp) {
+        ptx::setmaxnreg_dec<kRegCorr>();
+        correction_role<D, kBf16>(p, tmem, smem, bars, w);
     } else {
-        const int t = warp / 4;
-        if (t < n_tiles) softmax_tile<D, kBf16>(p, tmem, bars, w, t, q_row0);
+        ptx::setmaxnreg_dec<kRegOther>();
+        if (warp == kLoadWarp) {
+            if (lane == 0) producer<D>(&tmQ, &tmK, &tmV, p, sbase, bars, w);
+            __syncwarp();
+        } else if (warp == kMmaWarp) {
+            if (lane == 0) mma_issuer<D, kBf16>(p, sbase, tmem, bars, w);
+            __syncwarp();
+        }
     }
 
     ptx::tc_fence_before();
@@ -498,6 +627,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
     bool probed = false;
     bool supported = false;
+    int sm_count = 0;
     bool smem_set[4] = {false, false, false, false};
 };
 DeviceState g_dev[kMaxDevices];
@@ -521,12 +651,14 @@ fa2_status check_device(int* dev_out) {
     if (dev < 0 || dev >= kMaxDevices) return FA2_ERR_UNSUPPORTED;
     DeviceState& st = g_dev[dev];
     if (!st.probed) {
-        int major = 0, minor = 0;
+        int major = 0, minor = 0, sms = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return FA2_ERR_CUDA;
         std::lock_guard<std::mutex> lk(g_mu);
         st.supported = (major == 10 && minor == 3);
+        st.sm_count = sms;
         st.probed = true;
     }
     *dev_out = dev;
@@ -579,10 +711,10 @@ fa2_status fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, flo
     if (dtype != FA2_BF16 && dtype != FA2_FP16) return FA2_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return FA2_ERR_UNSUPPORTED;
     if (N % fa2::kBM != 0) return FA2_ERR_UNSUPPORTED;
-    // TMA coordinates and row indices are 32-bit; the grid's y extent is 65535.
+    // TMA coordinates and row indices are 32-bit.
     const long long rows_q = static_cast<long long>(B) * H_q * N;
     const long long groups = static_cast<long long>(B) * H_kv;
-    if (rows_q > 0x7FFFFFFFLL || groups > 65535) return FA2_ERR_UNSUPPORTED;
+    if (rows_q > 0x7FFFFFFFLL) return FA2_ERR_UNSUPPORTED;
 
     int dev = 0;
     fa2_status st = check_device(&dev);
@@ -601,10 +733,13 @@ fa2_status fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, flo
     p.wait_limit_ns = g_wait_limit_ns.load();
     p.n_kv_tiles = N / fa2::kBN;
     p.q_tiles = (H_q / H_kv) * (N / fa2::kBM);
+    p.pairs = (p.q_tiles + fa2::kNQ - 1) / fa2::kNQ;
+    p.total_items = static_cast<int>(p.pairs * groups);
     p.kv_rows = N;
     p.debug_flags = g_debug_flags.load();
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
-    const dim3 grid((p.q_tiles + fa2::kNQ - 1) / fa2::kNQ, static_cast<unsigned>(groups));
+    // Persistent grid: one CTA per SM (shared memory and TMEM admit one).
+    const dim3 grid(static_cast<unsigned>(std::min<long long>(p.total_items, g_dev[dev].sm_count)));
 
     const bool bf = dtype == FA2_BF16;
     if (d == 128)

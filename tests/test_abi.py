@@ -66,7 +66,6 @@ A = 1 << 20  # a 16-byte aligned fake address: never dereferenced on these paths
     ((A, A, A, A, A, 1, 1, 1, 200, 128, 0.1, 0), fa2.FA2_ERR_UNSUPPORTED),   # N % 128
     ((A, A, A, A, A, 1, 1, 1, 64, 64, 0.1, 1), fa2.FA2_ERR_UNSUPPORTED),     # N < block
     ((A, A, A, A, A, 2048, 8, 8, 131072, 128, 0.1, 0), fa2.FA2_ERR_UNSUPPORTED),  # rows >= 2^31
-    ((A, A, A, A, A, 65536, 1, 1, 128, 64, 0.1, 0), fa2.FA2_ERR_UNSUPPORTED),  # grid y > 65535
 ])
 def test_host_validation(lib, args, expected):
     assert fa2.fa2_fwd_gqa_ptr(*args) == expected
