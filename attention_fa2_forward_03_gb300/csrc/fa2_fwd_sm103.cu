@@ -16,8 +16,9 @@
 //             epilogue (O / l -> 16 bit, LSE) for both tiles
 //   WG3       warp 12: TMA producer (Q tiles, then K_0, V_0, K_1, V_1, ...
 //             through a ring of 128-byte-swizzled shared-memory stages);
-//             warp 13: TMEM allocator and the one thread that issues every
-//             tcgen05.mma / tcgen05.commit; warps 14-15 idle
+//             warp 13: TMEM allocator and MMA issuer (the warp runs the loop
+//             converged; elect.sync picks the lane that issues each
+//             tcgen05.mma / tcgen05.commit); warps 14-15 idle
 // Registers are moved between warpgroups with setmaxnreg (softmax 176,
 // correction 104, producer/MMA 56 per thread).
 // TMEM (512 columns x 128 lanes, fp32): S_0 | S_1 | O_0 | O_1. The softmax
@@ -236,7 +237,7 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmQ, const CUtensorM
 template <int D, int KK>
 __device__ __forceinline__ void qk_step(uint32_t dst, uint64_t qd, uint64_t kd, uint32_t idesc) {
     constexpr uint32_t off = ((KK / 4) * Layout<D>::kBlkBytes + (KK % 4) * 32) >> 4;
-    ptx::mma_ss_off<off, off>(dst, qd, kd, idesc, KK > 0 ? 1u : 0u);
+    ptx::mma_ss_off_elect<off, off>(dst, qd, kd, idesc, KK > 0 ? 1u : 0u);
 }
 
 template <int D, int... KK>
@@ -250,7 +251,7 @@ __device__ __forceinline__ void qk_steps(uint32_t dst, uint64_t qd, uint64_t kd,
 template <int KK>
 __device__ __forceinline__ void pv_step(uint32_t dst, uint32_t pa, uint64_t vd, uint32_t idesc, uint32_t acc) {
     constexpr uint32_t voff = (KK * 16 * 128) >> 4;
-    ptx::mma_ts_off<KK * 8, voff>(dst, pa, vd, idesc, KK > 0 ? 1u : acc);
+    ptx::mma_ts_off_elect<KK * 8, voff>(dst, pa, vd, idesc, KK > 0 ? 1u : acc);
 }
 
 template <int... KK>
@@ -281,7 +282,11 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint
         pv_steps(tmem + L::col_o(t), tmem + L::col_s(t), vd, kIdO, acc ? 1u : 0u,
                  std::make_integer_sequence<int, kBN / 16>{});
     };
-    auto wait_ring = [&](int r) { return w.wait(bars.kv_full(r % S), (r / S) & 1, kSiteKvFull); };
+    // Every lane of the warp waits; the result is made warp-uniform.
+    auto wait_u = [&](uint32_t bar, uint32_t parity, int site) {
+        return __shfl_sync(0xffffffffu, w.wait(bar, parity, site) ? 1 : 0, 0) != 0;
+    };
+    auto wait_ring = [&](int r) { return wait_u(bars.kv_full(r % S), (r / S) & 1, kSiteKvFull); };
 
     const int nkv = p.n_kv_tiles;
     int ring = 0;                 // K/V ring items consumed
@@ -290,15 +295,15 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint
     bool ok = true;
     for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
         const int nt = make_item(p, it).n_tiles;
-        for (int t = 0; t < nt && ok; ++t) ok = w.wait(bars.q_full(t), nq[t] & 1, kSiteQFull);
+        for (int t = 0; t < nt && ok; ++t) ok = wait_u(bars.q_full(t), nq[t] & 1, kSiteQFull);
         if (!ok || !(ok = wait_ring(ring))) break;
         ptx::tc_fence_after();
         for (int t = 0; t < nt; ++t) {
             issue_qk(t, stage_addr(ring));
-            ptx::tc_commit(bars.s_full(t));
-            if (nkv == 1) ptx::tc_commit(bars.q_empty(t));
+            ptx::tc_commit_elect(bars.s_full(t));
+            if (nkv == 1) ptx::tc_commit_elect(bars.q_empty(t));
         }
-        ptx::tc_commit(bars.kv_empty(ring % S));
+        ptx::tc_commit_elect(bars.kv_empty(ring % S));
         int k_ring = ring;
         ++ring;
         for (int j = 0; j < nkv; ++j) {
@@ -307,20 +312,20 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint
             if (!(ok = wait_ring(v_ring))) break;
             if (more) k_ring = ring++;
             for (int t = 0; t < nt; ++t) {
-                if (!(ok = w.wait(bars.p_full(t), np[t] & 1, kSitePFull))) break;
+                if (!(ok = wait_u(bars.p_full(t), np[t] & 1, kSitePFull))) break;
                 ++np[t];
                 ptx::tc_fence_after();
                 issue_pv(t, stage_addr(v_ring), j > 0);
-                if (t == nt - 1) ptx::tc_commit(bars.kv_empty(v_ring % S));
+                if (t == nt - 1) ptx::tc_commit_elect(bars.kv_empty(v_ring % S));
                 if (more) {
                     if (t == 0 && !(ok = wait_ring(k_ring))) break;
                     ptx::tc_fence_after();
                     issue_qk(t, stage_addr(k_ring));
-                    ptx::tc_commit(bars.s_full(t));
-                    if (j + 2 == nkv) ptx::tc_commit(bars.q_empty(t));
-                    if (t == nt - 1) ptx::tc_commit(bars.kv_empty(k_ring % S));
+                    ptx::tc_commit_elect(bars.s_full(t));
+                    if (j + 2 == nkv) ptx::tc_commit_elect(bars.q_empty(t));
+                    if (t == nt - 1) ptx::tc_commit_elect(bars.kv_empty(k_ring % S));
                 } else {
-                    ptx::tc_commit(bars.o_full(t));
+                    ptx::tc_commit_elect(bars.o_full(t));
                 }
             }
             if (!ok) break;
@@ -328,8 +333,9 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint
         for (int t = 0; t < nt; ++t) ++nq[t];
     }
     // Every MMA issued above must finish before the CTA frees its TMEM.
-    ptx::tc_commit(bars.mma_done());
+    ptx::tc_commit_elect(bars.mma_done());
     w.drain(bars.mma_done(), 0);
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------- softmax
@@ -596,8 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) producer<D>(&tmQ, &tmK, &tmV, p, sbase, bars, w);
             __syncwarp();
         } else if (warp == kMmaWarp) {
-            if (lane == 0) mma_issuer<D, kBf16>(p, sbase, tmem, bars, w);
-            __syncwarp();
+            mma_issuer<D, kBf16>(p, sbase, tmem, bars, w);  // whole warp, one lane issues
         }
     }
 

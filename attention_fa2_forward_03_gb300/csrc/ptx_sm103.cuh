@@ -187,6 +187,46 @@ __device__ __forceinline__ void mma_ts_off(uint32_t d_tmem, uint32_t a_tmem, uin
         : "memory");
 }
 
+// Warp-collective forms: the whole (converged) warp executes the sequence,
+// elect.sync picks one lane, and only that lane issues the MMA / commit. Keeping
+// the warp converged lets the operands stay warp-uniform, so issuing costs a
+// few cycles instead of a per-instruction move into uniform registers.
+template <uint32_t AOFF, uint32_t BOFF>
+__device__ __forceinline__ void mma_ss_off_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 a, b;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "add.s64 a, %1, %5;\n\t"
+        "add.s64 b, %2, %6;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "n"(AOFF), "n"(BOFF)
+        : "memory");
+}
+
+template <uint32_t AOFF, uint32_t BOFF>
+__device__ __forceinline__ void mma_ts_off_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "add.s32 a, %1, %5;\n\t"
+        "add.s64 b, %2, %6;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "n"(AOFF), "n"(BOFF)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
