@@ -233,31 +233,22 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmQ, const CUtensorM
 // ---------------------------------------------------------------- MMA issuer
 
 // S = Q K^T over d in steps of K = 16: both operands K-major, 128-byte
-// swizzle; step kk reads 64-column block kk/4 at byte offset 32*(kk%4).
-template <int D, int KK>
-__device__ __forceinline__ void qk_step(uint32_t dst, uint64_t qd, uint64_t kd, uint32_t idesc) {
-    constexpr uint32_t off = ((KK / 4) * Layout<D>::kBlkBytes + (KK % 4) * 32) >> 4;
-    ptx::mma_ss_off_elect<off, off>(dst, qd, kd, idesc, KK > 0 ? 1u : 0u);
-}
-
-template <int D, int... KK>
-__device__ __forceinline__ void qk_steps(uint32_t dst, uint64_t qd, uint64_t kd, uint32_t idesc,
-                                         std::integer_sequence<int, KK...>) {
-    (qk_step<D, KK>(dst, qd, kd, idesc), ...);
+// swizzle; step kk reads 64-column block kk/4 at byte offset 32*(kk%4)
+// (offsets below in 16-byte units).
+template <int D>
+__device__ __forceinline__ void qk_kloop(uint32_t dst, uint64_t qd, uint64_t kd, uint32_t idesc) {
+    constexpr uint32_t kBlk = Layout<D>::kBlkBytes >> 4;
+    if constexpr (D == 128)
+        ptx::mma_ss_kloop<2, 4, 6, kBlk, kBlk + 2, kBlk + 4, kBlk + 6, 2, 4, 6, kBlk, kBlk + 2, kBlk + 4, kBlk + 6, 8>(
+            dst, qd, kd, idesc, 0u);
+    else
+        ptx::mma_ss_kloop<2, 4, 6, 0, 0, 0, 0, 2, 4, 6, 0, 0, 0, 0, 4>(dst, qd, kd, idesc, 0u);
 }
 
 // O (+)= P V over the 128 keys of a tile in steps of K = 16: P from TMEM
 // (8 columns of packed pairs per step), V MN-major (16 rows of 128 B).
-template <int KK>
-__device__ __forceinline__ void pv_step(uint32_t dst, uint32_t pa, uint64_t vd, uint32_t idesc, uint32_t acc) {
-    constexpr uint32_t voff = (KK * 16 * 128) >> 4;
-    ptx::mma_ts_off_elect<KK * 8, voff>(dst, pa, vd, idesc, KK > 0 ? 1u : acc);
-}
-
-template <int... KK>
-__device__ __forceinline__ void pv_steps(uint32_t dst, uint32_t pa, uint64_t vd, uint32_t idesc, uint32_t acc,
-                                         std::integer_sequence<int, KK...>) {
-    (pv_step<KK>(dst, pa, vd, idesc, acc), ...);
+__device__ __forceinline__ void pv_kloop(uint32_t dst, uint32_t pa, uint64_t vd, uint32_t idesc, uint32_t acc) {
+    ptx::mma_ts_kloop8(dst, pa, vd, idesc, acc);
 }
 
 template <int D, bool kBf16>
@@ -275,12 +266,11 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint
     auto issue_qk = [&](int t, uint32_t kaddr) {
         const uint64_t qd = ptx::desc_sw128(sbase + L::kQOff + t * L::kTileBytes, 16, 1024);
         const uint64_t kd = ptx::desc_sw128(kaddr, 16, 1024);
-        qk_steps<D>(tmem + L::col_s(t), qd, kd, kIdS, std::make_integer_sequence<int, D / 16>{});
+        qk_kloop<D>(tmem + L::col_s(t), qd, kd, kIdS);
     };
     auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
         const uint64_t vd = ptx::desc_sw128(vaddr, L::kBlkBytes, 1024);
-        pv_steps(tmem + L::col_o(t), tmem + L::col_s(t), vd, kIdO, acc ? 1u : 0u,
-                 std::make_integer_sequence<int, kBN / 16>{});
+        pv_kloop(tmem + L::col_o(t), tmem + L::col_s(t), vd, kIdO, acc ? 1u : 0u);
     };
     // Every lane of the warp waits; the result is made warp-uniform.
     auto wait_u = [&](uint32_t bar, uint32_t parity, int site) {
@@ -310,7 +300,12 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint
             const bool more = j + 1 < nkv;
             const int v_ring = ring++;
             if (!(ok = wait_ring(v_ring))) break;
-            if (more) k_ring = ring++;
+            // K_{j+1} is waited for here, before P, so nothing but the MMAs
+            // sits between P becoming ready and the next QK being issued.
+            if (more) {
+                k_ring = ring++;
+                if (!(ok = wait_ring(k_ring))) break;
+            }
             for (int t = 0; t < nt; ++t) {
                 if (!(ok = wait_u(bars.p_full(t), np[t] & 1, kSitePFull))) break;
                 ++np[t];
@@ -318,8 +313,6 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint
                 issue_pv(t, stage_addr(v_ring), j > 0);
                 if (t == nt - 1) ptx::tc_commit_elect(bars.kv_empty(v_ring % S));
                 if (more) {
-                    if (t == 0 && !(ok = wait_ring(k_ring))) break;
-                    ptx::tc_fence_after();
                     issue_qk(t, stage_addr(k_ring));
                     ptx::tc_commit_elect(bars.s_full(t));
                     if (j + 2 == nkv) ptx::tc_commit_elect(bars.q_empty(t));

@@ -219,6 +219,95 @@ __device__ __forceinline__ void mma_ts_off_elect(uint32_t d_tmem, uint32_t a_tme
         : "memory");
 }
 
+
+// A whole K-loop of one GEMM (4 or 8 MMAs of K = 16) in one sequence: one
+// elect.sync, the accumulate predicates set once, and each step's descriptor
+// offsets (16-byte units, compile-time immediates) added to the low words of
+// the base descriptors. The start-address field occupies the low 14 bits and
+// every address stays below 256 KB, so the low-word add never carries.
+// Step 0 accumulates iff `acc`; later steps always accumulate.
+template <uint32_t A1, uint32_t A2, uint32_t A3, uint32_t A4, uint32_t A5, uint32_t A6, uint32_t A7,
+          uint32_t B1, uint32_t B2, uint32_t B3, uint32_t B4, uint32_t B5, uint32_t B6, uint32_t B7, int NSTEP>
+__device__ __forceinline__ void mma_ss_kloop(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t acc) {
+    static_assert(NSTEP == 4 || NSTEP == 8, "4 or 8 steps");
+    if constexpr (NSTEP == 8) {
+        asm volatile(
+            "{\n\t.reg .pred e, p0, pt;\n\t.reg .b32 alo, ahi, blo, bhi, t0, t1;\n\t.reg .b64 a, b;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "setp.ne.b32 p0, %4, 0;\n\t"
+            "setp.eq.b32 pt, %4, %4;\n\t"
+            "mov.b64 {alo, ahi}, %1;\n\t"
+            "mov.b64 {blo, bhi}, %2;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
+            "add.u32 t0, alo, %5;\n\tmov.b64 a, {t0, ahi};\n\tadd.u32 t1, blo, %12;\n\tmov.b64 b, {t1, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+            "add.u32 t0, alo, %6;\n\tmov.b64 a, {t0, ahi};\n\tadd.u32 t1, blo, %13;\n\tmov.b64 b, {t1, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+            "add.u32 t0, alo, %7;\n\tmov.b64 a, {t0, ahi};\n\tadd.u32 t1, blo, %14;\n\tmov.b64 b, {t1, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+            "add.u32 t0, alo, %8;\n\tmov.b64 a, {t0, ahi};\n\tadd.u32 t1, blo, %15;\n\tmov.b64 b, {t1, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+            "add.u32 t0, alo, %9;\n\tmov.b64 a, {t0, ahi};\n\tadd.u32 t1, blo, %16;\n\tmov.b64 b, {t1, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+            "add.u32 t0, alo, %10;\n\tmov.b64 a, {t0, ahi};\n\tadd.u32 t1, blo, %17;\n\tmov.b64 b, {t1, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+            "add.u32 t0, alo, %11;\n\tmov.b64 a, {t0, ahi};\n\tadd.u32 t1, blo, %18;\n\tmov.b64 b, {t1, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+            "}" ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc),
+            "n"(A1), "n"(A2), "n"(A3), "n"(A4), "n"(A5), "n"(A6), "n"(A7),
+            "n"(B1), "n"(B2), "n"(B3), "n"(B4), "n"(B5), "n"(B6), "n"(B7)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred e, p0, pt;\n\t.reg .b32 alo, ahi, blo, bhi, t0, t1;\n\t.reg .b64 a, b;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "setp.ne.b32 p0, %4, 0;\n\t"
+            "setp.eq.b32 pt, %4, %4;\n\t"
+            "mov.b64 {alo, ahi}, %1;\n\t"
+            "mov.b64 {blo, bhi}, %2;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
+            "add.u32 t0, alo, %5;\n\tmov.b64 a, {t0, ahi};\n\tadd.u32 t1, blo, %8;\n\tmov.b64 b, {t1, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+            "add.u32 t0, alo, %6;\n\tmov.b64 a, {t0, ahi};\n\tadd.u32 t1, blo, %9;\n\tmov.b64 b, {t1, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+            "add.u32 t0, alo, %7;\n\tmov.b64 a, {t0, ahi};\n\tadd.u32 t1, blo, %10;\n\tmov.b64 b, {t1, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+            "}" ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc),
+            "n"(A1), "n"(A2), "n"(A3), "n"(B1), "n"(B2), "n"(B3)
+            : "memory");
+    }
+}
+
+// Same for O += P V with P (A) read from TMEM: 8 steps, A advances 8
+// columns and B (V, MN-major) 2048 bytes per step.
+__device__ __forceinline__ void mma_ts_kloop8(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred e, p0, pt;\n\t.reg .b32 blo, bhi, t0, t1;\n\t.reg .b64 b;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\t"
+        "setp.eq.b32 pt, %4, %4;\n\t"
+        "mov.b64 {blo, bhi}, %2;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
+        "add.u32 t0, %1, 8;\n\tadd.u32 t1, blo, 128;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], b, %3, pt;\n\t"
+        "add.u32 t0, %1, 16;\n\tadd.u32 t1, blo, 256;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], b, %3, pt;\n\t"
+        "add.u32 t0, %1, 24;\n\tadd.u32 t1, blo, 384;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], b, %3, pt;\n\t"
+        "add.u32 t0, %1, 32;\n\tadd.u32 t1, blo, 512;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], b, %3, pt;\n\t"
+        "add.u32 t0, %1, 40;\n\tadd.u32 t1, blo, 640;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], b, %3, pt;\n\t"
+        "add.u32 t0, %1, 48;\n\tadd.u32 t1, blo, 768;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], b, %3, pt;\n\t"
+        "add.u32 t0, %1, 56;\n\tadd.u32 t1, blo, 896;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], b, %3, pt;\n\t"
+        "}" ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
 __device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
