@@ -405,8 +405,9 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
             l *= alpha;
             m = m_new;
 
-            // P = exp2(S*c - m) on pairs: one packed FMA, two MUFU ex2, one
-            // packed add into four partial row sums, one 16-bit pack.
+            // P = exp2(S*c - m) on pairs: one packed FMA, two MUFU ex2 (or the
+            // FMA-pipe polynomial), one packed add into four partial row sums,
+            // one 16-bit pack.
             const uint64_t nm2 = ptx::f2_pack(-m, -m);
             uint64_t acc[4] = {0, 0, 0, 0};
             uint32_t pk[kBN / 2];
@@ -414,10 +415,17 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
             for (int i = 0; i < kBN / 2; ++i) {
                 const uint64_t x =
                     ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, nm2);
-                float x0, x1;
-                ptx::f2_unpack(x, x0, x1);
-                const float p0 = ptx::ex2_approx(x0);
-                const float p1 = ptx::ex2_approx(x1);
+                // One pair in eight is exponentiated on the FMA pipe, which
+                // shortens the MUFU-bound stretch of this loop.
+                float p0, p1;
+                if ((i & 7) == 7) {
+                    ptx::f2_unpack(ptx::ex2_poly_f2(x), p0, p1);
+                } else {
+                    float x0, x1;
+                    ptx::f2_unpack(x, x0, x1);
+                    p0 = ptx::ex2_approx(x0);
+                    p1 = ptx::ex2_approx(x1);
+                }
                 acc[i & 3] = ptx::f2_add(acc[i & 3], ptx::f2_pack(p0, p1));
                 pk[i] = ptx::pack2<kBf16>(p0, p1);
             }

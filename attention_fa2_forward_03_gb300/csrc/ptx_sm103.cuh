@@ -489,6 +489,38 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
     return d;
 }
 
+
+// exp2 of a pair of x <= 0 on the FMA pipe instead of the MUFU, for a share
+// of the softmax's exponentials. Cody-Waite range reduction (Cody and Waite,
+// "Software Manual for the Elementary Functions", 1980): x = n + f with n the
+// nearest integer (by adding and subtracting 1.5 * 2^23) and |f| <= 1/2; 2^f
+// by a degree-3 polynomial with constant term exactly 1 whose other
+// coefficients are a relative-error minimax fit on [-1/2, 1/2] computed for
+// this kernel (max relative error 1.0e-4); 2^n is applied by adding n << 23 to
+// the result's bit pattern. x is clamped to -125 first so the scaled result
+// stays a normal number; exp2(0) is exactly 1.
+__device__ __forceinline__ uint64_t ex2_poly_f2(uint64_t x2) {
+    float x0, x1;
+    f2_unpack(x2, x0, x1);
+    x0 = fmaxf(x0, -125.0f);
+    x1 = fmaxf(x1, -125.0f);
+    const uint64_t xc = f2_pack(x0, x1);
+    const uint64_t t = f2_add(xc, f2_pack(12582912.0f, 12582912.0f));
+    const uint64_t r = f2_add(t, f2_pack(-12582912.0f, -12582912.0f));
+    const uint64_t f = f2_fma(r, f2_pack(-1.0f, -1.0f), xc);
+    uint64_t p = f2_fma(f2_pack(0.055009059607982635f, 0.055009059607982635f), f,
+                        f2_pack(0.2422109693288803f, 0.2422109693288803f));
+    p = f2_fma(p, f, f2_pack(0.6932829022407532f, 0.6932829022407532f));
+    p = f2_fma(p, f, f2_pack(1.0f, 1.0f));
+    float p0, p1, t0, t1;
+    f2_unpack(p, p0, p1);
+    f2_unpack(t, t0, t1);
+    // bits(t) = bits(1.5 * 2^23) + n and bits(1.5 * 2^23) << 23 vanishes mod 2^32
+    const uint32_t b0 = __float_as_uint(t0) * 8388608u + __float_as_uint(p0);
+    const uint32_t b1 = __float_as_uint(t1) * 8388608u + __float_as_uint(p1);
+    return f2_pack(__uint_as_float(b0), __uint_as_float(b1));
+}
+
 // Pack two fp32 values into a 16-bit pair: `lo` in bits 0..15, `hi` in 16..31,
 // each rounded to nearest-even. kBf16 selects bf16, otherwise fp16.
 template <bool kBf16>
