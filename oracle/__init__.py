@@ -54,6 +54,10 @@ def _load():
         lib.oracle_softmax_row.restype = ctypes.c_int
         lib.oracle_decode16.argtypes = [p, i64, ctypes.c_int, p]
         lib.oracle_decode16.restype = None
+        lib.oracle_attention_ex_rows.argtypes = [p, p, p, ctypes.c_int, i64, i64, i64, i64, i64, i64,
+                                                 ctypes.c_double, ctypes.c_int, p, i64, p, p,
+                                                 ctypes.c_int]
+        lib.oracle_attention_ex_rows.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -105,6 +109,39 @@ def attention(q, k, v, scale: float, dtype: int, rows=None, threads: int = 0):
         raise ValueError("oracle rejected the sizes")
     if rows is None:
         return o.reshape(B, Hq, N, d), lse.reshape(B, Hq, N)
+    return o, lse
+
+
+def attention_ex(q, k, v, scale: float, dtype: int, causal: bool = False, rows=None,
+                 threads: int = 0):
+    """Attention forward with independent query/key lengths and an optional
+    causal mask (key j allowed for query i iff j < min(Nk, i + 1 + Nk - Nq)).
+
+    q: uint16 [B, Hq, Nq, d]; k, v: uint16 [B, Hkv, Nk, d]. Rows with no
+    allowed key give o = 0 and lse = -inf. Returns (o, lse) shaped like
+    :func:`attention` (rows index [B, Hq, Nq]).
+    """
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nk, dk = k.shape
+    if (Bk, dk) != (B, d) or v.shape != k.shape:
+        raise ValueError("shape mismatch between q, k and v")
+    if rows is None:
+        nrows = B * Hq * Nq
+        rptr = None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        nrows = rows_arr.size
+        rptr = rows_arr.ctypes.data
+    o = np.empty((nrows, d), dtype=np.float64)
+    lse = np.empty(nrows, dtype=np.float64)
+    rc = _load().oracle_attention_ex_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, dtype,
+                                          B, Hq, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
+                                          rptr, nrows, o.ctypes.data, lse.ctypes.data, int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the sizes")
+    if rows is None:
+        return o.reshape(B, Hq, Nq, d), lse.reshape(B, Hq, Nq)
     return o, lse
 
 

@@ -30,6 +30,11 @@
  * Query Head Packing for MQA/GQA" (Colfax Research author page): query head h
  * reads KV head h / (Hq / Hkv).
  *
+ * The generalised form (oracle_attention_ex_rows) covers unequal and ragged
+ * query/key lengths and the causal mask, the variants the Ampere series
+ * excludes from its Kernel Specification (equal lengths, non-causal,
+ * lengths divisible by the block size).
+ *
  * Every function here is pinned by tests/test_oracle.py against closed forms,
  * invariants, a hand-computed case and an independent library computation.
  */
@@ -173,6 +178,82 @@ int oracle_softmax_row(const uint16_t* q, const uint16_t* k, int dtype, int64_t 
         l += p_out[j];
     }
     for (int64_t j = 0; j < N; ++j) p_out[j] /= l;
+    return 0;
+}
+
+/*
+ * Generalised forward: query length Nq and key length Nk may differ and need
+ * not be multiples of any block size, and an optional causal mask. Query row
+ * i may attend key j iff j < kend(i), with
+ *     kend(i) = Nk                          (non-causal)
+ *     kend(i) = min(Nk, i + 1 + Nk - Nq)    (causal, aligned to the end of
+ *                                            the key sequence)
+ * which for Nq = Nk is the usual lower-triangular mask j <= i. A row with no
+ * allowed key (causal with Nq > Nk) has o = 0 and lse = -inf.
+ *
+ * q: [B, Hq, Nq, d]; k, v: [B, Hkv, Nk, d]; rows index [B, Hq, Nq] flat
+ * (NULL = all). Returns 0, or -1 on invalid sizes.
+ */
+int oracle_attention_ex_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v, int dtype,
+                             int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d,
+                             double scale, int causal, const int64_t* rows, int64_t nrows,
+                             double* o_out, double* lse_out, int nthreads) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || Hq % Hkv) return -1;
+    if (!rows && nrows != B * Hq * Nq) return -1;
+    const int64_t G = Hq / Hkv;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+
+#pragma omp parallel
+    {
+        double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+        double* s = (double*)malloc(sizeof(double) * (size_t)Nk);
+        double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < nrows; ++r) {
+            const int64_t flat = rows ? rows[r] : r;
+            const int64_t i = flat % Nq;
+            const int64_t h = (flat / Nq) % Hq;
+            const int64_t b = flat / (Nq * Hq);
+            const int64_t hk = h / G;
+            const uint16_t* qp = q + ((b * Hq + h) * Nq + i) * d;
+            const uint16_t* kp = k + (b * Hkv + hk) * Nk * d;
+            const uint16_t* vp = v + (b * Hkv + hk) * Nk * d;
+            int64_t kend = Nk;
+            if (causal) {
+                const int64_t lim = i + 1 + Nk - Nq;
+                kend = lim < Nk ? lim : Nk;
+            }
+            if (kend <= 0) {
+                for (int64_t t = 0; t < d; ++t) o_out[r * d + t] = 0.0;
+                lse_out[r] = -INFINITY;
+                continue;
+            }
+            for (int64_t t = 0; t < d; ++t) qrow[t] = decode16(qp[t], dtype);
+            double m = -INFINITY;
+            for (int64_t j = 0; j < kend; ++j) {
+                double dot = 0.0;
+                for (int64_t t = 0; t < d; ++t) dot += qrow[t] * decode16(kp[j * d + t], dtype);
+                s[j] = scale * dot;
+                if (s[j] > m) m = s[j];
+            }
+            double l = 0.0;
+            for (int64_t t = 0; t < d; ++t) acc[t] = 0.0;
+            for (int64_t j = 0; j < kend; ++j) {
+                const double p = exp(s[j] - m);
+                l += p;
+                for (int64_t t = 0; t < d; ++t) acc[t] += p * decode16(vp[j * d + t], dtype);
+            }
+            for (int64_t t = 0; t < d; ++t) o_out[r * d + t] = acc[t] / l;
+            lse_out[r] = m + log(l);
+        }
+        free(qrow);
+        free(s);
+        free(acc);
+    }
     return 0;
 }
 

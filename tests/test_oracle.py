@@ -265,3 +265,91 @@ def test_oracle_rejects_bad_sizes():
     q, k, v = rand_inputs(15, 1, 3, 2, 16, 8)
     with pytest.raises(ValueError):
         oracle.attention(q, k, v, 0.1, gen.BF16)  # 3 query heads over 2 KV heads
+
+
+# ---------------------------------------------------------------- generalised form: ragged, unequal, causal
+
+def kend(i, nq, nk, causal):
+    return min(nk, i + 1 + nk - nq) if causal else nk
+
+
+def test_hand_causal_case():
+    g = json.load(open(os.path.join(GOLDEN, "hand_causal_n2_d1.json")))
+    q = exact_bf16(g["q"]).reshape(1, 1, 2, 1)
+    k = exact_bf16(g["k"]).reshape(1, 1, 2, 1)
+    v = exact_bf16(g["v"]).reshape(1, 1, 2, 1)
+    o, lse = oracle.attention_ex(q, k, v, math.log(3) / 2, gen.BF16, causal=True)
+    np.testing.assert_allclose(o[0, 0, :, 0], g["o"], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse[0, 0], [0.0, math.log(4)], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("nq,nk", [(5, 5), (7, 12), (12, 7), (130, 130), (1, 9)])
+def test_causal_zero_queries_give_prefix_means(nq, nk):
+    _, k, v = rand_inputs(40, 1, 2, 1, nk, 8)
+    q = np.zeros((1, 2, nq, 8), np.uint16)
+    o, lse = oracle.attention_ex(q, k, v, 0.3, gen.BF16, causal=True)
+    vd = oracle.decode16(v, gen.BF16)[0, 0]
+    for i in range(nq):
+        e = kend(i, nq, nk, True)
+        if e <= 0:
+            assert np.all(o[0, :, i] == 0.0) and np.all(np.isneginf(lse[0, :, i]))
+        else:
+            np.testing.assert_allclose(o[0, 0, i], vd[:e].mean(axis=0), rtol=0, atol=1e-13)
+            np.testing.assert_allclose(lse[0, :, i], math.log(e), rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("nq,nk", [(3, 10), (10, 3), (77, 200)])
+def test_unequal_lengths_zero_queries_give_mean(nq, nk):
+    _, k, v = rand_inputs(41, 2, 2, 2, nk, 16)
+    q = np.zeros((2, 2, nq, 16), np.uint16)
+    o, lse = oracle.attention_ex(q, k, v, 0.3, gen.BF16, causal=False)
+    vd = oracle.decode16(v, gen.BF16)
+    np.testing.assert_allclose(o, np.broadcast_to(vd.mean(axis=2, keepdims=True), o.shape), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, math.log(nk), rtol=0, atol=1e-13)
+
+
+def test_causal_first_row_is_first_value():
+    q, k, v = rand_inputs(42, 2, 3, 3, 40, 8)
+    o, lse = oracle.attention_ex(q, k, v, 0.2, gen.BF16, causal=True)
+    qd, kd, vd = (oracle.decode16(x, gen.BF16) for x in (q, k, v))
+    np.testing.assert_array_equal(o[:, :, 0], vd[:, :, 0])
+    np.testing.assert_allclose(lse[:, :, 0], 0.2 * np.sum(qd[:, :, 0] * kd[:, :, 0], -1), rtol=0, atol=1e-12)
+
+
+def test_causal_ignores_keys_past_the_mask():
+    q, k, v = rand_inputs(43, 1, 2, 2, 64, 16)
+    o1, l1 = oracle.attention_ex(q, k, v, 0.25, gen.BF16, causal=True)
+    k2, v2 = k.copy(), v.copy()
+    k2[:, :, 40:] = bf16_bits(np.full((1, 2, 24, 16), 3.0))
+    v2[:, :, 40:] = bf16_bits(np.full((1, 2, 24, 16), -7.0))
+    o2, l2 = oracle.attention_ex(q, k2, v2, 0.25, gen.BF16, causal=True)
+    np.testing.assert_array_equal(o1[:, :, :40], o2[:, :, :40])
+    np.testing.assert_array_equal(l1[:, :, :40], l2[:, :, :40])
+    assert np.max(np.abs(o1[:, :, 40:] - o2[:, :, 40:])) > 1e-3
+
+
+def test_non_causal_equal_lengths_reduces_to_attention():
+    q, k, v = rand_inputs(44, 1, 4, 2, 96, 32)
+    o1, l1 = oracle.attention(q, k, v, 0.2, gen.BF16)
+    o2, l2 = oracle.attention_ex(q, k, v, 0.2, gen.BF16, causal=False)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("nq,nk,causal", [(70, 70, True), (50, 90, True), (90, 50, True), (33, 100, False)])
+def test_generalised_library_crosscheck(nq, nk, causal):
+    torch = pytest.importorskip("torch")
+    q, _, _ = rand_inputs(45, 1, 4, 2, nq, 32)
+    _, k, v = rand_inputs(46, 1, 4, 2, nk, 32)
+    o, lse = oracle.attention_ex(q, k, v, 0.15, gen.BF16, causal=causal)
+    qd, kd, vd = (torch.from_numpy(oracle.decode16(x, gen.BF16)) for x in (q, k, v))
+    kd, vd = kd.repeat_interleave(2, dim=1), vd.repeat_interleave(2, dim=1)
+    s = 0.15 * torch.einsum("bhid,bhjd->bhij", qd, kd)
+    if causal:
+        i = torch.arange(nq)[:, None]
+        j = torch.arange(nk)[None, :]
+        s = s.masked_fill(j > i + (nk - nq), float("-inf"))
+    ref_lse = torch.logsumexp(s, dim=-1)
+    ref_o = torch.nan_to_num(torch.softmax(s, dim=-1)) @ vd
+    np.testing.assert_allclose(o, ref_o.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=0, atol=1e-12)
