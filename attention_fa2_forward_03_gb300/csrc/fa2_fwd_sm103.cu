@@ -83,6 +83,13 @@ struct Params {
     int kv_rows;         // N
     int debug_flags;
     float scale_log2;    // scale * log2(e)
+    // General mode only (ragged / unequal lengths, causal); tiles per head.
+    int nq, nk;          // query and key length per head
+    int causal;          // key j allowed for query i iff j < min(nk, i + 1 + nk - nq)
+    int heads_q;         // B * Hq
+    int hq;              // Hq
+    int group;           // Hq / Hkv
+    int tq;              // ceil(nq / 128): query tiles per head
 };
 
 template <int D>
@@ -171,6 +178,52 @@ __device__ __forceinline__ Item make_item(const Params& p, int item) {
     const int group = item / p.pairs;
     const int qt0 = kNQ * (item - group * p.pairs);
     return Item{min(kNQ, p.q_tiles - qt0), (group * p.q_tiles + qt0) * kBM, group * p.kv_rows};
+}
+
+// General mode: an item is tiles 2p, 2p+1 of one query head. Per tile, the
+// KV tiles it needs (nkv) and the first KV tile that needs masking (jmask):
+// row i may attend keys j < kend(i) = min(nk, i + 1 + nk - nq) when causal,
+// j < nk otherwise; kend grows with i, so the tile's last valid row sets nkv
+// and its first row sets jmask. Causal items run heaviest first.
+struct ItemG {
+    int n_tiles;
+    int head;      // b * Hq + hq
+    int kvhead;    // b * Hkv + hq / group
+    int q0;        // first row of tile 0 within the head
+    int nkv[2];
+    int jmask[2];
+};
+
+__device__ __forceinline__ int kend_of(const Params& p, int i) {
+    return p.causal ? min(p.nk, i + 1 + p.nk - p.nq) : p.nk;
+}
+
+__device__ __forceinline__ ItemG make_item_gen(const Params& p, int it) {
+    ItemG g;
+    int pidx;
+    if (p.causal) {
+        pidx = p.pairs - 1 - it / p.heads_q;
+        g.head = it % p.heads_q;
+    } else {
+        pidx = it % p.pairs;
+        g.head = it / p.pairs;
+    }
+    const int b = g.head / p.hq;
+    g.kvhead = b * (p.hq / p.group) + (g.head - b * p.hq) / p.group;
+    g.q0 = 2 * pidx * kBM;
+    g.n_tiles = min(kNQ, p.tq - 2 * pidx);
+    for (int t = 0; t < 2; ++t) {
+        g.nkv[t] = 0;
+        g.jmask[t] = 0;
+        if (t < g.n_tiles) {
+            const int r0 = g.q0 + t * kBM;
+            const int hi = kend_of(p, min(r0 + kBM - 1, p.nq - 1));
+            const int lo = kend_of(p, r0);
+            g.nkv[t] = hi <= 0 ? 0 : (hi + kBN - 1) / kBN;
+            g.jmask[t] = lo <= 0 ? 0 : lo / kBN;
+        }
+    }
+    return g;
 }
 
 // ---------------------------------------------------------------- producer
@@ -331,6 +384,137 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint
     __syncwarp();
 }
 
+
+// ---------------------------------------------------------------- general mode: producer and MMA
+
+template <int D>
+__device__ __forceinline__ void producer_gen(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                             const Params& p, uint32_t sbase, const Bars<D>& bars, const Waiter& w) {
+    using L = Layout<D>;
+    constexpr int S = L::kStages;
+    const bool load_q = (p.debug_flags & 1) == 0;
+    int ring = 0;
+    int nq[2] = {0, 0};
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+        const ItemG g = make_item_gen(p, it);
+        for (int t = 0; t < g.n_tiles && ok; ++t) {
+            if (g.nkv[t] == 0) continue;
+            if (!(ok = w.wait(bars.q_empty(t), (nq[t] & 1) ^ 1, kSiteQEmpty))) break;
+            if (load_q) {
+                const uint32_t dst = sbase + L::kQOff + t * L::kTileBytes;
+                ptx::mbar_arrive_expect_tx(bars.q_full(t), L::kTileBytes);
+#pragma unroll
+                for (int blk = 0; blk < D / 64; ++blk)
+                    ptx::tma_load_3d(dst + blk * L::kBlkBytes, tmQ, blk * 64, g.q0 + t * kBM, g.head, bars.q_full(t));
+            }
+            ++nq[t];
+        }
+        const int nmax = max(g.nkv[0], g.nkv[1]);
+        for (int k = 0; k < 2 * nmax && ok; ++k) {
+            const int s = ring % S;
+            if (!(ok = w.wait(bars.kv_empty(s), ((ring / S) & 1) ^ 1, kSiteKvEmpty))) break;
+            const uint32_t dst = sbase + L::kRingOff + s * L::kTileBytes;
+            const CUtensorMap* tm = (k & 1) ? tmV : tmK;
+            ptx::mbar_arrive_expect_tx(bars.kv_full(s), L::kTileBytes);
+#pragma unroll
+            for (int blk = 0; blk < D / 64; ++blk)
+                ptx::tma_load_3d(dst + blk * L::kBlkBytes, tm, blk * 64, (k >> 1) * kBN, g.kvhead, bars.kv_full(s));
+            ++ring;
+        }
+    }
+    if (!ok) {
+        const int first = ring > S ? ring - S : 0;
+        for (int r = first; r < ring; ++r) w.drain(bars.kv_full(r % S), (r / S) & 1);
+        if (load_q)
+            for (int t = 0; t < 2; ++t)
+                if (nq[t] > 0) w.drain(bars.q_full(t), (nq[t] - 1) & 1);
+    }
+}
+
+// Same issue order as mma_issuer, with a KV tile count per query tile: at KV
+// tile j only the tiles with j < nkv[t] take part, and each ring stage is
+// released after its last user.
+template <int D, bool kBf16>
+__device__ __forceinline__ void mma_issuer_gen(const Params& p, uint32_t sbase, uint32_t tmem, const Bars<D>& bars,
+                                               const Waiter& w) {
+    using L = Layout<D>;
+    constexpr int S = L::kStages;
+    constexpr uint32_t kAB = kBf16 ? 1u : 0u;
+    constexpr uint32_t kIdS = ptx::idesc_f16(kAB, 0, 0, kBM, kBN);
+    constexpr uint32_t kIdO = ptx::idesc_f16(kAB, 0, 1, kBM, D);
+    auto stage_addr = [&](int r) { return sbase + L::kRingOff + (r % S) * L::kTileBytes; };
+    auto issue_qk = [&](int t, uint32_t kaddr) {
+        const uint64_t qd = ptx::desc_sw128(sbase + L::kQOff + t * L::kTileBytes, 16, 1024);
+        const uint64_t kd = ptx::desc_sw128(kaddr, 16, 1024);
+        qk_kloop<D>(tmem + L::col_s(t), qd, kd, kIdS);
+    };
+    auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
+        const uint64_t vd = ptx::desc_sw128(vaddr, L::kBlkBytes, 1024);
+        pv_kloop(tmem + L::col_o(t), tmem + L::col_s(t), vd, kIdO, acc ? 1u : 0u);
+    };
+    auto wait_u = [&](uint32_t bar, uint32_t parity, int site) {
+        return __shfl_sync(0xffffffffu, w.wait(bar, parity, site) ? 1 : 0, 0) != 0;
+    };
+    auto wait_ring = [&](int r) { return wait_u(bars.kv_full(r % S), (r / S) & 1, kSiteKvFull); };
+
+    int ring = 0;
+    int nq[2] = {0, 0};
+    int np[2] = {0, 0};
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+        const ItemG g = make_item_gen(p, it);
+        const int nmax = max(g.nkv[0], g.nkv[1]);
+        if (nmax == 0) continue;
+        for (int t = 0; t < 2 && ok; ++t)
+            if (g.nkv[t] > 0) ok = wait_u(bars.q_full(t), nq[t] & 1, kSiteQFull);
+        if (!ok || !(ok = wait_ring(ring))) break;
+        ptx::tc_fence_after();
+        for (int t = 0; t < 2; ++t) {
+            if (g.nkv[t] == 0) continue;
+            issue_qk(t, stage_addr(ring));
+            ptx::tc_commit_elect(bars.s_full(t));
+            if (g.nkv[t] == 1) ptx::tc_commit_elect(bars.q_empty(t));
+        }
+        ptx::tc_commit_elect(bars.kv_empty(ring % S));
+        int k_ring = ring;
+        ++ring;
+        for (int j = 0; j < nmax; ++j) {
+            const bool more = j + 1 < nmax;
+            const int v_ring = ring++;
+            if (!(ok = wait_ring(v_ring))) break;
+            if (more) {
+                k_ring = ring++;
+                if (!(ok = wait_ring(k_ring))) break;
+            }
+            const int last_v = j < g.nkv[1] ? 1 : 0;                 // last tile reading V_j
+            const int last_k = (more && j + 1 < g.nkv[1]) ? 1 : 0;   // last tile reading K_{j+1}
+            for (int t = 0; t < 2; ++t) {
+                if (j >= g.nkv[t]) continue;
+                if (!(ok = wait_u(bars.p_full(t), np[t] & 1, kSitePFull))) break;
+                ++np[t];
+                ptx::tc_fence_after();
+                issue_pv(t, stage_addr(v_ring), j > 0);
+                if (t == last_v) ptx::tc_commit_elect(bars.kv_empty(v_ring % S));
+                if (j + 1 < g.nkv[t]) {
+                    issue_qk(t, stage_addr(k_ring));
+                    ptx::tc_commit_elect(bars.s_full(t));
+                    if (j + 2 == g.nkv[t]) ptx::tc_commit_elect(bars.q_empty(t));
+                    if (t == last_k) ptx::tc_commit_elect(bars.kv_empty(k_ring % S));
+                } else {
+                    ptx::tc_commit_elect(bars.o_full(t));
+                }
+            }
+            if (!ok) break;
+        }
+        for (int t = 0; t < 2; ++t)
+            if (g.nkv[t] > 0) ++nq[t];
+    }
+    ptx::tc_commit_elect(bars.mma_done());
+    w.drain(bars.mma_done(), 0);
+    __syncwarp();
+}
+
 // ---------------------------------------------------------------- softmax
 
 // 32-column TMEM load/store into slice [off, off+32) of a register array;
@@ -351,7 +535,7 @@ __device__ __forceinline__ void st_slice(uint32_t taddr, const uint32_t (&r)[N],
     if constexpr (N > 96) if (off == 96) ptx::tmem_st32_at<96 % N>(taddr, r);
 }
 
-template <int D, bool kBf16>
+template <int D, bool kBf16, bool kGen>
 __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uint8_t* smem, const Bars<D>& bars,
                                              const Waiter& w, int t) {
     using L = Layout<D>;
@@ -367,10 +551,20 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
     int n_s = 0;       // S tiles consumed (s_full / alpha / p_full phases)
     bool ok = true;
     for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
-        if (t >= make_item(p, it).n_tiles) continue;
+        int nkv, jmask = 0x7fffffff, kend_row = 0;
+        if constexpr (kGen) {
+            const ItemG g = make_item_gen(p, it);
+            if (t >= g.n_tiles || g.nkv[t] == 0) continue;
+            nkv = g.nkv[t];
+            jmask = g.jmask[t];
+            kend_row = kend_of(p, g.q0 + t * kBM + row);
+        } else {
+            if (t >= make_item(p, it).n_tiles) continue;
+            nkv = p.n_kv_tiles;
+        }
         float m = -INFINITY;  // running row max of the scaled scores, log2 units
         float l = 0.0f;       // running sum of exp2(s*c - m)
-        for (int j = 0; j < p.n_kv_tiles; ++j, ++n_s) {
+        for (int j = 0; j < nkv; ++j, ++n_s) {
             ok = w.wait(bars.s_full(t), n_s & 1, kSiteSFull);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
@@ -383,6 +577,15 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
             ptx::tmem_ld32_at<64>(row_addr + colS + 64, s);
             ptx::tmem_ld32_at<96>(row_addr + colS + 96, s);
             ptx::tmem_wait_ld();
+            if constexpr (kGen) {
+                // Keys at or past kend(row) (the causal diagonal, the end of
+                // a ragged key sequence, TMA's zero fill) get -inf.
+                if (j >= jmask) {
+                    const int lim = kend_row - j * kBN;
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) s[c] = c < lim ? s[c] : 0xFF800000u;
+                }
+            }
 
             // Row max: eight independent chains of 3-input max, then combine.
             float mx[8];
@@ -404,11 +607,14 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
             ptx::mbar_arrive(bars.alpha_ready(t));
             l *= alpha;
             m = m_new;
+            // A row with no allowed key so far keeps m = -inf; exponentiate
+            // against 0 then, so its weights are exp2(-inf) = 0.
+            const float m_use = (kGen && m == -INFINITY) ? 0.0f : m;
 
             // P = exp2(S*c - m) on pairs: one packed FMA, two MUFU ex2 (or the
             // FMA-pipe polynomial), one packed add into four partial row sums,
             // one 16-bit pack.
-            const uint64_t nm2 = ptx::f2_pack(-m, -m);
+            const uint64_t nm2 = ptx::f2_pack(-m_use, -m_use);
             uint64_t acc[4] = {0, 0, 0, 0};
             uint32_t pk[kBN / 2];
 #pragma unroll
@@ -418,7 +624,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
                 // One pair in eight is exponentiated on the FMA pipe, which
                 // shortens the MUFU-bound stretch of this loop.
                 float p0, p1;
-                if ((i & 7) == 7) {
+                if (!kGen && (i & 7) == 7) {  // masked -inf keys need the MUFU's exact 0
                     ptx::f2_unpack(ptx::ex2_poly_f2(x), p0, p1);
                 } else {
                     float x0, x1;
@@ -434,7 +640,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
             l += a0 + a1;
             ptx::tmem_st32_at<0>(row_addr + colS, pk);
             ptx::tmem_st32_at<32>(row_addr + colS + 32, pk);
-            if (j + 1 == p.n_kv_tiles) {
+            if (j + 1 == nkv) {
                 m_buf[row] = m;
                 l_buf[row] = l;
                 ptx::mbar_arrive(bars.stats_ready(t));
@@ -448,7 +654,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
 
 // ---------------------------------------------------------------- correction + epilogue
 
-template <int D, bool kBf16>
+template <int D, bool kBf16, bool kGen>
 __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, uint8_t* smem, const Bars<D>& bars,
                                                 const Waiter& w) {
     using L = Layout<D>;
@@ -463,9 +669,26 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
     int n_items[2] = {0, 0};
     bool ok = true;
     for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
-        const Item item = make_item(p, it);
-        for (int j = 0; j < p.n_kv_tiles && ok; ++j) {
-            for (int t = 0; t < item.n_tiles; ++t) {
+        // row0: first row of tile 0 in the output view; q0: the same row's
+        // index within its head (general mode, for the ragged-end check).
+        int n_tiles, nkv[2], row0, q0 = 0;
+        if constexpr (kGen) {
+            const ItemG g = make_item_gen(p, it);
+            n_tiles = g.n_tiles;
+            nkv[0] = g.nkv[0];
+            nkv[1] = g.nkv[1];
+            row0 = g.head * p.nq + g.q0;
+            q0 = g.q0;
+        } else {
+            const Item item = make_item(p, it);
+            n_tiles = item.n_tiles;
+            nkv[0] = nkv[1] = p.n_kv_tiles;
+            row0 = item.q_row0;
+        }
+        const int nmax = max(nkv[0], n_tiles > 1 ? nkv[1] : 0);
+        for (int j = 0; j < nmax && ok; ++j) {
+            for (int t = 0; t < n_tiles; ++t) {
+                if (j >= nkv[t]) continue;
                 ok = w.wait(bars.alpha_ready(t), n_s[t] & 1, kSiteAlpha);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
@@ -506,7 +729,20 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
         // Epilogue for each tile of the item: O / l -> 16 bit, LSE. The next
         // item's first PV overwrites O only after this warpgroup's next
         // p_full arrival, which comes after these loads.
-        for (int t = 0; t < item.n_tiles && ok; ++t) {
+        for (int t = 0; t < n_tiles && ok; ++t) {
+            const int grow = row0 + t * kBM + row;
+            // Rows past a ragged query end are computed but not stored.
+            const bool valid = !kGen || q0 + t * kBM + row < p.nq;
+            if (kGen && nkv[t] == 0) {
+                // No row of this tile may attend any key: O = 0, LSE = -inf.
+                if (valid) {
+                    uint4* z = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + static_cast<size_t>(grow) * D);
+#pragma unroll
+                    for (int v = 0; v < D / 8; ++v) z[v] = make_uint4(0, 0, 0, 0);
+                    p.lse[grow] = -INFINITY;
+                }
+                continue;
+            }
             ok = w.wait(bars.stats_ready(t), n_items[t] & 1, kSiteStats);
             if (ok) ok = w.wait(bars.o_full(t), n_items[t] & 1, kSiteOFull);
             if (!__all_sync(0xffffffffu, ok)) {
@@ -517,8 +753,8 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
             ptx::tc_fence_after();
             const float m = rowbuf[(2 + t) * kBM + row];
             const float l = rowbuf[(4 + t) * kBM + row];
-            const int grow = item.q_row0 + t * kBM + row;
-            const float inv_l = ptx::rcp_approx(l);
+            // l = 0 only for a row with no allowed key: O = 0, LSE = -inf.
+            const float inv_l = (!kGen || l > 0.0f) ? ptx::rcp_approx(l) : 0.0f;
             const uint32_t colO = L::col_o(t);
             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + static_cast<size_t>(grow) * D);
 #pragma unroll
@@ -530,11 +766,14 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
 #pragma unroll
                 for (int i = 0; i < kChunk / 2; ++i)
                     hv[i] = ptx::pack2<kBf16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+                if (valid) {
 #pragma unroll
-                for (int v = 0; v < kChunk / 8; ++v)
-                    dst[h / 8 + v] = make_uint4(hv[4 * v], hv[4 * v + 1], hv[4 * v + 2], hv[4 * v + 3]);
+                    for (int v = 0; v < kChunk / 8; ++v)
+                        dst[h / 8 + v] = make_uint4(hv[4 * v], hv[4 * v + 1], hv[4 * v + 2], hv[4 * v + 3]);
+                }
             }
-            p.lse[grow] = (m + ptx::lg2_approx(l)) * 0.69314718055994530942f;
+            if (valid)
+                p.lse[grow] = (!kGen || l > 0.0f) ? (m + ptx::lg2_approx(l)) * 0.69314718055994530942f : -INFINITY;
         }
         ptx::tc_fence_before();
     }
@@ -542,7 +781,7 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
 
 // ---------------------------------------------------------------- kernel
 
-template <int D, bool kBf16>
+template <int D, bool kBf16, bool kGen>
 __global__ void __launch_bounds__(kThreads, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -593,17 +832,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < kCorrWarp0) {
         ptx::setmaxnreg_inc<kRegSoftmax>();
-        softmax_role<D, kBf16>(p, tmem, smem, bars, w, warp / 4);
+        softmax_role<D, kBf16, kGen>(p, tmem, smem, bars, w, warp / 4);
     } else if (warp < kLoadWarp) {
         ptx::setmaxnreg_dec<kRegCorr>();
-        correction_role<D, kBf16>(p, tmem, smem, bars, w);
+        correction_role<D, kBf16, kGen>(p, tmem, smem, bars, w);
     } else {
         ptx::setmaxnreg_dec<kRegOther>();
         if (warp == kLoadWarp) {
-            if (lane == 0) producer<D>(&tmQ, &tmK, &tmV, p, sbase, bars, w);
+            if (lane == 0) {
+                if constexpr (kGen)
+                    producer_gen<D>(&tmQ, &tmK, &tmV, p, sbase, bars, w);
+                else
+                    producer<D>(&tmQ, &tmK, &tmV, p, sbase, bars, w);
+            }
             __syncwarp();
         } else if (warp == kMmaWarp) {
-            mma_issuer<D, kBf16>(p, sbase, tmem, bars, w);  // whole warp, one lane issues
+            if constexpr (kGen)
+                mma_issuer_gen<D, kBf16>(p, sbase, tmem, bars, w);
+            else
+                mma_issuer<D, kBf16>(p, sbase, tmem, bars, w);  // whole warp, one lane issues
         }
     }
 
@@ -634,7 +881,7 @@ struct DeviceState {
     bool probed = false;
     bool supported = false;
     int sm_count = 0;
-    bool smem_set[4] = {false, false, false, false};
+    bool smem_set[8] = {false, false, false, false, false, false, false, false};
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -684,12 +931,25 @@ fa2_status encode_map(CUtensorMap* m, const void* ptr, uint64_t rows, int d) {
     return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
 }
 
-template <int D, bool kBf16>
+// 3-D view [mats, rows, d] of a 16-bit tensor (general mode): a box of 128
+// rows never crosses into the next head, and rows past `rows` read as zero.
+fa2_status encode_map_3d(CUtensorMap* m, const void* ptr, uint64_t mats, uint64_t rows, int d) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), rows, mats};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, rows * static_cast<cuuint64_t>(d) * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                          es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
+}
+
+template <int D, bool kBf16, bool kGen = false>
 fa2_status launch(int dev, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                   const Params& p, dim3 grid, cudaStream_t stream) {
     constexpr int kSmem = Layout<D>::kSmemBytes;
-    auto kern = fa2::fa2_fwd_kernel<D, kBf16>;
-    const int slot = (D == 128 ? 0 : 2) + (kBf16 ? 0 : 1);
+    auto kern = fa2::fa2_fwd_kernel<D, kBf16, kGen>;
+    const int slot = (D == 128 ? 0 : 2) + (kBf16 ? 0 : 1) + (kGen ? 4 : 0);
     if (!g_dev[dev].smem_set[slot]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
             return FA2_ERR_CUDA;
@@ -758,6 +1018,64 @@ fa2_status fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, flo
 fa2_status fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
                    int d, float scale, fa2_dtype dtype, cudaStream_t stream) {
     return fa2_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, scale, dtype, stream);
+}
+
+fa2_status fa2_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
+                      int H_kv, int N_q, int N_k, int d, float scale, int causal, fa2_dtype dtype,
+                      cudaStream_t stream) {
+    if (!q || !k || !v || !o || !lse) return FA2_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA2_ERR_INVALID_ARG;
+    if (B <= 0 || H_q <= 0 || H_kv <= 0 || N_q <= 0 || N_k <= 0 || d <= 0) return FA2_ERR_INVALID_ARG;
+    if (H_q % H_kv != 0) return FA2_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.0f)) return FA2_ERR_INVALID_ARG;
+    if (dtype != FA2_BF16 && dtype != FA2_FP16) return FA2_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA2_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA2_ERR_UNSUPPORTED;
+    // The plain case is the multiple-of-128 kernel.
+    if (!causal && N_q == N_k && N_q % fa2::kBM == 0)
+        return fa2_fwd_gqa(q, k, v, o, lse, B, H_q, H_kv, N_q, d, scale, dtype, stream);
+    const long long heads_q = static_cast<long long>(B) * H_q;
+    const long long rows_q = heads_q * N_q;
+    const long long rows_kv = static_cast<long long>(B) * H_kv * N_k;
+    const long long tq = (N_q + fa2::kBM - 1) / fa2::kBM;
+    const long long items = heads_q * ((tq + fa2::kNQ - 1) / fa2::kNQ);
+    if (rows_q > 0x7FFFFFFFLL || rows_kv > 0x7FFFFFFFLL || items > 0x7FFFFFFFLL) return FA2_ERR_UNSUPPORTED;
+
+    int dev = 0;
+    fa2_status st = check_device(&dev);
+    if (st != FA2_OK) return st;
+    if ((st = get_encoder()) != FA2_OK) return st;
+
+    CUtensorMap mq, mk, mv;
+    if (encode_map_3d(&mq, q, static_cast<uint64_t>(heads_q), static_cast<uint64_t>(N_q), d) != FA2_OK ||
+        encode_map_3d(&mk, k, static_cast<uint64_t>(B) * H_kv, static_cast<uint64_t>(N_k), d) != FA2_OK ||
+        encode_map_3d(&mv, v, static_cast<uint64_t>(B) * H_kv, static_cast<uint64_t>(N_k), d) != FA2_OK)
+        return FA2_ERR_CUDA;
+
+    Params p{};
+    p.o = o;
+    p.lse = lse;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    p.debug_flags = g_debug_flags.load();
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.nq = N_q;
+    p.nk = N_k;
+    p.causal = causal;
+    p.heads_q = static_cast<int>(heads_q);
+    p.hq = H_q;
+    p.group = H_q / H_kv;
+    p.tq = static_cast<int>(tq);
+    p.pairs = static_cast<int>((tq + fa2::kNQ - 1) / fa2::kNQ);
+    p.total_items = static_cast<int>(items);
+    const dim3 grid(static_cast<unsigned>(std::min<long long>(items, g_dev[dev].sm_count)));
+
+    const bool bf = dtype == FA2_BF16;
+    if (d == 128)
+        return bf ? launch<128, true, true>(dev, mq, mk, mv, p, grid, stream)
+                  : launch<128, false, true>(dev, mq, mk, mv, p, grid, stream);
+    return bf ? launch<64, true, true>(dev, mq, mk, mv, p, grid, stream)
+              : launch<64, false, true>(dev, mq, mk, mv, p, grid, stream);
 }
 
 fa2_status fa2_check_status(cudaStream_t stream) {

@@ -22,7 +22,7 @@ FA2_ERR_CUDA = 3
 FA2_ERR_TIMEOUT = 4
 
 # symbols declared in include/fa2.h
-EXPORTS = ("fa2_fwd", "fa2_fwd_gqa", "fa2_check_status", "fa2_status_string",
+EXPORTS = ("fa2_fwd", "fa2_fwd_gqa", "fa2_fwd_ex", "fa2_check_status", "fa2_status_string",
            "fa2_set_wait_limit_ns", "fa2_set_debug_flags", "fa2_version")
 
 _lib = None
@@ -48,6 +48,8 @@ def load(path: str = LIB_PATH):
     lib.fa2_fwd.restype = i
     lib.fa2_fwd_gqa.argtypes = [p, p, p, p, p, i, i, i, i, i, f, i, p]
     lib.fa2_fwd_gqa.restype = i
+    lib.fa2_fwd_ex.argtypes = [p, p, p, p, p, i, i, i, i, i, i, f, i, i, p]
+    lib.fa2_fwd_ex.restype = i
     lib.fa2_check_status.argtypes = [p]
     lib.fa2_check_status.restype = i
     lib.fa2_status_string.argtypes = [i]
@@ -77,6 +79,12 @@ def fa2_fwd_gqa_ptr(q, k, v, o, lse, B, H_q, H_kv, N, d, scale, dtype, stream=0)
 def fa2_fwd_ptr(q, k, v, o, lse, B, H, N, d, scale, dtype, stream=0) -> int:
     """fa2_fwd on raw device addresses (ints); returns the status code."""
     return load().fa2_fwd(q, k, v, o, lse, B, H, N, d, float(scale), int(dtype), stream or None)
+
+
+def fa2_fwd_ex_ptr(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, scale, causal, dtype, stream=0) -> int:
+    """fa2_fwd_ex on raw device addresses (ints); returns the status code."""
+    return load().fa2_fwd_ex(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, float(scale), int(causal),
+                             int(dtype), stream or None)
 
 
 def fa2_check_status(stream=0) -> int:
@@ -148,6 +156,40 @@ def fa2_fwd_gqa(q, k, v, o=None, lse=None, scale=None, stream=None):
                          B, Hq, Hkv, N, d, scale, _dtype_code(q), _stream_handle(stream, q.device))
     if rc != FA2_OK:
         raise FA2Error(rc, "fa2_fwd_gqa")
+    return o, lse
+
+
+def fa2_fwd_ex(q, k, v, o=None, lse=None, scale=None, causal=False, stream=None):
+    """General attention forward: q [B,Hq,Nq,d], k/v [B,Hkv,Nk,d], any Nq, Nk,
+    optional causal mask (end-aligned). Returns (o, lse)."""
+    import torch
+
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, H, N, d]")
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Hkv, Nk, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, Hkv, Nk, d] with q's B and d")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k and v must be contiguous CUDA tensors")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    if o.shape != q.shape or o.dtype != q.dtype or not o.is_contiguous():
+        raise ValueError("o must be a contiguous tensor like q")
+    if tuple(lse.shape) != (B, Hq, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, Hq, Nq]")
+    if scale is None:
+        scale = d ** -0.5
+    rc = fa2_fwd_ex_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        B, Hq, Hkv, Nq, Nk, d, scale, bool(causal), _dtype_code(q),
+                        _stream_handle(stream, q.device))
+    if rc != FA2_OK:
+        raise FA2Error(rc, "fa2_fwd_ex")
     return o, lse
 
 

@@ -91,6 +91,26 @@ fa2_status fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, flo
                        fa2_dtype dtype, cudaStream_t stream);
 
 /*
+ * General attention forward: query and key lengths may differ and need not be
+ * multiples of 128, with an optional causal mask. This goes beyond the
+ * "Kernel Specification" of "FlashAttention-2 from scratch on Ampere,
+ * Part 1" (equal lengths, non-causal, lengths divisible by the block size),
+ * which excludes these variants; they are built here as extensions.
+ *   q, o : [B, H_q, N_q, d]; k, v : [B, H_kv, N_k, d]; lse : [B, H_q, N_q]
+ *   N_q, N_k : positive, any value
+ *   causal   : 0 or 1. With 1, query row i attends key j iff
+ *              j < min(N_k, i + 1 + N_k - N_q) (the mask aligned to the end of
+ *              the key sequence; j <= i when N_q == N_k). A row with no
+ *              allowed key gets O = 0 and LSE = -inf.
+ * Other arguments, layouts and errors as fa2_fwd_gqa (causal not in {0, 1}
+ * is FA2_ERR_INVALID_ARG; no N % 128 restriction). The non-causal
+ * equal-length case with N % 128 == 0 runs the same kernel as fa2_fwd_gqa.
+ */
+fa2_status fa2_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int H_q, int H_kv, int N_q, int N_k, int d, float scale,
+                      int causal, fa2_dtype dtype, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word. Returns FA2_ERR_TIMEOUT if a kernel since the last check abandoned a
  * wait (its outputs are then undefined), FA2_ERR_CUDA if the stream reported

@@ -71,6 +71,23 @@ def test_host_validation(lib, args, expected):
     assert fa2.fa2_fwd_gqa_ptr(*args) == expected
 
 
+@pytest.mark.parametrize("args,expected", [
+    # (q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, dtype)
+    ((0, A, A, A, A, 1, 1, 1, 100, 70, 128, 0.1, 1, 0), fa2.FA2_ERR_INVALID_ARG),   # NULL q
+    ((A, A, A, A, A + 4, 1, 1, 1, 100, 70, 128, 0.1, 1, 0), fa2.FA2_ERR_INVALID_ARG),  # lse align
+    ((A, A, A, A, A, 1, 1, 1, 0, 70, 128, 0.1, 1, 0), fa2.FA2_ERR_INVALID_ARG),     # Nq = 0
+    ((A, A, A, A, A, 1, 1, 1, 100, 0, 128, 0.1, 1, 0), fa2.FA2_ERR_INVALID_ARG),    # Nk = 0
+    ((A, A, A, A, A, 1, 3, 2, 100, 70, 128, 0.1, 0, 0), fa2.FA2_ERR_INVALID_ARG),   # Hq % Hkv
+    ((A, A, A, A, A, 1, 1, 1, 100, 70, 128, 0.1, 2, 0), fa2.FA2_ERR_INVALID_ARG),   # causal = 2
+    ((A, A, A, A, A, 1, 1, 1, 100, 70, 128, -0.1, 1, 0), fa2.FA2_ERR_INVALID_ARG),  # scale
+    ((A, A, A, A, A, 1, 1, 1, 100, 70, 96, 0.1, 1, 0), fa2.FA2_ERR_UNSUPPORTED),    # d = 96
+    ((A, A, A, A, A, 1, 1, 1, 100, 70, 128, 0.1, 1, 5), fa2.FA2_ERR_INVALID_ARG),   # dtype
+    ((A, A, A, A, A, 4096, 8, 8, 65537, 7, 64, 0.1, 0, 0), fa2.FA2_ERR_UNSUPPORTED),  # rows >= 2^31
+])
+def test_general_entry_host_validation(lib, args, expected):
+    assert fa2.fa2_fwd_ex_ptr(*args) == expected
+
+
 def test_mha_entry_forwards_to_gqa(lib):
     assert fa2.fa2_fwd_ptr(0, A, A, A, A, 1, 1, 128, 128, 0.1, 0) == fa2.FA2_ERR_INVALID_ARG
     assert fa2.fa2_fwd_ptr(A, A, A, A, A, 1, 1, 128, 80, 0.1, 0) == fa2.FA2_ERR_UNSUPPORTED

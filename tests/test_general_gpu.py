@@ -1,0 +1,128 @@
+"""Parity of the general entry point (fa2_fwd_ex: unequal and ragged lengths,
+causal mask) with the fp64 oracle, through the C ABI.
+
+Same tolerances as the plain path: |O_gpu - O_ref| <= 1e-2 + 1e-2*|O_ref|
+(bf16) or 5e-3 + 5e-3*|O_ref| (fp16), |LSE_gpu - LSE_ref| <= 1e-3; rows with
+no allowed key must give exactly O = 0 and LSE = -inf.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def to_dev(x, dtype):
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to("cuda")
+    return t.view(torch.bfloat16 if dtype == gen.BF16 else torch.float16)
+
+
+def inputs(seed, B, Hq, Hkv, Nq, Nk, d, dtype, amp=1.0):
+    q, _, _ = gen.make_qkv(seed, B, Hq, Hkv, Nq, d, dtype, amp)
+    _, k, v = gen.make_qkv(seed + 1, B, Hq, Hkv, Nk, d, dtype, amp)
+    return q, k, v
+
+
+def run_ex(fa2, q, k, v, dtype, scale, causal):
+    import torch
+
+    o, lse = fa2.fa2_fwd_ex(to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype), scale=scale, causal=causal)
+    assert fa2.fa2_check_status(torch.cuda.current_stream().cuda_stream) == fa2.FA2_OK
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def assert_parity(o, lse, o_ref, lse_ref, dtype, what):
+    t = 1e-2 if dtype == gen.BF16 else 5e-3
+    empty = np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(lse), empty), f"{what}: -inf rows differ"
+    assert np.all(o[empty] == 0.0), f"{what}: empty rows must be 0"
+    full = ~empty
+    err = np.abs(o[full] - o_ref[full])
+    bad = err > t + t * np.abs(o_ref[full])
+    assert not bad.any(), f"{what}: {int(bad.sum())} O elements out of tolerance, worst {err.max():.4g}"
+    if full.any():
+        assert np.max(np.abs(lse[full] - lse_ref[full])) <= 1e-3, what
+    assert np.isfinite(o).all()
+
+
+CASES = [
+    # B, Hq, Hkv, Nq, Nk, d, dtype, causal, amp
+    (1, 1, 1, 128, 128, 128, gen.BF16, True, 1.0),
+    (1, 2, 2, 512, 512, 128, gen.BF16, True, 1.0),
+    (2, 4, 2, 384, 384, 64, gen.FP16, True, 1.0),     # odd tile count per head
+    (1, 2, 2, 200, 200, 128, gen.BF16, False, 1.0),   # ragged, non-causal
+    (1, 2, 1, 200, 200, 128, gen.BF16, True, 1.0),    # ragged, causal, grouped heads
+    (1, 2, 2, 100, 300, 128, gen.BF16, False, 1.0),   # Nq < Nk
+    (1, 2, 2, 100, 300, 64, gen.BF16, True, 1.0),     # causal, Nq < Nk
+    (1, 2, 2, 300, 100, 128, gen.BF16, True, 1.0),    # causal, Nq > Nk: empty rows
+    (1, 1, 1, 1, 1, 128, gen.BF16, False, 1.0),
+    (1, 1, 1, 1, 1000, 64, gen.BF16, True, 1.0),
+    (1, 1, 1, 1000, 1, 64, gen.BF16, True, 1.0),      # only the last row attends
+    (1, 2, 2, 1000, 1000, 128, gen.BF16, True, 3.0),  # sharp softmax, causal
+    (2, 4, 4, 129, 257, 128, gen.FP16, False, 1.0),
+    (1, 8, 2, 640, 640, 128, gen.BF16, True, 1.0),    # grouped heads, causal
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,dtype,causal,amp", CASES)
+def test_general_every_element(gpu_lib, B, Hq, Hkv, Nq, Nk, d, dtype, causal, amp):
+    q, k, v = inputs(3000 + Nq + 7 * Nk + d, B, Hq, Hkv, Nq, Nk, d, dtype, amp)
+    scale = 1 / math.sqrt(d)
+    o, lse = run_ex(gpu_lib, q, k, v, dtype, scale, causal)
+    o_ref, lse_ref = oracle.attention_ex(q, k, v, scale, dtype, causal=causal)
+    assert_parity(o, lse, o_ref, lse_ref, dtype, f"B{B} Hq{Hq} Hkv{Hkv} Nq{Nq} Nk{Nk} d{d} causal{causal}")
+
+
+def test_causal_zero_queries_give_prefix_means(gpu_lib):
+    Nq = Nk = 384
+    _, k, v = inputs(3100, 1, 2, 2, Nq, Nk, 128, gen.BF16)
+    q = np.zeros((1, 2, Nq, 128), np.uint16)
+    o, lse = run_ex(gpu_lib, q, k, v, gen.BF16, 128 ** -0.5, True)
+    vd = oracle.decode16(v, gen.BF16)
+    ref = np.cumsum(vd, axis=2) / np.arange(1, Nk + 1)[None, None, :, None]
+    assert_parity(o, lse, ref, np.broadcast_to(np.log(np.arange(1, Nq + 1)), lse.shape), gen.BF16,
+                  "causal Q=0")
+
+
+def test_plain_case_matches_fast_entry_bitwise(gpu_lib):
+    import torch
+
+    q, k, v = gen.make_qkv(3200, 1, 4, 2, 256, 128, gen.BF16)
+    tq, tk, tv = (to_dev(x, gen.BF16) for x in (q, k, v))
+    o1, l1 = gpu_lib.fa2_fwd_gqa(tq, tk, tv, scale=0.1)
+    o2, l2 = gpu_lib.fa2_fwd_ex(tq, tk, tv, scale=0.1, causal=False)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_general_path_on_multiple_of_128_agrees_with_fast_path(gpu_lib):
+    """Causal=False with unequal multiples of 128 runs the general kernel."""
+    q, k, v = inputs(3300, 1, 2, 2, 256, 384, 128, gen.BF16)
+    o, lse = run_ex(gpu_lib, q, k, v, gen.BF16, 0.09, False)
+    o_ref, lse_ref = oracle.attention_ex(q, k, v, 0.09, gen.BF16, causal=False)
+    assert_parity(o, lse, o_ref, lse_ref, gen.BF16, "general 256x384")
+
+
+def test_causal_full_size_sampled_rows(gpu_lib):
+    """B=4, H=16, N=4096, d=128, causal: sampled rows against the oracle."""
+    import torch
+
+    B, H, N, d = 4, 16, 4096, 128
+    q, k, v = gen.make_qkv(3400, B, H, H, N, d, gen.BF16)
+    o, lse = gpu_lib.fa2_fwd_ex(to_dev(q, gen.BF16), to_dev(k, gen.BF16), to_dev(v, gen.BF16),
+                                scale=d ** -0.5, causal=True)
+    assert gpu_lib.fa2_check_status(torch.cuda.current_stream().cuda_stream) == gpu_lib.FA2_OK
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([rng.integers(0, B * H * N, 160),
+                                     [0, 1, 127, 128, N - 1, N, 5 * N + 4095, B * H * N - 1]]))
+    idx = torch.from_numpy(rows).cuda()
+    o_s = o.reshape(-1, d).index_select(0, idx).float().cpu().numpy().astype(np.float64)
+    l_s = lse.reshape(-1).index_select(0, idx).cpu().numpy().astype(np.float64)
+    o_ref, lse_ref = oracle.attention_ex(q, k, v, d ** -0.5, gen.BF16, causal=True, rows=rows)
+    assert_parity(o_s, l_s, o_ref, lse_ref, gen.BF16, "causal B4 H16 N4096")
+    assert bool(torch.isfinite(o.float()).all())
