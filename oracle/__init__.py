@@ -58,6 +58,12 @@ def _load():
                                                  ctypes.c_double, ctypes.c_int, p, i64, p, p,
                                                  ctypes.c_int]
         lib.oracle_attention_ex_rows.restype = ctypes.c_int
+        lib.oracle_attention_bwd.argtypes = [p, p, p, p, ctypes.c_int, i64, i64, i64, i64, i64,
+                                             ctypes.c_double, ctypes.c_int, p, p, p]
+        lib.oracle_attention_bwd.restype = ctypes.c_int
+        lib.oracle_attention_f64.argtypes = [p, p, p, i64, i64, i64, i64, i64, ctypes.c_double,
+                                             ctypes.c_int, p]
+        lib.oracle_attention_f64.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -143,6 +149,40 @@ def attention_ex(q, k, v, scale: float, dtype: int, causal: bool = False, rows=N
     if rows is None:
         return o.reshape(B, Hq, Nq, d), lse.reshape(B, Hq, Nq)
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, scale: float, dtype: int, causal: bool = False):
+    """Gradients (dq, dk, dv) of attention for upstream gradient dout, fp64.
+
+    q, dout: uint16 [B, Hq, N, d]; k, v: uint16 [B, Hkv, N, d]. With grouped
+    heads dk and dv sum over the query heads of each KV head.
+    """
+    q, k, v, dout = _u16(q), _u16(k), _u16(v), _u16(dout)
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, N, d) or v.shape != k.shape or dout.shape != q.shape:
+        raise ValueError("shape mismatch")
+    dq = np.empty(q.shape, dtype=np.float64)
+    dk = np.empty(k.shape, dtype=np.float64)
+    dv = np.empty(v.shape, dtype=np.float64)
+    rc = _load().oracle_attention_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data,
+                                      dtype, B, Hq, Hkv, N, d, float(scale), int(bool(causal)),
+                                      dq.ctypes.data, dk.ctypes.data, dv.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle rejected the sizes")
+    return dq, dk, dv
+
+
+def attention_f64(q, k, v, scale: float, causal: bool = False) -> np.ndarray:
+    """Forward on float64 inputs (q [B,Hq,N,d], k/v [B,Hkv,N,d]); returns o."""
+    q, k, v = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v))
+    B, Hq, N, d = q.shape
+    o = np.empty(q.shape, dtype=np.float64)
+    rc = _load().oracle_attention_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data, B, Hq, k.shape[1], N,
+                                      d, float(scale), int(bool(causal)), o.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle rejected the sizes")
+    return o
 
 
 def softmax_row(q, k, scale: float, dtype: int, row: int) -> np.ndarray:

@@ -257,6 +257,140 @@ int oracle_attention_ex_rows(const uint16_t* q, const uint16_t* k, const uint16_
     return 0;
 }
 
+/*
+ * Backward pass of attention in fp64, by its definition (the gradient of the
+ * forward above with respect to q, k and v for an upstream gradient dO):
+ *     S = scale Q K^T (causal: keys j >= kend(i) excluded), P = softmax(S),
+ *     O = P V, D_i = sum_t dO_it O_it, dP = dO V^T,
+ *     dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO.
+ * With grouped heads, dK and dV of a KV head sum over its query heads.
+ * Inputs q, k, v, dout are 16-bit patterns ([B,Hq,N,d], [B,Hkv,N,d],
+ * [B,Hkv,N,d], [B,Hq,N,d]); outputs are doubles of the same shapes as q, k, v.
+ * Equal query/key lengths N. Rows with no allowed key contribute nothing.
+ */
+int oracle_attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
+                         int dtype, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
+                         double scale, int causal, double* dq, double* dk, double* dv) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || Hq % Hkv) return -1;
+    const int64_t G = Hq / Hkv;
+    for (int64_t i = 0; i < B * Hkv * N * d; ++i) {
+        dk[i] = 0.0;
+        dv[i] = 0.0;
+    }
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t hk = 0; hk < Hkv; ++hk) {
+            const uint16_t* kp = k + (b * Hkv + hk) * N * d;
+            const uint16_t* vp = v + (b * Hkv + hk) * N * d;
+            double* dkp = dk + (b * Hkv + hk) * N * d;
+            double* dvp = dv + (b * Hkv + hk) * N * d;
+            for (int64_t g = 0; g < G; ++g) {
+                const int64_t h = hk * G + g;
+                const uint16_t* qp = q + (b * Hq + h) * N * d;
+                const uint16_t* dop = dout + (b * Hq + h) * N * d;
+                double* dqp = dq + (b * Hq + h) * N * d;
+#pragma omp parallel
+                {
+                    double* P = (double*)malloc(sizeof(double) * (size_t)N);
+                    double* dS = (double*)malloc(sizeof(double) * (size_t)N);
+                    double* o = (double*)malloc(sizeof(double) * (size_t)d);
+                    /* per query row: P, D, dS and dQ; dK and dV rows are
+                       accumulated under a lock-free reduction per thread */
+                    double* dkl = (double*)calloc((size_t)(N * d), sizeof(double));
+                    double* dvl = (double*)calloc((size_t)(N * d), sizeof(double));
+#pragma omp for schedule(dynamic, 4)
+                    for (int64_t i = 0; i < N; ++i) {
+                        const int64_t kend = causal ? (i + 1 < N ? i + 1 : N) : N;
+                        double m = -INFINITY;
+                        for (int64_t j = 0; j < kend; ++j) {
+                            double dot = 0.0;
+                            for (int64_t t = 0; t < d; ++t)
+                                dot += decode16(qp[i * d + t], dtype) * decode16(kp[j * d + t], dtype);
+                            P[j] = scale * dot;
+                            if (P[j] > m) m = P[j];
+                        }
+                        double l = 0.0;
+                        for (int64_t j = 0; j < kend; ++j) {
+                            P[j] = exp(P[j] - m);
+                            l += P[j];
+                        }
+                        for (int64_t t = 0; t < d; ++t) o[t] = 0.0;
+                        for (int64_t j = 0; j < kend; ++j) {
+                            P[j] /= l;
+                            for (int64_t t = 0; t < d; ++t) o[t] += P[j] * decode16(vp[j * d + t], dtype);
+                        }
+                        double Di = 0.0;
+                        for (int64_t t = 0; t < d; ++t) Di += decode16(dop[i * d + t], dtype) * o[t];
+                        for (int64_t j = 0; j < kend; ++j) {
+                            double dp = 0.0;
+                            for (int64_t t = 0; t < d; ++t)
+                                dp += decode16(dop[i * d + t], dtype) * decode16(vp[j * d + t], dtype);
+                            dS[j] = P[j] * (dp - Di);
+                        }
+                        for (int64_t t = 0; t < d; ++t) {
+                            double acc = 0.0;
+                            for (int64_t j = 0; j < kend; ++j) acc += dS[j] * decode16(kp[j * d + t], dtype);
+                            dqp[i * d + t] = scale * acc;
+                        }
+                        for (int64_t j = 0; j < kend; ++j)
+                            for (int64_t t = 0; t < d; ++t) {
+                                dkl[j * d + t] += scale * dS[j] * decode16(qp[i * d + t], dtype);
+                                dvl[j * d + t] += P[j] * decode16(dop[i * d + t], dtype);
+                            }
+                    }
+#pragma omp critical
+                    {
+                        for (int64_t x = 0; x < N * d; ++x) {
+                            dkp[x] += dkl[x];
+                            dvp[x] += dvl[x];
+                        }
+                    }
+                    free(P);
+                    free(dS);
+                    free(o);
+                    free(dkl);
+                    free(dvl);
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Forward on double inputs (no 16-bit decoding), all rows, for the
+ * finite-difference pin of the backward: out o [B,Hq,N,d].
+ */
+int oracle_attention_f64(const double* q, const double* k, const double* v, int64_t B, int64_t Hq,
+                         int64_t Hkv, int64_t N, int64_t d, double scale, int causal, double* o) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || Hq % Hkv) return -1;
+    const int64_t G = Hq / Hkv;
+    double* s = (double*)malloc(sizeof(double) * (size_t)N);
+    for (int64_t r = 0; r < B * Hq * N; ++r) {
+        const int64_t i = r % N, h = (r / N) % Hq, b = r / (N * Hq), hk = h / G;
+        const double* qp = q + r * d;
+        const double* kp = k + (b * Hkv + hk) * N * d;
+        const double* vp = v + (b * Hkv + hk) * N * d;
+        const int64_t kend = causal ? (i + 1 < N ? i + 1 : N) : N;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < kend; ++j) {
+            double dot = 0.0;
+            for (int64_t t = 0; t < d; ++t) dot += qp[t] * kp[j * d + t];
+            s[j] = scale * dot;
+            if (s[j] > m) m = s[j];
+        }
+        double l = 0.0;
+        for (int64_t t = 0; t < d; ++t) o[r * d + t] = 0.0;
+        for (int64_t j = 0; j < kend; ++j) {
+            const double p = exp(s[j] - m);
+            l += p;
+            for (int64_t t = 0; t < d; ++t) o[r * d + t] += p * vp[j * d + t];
+        }
+        for (int64_t t = 0; t < d; ++t) o[r * d + t] /= l;
+    }
+    free(s);
+    return 0;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -353,3 +353,73 @@ def test_generalised_library_crosscheck(nq, nk, causal):
     ref_o = torch.nan_to_num(torch.softmax(s, dim=-1)) @ vd
     np.testing.assert_allclose(o, ref_o.numpy(), rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- backward
+
+def bwd_inputs(seed, B, Hq, Hkv, N, d, dtype=gen.BF16):
+    q, k, v = rand_inputs(seed, B, Hq, Hkv, N, d, dtype)
+    do, _, _ = rand_inputs(seed + 1, B, Hq, Hkv, N, d, dtype)
+    return q, k, v, do
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_finite_differences(causal):
+    B, Hq, Hkv, N, d, scale = 1, 2, 1, 12, 8, 0.35
+    q, k, v, do = bwd_inputs(50, B, Hq, Hkv, N, d)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, scale, gen.BF16, causal=causal)
+    qd, kd, vd, dod = (oracle.decode16(x, gen.BF16) for x in (q, k, v, do))
+
+    def loss(qq, kk, vv):
+        return float(np.sum(dod * oracle.attention_f64(qq, kk, vv, scale, causal)))
+
+    rng = np.random.default_rng(1)
+    eps = 1e-6
+    for name, x, g in (("q", qd, dq), ("k", kd, dk), ("v", vd, dv)):
+        for _ in range(6):
+            idx = tuple(rng.integers(0, s) for s in x.shape)
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = {"q": (xp, kd, vd), "k": (qd, xp, vd), "v": (qd, kd, xp)}[name]
+            args_m = {"q": (xm, kd, vd), "k": (qd, xm, vd), "v": (qd, kd, xm)}[name]
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            assert abs(fd - g[idx]) <= 1e-6 * (1 + abs(fd)), (name, idx, fd, g[idx])
+
+
+@pytest.mark.parametrize("causal,Hq,Hkv", [(False, 2, 2), (True, 4, 2), (True, 2, 1)])
+def test_backward_library_crosscheck(causal, Hq, Hkv):
+    torch = pytest.importorskip("torch")
+    B, N, d, scale = 2, 40, 16, 0.25
+    q, k, v, do = bwd_inputs(51, B, Hq, Hkv, N, d)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, scale, gen.BF16, causal=causal)
+    qt, kt, vt = (torch.from_numpy(oracle.decode16(x, gen.BF16)).requires_grad_() for x in (q, k, v))
+    dot = torch.from_numpy(oracle.decode16(do, gen.BF16))
+    G = Hq // Hkv
+    s = scale * torch.einsum("bhid,bhjd->bhij", qt, kt.repeat_interleave(G, 1))
+    if causal:
+        s = s.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
+    o = torch.softmax(s, -1) @ vt.repeat_interleave(G, 1)
+    o.backward(dot)
+    np.testing.assert_allclose(dq, qt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk, kt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, vt.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_backward_closed_forms():
+    B, Hq, Hkv, N, d = 1, 2, 2, 30, 8
+    q, k, _, do = bwd_inputs(52, B, Hq, Hkv, N, d)
+    # constant values: O = v for every row, dP_ij = dO_i . v = D_i, so dS = 0
+    v = np.full((B, Hkv, N, d), 0x3FC0, np.uint16)  # bf16 1.5
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, 0.3, gen.BF16)
+    assert np.max(np.abs(dq)) < 1e-12 and np.max(np.abs(dk)) < 1e-12
+    # each row of dS sums to zero, so sum_j dK_j = scale * sum_i q_i * 0 = 0
+    _, _, v2 = rand_inputs(53, B, Hq, Hkv, N, d)
+    for causal in (False, True):
+        _, dk2, dv2 = oracle.attention_bwd(q, k, v2, do, 0.3, gen.BF16, causal=causal)
+        np.testing.assert_allclose(dk2.sum(axis=2), 0.0, atol=1e-12)
+        # sum_j dV_j = sum_i dO_i (rows of P sum to one)
+        np.testing.assert_allclose(dv2.sum(axis=2), oracle.decode16(do, gen.BF16).sum(axis=2), atol=1e-11)
+    # zero upstream gradient: zero gradients
+    dq0, dk0, dv0 = oracle.attention_bwd(q, k, v2, np.zeros_like(do), 0.3, gen.BF16)
+    assert not dq0.any() and not dk0.any() and not dv0.any()
