@@ -1,0 +1,496 @@
+// Backward pass of the attention forward in fa2_fwd_sm103.cu (included by
+// it, so both share the status word and the PTX wrappers).
+//
+// The forward pages exclude the backward pass ("FlashAttention-2 from
+// scratch on Ampere, Part 1", Kernel Specification: forward pass only); the
+// forward keeps the per-row logsumexp so the backward can recompute
+// P = exp(S - LSE) tile by tile instead of storing it. With D = rowsum(dO o O):
+//     dP = dO V^T, dS = P o (dP - D), dV = P^T dO, dK = scale dS^T Q,
+//     dQ = scale dS K.
+// Three kernels, all on one stream, none using atomics:
+//   fa2_bwd_delta_kernel  D for every query row (memory bound)
+//   fa2_bwd_dkdv_kernel   one CTA per 128-key tile: S^T = K Q^T and
+//                         dP^T = V dO^T (keys in TMEM lanes), P^T and dS^T
+//                         formed by the elementwise warps and written back
+//                         to TMEM as 16-bit, then dV += P^T dO and
+//                         dK += dS^T Q as MMAs with A from TMEM; dK and dV
+//                         accumulate over every query tile (and every query
+//                         head of a KV head) in TMEM
+//   fa2_bwd_dq_kernel     one CTA per 128-query tile: S = Q K^T,
+//                         dP = dO V^T, dS in TMEM, dQ += dS K
+// Warps 0-3 elementwise (thread = TMEM lane), warp 4 TMA producer, warp 5
+// TMEM allocator and MMA issuer. TMEM: S | dP | two d-column accumulators.
+#pragma once
+
+namespace fa2 {
+namespace bwd {
+
+constexpr int kThreads = 192;
+constexpr int kLoadWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kStages = 2;
+
+struct Params {
+    const void* o;        // forward output [rows, D]
+    const float* lse;     // forward logsumexp [rows]
+    const void* dout;     // upstream gradient [rows, D]
+    float* delta;         // D = rowsum(dO o O) [rows]
+    void* dq;             // [B*Hq*N, D]
+    void* dk;             // [B*Hkv*N, D]
+    void* dv;             // [B*Hkv*N, D]
+    long long wait_limit_ns;
+    int n_tiles;          // N / 128
+    int hq, group;        // Hq, Hq / Hkv
+    int causal;
+    float scale;          // softmax scale
+    float scale_log2;     // scale * log2(e)
+};
+
+// Shared memory (1024-aligned). dK/dV kernel: K, V tiles once, then a ring of
+// stages each holding one Q tile, one dO tile and their 128 LSE and D values.
+// dQ kernel: Q and dO tiles once, then a ring of stages each holding K and V.
+template <int D>
+struct BwdLayout {
+    static constexpr int kBlkBytes = 128 * 128;
+    static constexpr int kTileBytes = 128 * D * 2;
+    static constexpr int kFixedOff = 0;                          // two fixed tiles
+    static constexpr int kRingOff = 2 * kTileBytes;
+    static constexpr int kStageBytes = 2 * kTileBytes + 1024;    // two tiles + LSE + D
+    static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
+    // fixed_full, stage_full[S], stage_empty[S], s_full, p_full, acc_full
+    static constexpr int kNumBars = 1 + 2 * kStages + 3;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
+};
+
+template <int D>
+struct BwdBars {
+    uint32_t base;
+    __device__ uint32_t fixed_full() const { return base; }
+    __device__ uint32_t stage_full(int s) const { return base + 8 * (1 + s); }
+    __device__ uint32_t stage_empty(int s) const { return base + 8 * (1 + kStages + s); }
+    __device__ uint32_t s_full() const { return base + 8 * (1 + 2 * kStages); }
+    __device__ uint32_t p_full() const { return base + 8 * (2 + 2 * kStages); }
+    __device__ uint32_t acc_full() const { return base + 8 * (3 + 2 * kStages); }
+};
+
+// ---------------------------------------------------------------- D = rowsum(dO o O)
+
+// 16 lanes per row, each one 16-byte chunk of dO and O (d = 128) or one
+// 8-byte... the row is split into 16 equal 16-bit runs.
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(256) fa2_bwd_delta_kernel(const void* o, const void* dout, float* delta,
+                                                            long long rows) {
+    constexpr int kPer = D / 16;  // 16-bit values per lane
+    const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / 16;
+    const int part = threadIdx.x & 15;
+    float acc = 0.0f;
+    if (row < rows) {
+        const uint16_t* op = static_cast<const uint16_t*>(o) + row * D + part * kPer;
+        const uint16_t* dp = static_cast<const uint16_t*>(dout) + row * D + part * kPer;
+        uint32_t ov[kPer / 2], dv[kPer / 2];
+        if constexpr (kPer == 8) {
+            const uint4 a = *reinterpret_cast<const uint4*>(op);
+            const uint4 b = *reinterpret_cast<const uint4*>(dp);
+            ov[0] = a.x; ov[1] = a.y; ov[2] = a.z; ov[3] = a.w;
+            dv[0] = b.x; dv[1] = b.y; dv[2] = b.z; dv[3] = b.w;
+        } else {
+            const uint2 a = *reinterpret_cast<const uint2*>(op);
+            const uint2 b = *reinterpret_cast<const uint2*>(dp);
+            ov[0] = a.x; ov[1] = a.y;
+            dv[0] = b.x; dv[1] = b.y;
+        }
+#pragma unroll
+        for (int i = 0; i < kPer / 2; ++i) {
+            float o0, o1, d0, d1;
+            ptx::unpack2<kBf16>(ov[i], o0, o1);
+            ptx::unpack2<kBf16>(dv[i], d0, d1);
+            acc = fmaf(o0, d0, acc);
+            acc = fmaf(o1, d1, acc);
+        }
+    }
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows && part == 0) delta[row] = acc;
+}
+
+// ---------------------------------------------------------------- shared pieces
+
+__device__ __forceinline__ void store_row_16(void* base, long long row, int d, int col0, const uint32_t (&h)[16]) {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + row * d + col0);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+}
+
+// Write a d-column fp32 TMEM accumulator row (times `mul`) as 16-bit.
+template <int D, bool kBf16>
+__device__ __forceinline__ void store_acc_row(uint32_t row_addr, uint32_t col, float mul, void* out,
+                                              long long grow) {
+#pragma unroll 1
+    for (int cc = 0; cc < D; cc += 32) {
+        uint32_t a[32];
+        ptx::tmem_ld32(row_addr + col + cc, a);
+        ptx::tmem_wait_ld();
+        uint32_t h[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            h[i] = ptx::pack2<kBf16>(__uint_as_float(a[2 * i]) * mul, __uint_as_float(a[2 * i + 1]) * mul);
+        store_row_16(out, grow, D, cc, h);
+    }
+}
+
+// ---------------------------------------------------------------- dK, dV
+
+// Step n of a dK/dV CTA: query head g (of the KV head's group), query tile i.
+__device__ __forceinline__ void dkdv_step(const Params& p, int kt, int n, int& g, int& i) {
+    const int first = p.causal ? kt : 0;
+    const int per = p.n_tiles - first;
+    g = n / per;
+    i = first + n % per;
+}
+
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa2_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                        const Params p) {
+    using L = BwdLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = ptx::smem_addr(smem);
+    const BwdBars<D> bars{sbase + L::kBarOff};
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    const int kt = blockIdx.x;                 // key tile
+    const int kvh = blockIdx.y;                // b * Hkv + kv head
+    const int b = kvh / (p.hq / p.group);
+    const int hk = kvh - b * (p.hq / p.group);
+    const int steps = p.group * (p.n_tiles - (p.causal ? kt : 0));
+    const long long kv_row0 = static_cast<long long>(kvh) * p.n_tiles * 128 + kt * 128;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bars.fixed_full(), 1);
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(bars.stage_full(s), 1);
+            ptx::mbar_init(bars.stage_empty(s), 1);
+        }
+        ptx::mbar_init(bars.s_full(), 1);
+        ptx::mbar_init(bars.p_full(), 128);
+        ptx::mbar_init(bars.acc_full(), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Waiter w{abort_flag, p.wait_limit_ns};
+    auto q_row = [&](int g, int i) {
+        return (static_cast<long long>(b) * p.hq + hk * p.group + g) * p.n_tiles * 128 + i * 128;
+    };
+
+    if (warp == kLoadWarp) {
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(bars.fixed_full(), 2 * L::kTileBytes);
+#pragma unroll
+            for (int blk = 0; blk < D / 64; ++blk) {
+                ptx::tma_load_2d(sbase + L::kFixedOff + blk * L::kBlkBytes, &tmK, blk * 64,
+                                 static_cast<int>(kv_row0), bars.fixed_full());
+                ptx::tma_load_2d(sbase + L::kFixedOff + L::kTileBytes + blk * L::kBlkBytes, &tmV, blk * 64,
+                                 static_cast<int>(kv_row0), bars.fixed_full());
+            }
+            int n = 0;
+            for (; n < steps; ++n) {
+                const int s = n % kStages;
+                if (!w.wait(bars.stage_empty(s), ((n / kStages) & 1) ^ 1, kSiteKvEmpty)) break;
+                int g, i;
+                dkdv_step(p, kt, n, g, i);
+                const long long qr = q_row(g, i);
+                const uint32_t st = sbase + L::kRingOff + s * L::kStageBytes;
+                ptx::mbar_arrive_expect_tx(bars.stage_full(s), 2 * L::kTileBytes + 1024);
+#pragma unroll
+                for (int blk = 0; blk < D / 64; ++blk) {
+                    ptx::tma_load_2d(st + blk * L::kBlkBytes, &tmQ, blk * 64, static_cast<int>(qr), bars.stage_full(s));
+                    ptx::tma_load_2d(st + L::kTileBytes + blk * L::kBlkBytes, &tmDO, blk * 64, static_cast<int>(qr),
+                                     bars.stage_full(s));
+                }
+                ptx::bulk_load(st + 2 * L::kTileBytes, p.lse + qr, 512, bars.stage_full(s));
+                ptx::bulk_load(st + 2 * L::kTileBytes + 512, p.delta + qr, 512, bars.stage_full(s));
+            }
+            if (n < steps) {
+                const int first = n > kStages ? n - kStages : 0;
+                for (int r = first; r < n; ++r) w.drain(bars.stage_full(r % kStages), (r / kStages) & 1);
+            }
+            w.drain(bars.fixed_full(), 0);
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        constexpr uint32_t kAB = kBf16 ? 1u : 0u;
+        constexpr uint32_t kIdT = ptx::idesc_f16(kAB, 0, 0, 128, 128);  // S^T, dP^T: both K-major
+        constexpr uint32_t kIdA = ptx::idesc_f16(kAB, 0, 1, 128, D);    // dV, dK: B MN-major
+        auto wait_u = [&](uint32_t bar, uint32_t parity, int site) {
+            return __shfl_sync(0xffffffffu, w.wait(bar, parity, site) ? 1 : 0, 0) != 0;
+        };
+        bool ok = wait_u(bars.fixed_full(), 0, kSiteQFull);
+        const uint64_t kdesc = ptx::desc_sw128(sbase + L::kFixedOff, 16, 1024);
+        const uint64_t vdesc = ptx::desc_sw128(sbase + L::kFixedOff + L::kTileBytes, 16, 1024);
+        for (int n = 0; n < steps && ok; ++n) {
+            const int s = n % kStages;
+            if (!(ok = wait_u(bars.stage_full(s), (n / kStages) & 1, kSiteKvFull))) break;
+            ptx::tc_fence_after();
+            const uint32_t st = sbase + L::kRingOff + s * L::kStageBytes;
+            qk_kloop<D>(tmem + L::kColS, kdesc, ptx::desc_sw128(st, 16, 1024), kIdT);
+            qk_kloop<D>(tmem + L::kColDP, vdesc, ptx::desc_sw128(st + L::kTileBytes, 16, 1024), kIdT);
+            ptx::tc_commit_elect(bars.s_full());
+            if (!(ok = wait_u(bars.p_full(), n & 1, kSitePFull))) break;
+            ptx::tc_fence_after();
+            // dV += P^T dO, dK += dS^T Q (P^T, dS^T 16-bit in the first half
+            // of their fp32 columns; dO and Q as MN-major B operands)
+            pv_kloop(tmem + L::kColAcc0, tmem + L::kColS, ptx::desc_sw128(st + L::kTileBytes, L::kBlkBytes, 1024),
+                     kIdA, n > 0 ? 1u : 0u);
+            pv_kloop(tmem + L::kColAcc1, tmem + L::kColDP, ptx::desc_sw128(st, L::kBlkBytes, 1024), kIdA,
+                     n > 0 ? 1u : 0u);
+            ptx::tc_commit_elect(bars.stage_empty(s));
+        }
+        ptx::tc_commit_elect(bars.acc_full());
+        w.drain(bars.acc_full(), 0);
+        __syncwarp();
+    } else {
+        // elementwise: thread = key row of the tile = TMEM lane
+        const int row = threadIdx.x;
+        const uint32_t row_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+        const float c = p.scale_log2;
+        constexpr float kLog2e = 1.4426950408889634f;
+        bool ok = true;
+        for (int n = 0; n < steps; ++n) {
+            const int s = n % kStages;
+            ok = w.wait(bars.s_full(), n & 1, kSiteSFull);
+            if (ok) ok = w.wait(bars.stage_full(s), (n / kStages) & 1, kSiteKvFull);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            int g, i;
+            dkdv_step(p, kt, n, g, i);
+            const bool diag = p.causal && i == kt;  // query q may see key k only if q >= k
+            const float* lse = reinterpret_cast<const float*>(smem + L::kRingOff + s * L::kStageBytes +
+                                                              2 * L::kTileBytes);
+            const float* dl = lse + 128;
+#pragma unroll 1
+            for (int cc = 0; cc < 128; cc += 32) {
+                uint32_t sv[32], dp[32];
+                ptx::tmem_ld32(row_addr + L::kColS + cc, sv);
+                ptx::tmem_ld32(row_addr + L::kColDP + cc, dp);
+                ptx::tmem_wait_ld();
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    float pv[2], ds[2];
+#pragma unroll
+                    for (int y = 0; y < 2; ++y) {
+                        const int qc = cc + 2 * x + y;
+                        float pp = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * x + y]), c, -lse[qc] * kLog2e));
+                        if (diag && qc < row) pp = 0.0f;
+                        pv[y] = pp;
+                        ds[y] = pp * (__uint_as_float(dp[2 * x + y]) - dl[qc]);
+                    }
+                    pk[x] = ptx::pack2<kBf16>(pv[0], pv[1]);
+                    dk[x] = ptx::pack2<kBf16>(ds[0], ds[1]);
+                }
+                ptx::tmem_st16(row_addr + L::kColS + cc / 2, pk);
+                ptx::tmem_st16(row_addr + L::kColDP + cc / 2, dk);
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bars.p_full());
+        }
+        if (ok) ok = w.wait(bars.acc_full(), 0, kSiteOFull);
+        if (__all_sync(0xffffffffu, ok)) {
+            ptx::tc_fence_after();
+            const long long grow = kv_row0 + row;
+            store_acc_row<D, kBf16>(row_addr, L::kColAcc0, 1.0f, p.dv, grow);
+            store_acc_row<D, kBf16>(row_addr, L::kColAcc1, p.scale, p.dk, grow);
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------- dQ
+
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa2_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                      const Params p) {
+    using L = BwdLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = ptx::smem_addr(smem);
+    const BwdBars<D> bars{sbase + L::kBarOff};
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    const int qt = blockIdx.x;                 // query tile
+    const int qh = blockIdx.y;                 // b * Hq + query head
+    const int b = qh / p.hq;
+    const int hkv = (qh - b * p.hq) / p.group;
+    const long long q_row0 = static_cast<long long>(qh) * p.n_tiles * 128 + qt * 128;
+    const long long kv_base = (static_cast<long long>(b) * (p.hq / p.group) + hkv) * p.n_tiles * 128;
+    const int steps = p.causal ? qt + 1 : p.n_tiles;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bars.fixed_full(), 1);
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(bars.stage_full(s), 1);
+            ptx::mbar_init(bars.stage_empty(s), 1);
+        }
+        ptx::mbar_init(bars.s_full(), 1);
+        ptx::mbar_init(bars.p_full(), 128);
+        ptx::mbar_init(bars.acc_full(), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Waiter w{abort_flag, p.wait_limit_ns};
+
+    if (warp == kLoadWarp) {
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(bars.fixed_full(), 2 * L::kTileBytes);
+#pragma unroll
+            for (int blk = 0; blk < D / 64; ++blk) {
+                ptx::tma_load_2d(sbase + L::kFixedOff + blk * L::kBlkBytes, &tmQ, blk * 64,
+                                 static_cast<int>(q_row0), bars.fixed_full());
+                ptx::tma_load_2d(sbase + L::kFixedOff + L::kTileBytes + blk * L::kBlkBytes, &tmDO, blk * 64,
+                                 static_cast<int>(q_row0), bars.fixed_full());
+            }
+            int n = 0;
+            for (; n < steps; ++n) {
+                const int s = n % kStages;
+                if (!w.wait(bars.stage_empty(s), ((n / kStages) & 1) ^ 1, kSiteKvEmpty)) break;
+                const long long kr = kv_base + n * 128;
+                const uint32_t st = sbase + L::kRingOff + s * L::kStageBytes;
+                ptx::mbar_arrive_expect_tx(bars.stage_full(s), 2 * L::kTileBytes);
+#pragma unroll
+                for (int blk = 0; blk < D / 64; ++blk) {
+                    ptx::tma_load_2d(st + blk * L::kBlkBytes, &tmK, blk * 64, static_cast<int>(kr), bars.stage_full(s));
+                    ptx::tma_load_2d(st + L::kTileBytes + blk * L::kBlkBytes, &tmV, blk * 64, static_cast<int>(kr),
+                                     bars.stage_full(s));
+                }
+            }
+            if (n < steps) {
+                const int first = n > kStages ? n - kStages : 0;
+                for (int r = first; r < n; ++r) w.drain(bars.stage_full(r % kStages), (r / kStages) & 1);
+            }
+            w.drain(bars.fixed_full(), 0);
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        constexpr uint32_t kAB = kBf16 ? 1u : 0u;
+        constexpr uint32_t kIdS = ptx::idesc_f16(kAB, 0, 0, 128, 128);  // S, dP: both K-major
+        constexpr uint32_t kIdQ = ptx::idesc_f16(kAB, 0, 1, 128, D);    // dQ += dS K: K MN-major
+        auto wait_u = [&](uint32_t bar, uint32_t parity, int site) {
+            return __shfl_sync(0xffffffffu, w.wait(bar, parity, site) ? 1 : 0, 0) != 0;
+        };
+        bool ok = wait_u(bars.fixed_full(), 0, kSiteQFull);
+        const uint64_t qdesc = ptx::desc_sw128(sbase + L::kFixedOff, 16, 1024);
+        const uint64_t dodesc = ptx::desc_sw128(sbase + L::kFixedOff + L::kTileBytes, 16, 1024);
+        for (int n = 0; n < steps && ok; ++n) {
+            const int s = n % kStages;
+            if (!(ok = wait_u(bars.stage_full(s), (n / kStages) & 1, kSiteKvFull))) break;
+            ptx::tc_fence_after();
+            const uint32_t st = sbase + L::kRingOff + s * L::kStageBytes;
+            qk_kloop<D>(tmem + L::kColS, qdesc, ptx::desc_sw128(st, 16, 1024), kIdS);
+            qk_kloop<D>(tmem + L::kColDP, dodesc, ptx::desc_sw128(st + L::kTileBytes, 16, 1024), kIdS);
+            ptx::tc_commit_elect(bars.s_full());
+            if (!(ok = wait_u(bars.p_full(), n & 1, kSitePFull))) break;
+            ptx::tc_fence_after();
+            pv_kloop(tmem + L::kColAcc0, tmem + L::kColDP, ptx::desc_sw128(st, L::kBlkBytes, 1024), kIdQ,
+                     n > 0 ? 1u : 0u);
+            ptx::tc_commit_elect(bars.stage_empty(s));
+        }
+        ptx::tc_commit_elect(bars.acc_full());
+        w.drain(bars.acc_full(), 0);
+        __syncwarp();
+    } else {
+        // elementwise: thread = query row of the tile = TMEM lane
+        const int row = threadIdx.x;
+        const uint32_t row_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+        const float c = p.scale_log2;
+        const float lse2 = p.lse[q_row0 + row] * 1.4426950408889634f;
+        const float dl = p.delta[q_row0 + row];
+        bool ok = true;
+        for (int n = 0; n < steps; ++n) {
+            ok = w.wait(bars.s_full(), n & 1, kSiteSFull);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const bool diag = p.causal && n == qt;  // key k visible to query q only if k <= q
+#pragma unroll 1
+            for (int cc = 0; cc < 128; cc += 32) {
+                uint32_t sv[32], dp[32];
+                ptx::tmem_ld32(row_addr + L::kColS + cc, sv);
+                ptx::tmem_ld32(row_addr + L::kColDP + cc, dp);
+                ptx::tmem_wait_ld();
+                uint32_t dk[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    float ds[2];
+#pragma unroll
+                    for (int y = 0; y < 2; ++y) {
+                        const int kc = cc + 2 * x + y;
+                        float pp = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * x + y]), c, -lse2));
+                        if (diag && kc > row) pp = 0.0f;
+                        ds[y] = pp * (__uint_as_float(dp[2 * x + y]) - dl);
+                    }
+                    dk[x] = ptx::pack2<kBf16>(ds[0], ds[1]);
+                }
+                ptx::tmem_st16(row_addr + L::kColDP + cc / 2, dk);
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bars.p_full());
+        }
+        if (ok) ok = w.wait(bars.acc_full(), 0, kSiteOFull);
+        if (__all_sync(0xffffffffu, ok)) {
+            ptx::tc_fence_after();
+            store_acc_row<D, kBf16>(row_addr, L::kColAcc0, p.scale, p.dq, q_row0 + row);
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace bwd
+}  // namespace fa2

@@ -864,6 +864,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace fa2
 
+#include "fa2_bwd_sm103.cuh"
+
 // ==================================================================== host
 
 namespace {
@@ -881,7 +883,7 @@ struct DeviceState {
     bool probed = false;
     bool supported = false;
     int sm_count = 0;
-    bool smem_set[8] = {false, false, false, false, false, false, false, false};
+    bool smem_set[12] = {};
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -1076,6 +1078,76 @@ fa2_status fa2_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
                   : launch<128, false, true>(dev, mq, mk, mv, p, grid, stream);
     return bf ? launch<64, true, true>(dev, mq, mk, mv, p, grid, stream)
               : launch<64, false, true>(dev, mq, mk, mv, p, grid, stream);
+}
+
+fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H_q, int H_kv,
+                   int N, int d, float scale, int causal, fa2_dtype dtype, cudaStream_t stream) {
+    const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv, delta};
+    for (const void* x : ptrs)
+        if (!x || !aligned16(x)) return FA2_ERR_INVALID_ARG;
+    if (B <= 0 || H_q <= 0 || H_kv <= 0 || N <= 0 || d <= 0) return FA2_ERR_INVALID_ARG;
+    if (H_q % H_kv != 0) return FA2_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.0f)) return FA2_ERR_INVALID_ARG;
+    if (dtype != FA2_BF16 && dtype != FA2_FP16) return FA2_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA2_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA2_ERR_UNSUPPORTED;
+    if (N % fa2::kBM != 0) return FA2_ERR_UNSUPPORTED;
+    const long long rows_q = static_cast<long long>(B) * H_q * N;
+    if (rows_q > 0x7FFFFFFFLL || static_cast<long long>(B) * H_q > 65535) return FA2_ERR_UNSUPPORTED;
+
+    int dev = 0;
+    fa2_status st = check_device(&dev);
+    if (st != FA2_OK) return st;
+    if ((st = get_encoder()) != FA2_OK) return st;
+    CUtensorMap mq, mk, mv, mdo;
+    const uint64_t rows_kv = static_cast<uint64_t>(B) * H_kv * N;
+    if (encode_map(&mq, q, static_cast<uint64_t>(rows_q), d) != FA2_OK || encode_map(&mk, k, rows_kv, d) != FA2_OK ||
+        encode_map(&mv, v, rows_kv, d) != FA2_OK || encode_map(&mdo, dout, static_cast<uint64_t>(rows_q), d) != FA2_OK)
+        return FA2_ERR_CUDA;
+
+    fa2::bwd::Params p{};
+    p.o = o;
+    p.lse = lse;
+    p.dout = dout;
+    p.delta = delta;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    p.n_tiles = N / fa2::kBM;
+    p.hq = H_q;
+    p.group = H_q / H_kv;
+    p.causal = causal;
+    p.scale = scale;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    const bool bf = dtype == FA2_BF16;
+    const dim3 gdelta(static_cast<unsigned>((rows_q + 15) / 16));
+    const dim3 gkv(static_cast<unsigned>(p.n_tiles), static_cast<unsigned>(B * H_kv));
+    const dim3 gq(static_cast<unsigned>(p.n_tiles), static_cast<unsigned>(B * H_q));
+
+    auto run = [&](auto delta_k, auto dkdv_k, auto dq_k, int smem, int slot) -> fa2_status {
+        if (!g_dev[dev].smem_set[slot]) {
+            if (cudaFuncSetAttribute(dkdv_k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+                cudaFuncSetAttribute(dq_k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+                return FA2_ERR_CUDA;
+            std::lock_guard<std::mutex> lk(g_mu);
+            g_dev[dev].smem_set[slot] = true;
+        }
+        delta_k<<<gdelta, 256, 0, stream>>>(o, dout, delta, rows_q);
+        dkdv_k<<<gkv, fa2::bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
+        dq_k<<<gq, fa2::bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
+        return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+    };
+    if (d == 128)
+        return bf ? run(fa2::bwd::fa2_bwd_delta_kernel<128, true>, fa2::bwd::fa2_bwd_dkdv_kernel<128, true>,
+                        fa2::bwd::fa2_bwd_dq_kernel<128, true>, fa2::bwd::BwdLayout<128>::kSmemBytes, 8)
+                  : run(fa2::bwd::fa2_bwd_delta_kernel<128, false>, fa2::bwd::fa2_bwd_dkdv_kernel<128, false>,
+                        fa2::bwd::fa2_bwd_dq_kernel<128, false>, fa2::bwd::BwdLayout<128>::kSmemBytes, 9);
+    return bf ? run(fa2::bwd::fa2_bwd_delta_kernel<64, true>, fa2::bwd::fa2_bwd_dkdv_kernel<64, true>,
+                    fa2::bwd::fa2_bwd_dq_kernel<64, true>, fa2::bwd::BwdLayout<64>::kSmemBytes, 10)
+              : run(fa2::bwd::fa2_bwd_delta_kernel<64, false>, fa2::bwd::fa2_bwd_dkdv_kernel<64, false>,
+                    fa2::bwd::fa2_bwd_dq_kernel<64, false>, fa2::bwd::BwdLayout<64>::kSmemBytes, 11);
 }
 
 fa2_status fa2_check_status(cudaStream_t stream) {

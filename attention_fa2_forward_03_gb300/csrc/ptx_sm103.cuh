@@ -92,6 +92,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
+// Plain bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // Prefetch a 2-D tile into L2 (no shared-memory destination, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
@@ -531,6 +540,19 @@ __device__ __forceinline__ uint64_t ex2_poly_f2(uint64_t x2) {
     const uint32_t b0 = __float_as_uint(t0) * 8388608u + __float_as_uint(p0);
     const uint32_t b1 = __float_as_uint(t1) * 8388608u + __float_as_uint(p1);
     return f2_pack(__uint_as_float(b0), __uint_as_float(b1));
+}
+
+// Widen a 16-bit pair (lo in bits 0..15) to two fp32 values, exactly.
+template <bool kBf16>
+__device__ __forceinline__ void unpack2(uint32_t v, float& lo, float& hi) {
+    if constexpr (kBf16) {
+        lo = __uint_as_float(v << 16);
+        hi = __uint_as_float(v & 0xFFFF0000u);
+    } else {
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+            : "=f"(lo), "=f"(hi)
+            : "r"(v));
+    }
 }
 
 // Pack two fp32 values into a 16-bit pair: `lo` in bits 0..15, `hi` in 16..31,

@@ -22,7 +22,7 @@ FA2_ERR_CUDA = 3
 FA2_ERR_TIMEOUT = 4
 
 # symbols declared in include/fa2.h
-EXPORTS = ("fa2_fwd", "fa2_fwd_gqa", "fa2_fwd_ex", "fa2_check_status", "fa2_status_string",
+EXPORTS = ("fa2_fwd", "fa2_fwd_gqa", "fa2_fwd_ex", "fa2_bwd", "fa2_check_status", "fa2_status_string",
            "fa2_set_wait_limit_ns", "fa2_set_debug_flags", "fa2_version")
 
 _lib = None
@@ -50,6 +50,8 @@ def load(path: str = LIB_PATH):
     lib.fa2_fwd_gqa.restype = i
     lib.fa2_fwd_ex.argtypes = [p, p, p, p, p, i, i, i, i, i, i, f, i, i, p]
     lib.fa2_fwd_ex.restype = i
+    lib.fa2_bwd.argtypes = [p, p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, i, i, p]
+    lib.fa2_bwd.restype = i
     lib.fa2_check_status.argtypes = [p]
     lib.fa2_check_status.restype = i
     lib.fa2_status_string.argtypes = [i]
@@ -85,6 +87,13 @@ def fa2_fwd_ex_ptr(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, scale, causal, dt
     """fa2_fwd_ex on raw device addresses (ints); returns the status code."""
     return load().fa2_fwd_ex(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, float(scale), int(causal),
                              int(dtype), stream or None)
+
+
+def fa2_bwd_ptr(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H_q, H_kv, N, d, scale, causal, dtype,
+                stream=0) -> int:
+    """fa2_bwd on raw device addresses (ints); returns the status code."""
+    return load().fa2_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H_q, H_kv, N, d, float(scale),
+                          int(causal), int(dtype), stream or None)
 
 
 def fa2_check_status(stream=0) -> int:
@@ -191,6 +200,37 @@ def fa2_fwd_ex(q, k, v, o=None, lse=None, scale=None, causal=False, stream=None)
     if rc != FA2_OK:
         raise FA2Error(rc, "fa2_fwd_ex")
     return o, lse
+
+
+def fa2_bwd(q, k, v, o, lse, dout, scale=None, causal=False, dq=None, dk=None, dv=None, delta=None,
+            stream=None):
+    """Gradients (dq, dk, dv) of the forward for upstream gradient dout.
+
+    q, o, dout: [B, Hq, N, d]; k, v: [B, Hkv, N, d]; lse: fp32 [B, Hq, N]
+    from the forward. Outputs and the fp32 workspace `delta` [B, Hq, N] are
+    allocated with torch when not given (device-memory plumbing only).
+    """
+    import torch
+
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    for t in (q, k, v, o, dout, lse):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    if tuple(k.shape) != (B, Hkv, N, d) or v.shape != k.shape or o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("shape mismatch")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    delta = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if delta is None else delta
+    if scale is None:
+        scale = d ** -0.5
+    rc = fa2_bwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr(), B, Hq, Hkv, N, d, scale,
+                     bool(causal), _dtype_code(q), _stream_handle(stream, q.device))
+    if rc != FA2_OK:
+        raise FA2Error(rc, "fa2_bwd")
+    return dq, dk, dv
 
 
 def fa2_fwd(q, k, v, o=None, lse=None, scale=None, stream=None):

@@ -111,6 +111,30 @@ fa2_status fa2_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
                       int causal, fa2_dtype dtype, cudaStream_t stream);
 
 /*
+ * Attention backward (gradients of fa2_fwd / fa2_fwd_gqa with optional
+ * causal mask, equal lengths N, N % 128 == 0). The forward pages exclude the
+ * backward pass ("FlashAttention-2 from scratch on Ampere, Part 1", Kernel
+ * Specification: forward pass only); it is built here as an extension and
+ * recomputes P = exp(scale*S - LSE) from the forward's logsumexp:
+ *     D = rowsum(dO o O), dP = dO V^T, dS = P o (dP - D),
+ *     dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO
+ * (grouped KV heads: dK, dV summed over the query heads that share them).
+ *   q, o, dout, dq : [B, H_q, N, d] 16-bit (q, o, dout read; dq written)
+ *   k, v, dk, dv   : [B, H_kv, N, d] 16-bit (k, v read; dk, dv written)
+ *   lse            : [B, H_q, N] fp32, the forward's logsumexp (read)
+ *   delta          : [B, H_q, N] fp32, caller-owned workspace; the call
+ *                    writes D into it and then reads it back
+ *   causal         : 0 or 1 (same mask as the forward with N_q == N_k)
+ * All pointers device memory, 16-byte aligned. Launches three kernels on
+ * `stream` (D, then dK/dV, then dQ); allocates nothing. Errors as
+ * fa2_fwd_gqa; B*H_q > 65535 is FA2_ERR_UNSUPPORTED.
+ */
+fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dout, void* dq, void* dk, void* dv, float* delta,
+                   int B, int H_q, int H_kv, int N, int d, float scale, int causal,
+                   fa2_dtype dtype, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word. Returns FA2_ERR_TIMEOUT if a kernel since the last check abandoned a
  * wait (its outputs are then undefined), FA2_ERR_CUDA if the stream reported

@@ -88,6 +88,18 @@ def test_general_entry_host_validation(lib, args, expected):
     assert fa2.fa2_fwd_ex_ptr(*args) == expected
 
 
+def test_backward_host_validation(lib):
+    f = fa2.fa2_bwd_ptr
+    ok = [A] * 10
+    assert f(*([0] + ok[1:]), 1, 1, 1, 128, 128, 0.1, 0, 0) == fa2.FA2_ERR_INVALID_ARG   # NULL q
+    assert f(*(ok[:9] + [A + 4]), 1, 1, 1, 128, 128, 0.1, 0, 0) == fa2.FA2_ERR_INVALID_ARG  # delta align
+    assert f(*ok, 1, 1, 1, 128, 128, 0.1, 3, 0) == fa2.FA2_ERR_INVALID_ARG          # causal
+    assert f(*ok, 1, 3, 2, 128, 128, 0.1, 0, 0) == fa2.FA2_ERR_INVALID_ARG          # Hq % Hkv
+    assert f(*ok, 1, 1, 1, 100, 128, 0.1, 0, 0) == fa2.FA2_ERR_UNSUPPORTED          # N % 128
+    assert f(*ok, 1, 1, 1, 128, 80, 0.1, 0, 0) == fa2.FA2_ERR_UNSUPPORTED           # d
+    assert f(*ok, 1, 70000, 1, 128, 64, 0.1, 0, 0) == fa2.FA2_ERR_UNSUPPORTED       # B*Hq > 65535
+
+
 def test_mha_entry_forwards_to_gqa(lib):
     assert fa2.fa2_fwd_ptr(0, A, A, A, A, 1, 1, 128, 128, 0.1, 0) == fa2.FA2_ERR_INVALID_ARG
     assert fa2.fa2_fwd_ptr(A, A, A, A, A, 1, 1, 128, 80, 0.1, 0) == fa2.FA2_ERR_UNSUPPORTED
