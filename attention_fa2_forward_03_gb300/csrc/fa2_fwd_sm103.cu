@@ -1150,6 +1150,46 @@ fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, c
                     fa2::bwd::fa2_bwd_dq_kernel<64, false>, fa2::bwd::BwdLayout<64>::kSmemBytes, 11);
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------- backward without allocation
+
+// Scratch for fa2_bwd_noalloc: the per-row D = rowsum(dO o O) of the
+// backward, for at most kNoAllocMaxRows query rows (4 MiB of fp32). Every GPU
+// that loads this library keeps this array until the process exits. On the
+// host the name only stands for the array: its device address comes from
+// cudaGetSymbolAddress, once per device.
+static constexpr long long kNoAllocMaxRows = 1LL << 20;
+static __device__ __align__(256) float fa2_noalloc_delta[kNoAllocMaxRows];
+
+namespace {
+float* g_noalloc_delta_ptr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" {
+
+fa2_status fa2_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                           const void* dout, void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int N,
+                           int d, float scale, int causal, fa2_dtype dtype, cudaStream_t stream) {
+    if (B <= 0 || H_q <= 0 || N <= 0) return FA2_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * H_q * N > kNoAllocMaxRows) return FA2_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA2_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FA2_ERR_UNSUPPORTED;
+    if (!g_noalloc_delta_ptr[dev]) {
+        // First call on this device (which is current): find the array's
+        // device address.
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, fa2_noalloc_delta) != cudaSuccess || !ptr) return FA2_ERR_CUDA;
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_noalloc_delta_ptr[dev] = static_cast<float*>(ptr);
+    }
+    // D is written in full by the first kernel of the backward before it is
+    // read, so nothing left from an earlier call needs clearing.
+    return fa2_bwd(q, k, v, o, lse, dout, dq, dk, dv, g_noalloc_delta_ptr[dev], B, H_q, H_kv, N, d, scale, causal,
+                   dtype, stream);
+}
+
 fa2_status fa2_check_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return FA2_ERR_CUDA;
     int v = 0;

@@ -22,7 +22,8 @@ FA2_ERR_CUDA = 3
 FA2_ERR_TIMEOUT = 4
 
 # symbols declared in include/fa2.h
-EXPORTS = ("fa2_fwd", "fa2_fwd_gqa", "fa2_fwd_ex", "fa2_bwd", "fa2_check_status", "fa2_status_string",
+EXPORTS = ("fa2_fwd", "fa2_fwd_gqa", "fa2_fwd_ex", "fa2_bwd", "fa2_bwd_noalloc", "fa2_check_status",
+           "fa2_status_string",
            "fa2_set_wait_limit_ns", "fa2_set_debug_flags", "fa2_version")
 
 _lib = None
@@ -52,6 +53,8 @@ def load(path: str = LIB_PATH):
     lib.fa2_fwd_ex.restype = i
     lib.fa2_bwd.argtypes = [p, p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, i, i, p]
     lib.fa2_bwd.restype = i
+    lib.fa2_bwd_noalloc.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, i, i, p]
+    lib.fa2_bwd_noalloc.restype = i
     lib.fa2_check_status.argtypes = [p]
     lib.fa2_check_status.restype = i
     lib.fa2_status_string.argtypes = [i]
@@ -94,6 +97,15 @@ def fa2_bwd_ptr(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H_q, H_kv, N, d, sc
     """fa2_bwd on raw device addresses (ints); returns the status code."""
     return load().fa2_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H_q, H_kv, N, d, float(scale),
                           int(causal), int(dtype), stream or None)
+
+
+def fa2_bwd_noalloc_ptr(q, k, v, o, lse, dout, dq, dk, dv, B, H_q, H_kv, N, d, scale, causal, dtype,
+                        stream=0) -> int:
+    """fa2_bwd_noalloc on raw device addresses (ints): the backward without a
+    caller-provided workspace, for callers that cannot allocate device
+    memory (at most 2**20 query rows). Returns the status code."""
+    return load().fa2_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H_q, H_kv, N, d, float(scale),
+                                  int(causal), int(dtype), stream or None)
 
 
 def fa2_check_status(stream=0) -> int:

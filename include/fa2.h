@@ -135,6 +135,31 @@ fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, c
                    fa2_dtype dtype, cudaStream_t stream);
 
 /*
+ * fa2_bwd without the `delta` workspace, for callers that cannot allocate
+ * device memory: a plugin handed only its input and output tensors by a host
+ * framework that owns every device allocation, or code running where a
+ * device allocation is not allowed or its implicit synchronisation cannot be
+ * afforded. (The source pages have no counterpart; this is an interface
+ * convenience of this library.)
+ *
+ * Same arguments and results as fa2_bwd minus `delta`. D = rowsum(dO o O)
+ * lives instead in a fixed device array inside this library, sized for
+ * B * H_q * N <= 1048576 query rows (4 MiB of fp32, held on every GPU that
+ * loads the library until the process exits); larger problems return
+ * FA2_ERR_UNSUPPORTED and launch nothing. Nothing is allocated by the call.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture. Every call uses the same array: calls that may overlap on
+ * the GPU (other streams, other host threads) race on it and must be
+ * ordered by the caller. The array keeps the last call's D; each call
+ * rewrites the rows it uses before reading them.
+ */
+fa2_status fa2_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                           const void* dout, void* dq, void* dk, void* dv,
+                           int B, int H_q, int H_kv, int N, int d, float scale, int causal,
+                           fa2_dtype dtype, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word. Returns FA2_ERR_TIMEOUT if a kernel since the last check abandoned a
  * wait (its outputs are then undefined), FA2_ERR_CUDA if the stream reported
