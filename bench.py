@@ -7,7 +7,16 @@ seeded N(0,1) inputs. Metric: attention-forward TFLOP/s counted as 4*B*H*N^2*d
 per step. Prints ONE JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--pass fwd|fwd_causal|bwd|bwd_causal]
                     [--impl ours|reference] [--no-cpu-baseline]
+
+--pass picks what one step runs (default fwd, the line above):
+  fwd_causal  fa2_fwd_ex with the causal mask; FLOPs counted over the
+              unmasked (query, key) pairs only, 4*d*sum_i(i+1) per head
+  bwd         fa2_bwd (D = rowsum(dO*O), then dK/dV, then dQ: three
+              launches); FLOPs counted as 2.5x the forward's (the five
+              GEMMs of the backward), inputs from one forward call
+  bwd_causal  the same with the causal mask
 
 --impl reference times the fp64 CPU oracle (test infrastructure) on the host
 cores over a bounded sample of the same workload: a deliberately slow
@@ -43,16 +52,16 @@ METRIC = "attention fwd TFLOP/s (4BHN²d) at 1 GB300; % of dense BF16 tensor pea
 UNIT = "TFLOP/s"
 L2_BYTES = 129 * 1024 * 1024
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
-KERNEL_SOURCES = [
-    os.path.join(ROOT, "attention_fa2_forward_03_gb300", "csrc", "fa2_fwd_sm103.cu"),
-    os.path.join(ROOT, "attention_fa2_forward_03_gb300", "csrc", "ptx_sm103.cuh"),
-]
+CSRC = os.path.join(ROOT, "attention_fa2_forward_03_gb300", "csrc")
+KERNEL_SOURCES = [os.path.join(CSRC, "fa2_fwd_sm103.cu"), os.path.join(CSRC, "ptx_sm103.cuh")]
+BWD_SOURCES = KERNEL_SOURCES + [os.path.join(CSRC, "fa2_bwd_sm103.cuh")]
+PASSES = ("fwd", "fwd_causal", "bwd", "bwd_causal")
 REASON_FIELDS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(which: str = "fwd") -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in (BWD_SOURCES if which.startswith("bwd") else KERNEL_SOURCES):
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -193,23 +202,53 @@ def load_peak():
         return 1900.0, "fallback (1.9 PFLOP/s bf16 burst)"
 
 
-def load_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source for this workload; else None."""
+def traffic_key(workload: str, which: str) -> str:
+    return workload if which == "fwd" else f"{workload}:{which}"
+
+
+def load_traffic(workload: str, which: str = "fwd"):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source for this workload
+    and pass; else None."""
     try:
         with open(TRAFFIC_FILE) as fh:
             rec = json.load(fh)
     except (OSError, ValueError):
         return None
-    entry = rec.get(workload)
-    if not entry or entry.get("kernel_source_sha") != kernel_source_hash():
+    entry = rec.get(traffic_key(workload, which))
+    if not entry or entry.get("kernel_source_sha") != kernel_source_hash(which):
         return None
     return entry.get("dram_bytes_per_launch")
 
 
+# ------------------------------------------------------------------ work per pass
+
+def causal_pairs(N: int) -> int:
+    """Unmasked (query, key) pairs of one causal head with equal lengths."""
+    return N * (N + 1) // 2
+
+
+def pass_flops(w, which: str) -> float:
+    """Algorithmic FLOPs of one step: 4*d per unmasked (query, key) pair for
+    the forward, 2.5x that for the backward."""
+    pairs = causal_pairs(w.N) if which.endswith("causal") else w.N * w.N
+    fwd = 4.0 * w.B * w.Hq * pairs * w.d
+    return fwd * (2.5 if which.startswith("bwd") else 1.0)
+
+
+def pass_bytes(w, which: str) -> int:
+    """Algorithmic HBM bytes of one step: every tensor read or written once."""
+    if not which.startswith("bwd"):
+        return w.alg_bytes
+    q = w.B * w.Hq * w.N * w.d * 2
+    kv = w.B * w.Hkv * w.N * w.d * 2
+    # reads q, k, v, o, dO, lse; writes dq, dk, dv (delta: written and read once)
+    return 3 * q + 2 * kv + 4 * w.B * w.Hq * w.N + q + 2 * kv + 8 * w.B * w.Hq * w.N
+
+
 # ------------------------------------------------------------------ CPU oracle timing
 
-def oracle_rows_for(w, seconds: float, q, k, v):
+def oracle_rows_for(w, seconds: float, q, k, v, causal: bool = False):
     """Rows per second of the fp64 oracle on this host, then a seeded row
     sample sized to take about `seconds`."""
     import oracle
@@ -218,61 +257,111 @@ def oracle_rows_for(w, seconds: float, q, k, v):
     total = w.B * w.Hq * w.N
     calib = rng.integers(0, total, 64)
     t0 = time.perf_counter()
-    oracle.attention(q, k, v, w.scale, w.dtype, rows=calib)
+    if causal:
+        oracle.attention_ex(q, k, v, w.scale, w.dtype, causal=True, rows=calib)
+    else:
+        oracle.attention(q, k, v, w.scale, w.dtype, rows=calib)
     rate = 64 / max(time.perf_counter() - t0, 1e-6)
     n = int(max(1, min(total, rate * seconds)))
     return rng.integers(0, total, n), oracle.max_threads()
 
 
-def time_oracle(w, q, k, v, seconds: float):
-    import oracle
+class OracleSample:
+    """A bounded piece of one step's work for the fp64 CPU oracle.
 
-    rows, cores = oracle_rows_for(w, seconds, q, k, v)
+    Forward passes: a seeded sample of query rows (full key length).
+    Backward passes: the whole backward of one KV-head group (batch 0, KV
+    head 0 and its query heads, full N): dK and dV need every query row.
+    """
+
+    def __init__(self, w, which: str, seconds: float, q, k, v):
+        import oracle
+
+        self.oracle, self.w, self.which = oracle, w, which
+        self.causal = which.endswith("causal")
+        self.cores = oracle.max_threads()
+        if which.startswith("bwd"):
+            G = w.Hq // w.Hkv
+            self.q, self.k, self.v = (np.ascontiguousarray(x[:1, :h]) for x, h in
+                                      ((q, G), (k, 1), (v, 1)))
+            self.do = np.ascontiguousarray(w.grad_output()[:1, :G])
+            pairs = causal_pairs(w.N) if self.causal else w.N * w.N
+            self.flops = 10.0 * G * pairs * w.d
+            self.desc = (f"backward of one KV-head group (b=0, kv head 0, {G} query head(s), "
+                         f"N={w.N}) of the {w.B * w.Hkv}-group workload per step; fp64 C oracle, OpenMP")
+        else:
+            self.q, self.k, self.v = q, k, v
+            self.rows, _ = oracle_rows_for(w, seconds, q, k, v, self.causal)
+            i = self.rows % w.N
+            keys = (i + 1) if self.causal else np.full(self.rows.shape, w.N)
+            self.flops = 4.0 * w.d * float(keys.sum())
+            self.desc = (f"{len(self.rows)} seeded query rows of the {w.B * w.Hq * w.N}-row "
+                         f"workload per step (full key length N={w.N}"
+                         f"{', causal' if self.causal else ''}); fp64 C oracle, OpenMP")
+
+    def run(self):
+        o, w = self.oracle, self.w
+        if self.which.startswith("bwd"):
+            o.attention_bwd(self.q, self.k, self.v, self.do, w.scale, w.dtype, causal=self.causal)
+        elif self.causal:
+            o.attention_ex(self.q, self.k, self.v, w.scale, w.dtype, causal=True, rows=self.rows)
+        else:
+            o.attention(self.q, self.k, self.v, w.scale, w.dtype, rows=self.rows)
+
+
+def time_oracle(w, which: str, q, k, v, seconds: float):
+    sample = OracleSample(w, which, seconds, q, k, v)
     t0 = time.perf_counter()
-    oracle.attention(q, k, v, w.scale, w.dtype, rows=rows)
+    sample.run()
     dt = time.perf_counter() - t0
-    flops = 4.0 * w.N * w.d * len(rows)
-    return flops / dt / 1e12, cores, len(rows), dt
+    return sample.flops / dt / 1e12, sample.cores, sample.desc, dt
 
 
 # ------------------------------------------------------------------ arms
 
 def run_reference(args, dist, w):
-    """fp64 CPU oracle as the reference arm: each step a bounded row sample."""
+    """fp64 CPU oracle as the reference arm: each step a bounded sample."""
     if dist.rank != 0:
         return None
-    import oracle
-
     q, k, v = w.inputs()
     total_budget = 120.0
     per_step = total_budget / max(1, args.steps + args.warmup)
-    rows, cores = oracle_rows_for(w, per_step, q, k, v)
+    sample = OracleSample(w, args.pass_, per_step, q, k, v)
     for _ in range(args.warmup):
-        oracle.attention(q, k, v, w.scale, w.dtype, rows=rows)
+        sample.run()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.attention(q, k, v, w.scale, w.dtype, rows=rows)
+        sample.run()
     dt = time.perf_counter() - t0
-    value = 4.0 * w.N * w.d * len(rows) * args.steps / dt / 1e12
-    sample = (f"{len(rows)} seeded query rows of the {w.B * w.Hq * w.N}-row workload per step "
-              f"(full key length N={w.N}); fp64 C oracle, OpenMP")
+    value = sample.flops * args.steps / dt / 1e12
     return {
         "impl": "reference",
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "metric": metric_of(args.pass_), "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w, args.gpus),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": sample},
+        "config": config_of(w, args.gpus, args.pass_),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": sample.cores, "kind": "oracle",
+                         "sample": sample.desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
-def config_of(w, n_gpus):
-    return {"workload": w.name, "B": w.B, "H_q": w.Hq, "H_kv": w.Hkv, "N": w.N, "d": w.d,
-            "dtype": "bf16" if w.dtype == gen.BF16 else "fp16",
-            "causal": False, "scale": "1/sqrt(d)", "inputs": f"N(0,1)x{w.amp:g} seed {w.seed}",
+def metric_of(which: str) -> str:
+    if which == "fwd":
+        return METRIC
+    if which == "fwd_causal":
+        return "attention fwd causal TFLOP/s (4d per unmasked pair) at 1 GB300"
+    return ("attention bwd TFLOP/s (2.5x forward FLOPs" +
+            (", causal" if which == "bwd_causal" else "") + ") at 1 GB300")
+
+
+def config_of(w, n_gpus, which: str = "fwd"):
+    return {"workload": w.name, "pass": which, "B": w.B, "H_q": w.Hq, "H_kv": w.Hkv, "N": w.N,
+            "d": w.d, "dtype": "bf16" if w.dtype == gen.BF16 else "fp16",
+            "causal": which.endswith("causal"), "scale": "1/sqrt(d)",
+            "inputs": f"N(0,1)x{w.amp:g} seed {w.seed}"
+                      + (f"; dO N(0,1) seed {w.seed + 50000}" if which.startswith("bwd") else ""),
             "global_batch": w.B * n_gpus, "seq_len": w.N,
             "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU",
             "l2": l2_note(w)}
@@ -289,6 +378,103 @@ def l2_note(w) -> str:
     return f"L2 flushed between timed steps (256 MiB write); Q+K+V = {mib:.1f} MiB"
 
 
+class Step:
+    """Device tensors and the C-ABI call of one step of a pass."""
+
+    def __init__(self, fa2, torch, w, which, dev, stream, q, k, v):
+        self.fa2, self.torch, self.w, self.which, self.stream = fa2, torch, w, which, stream
+        self.tdt = torch.bfloat16 if w.dtype == gen.BF16 else torch.float16
+        self.causal = which.endswith("causal")
+        self.bwd = which.startswith("bwd")
+
+        def up(x):
+            return torch.from_numpy(x.view(np.int16)).to(dev).view(self.tdt)
+
+        self.tq, self.tk, self.tv = up(q), up(k), up(v)
+        self.o = torch.empty_like(self.tq)
+        self.lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
+        if self.bwd:
+            self.tdo = up(w.grad_output())
+            fa2.fa2_fwd_ex(self.tq, self.tk, self.tv, self.o, self.lse, scale=w.scale,
+                           causal=self.causal, stream=stream)
+            self.dq = torch.empty_like(self.tq)
+            self.dk = torch.empty_like(self.tk)
+            self.dv = torch.empty_like(self.tv)
+            self.delta = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
+        # launches of this library's kernels per step
+        self.launches = 3 if self.bwd else 1
+        if self.bwd:
+            self.kernel = "fa2_bwd (delta + dK/dV + dQ kernels)"
+        else:
+            self.kernel = (f"fa2_fwd_kernel<{w.d},{'bf16' if w.dtype == gen.BF16 else 'fp16'}"
+                           f"{',general' if self.causal else ''}>")
+
+    def __call__(self):
+        w, f, s = self.w, self.fa2, self.stream.cuda_stream
+        if self.bwd:
+            rc = f.fa2_bwd_ptr(self.tq.data_ptr(), self.tk.data_ptr(), self.tv.data_ptr(),
+                               self.o.data_ptr(), self.lse.data_ptr(), self.tdo.data_ptr(),
+                               self.dq.data_ptr(), self.dk.data_ptr(), self.dv.data_ptr(),
+                               self.delta.data_ptr(), w.B, w.Hq, w.Hkv, w.N, w.d, w.scale,
+                               self.causal, w.dtype, s)
+            name = "fa2_bwd"
+        elif self.causal:
+            rc = f.fa2_fwd_ex_ptr(self.tq.data_ptr(), self.tk.data_ptr(), self.tv.data_ptr(),
+                                  self.o.data_ptr(), self.lse.data_ptr(), w.B, w.Hq, w.Hkv, w.N,
+                                  w.N, w.d, w.scale, True, w.dtype, s)
+            name = "fa2_fwd_ex"
+        else:
+            rc = f.fa2_fwd_gqa_ptr(self.tq.data_ptr(), self.tk.data_ptr(), self.tv.data_ptr(),
+                                   self.o.data_ptr(), self.lse.data_ptr(), w.B, w.Hq, w.Hkv, w.N,
+                                   w.d, w.scale, w.dtype, s)
+            name = "fa2_fwd_gqa"
+        if rc != f.FA2_OK:
+            raise RuntimeError(f"{name}: {f.status_string(rc)}")
+
+    def e2e(self, host):
+        """One end-to-end step through the public torch-level binding: the
+        step's inputs from pinned host memory to the device, the call, the
+        results back to pinned host memory."""
+        f, st = self.fa2, self.stream
+        ins, outs = host
+        if self.bwd:
+            dev_in = (self.tq, self.tk, self.tv, self.o, self.lse, self.tdo)
+            for d_, h_ in zip(dev_in, ins):
+                d_.copy_(h_, non_blocking=True)
+            f.fa2_bwd(self.tq, self.tk, self.tv, self.o, self.lse, self.tdo, scale=self.w.scale,
+                      causal=self.causal, dq=self.dq, dk=self.dk, dv=self.dv, delta=self.delta,
+                      stream=st)
+            dev_out = (self.dq, self.dk, self.dv)
+        else:
+            for d_, h_ in zip((self.tq, self.tk, self.tv), ins):
+                d_.copy_(h_, non_blocking=True)
+            if self.causal:
+                f.fa2_fwd_ex(self.tq, self.tk, self.tv, self.o, self.lse, scale=self.w.scale,
+                             causal=True, stream=st)
+            else:
+                f.fa2_fwd_gqa(self.tq, self.tk, self.tv, self.o, self.lse, scale=self.w.scale,
+                              stream=st)
+            dev_out = (self.o, self.lse)
+        for h_, d_ in zip(outs, dev_out):
+            h_.copy_(d_, non_blocking=True)
+
+    def host_buffers(self):
+        """Pinned host copies of the step's inputs and room for its results."""
+        def pin(t):
+            return t.detach().cpu().pin_memory()
+
+        if self.bwd:
+            ins = tuple(pin(t) for t in (self.tq, self.tk, self.tv, self.o, self.lse, self.tdo))
+            outs = tuple(self.torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                         for t in (self.dq, self.dk, self.dv))
+        else:
+            ins = tuple(pin(t) for t in (self.tq, self.tk, self.tv))
+            outs = tuple(self.torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                         for t in (self.o, self.lse))
+        nbytes = [sum(t.numel() * t.element_size() for t in x) for x in (ins, outs)]
+        return (ins, outs), nbytes[0], nbytes[1]
+
+
 def run_ours(args, dist, w):
     import torch
 
@@ -301,24 +487,11 @@ def run_ours(args, dist, w):
     stream = torch.cuda.current_stream(dev)
 
     q, k, v = w.inputs()
-    tdt = torch.bfloat16 if w.dtype == gen.BF16 else torch.float16
-
-    def up(x):
-        return torch.from_numpy(x.view(np.int16)).to(dev).view(tdt)
-
-    tq, tk, tv = up(q), up(k), up(v)
-    o = torch.empty_like(tq)
-    lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
+    step = Step(fa2, torch, w, args.pass_, dev, stream, q, k, v)
+    flops = pass_flops(w, args.pass_)
     flush = None
     if qkv_bytes(w) <= L2_BYTES:
         flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
-
-    def step():
-        rc = fa2.fa2_fwd_gqa_ptr(tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), o.data_ptr(),
-                                 lse.data_ptr(), w.B, w.Hq, w.Hkv, w.N, w.d, w.scale, w.dtype,
-                                 stream.cuda_stream)
-        if rc != fa2.FA2_OK:
-            raise RuntimeError(f"fa2_fwd_gqa: {fa2.status_string(rc)}")
 
     for _ in range(args.warmup):
         if flush is not None:
@@ -360,71 +533,53 @@ def run_ours(args, dist, w):
         time.sleep(0.25)
         clocks.stop()
 
-    value, max_region_ms = aggregate_throughput(dist, float(w.flops) * args.steps, region_ms, dev)
+    value, max_region_ms = aggregate_throughput(dist, flops * args.steps, region_ms, dev)
 
-    # end to end through the public binding: pinned host inputs -> device ->
-    # kernel -> device -> pinned host outputs, every step
-    hq, hk, hv = (torch.from_numpy(x.view(np.int16)).view(tdt).pin_memory() for x in (q, k, v))
-    ho = torch.empty(o.shape, dtype=tdt).pin_memory()
-    hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    # end to end through the public binding, every step: pinned host inputs
+    # -> device -> kernels -> device -> pinned host results
+    host, h2d, d2h = step.host_buffers()
     e2e_steps = max(3, min(args.steps, 50))
-
-    def e2e_step():
-        tq.copy_(hq, non_blocking=True)
-        tk.copy_(hk, non_blocking=True)
-        tv.copy_(hv, non_blocking=True)
-        fa2.fa2_fwd_gqa(tq, tk, tv, o, lse, scale=w.scale, stream=stream)
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
-
     for _ in range(2):
-        e2e_step()
+        step.e2e(host)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     dist.barrier()
     torch.cuda.synchronize(dev)
     e0.record(stream)
     for _ in range(e2e_steps):
-        e2e_step()
+        step.e2e(host)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     dist.barrier()
-    e2e_value, e2e_ms = aggregate_throughput(dist, float(w.flops) * e2e_steps,
-                                             e0.elapsed_time(e1), dev)
-    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
-    d2h = ho.numel() * 2 + hl.numel() * 4
+    e2e_value, e2e_ms = aggregate_throughput(dist, flops * e2e_steps, e0.elapsed_time(e1), dev)
 
     result = None
     if dist.rank == 0:
         peak, peak_src = load_peak()
-        achieved = w.flops / (kernel_ms * 1e-3) / 1e12
-        traffic = load_traffic(w.name)
+        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        nbytes = pass_bytes(w, args.pass_)
         result = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
+            "metric": metric_of(args.pass_), "value": value, "unit": UNIT, "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": max_region_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if w.dtype == gen.BF16 else "fp16", "data": "synthetic",
-            "config": config_of(w, dist.world),
+            "config": config_of(w, dist.world, args.pass_),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                         "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": peak_src,
-                         "kernel": f"fa2_fwd_kernel<{w.d},{'bf16' if w.dtype == gen.BF16 else 'fp16'}>",
-                         "kernel_ms": kernel_ms,
-                         "alg_flops_per_launch": w.flops, "alg_bytes_per_launch": w.alg_bytes,
-                         "hbm_gbs_alg": w.alg_bytes / (kernel_ms * 1e-3) / 1e9},
+                         "frac": achieved / peak, "traffic": load_traffic(w.name, args.pass_),
+                         "peak_source": peak_src, "kernel": step.kernel, "kernel_ms": kernel_ms,
+                         "alg_flops_per_launch": flops, "alg_bytes_per_launch": nbytes,
+                         "hbm_gbs_alg": nbytes / (kernel_ms * 1e-3) / 1e9},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                     "ms_per_step": e2e_ms / e2e_steps},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * step.launches,
             "clocks": clocks.summary(),
         }
         if dist.world == 1 and not args.no_cpu_baseline:
-            cv, cores, nrows, dt = time_oracle(w, q, k, v, args.cpu_seconds)
-            result["cpu_baseline"] = {
-                "value": cv, "unit": UNIT, "cores": cores, "kind": "oracle",
-                "sample": (f"{nrows} seeded query rows of the {w.B * w.Hq * w.N}-row workload, "
-                           f"full key length N={w.N}; fp64 C oracle, OpenMP, {dt:.1f} s")}
+            cv, cores, desc, dt = time_oracle(w, args.pass_, q, k, v, args.cpu_seconds)
+            result["cpu_baseline"] = {"value": cv, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                      "sample": f"{desc}, {dt:.1f} s"}
     return result
 
 
@@ -434,6 +589,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(gen.WORKLOADS))
+    ap.add_argument("--pass", dest="pass_", default="fwd", choices=PASSES)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -130,6 +130,16 @@ def make_qkv(seed: int, B: int, Hq: int, Hkv: int, N: int, d: int,
     return tuple(out)
 
 
+def make_tensor(seed: int, shape, dtype: int = BF16, amp: float = 1.0) -> np.ndarray:
+    """One tensor of iid N(0, amp^2) values rounded to 16 bits (uint16 bits),
+    from the start of the stream of ``seed``."""
+    count = int(np.prod(shape))
+    vals = normals(seed, 0, count)
+    if amp != 1.0:
+        vals *= amp
+    return round_to_16bit(vals, dtype).reshape(shape)
+
+
 @dataclass(frozen=True)
 class Workload:
     """One attention-forward workload: shapes, dtype, scale and input recipe."""
@@ -161,6 +171,11 @@ class Workload:
     def inputs(self):
         return make_qkv(self.seed, self.B, self.Hq, self.Hkv, self.N, self.d,
                         self.dtype, self.amp)
+
+    def grad_output(self):
+        """The upstream gradient dO [B,Hq,N,d] for backward runs: N(0,1)
+        from seed + 50000 (independent of Q, K and V)."""
+        return make_tensor(self.seed + 50000, (self.B, self.Hq, self.N, self.d), self.dtype)
 
 
 def _sweep():
