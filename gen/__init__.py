@@ -19,6 +19,12 @@ Recipe (one portable stream per workload):
   round-to-nearest-even.
 * Q, K and V are drawn in that order from one stream: Q takes the first |Q|
   normals, K the next |K|, V the next |V|.
+* FP8 workloads (e4m3 inputs) draw the same normals and quantise each tensor
+  per (batch, KV head) group -- for Q the group is the query heads that share
+  that KV head: descale = max|x| / 448 over the group (1 if the group is all
+  zero), code = e4m3(x / descale) rounded to nearest-even from double,
+  saturating at the largest finite e4m3 value 448. The dequantised input is
+  code * descale.
 
 Everything is vectorised with numpy and processed in bounded chunks, so the
 largest workloads (about 10**8 values) need a few hundred MB of host memory.
@@ -39,12 +45,17 @@ __all__ = [
     "round_to_16bit",
     "bits_to_float32",
     "make_qkv",
+    "E4M3",
+    "e4m3_encode",
+    "make_qkv_fp8",
     "WORKLOADS",
     "workload",
 ]
 
 BF16 = 0
 FP16 = 1
+E4M3 = 2        # 8-bit float, 4 exponent bits (bias 7), 3 mantissa bits, no infinities
+E4M3_MAX = 448.0
 
 _GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
@@ -140,6 +151,54 @@ def make_tensor(seed: int, shape, dtype: int = BF16, amp: float = 1.0) -> np.nda
     return round_to_16bit(vals, dtype).reshape(shape)
 
 
+def _e4m3_table() -> np.ndarray:
+    """Values of the 127 non-negative finite e4m3 codes 0x00..0x7E, in code
+    order (which is value order): subnormals m/8 * 2**-6 for exponent field 0,
+    (1 + m/8) * 2**(e - 7) otherwise."""
+    codes = np.arange(127)
+    e, m = codes >> 3, codes & 7
+    return np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7.0))
+
+
+_E4M3 = _e4m3_table()
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """e4m3 codes (uint8) of doubles: nearest value, ties to the even code,
+    magnitudes above 448 saturate to 448 (input quantisation only)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    hi = np.clip(np.searchsorted(_E4M3, a, side="left"), 1, 126)
+    lo = hi - 1
+    dlo, dhi = a - _E4M3[lo], _E4M3[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    code = np.where(a == 0.0, 0, code).astype(np.uint8)
+    return code | np.where(x < 0, 0x80, 0).astype(np.uint8)
+
+
+def make_qkv_fp8(seed: int, B: int, Hq: int, Hkv: int, N: int, d: int, amp: float = 1.0):
+    """FP8 inputs: (q, k, v, q_descale, k_descale, v_descale). q [B,Hq,N,d],
+    k and v [B,Hkv,N,d] as e4m3 codes (uint8); descales float32 [B*Hkv],
+    exactly representable in fp32 (they are rounded to fp32 before the
+    codes are computed)."""
+    nq = B * Hq * N * d
+    nkv = B * Hkv * N * d
+    out, scales = [], []
+    start = 0
+    for count, shape in ((nq, (B, Hq, N, d)), (nkv, (B, Hkv, N, d)), (nkv, (B, Hkv, N, d))):
+        vals = normals(seed, start, count).reshape(shape)
+        if amp != 1.0:
+            vals *= amp
+        g = vals.reshape(B * Hkv, -1)
+        amax = np.abs(g).max(axis=1)
+        descale = np.where(amax > 0, amax / E4M3_MAX, 1.0).astype(np.float32).astype(np.float64)
+        out.append(e4m3_encode(g / descale[:, None]).reshape(shape))
+        scales.append(descale.astype(np.float32))
+        start += count + (count % 2)
+    return (*out, *scales)
+
+
 @dataclass(frozen=True)
 class Workload:
     """One attention-forward workload: shapes, dtype, scale and input recipe."""
@@ -164,11 +223,23 @@ class Workload:
 
     @property
     def alg_bytes(self) -> int:
-        q = self.B * self.Hq * self.N * self.d * 2
-        kv = self.B * self.Hkv * self.N * self.d * 2
-        return 2 * q + 2 * kv + 4 * self.B * self.Hq * self.N
+        """Q, K, V read once, O (16-bit) and LSE written once; FP8 inputs are
+        one byte per element (plus 12 bytes of descales per KV head)."""
+        es = 1 if self.fp8 else 2
+        q = self.B * self.Hq * self.N * self.d
+        kv = self.B * self.Hkv * self.N * self.d
+        extra = 12 * self.B * self.Hkv if self.fp8 else 0
+        return es * q + 2 * es * kv + 2 * q + 4 * self.B * self.Hq * self.N + extra
+
+    @property
+    def fp8(self) -> bool:
+        return self.dtype == E4M3
 
     def inputs(self):
+        """16-bit workloads: (q, k, v) bit patterns. FP8 workloads:
+        (q, k, v, q_descale, k_descale, v_descale)."""
+        if self.fp8:
+            return make_qkv_fp8(self.seed, self.B, self.Hq, self.Hkv, self.N, self.d, self.amp)
         return make_qkv(self.seed, self.B, self.Hq, self.Hkv, self.N, self.d,
                         self.dtype, self.amp)
 
@@ -193,6 +264,9 @@ WORKLOADS = {w.name: w for w in [
     *_sweep(),
     Workload("sharp_B8_H32_N2048_d64_bf16_x3", 8, 32, 32, 2048, 64, BF16, 1003, 3.0),
     Workload("gqa_B2_Hq32_Hkv8_N8192_d128_bf16", 2, 32, 8, 8192, 128, BF16, 1004),
+    Workload("fp8_mha_B4_H16_N4096_d128_e4m3", 4, 16, 16, 4096, 128, E4M3, 1101),
+    Workload("fp8_gqa_B2_Hq32_Hkv8_N8192_d128_e4m3", 2, 32, 8, 8192, 128, E4M3, 1104),
+    Workload("fp8_sweep_N16384_d128_e4m3", 1, 16, 16, 16384, 128, E4M3, 1102 + 16384),
 ]}
 
 

@@ -64,6 +64,14 @@ def _load():
         lib.oracle_attention_f64.argtypes = [p, p, p, i64, i64, i64, i64, i64, ctypes.c_double,
                                              ctypes.c_int, p]
         lib.oracle_attention_f64.restype = ctypes.c_int
+        lib.oracle_decode_e4m3.argtypes = [p, i64, p]
+        lib.oracle_decode_e4m3.restype = None
+        lib.oracle_round_e4m3.argtypes = [p, i64, p]
+        lib.oracle_round_e4m3.restype = None
+        lib.oracle_attention_fp8_rows.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64,
+                                                  ctypes.c_double, ctypes.c_int, p, i64, p, p, p, p,
+                                                  ctypes.c_int]
+        lib.oracle_attention_fp8_rows.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -183,6 +191,63 @@ def attention_f64(q, k, v, scale: float, causal: bool = False) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle rejected the sizes")
     return o
+
+
+def decode_e4m3(codes) -> np.ndarray:
+    """Exact double values of e4m3 codes (uint8)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_decode_e4m3(c.ctypes.data, c.size, out.ctypes.data)
+    return out
+
+
+def round_e4m3(x) -> np.ndarray:
+    """Doubles rounded to the nearest e4m3 value (ties to even, saturating at 448)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.float64)
+    _load().oracle_round_e4m3(x.ctypes.data, x.size, out.ctypes.data)
+    return out
+
+
+def attention_fp8(q, k, v, q_descale, k_descale, v_descale, scale: float, round_p: bool = True,
+                  rows=None, threads: int = 0):
+    """Attention forward on e4m3 inputs with per-(batch, KV head) descales.
+
+    q: uint8 [B, Hq, N, d]; k, v: uint8 [B, Hkv, N, d]; descales: [B*Hkv].
+    round_p=True follows the FP8 method (P scaled by 2^8 and rounded to e4m3
+    before the P.V product); round_p=False is the plain definition on the
+    dequantised inputs. Returns (o, lse, a, b): o, a, b [B, Hq, N, d] (or
+    [len(rows), d]) and lse [B, Hq, N] (or [len(rows)]), where
+    a = sum_j p_j |v_j| / l and b = sum_j |v_j| / l elementwise.
+    """
+    q, k, v = (np.ascontiguousarray(x, dtype=np.uint8) for x in (q, k, v))
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, N, d) or v.shape != k.shape:
+        raise ValueError("shape mismatch between q, k and v")
+    qd, kd, vd = (np.ascontiguousarray(x, dtype=np.float64).reshape(-1) for x in
+                  (q_descale, k_descale, v_descale))
+    if not (qd.size == kd.size == vd.size == B * Hkv):
+        raise ValueError("descales must have B*Hkv entries")
+    if rows is None:
+        nrows, rptr = B * Hq * N, None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        nrows, rptr = rows_arr.size, rows_arr.ctypes.data
+    o = np.empty((nrows, d), dtype=np.float64)
+    a = np.empty((nrows, d), dtype=np.float64)
+    b = np.empty((nrows, d), dtype=np.float64)
+    lse = np.empty(nrows, dtype=np.float64)
+    rc = _load().oracle_attention_fp8_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, qd.ctypes.data,
+                                           kd.ctypes.data, vd.ctypes.data, B, Hq, Hkv, N, d, float(scale),
+                                           int(bool(round_p)), rptr, nrows, o.ctypes.data, lse.ctypes.data,
+                                           a.ctypes.data, b.ctypes.data, int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the sizes")
+    if rows is None:
+        shp = (B, Hq, N, d)
+        return o.reshape(shp), lse.reshape(B, Hq, N), a.reshape(shp), b.reshape(shp)
+    return o, lse, a, b
 
 
 def softmax_row(q, k, scale: float, dtype: int, row: int) -> np.ndarray:

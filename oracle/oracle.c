@@ -391,6 +391,148 @@ int oracle_attention_f64(const double* q, const double* k, const double* v, int6
     return 0;
 }
 
+/*
+ * FP8 (e4m3) inputs with in-kernel scaling: the variant the Character.AI /
+ * Colfax article "FlashAttention-3 for Inference: INT8 Quantization and Query
+ * Head Packing for MQA/GQA" (Colfax Research author page) names -- quantised
+ * Q, K, V consumed directly by an attention kernel that applies their scales
+ * itself. The pages give only the article's title and summary, so the form
+ * here is the plainest one consistent with it:
+ *
+ *   inputs   e4m3 codes q, k, v with one fp32 descale per (batch, KV head)
+ *            for each tensor (the query heads of a KV head share the Q one);
+ *            the represented values are code * descale
+ *   method   attention on the dequantised values, except that the softmax
+ *            weights fed to the P.V product are scaled by 2^8 and rounded to
+ *            e4m3 (the P.V product runs on FP8 operands), while l sums the
+ *            unrounded weights:
+ *              s_j = scale * <qdeq, kdeq_j>,  m = max_j s_j
+ *              p_j = exp(s_j - m),            l = sum_j p_j
+ *              w_j = e4m3(256 * p_j) / 256    (round_p = 1)   or p_j (round_p = 0)
+ *              o   = (sum_j w_j vdeq_j) / l,  lse = m + ln(l)
+ *
+ * With round_p = 0 this is the plain definition on the dequantised inputs
+ * (the quantity the method approximates); with round_p = 1 it follows the
+ * method's steps. Two auxiliary row sums bound the effect of rounding P:
+ *   a_t = sum_j p_j |vdeq_{j,t}| / l,    b_t = sum_j |vdeq_{j,t}| / l.
+ */
+
+/* Exact value of an e4m3 code (OCP 8-bit floating point, E4M3: sign, 4-bit
+ * exponent with bias 7, 3-bit fraction; exponent 0 encodes subnormals
+ * f/8 * 2^-6; S.1111.111 is NaN; there are no infinities). */
+static double decode_e4m3(uint8_t c) {
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xF;
+    int f = c & 7;
+    double v;
+    if (e == 15 && f == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)f, -9);
+    else
+        v = ldexp((double)(8 + f), e - 10);
+    return sign ? -v : v;
+}
+
+/* x >= 0 rounded to the nearest e4m3 value, ties to even, saturating at 448:
+ * with the binade's spacing u (2^-9 below 2^-6, else 2^(floor(log2 x) - 3)),
+ * round x/u to the nearest integer with rint (the default rounding mode,
+ * nearest-even), whose parity is the parity of the code. */
+static double round_e4m3(double x) {
+    if (!(x > 0.0)) return 0.0;
+    if (x >= 448.0) return 448.0;
+    int ex;
+    frexp(x, &ex);                  /* x = f * 2^ex, f in [0.5, 1): floor(log2 x) = ex - 1 */
+    int e = ex - 1;
+    if (e < -6) e = -6;             /* subnormal range shares the spacing of [2^-6, 2^-5) */
+    double u = ldexp(1.0, e - 3);
+    double r = rint(x / u) * u;
+    return r > 448.0 ? 448.0 : r;
+}
+
+void oracle_decode_e4m3(const uint8_t* codes, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = decode_e4m3(codes[i]);
+}
+
+void oracle_round_e4m3(const double* x, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = x[i] < 0.0 ? -round_e4m3(-x[i]) : round_e4m3(x[i]);
+}
+
+/*
+ * q: [B, Hq, N, d] e4m3 codes; k, v: [B, Hkv, N, d] codes; qd, kd, vd:
+ * [B*Hkv] descales. rows: flat query rows (b*Hq + h)*N + i or NULL for all.
+ * o, a, bsum: [nrows, d]; lse: [nrows]. a and bsum may be NULL.
+ */
+int oracle_attention_fp8_rows(const uint8_t* q, const uint8_t* k, const uint8_t* v, const double* qd,
+                              const double* kd, const double* vd, int64_t B, int64_t Hq, int64_t Hkv,
+                              int64_t N, int64_t d, double scale, int round_p, const int64_t* rows,
+                              int64_t nrows, double* o_out, double* lse_out, double* a_out, double* b_out,
+                              int nthreads) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || Hq % Hkv) return -1;
+    if (!rows && nrows != B * Hq * N) return -1;
+    const int64_t G = Hq / Hkv;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+
+#pragma omp parallel
+    {
+        double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+        double* s = (double*)malloc(sizeof(double) * (size_t)N);
+        double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+        double* aa = (double*)malloc(sizeof(double) * (size_t)d);
+        double* bb = (double*)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < nrows; ++r) {
+            const int64_t flat = rows ? rows[r] : r;
+            const int64_t i = flat % N;
+            const int64_t h = (flat / N) % Hq;
+            const int64_t b = flat / (N * Hq);
+            const int64_t g = b * Hkv + h / G;      /* the (batch, KV head) group */
+            const uint8_t* qp = q + ((b * Hq + h) * N + i) * d;
+            const uint8_t* kp = k + g * N * d;
+            const uint8_t* vp = v + g * N * d;
+
+            /* dequantised inputs: code * descale */
+            for (int64_t t = 0; t < d; ++t) qrow[t] = decode_e4m3(qp[t]) * qd[g];
+            double m = -INFINITY;
+            for (int64_t j = 0; j < N; ++j) {
+                double dot = 0.0;
+                for (int64_t t = 0; t < d; ++t) dot += qrow[t] * (decode_e4m3(kp[j * d + t]) * kd[g]);
+                s[j] = scale * dot;
+                if (s[j] > m) m = s[j];
+            }
+            double l = 0.0;
+            for (int64_t t = 0; t < d; ++t) acc[t] = aa[t] = bb[t] = 0.0;
+            for (int64_t j = 0; j < N; ++j) {
+                const double pj = exp(s[j] - m);
+                l += pj;
+                const double wj = round_p ? round_e4m3(256.0 * pj) / 256.0 : pj;
+                for (int64_t t = 0; t < d; ++t) {
+                    const double vv = decode_e4m3(vp[j * d + t]) * vd[g];
+                    acc[t] += wj * vv;
+                    aa[t] += pj * fabs(vv);
+                    bb[t] += fabs(vv);
+                }
+            }
+            for (int64_t t = 0; t < d; ++t) {
+                o_out[r * d + t] = acc[t] / l;
+                if (a_out) a_out[r * d + t] = aa[t] / l;
+                if (b_out) b_out[r * d + t] = bb[t] / l;
+            }
+            lse_out[r] = m + log(l);
+        }
+        free(qrow);
+        free(s);
+        free(acc);
+        free(aa);
+        free(bb);
+    }
+    return 0;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -423,3 +423,151 @@ def test_backward_closed_forms():
     # zero upstream gradient: zero gradients
     dq0, dk0, dv0 = oracle.attention_bwd(q, k, v2, np.zeros_like(do), 0.3, gen.BF16)
     assert not dq0.any() and not dk0.any() and not dv0.any()
+
+
+# ---------------------------------------------------------------- FP8 (e4m3) inputs
+
+def _torch_e4m3():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    return torch
+
+
+def test_e4m3_decode_matches_torch_on_every_code():
+    torch = _torch_e4m3()
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.decode_e4m3(codes)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan) and nan.sum() == 2   # 0x7F and 0xFF
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9 and ours[0x08] == 2.0 ** -6
+
+
+def test_e4m3_rounding_matches_torch_and_the_generator():
+    torch = _torch_e4m3()
+    rng = np.random.default_rng(5)
+    vals = oracle.decode_e4m3(np.arange(127, dtype=np.uint8))
+    mids = (vals[:-1] + vals[1:]) / 2                    # exact ties: go to the even code
+    x = np.concatenate([rng.uniform(-448, 448, 20000), rng.uniform(-2.0 ** -5, 2.0 ** -5, 20000),
+                        mids, -mids, vals, rng.normal(0, 3, 5000)])
+    ours = oracle.round_e4m3(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(ours, ref)
+    assert np.array_equal(ours, oracle.decode_e4m3(gen.e4m3_encode(x)))
+    # ties to even: 17 lies between 16 (code 0x58) and 18 (0x59)
+    assert oracle.round_e4m3(np.array([17.0, 2.0 ** -10, 1.5 * 2.0 ** -9]))[0] == 16.0
+    # saturation above the largest finite value (the GPU conversion is .satfinite)
+    assert oracle.round_e4m3(np.array([460.0, 1e6]))[1] == 448.0
+
+
+def test_fp8_hand_case():
+    with open(os.path.join(GOLDEN, "hand_fp8_n2_d1.json")) as fh:
+        g = json.load(fh)
+    scale = math.log(3.0) / 2.0
+    for case in g["cases"]:
+        q = np.array(case["q_codes"], dtype=np.uint8).reshape(1, 1, 1, 1)
+        k = np.array(case["k_codes"], dtype=np.uint8).reshape(1, 1, 2, 1)
+        v = np.array(case["v_codes"], dtype=np.uint8).reshape(1, 1, 2, 1)
+        # query row 0 only has N = 2 keys: make a 2-row problem with the same query twice
+        q2 = np.concatenate([q, q], axis=2)
+        qd, kd, vd = ([x] for x in case["descales"])
+        o, lse, a, b = oracle.attention_fp8(q2, k, v, qd, kd, vd, scale, round_p=True)
+        assert o[0, 0, 0, 0] == pytest.approx(g["o_method"], abs=1e-14)
+        assert lse[0, 0, 0] == pytest.approx(math.log(4.0), abs=1e-14)
+        assert a[0, 0, 0, 0] == pytest.approx(g["a"], abs=1e-14)
+        assert b[0, 0, 0, 0] == pytest.approx(g["b"], abs=1e-14)
+        o, lse, _, _ = oracle.attention_fp8(q2, k, v, qd, kd, vd, scale, round_p=False)
+        assert o[0, 0, 0, 0] == pytest.approx(g["o_plain"], abs=1e-14)
+
+
+def _fp8_inputs(seed, B=1, Hq=2, Hkv=1, N=64, d=32, amp=1.0):
+    return gen.make_qkv_fp8(seed, B, Hq, Hkv, N, d, amp)
+
+
+def _dequant(codes, descale, heads_per_group):
+    B, H = codes.shape[:2]
+    x = oracle.decode_e4m3(codes)
+    ds = np.asarray(descale, dtype=np.float64).reshape(B, -1)
+    return x * np.repeat(ds, heads_per_group, axis=1)[:, :, None, None]
+
+
+def test_fp8_plain_mode_is_attention_on_dequantised_inputs():
+    torch = pytest.importorskip("torch")
+    B, Hq, Hkv, N, d = 2, 4, 2, 96, 32
+    q, k, v, qd, kd, vd = _fp8_inputs(21, B, Hq, Hkv, N, d)
+    scale = 0.3
+    o, lse, _, _ = oracle.attention_fp8(q, k, v, qd, kd, vd, scale, round_p=False)
+    G = Hq // Hkv
+    qx, kx, vx = _dequant(q, qd, G), _dequant(k, kd, 1), _dequant(v, vd, 1)
+    ref = oracle.attention_f64(qx, kx, vx, scale)
+    assert np.max(np.abs(o - ref)) < 1e-12
+    # and an independent library computation of the same thing
+    kr = torch.from_numpy(np.repeat(kx, G, axis=1))
+    vr = torch.from_numpy(np.repeat(vx, G, axis=1))
+    s = torch.from_numpy(qx) @ kr.transpose(-1, -2) * scale
+    lib = (torch.softmax(s, -1) @ vr).numpy()
+    assert np.max(np.abs(o - lib)) < 1e-12
+    assert np.max(np.abs(lse - torch.logsumexp(s, -1).numpy())) < 1e-12
+
+
+def test_fp8_method_equals_plain_when_weights_are_e4m3_exact():
+    # scores (0, -ln 2, -2 ln 2, -3 ln 2) give 256 p = 256, 128, 64, 32: exact in e4m3
+    scale = math.log(2.0)
+    q = np.full((1, 1, 4, 1), 0x38, dtype=np.uint8)            # q = 1
+    kvals = np.array([0.0, -1.0, -2.0, -3.0])
+    k = gen.e4m3_encode(kvals).reshape(1, 1, 4, 1)
+    assert np.array_equal(oracle.decode_e4m3(k).ravel(), kvals)
+    v = gen.e4m3_encode(np.array([1.0, -2.0, 3.0, 0.5])).reshape(1, 1, 4, 1)
+    one = [1.0]
+    om, lm, _, _ = oracle.attention_fp8(q, k, v, one, one, one, scale, round_p=True)
+    op, lp, _, _ = oracle.attention_fp8(q, k, v, one, one, one, scale, round_p=False)
+    assert np.array_equal(om, op) and np.array_equal(lm, lp)
+    assert om[0, 0, 0, 0] == pytest.approx((1 - 1.0 + 0.75 + 0.0625) / 1.875, abs=1e-15)
+
+
+def test_fp8_rounding_error_within_its_bound():
+    # |o_method - o_plain| <= 2^-4 a + 2^-18 b elementwise (relative rounding
+    # error 2^-4 of e4m3 normals, absolute 2^-10 / 2^8 below 2^-6 * 2^8)
+    q, k, v, qd, kd, vd = _fp8_inputs(22, 1, 2, 1, 512, 64, amp=2.0)
+    om, lm, a, b = oracle.attention_fp8(q, k, v, qd, kd, vd, 0.125, round_p=True)
+    op, lp, _, _ = oracle.attention_fp8(q, k, v, qd, kd, vd, 0.125, round_p=False)
+    err = np.abs(om - op)
+    assert np.all(err <= 2.0 ** -4 * a + 2.0 ** -18 * b + 1e-15)
+    assert err.max() > 0                     # rounding does change the result
+    assert np.array_equal(lm, lp)            # l uses the unrounded weights
+    # V = constant c: the plain output is c, the method's stays within 2^-4 c
+    vc = np.full_like(v, 0x40)                # 2.0
+    om, _, _, _ = oracle.attention_fp8(q, k, vc, qd, kd, [1.0], 0.125, round_p=True)
+    op, _, _, _ = oracle.attention_fp8(q, k, vc, qd, kd, [1.0], 0.125, round_p=False)
+    assert np.max(np.abs(op - 2.0)) < 1e-12
+    assert np.max(np.abs(om - 2.0)) <= 2.0 ** -4 * 2.0
+
+
+def test_fp8_grouped_heads_equal_repeated_heads():
+    B, Hq, Hkv, N, d = 2, 4, 2, 64, 32
+    q, k, v, qd, kd, vd = _fp8_inputs(23, B, Hq, Hkv, N, d)
+    G = Hq // Hkv
+    og, lg, _, _ = oracle.attention_fp8(q, k, v, qd, kd, vd, 0.2)
+    # MHA on repeated K/V: each query head becomes its own group with the
+    # descales of its KV head
+    rep = lambda x: np.repeat(x, G, axis=1)
+    repd = lambda s: np.repeat(np.asarray(s).reshape(B, Hkv), G, axis=1).ravel()
+    om, lm, _, _ = oracle.attention_fp8(q, rep(k), rep(v), repd(qd), repd(kd), repd(vd), 0.2)
+    assert np.array_equal(og, om) and np.array_equal(lg, lm)
+
+
+def test_fp8_generator_quantisation():
+    B, Hq, Hkv, N, d = 2, 4, 2, 64, 32
+    q, k, v, qd, kd, vd = gen.make_qkv_fp8(31, B, Hq, Hkv, N, d)
+    assert q.dtype == np.uint8 and qd.dtype == np.float32 and qd.shape == (B * Hkv,)
+    x = gen.normals(31, 0, q.size).reshape(q.shape)
+    G = Hq // Hkv
+    for t, ds, heads in ((q, qd, G), (k, kd, 1), (v, vd, 1)):
+        deq = _dequant(t, ds, heads)
+        groups = np.abs(t.reshape(B * Hkv, -1) & 0x7F).max(axis=1)
+        assert np.all(groups == 0x7E)                      # every group reaches 448
+    deq = _dequant(q, qd, G)
+    rel = np.abs(deq - x) / np.maximum(np.abs(x), 2.0 ** -6 * np.repeat(qd.reshape(B, Hkv), G, 1)[:, :, None, None])
+    assert rel.max() <= 2.0 ** -4 + 1e-6
