@@ -69,8 +69,7 @@ def _load():
         lib.oracle_round_e4m3.argtypes = [p, i64, p]
         lib.oracle_round_e4m3.restype = None
         lib.oracle_attention_fp8_rows.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64,
-                                                  ctypes.c_double, ctypes.c_int, p, i64, p, p, p, p,
-                                                  ctypes.c_int]
+                                                  ctypes.c_double, i64, p, i64, p, p, p, p, p, ctypes.c_int]
         lib.oracle_attention_fp8_rows.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -209,16 +208,18 @@ def round_e4m3(x) -> np.ndarray:
     return out
 
 
-def attention_fp8(q, k, v, q_descale, k_descale, v_descale, scale: float, round_p: bool = True,
-                  rows=None, threads: int = 0):
-    """Attention forward on e4m3 inputs with per-(batch, KV head) descales.
+def attention_fp8_both(q, k, v, q_descale, k_descale, v_descale, scale: float, rows=None,
+                       threads: int = 0, bc: int = 128):
+    """Attention forward on e4m3 inputs with per-(batch, KV head) descales,
+    in one pass: returns (o_method, o_plain, lse, a, b).
 
     q: uint8 [B, Hq, N, d]; k, v: uint8 [B, Hkv, N, d]; descales: [B*Hkv].
-    round_p=True follows the FP8 method (P scaled by 2^8 and rounded to e4m3
-    before the P.V product); round_p=False is the plain definition on the
-    dequantised inputs. Returns (o, lse, a, b): o, a, b [B, Hq, N, d] (or
-    [len(rows), d]) and lse [B, Hq, N] (or [len(rows)]), where
-    a = sum_j p_j |v_j| / l and b = sum_j |v_j| / l elementwise.
+    o_method follows the FP8 method: the online softmax over key tiles of bc
+    keys, with each tile's weights scaled by 2^8 and rounded to e4m3 (against
+    the tile's running max) before the P.V product; o_plain is the plain
+    definition on the dequantised inputs. o_*, a, b: [B, Hq, N, d] (or [len(rows), d]); lse:
+    [B, Hq, N] (or [len(rows)]); a = sum_j p_j |v_j| / l and
+    b = sum_j |v_j| / l elementwise.
     """
     q, k, v = (np.ascontiguousarray(x, dtype=np.uint8) for x in (q, k, v))
     B, Hq, N, d = q.shape
@@ -234,20 +235,26 @@ def attention_fp8(q, k, v, q_descale, k_descale, v_descale, scale: float, round_
     else:
         rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
         nrows, rptr = rows_arr.size, rows_arr.ctypes.data
-    o = np.empty((nrows, d), dtype=np.float64)
-    a = np.empty((nrows, d), dtype=np.float64)
-    b = np.empty((nrows, d), dtype=np.float64)
+    om, op, a, b = (np.empty((nrows, d), dtype=np.float64) for _ in range(4))
     lse = np.empty(nrows, dtype=np.float64)
     rc = _load().oracle_attention_fp8_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, qd.ctypes.data,
                                            kd.ctypes.data, vd.ctypes.data, B, Hq, Hkv, N, d, float(scale),
-                                           int(bool(round_p)), rptr, nrows, o.ctypes.data, lse.ctypes.data,
+                                           int(bc), rptr, nrows, om.ctypes.data, op.ctypes.data, lse.ctypes.data,
                                            a.ctypes.data, b.ctypes.data, int(threads))
     if rc != 0:
         raise ValueError("oracle rejected the sizes")
     if rows is None:
         shp = (B, Hq, N, d)
-        return o.reshape(shp), lse.reshape(B, Hq, N), a.reshape(shp), b.reshape(shp)
-    return o, lse, a, b
+        return om.reshape(shp), op.reshape(shp), lse.reshape(B, Hq, N), a.reshape(shp), b.reshape(shp)
+    return om, op, lse, a, b
+
+
+def attention_fp8(q, k, v, q_descale, k_descale, v_descale, scale: float, round_p: bool = True,
+                  rows=None, threads: int = 0, bc: int = 128):
+    """(o, lse, a, b) of :func:`attention_fp8_both`, with o the method's
+    output (round_p=True) or the plain definition's (round_p=False)."""
+    om, op, lse, a, b = attention_fp8_both(q, k, v, q_descale, k_descale, v_descale, scale, rows, threads, bc)
+    return (om if round_p else op), lse, a, b
 
 
 def softmax_row(q, k, scale: float, dtype: int, row: int) -> np.ndarray:

@@ -402,19 +402,28 @@ int oracle_attention_f64(const double* q, const double* k, const double* v, int6
  *   inputs   e4m3 codes q, k, v with one fp32 descale per (batch, KV head)
  *            for each tensor (the query heads of a KV head share the Q one);
  *            the represented values are code * descale
- *   method   attention on the dequantised values, except that the softmax
- *            weights fed to the P.V product are scaled by 2^8 and rounded to
- *            e4m3 (the P.V product runs on FP8 operands), while l sums the
- *            unrounded weights:
- *              s_j = scale * <qdeq, kdeq_j>,  m = max_j s_j
- *              p_j = exp(s_j - m),            l = sum_j p_j
- *              w_j = e4m3(256 * p_j) / 256    (round_p = 1)   or p_j (round_p = 0)
- *              o   = (sum_j w_j vdeq_j) / l,  lse = m + ln(l)
- *
- * With round_p = 0 this is the plain definition on the dequantised inputs
- * (the quantity the method approximates); with round_p = 1 it follows the
- * method's steps. Two auxiliary row sums bound the effect of rounding P:
- *   a_t = sum_j p_j |vdeq_{j,t}| / l,    b_t = sum_j |vdeq_{j,t}| / l.
+ *   method   FlashAttention-2's forward over key tiles of bc keys (the
+ *            online softmax of "A Case Study in CUDA Kernel Fusion:
+ *            Implementing FlashAttention-2 on NVIDIA Hopper Architecture
+ *            using the CUTLASS Library", abstract, and the Ampere series'
+ *            algorithm): for tile T = keys [T*bc, (T+1)*bc)
+ *              m_T = max(m_{T-1}, max_{j in T} s_j)
+ *              p_j = exp(s_j - m_T)                       (j in T)
+ *              l_T = exp(m_{T-1} - m_T) l_{T-1} + sum_{j in T} p_j
+ *              o_T = exp(m_{T-1} - m_T) o_{T-1} + sum_{j in T} w_j vdeq_j
+ *            with the P.V product on FP8 operands: w_j = e4m3(256 p_j) / 256,
+ *            P scaled by 2^8 and rounded to e4m3 against the running max of
+ *            its tile; l sums the unrounded p_j. o = o_last / l_last,
+ *            lse = m_last + ln(l_last).
+ *   plain    the definition on the dequantised inputs, the quantity the
+ *            method approximates: p_j = exp(s_j - max_j s_j), o = sum p_j
+ *            vdeq_j / sum p_j.
+ * Where the rounding happens relative to a running max, the rounded weights
+ * of a tile depend on the tiling, so the method output depends on bc (the
+ * kernel's key tile is 128); with bc >= N it rounds against the final max.
+ * Two auxiliary row sums bound the effect of rounding P (any bc):
+ *   a_t = sum_j p_j |vdeq_{j,t}| / l,    b_t = sum_j |vdeq_{j,t}| / l
+ * with p_j and l of the plain definition.
  */
 
 /* Exact value of an e4m3 code (OCP 8-bit floating point, E4M3: sign, 4-bit
@@ -460,15 +469,16 @@ void oracle_round_e4m3(const double* x, int64_t n, double* out) {
 
 /*
  * q: [B, Hq, N, d] e4m3 codes; k, v: [B, Hkv, N, d] codes; qd, kd, vd:
- * [B*Hkv] descales. rows: flat query rows (b*Hq + h)*N + i or NULL for all.
- * o, a, bsum: [nrows, d]; lse: [nrows]. a and bsum may be NULL.
+ * [B*Hkv] descales. bc: key tile of the method (>= 1). rows: flat query rows
+ * (b*Hq + h)*N + i or NULL for all. o_method, o_plain, a_out, b_out:
+ * [nrows, d], each may be NULL; lse: [nrows] (the plain definition's).
  */
 int oracle_attention_fp8_rows(const uint8_t* q, const uint8_t* k, const uint8_t* v, const double* qd,
                               const double* kd, const double* vd, int64_t B, int64_t Hq, int64_t Hkv,
-                              int64_t N, int64_t d, double scale, int round_p, const int64_t* rows,
-                              int64_t nrows, double* o_out, double* lse_out, double* a_out, double* b_out,
-                              int nthreads) {
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || Hq % Hkv) return -1;
+                              int64_t N, int64_t d, double scale, int64_t bc, const int64_t* rows,
+                              int64_t nrows, double* o_method, double* o_plain, double* lse_out,
+                              double* a_out, double* b_out, int nthreads) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || Hq % Hkv || bc <= 0) return -1;
     if (!rows && nrows != B * Hq * N) return -1;
     const int64_t G = Hq / Hkv;
 #ifdef _OPENMP
@@ -477,11 +487,15 @@ int oracle_attention_fp8_rows(const uint8_t* q, const uint8_t* k, const uint8_t*
     (void)nthreads;
 #endif
 
+    double tab[256];               /* code -> value, so the loops below decode by lookup */
+    for (int c = 0; c < 256; ++c) tab[c] = decode_e4m3((uint8_t)c);
+
 #pragma omp parallel
     {
         double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
         double* s = (double*)malloc(sizeof(double) * (size_t)N);
         double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+        double* accp = (double*)malloc(sizeof(double) * (size_t)d);
         double* aa = (double*)malloc(sizeof(double) * (size_t)d);
         double* bb = (double*)malloc(sizeof(double) * (size_t)d);
 #pragma omp for schedule(dynamic, 4)
@@ -496,29 +510,49 @@ int oracle_attention_fp8_rows(const uint8_t* q, const uint8_t* k, const uint8_t*
             const uint8_t* vp = v + g * N * d;
 
             /* dequantised inputs: code * descale */
-            for (int64_t t = 0; t < d; ++t) qrow[t] = decode_e4m3(qp[t]) * qd[g];
+            for (int64_t t = 0; t < d; ++t) qrow[t] = tab[qp[t]] * qd[g];
             double m = -INFINITY;
             for (int64_t j = 0; j < N; ++j) {
                 double dot = 0.0;
-                for (int64_t t = 0; t < d; ++t) dot += qrow[t] * (decode_e4m3(kp[j * d + t]) * kd[g]);
+                for (int64_t t = 0; t < d; ++t) dot += qrow[t] * (tab[kp[j * d + t]] * kd[g]);
                 s[j] = scale * dot;
                 if (s[j] > m) m = s[j];
             }
+            /* plain definition and the two bounding sums */
             double l = 0.0;
-            for (int64_t t = 0; t < d; ++t) acc[t] = aa[t] = bb[t] = 0.0;
+            for (int64_t t = 0; t < d; ++t) accp[t] = aa[t] = bb[t] = 0.0;
             for (int64_t j = 0; j < N; ++j) {
                 const double pj = exp(s[j] - m);
                 l += pj;
-                const double wj = round_p ? round_e4m3(256.0 * pj) / 256.0 : pj;
                 for (int64_t t = 0; t < d; ++t) {
-                    const double vv = decode_e4m3(vp[j * d + t]) * vd[g];
-                    acc[t] += wj * vv;
+                    const double vv = tab[vp[j * d + t]] * vd[g];
+                    accp[t] += pj * vv;
                     aa[t] += pj * fabs(vv);
                     bb[t] += fabs(vv);
                 }
             }
+            /* the method: online softmax over key tiles, P rounded per tile */
+            double mt = -INFINITY, lt = 0.0;
+            for (int64_t t = 0; t < d; ++t) acc[t] = 0.0;
+            for (int64_t j0 = 0; j0 < N; j0 += bc) {
+                const int64_t j1 = j0 + bc < N ? j0 + bc : N;
+                double mnew = mt;
+                for (int64_t j = j0; j < j1; ++j)
+                    if (s[j] > mnew) mnew = s[j];
+                const double alpha = mt == -INFINITY ? 0.0 : exp(mt - mnew);
+                lt *= alpha;
+                for (int64_t t = 0; t < d; ++t) acc[t] *= alpha;
+                mt = mnew;
+                for (int64_t j = j0; j < j1; ++j) {
+                    const double pj = exp(s[j] - mt);
+                    lt += pj;
+                    const double wj = round_e4m3(256.0 * pj) / 256.0;
+                    for (int64_t t = 0; t < d; ++t) acc[t] += wj * (tab[vp[j * d + t]] * vd[g]);
+                }
+            }
             for (int64_t t = 0; t < d; ++t) {
-                o_out[r * d + t] = acc[t] / l;
+                if (o_method) o_method[r * d + t] = acc[t] / lt;
+                if (o_plain) o_plain[r * d + t] = accp[t] / l;
                 if (a_out) a_out[r * d + t] = aa[t] / l;
                 if (b_out) b_out[r * d + t] = bb[t] / l;
             }
@@ -527,6 +561,7 @@ int oracle_attention_fp8_rows(const uint8_t* q, const uint8_t* k, const uint8_t*
         free(qrow);
         free(s);
         free(acc);
+        free(accp);
         free(aa);
         free(bb);
     }

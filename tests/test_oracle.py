@@ -473,8 +473,10 @@ def test_fp8_hand_case():
         # query row 0 only has N = 2 keys: make a 2-row problem with the same query twice
         q2 = np.concatenate([q, q], axis=2)
         qd, kd, vd = ([x] for x in case["descales"])
-        o, lse, a, b = oracle.attention_fp8(q2, k, v, qd, kd, vd, scale, round_p=True)
+        o, lse, a, b = oracle.attention_fp8(q2, k, v, qd, kd, vd, scale, round_p=True, bc=g["bc_for_o_method"])
         assert o[0, 0, 0, 0] == pytest.approx(g["o_method"], abs=1e-14)
+        o1, _, _, _ = oracle.attention_fp8(q2, k, v, qd, kd, vd, scale, round_p=True, bc=1)
+        assert o1[0, 0, 0, 0] == pytest.approx(g["o_method_bc1"], abs=1e-14)
         assert lse[0, 0, 0] == pytest.approx(math.log(4.0), abs=1e-14)
         assert a[0, 0, 0, 0] == pytest.approx(g["a"], abs=1e-14)
         assert b[0, 0, 0, 0] == pytest.approx(g["b"], abs=1e-14)
@@ -571,3 +573,30 @@ def test_fp8_generator_quantisation():
     deq = _dequant(q, qd, G)
     rel = np.abs(deq - x) / np.maximum(np.abs(x), 2.0 ** -6 * np.repeat(qd.reshape(B, Hkv), G, 1)[:, :, None, None])
     assert rel.max() <= 2.0 ** -4 + 1e-6
+
+
+def test_fp8_tiling_changes_nothing_when_the_max_comes_first():
+    # Online softmax over key tiles: if every row's largest score sits in the
+    # first tile, the running max is final from the first tile on, so each
+    # weight is rounded exactly as without tiling (bc >= N).
+    N, d = 300, 16
+    q, k, v, qd, kd, vd = gen.make_qkv_fp8(41, 1, 1, 1, N, d)
+    q = q[:, :, :1].copy()
+    k = k.copy()
+    k[0, 0, 0] = q[0, 0, 0]                 # key 0 parallel to the query
+    one = [1.0]
+    qx = oracle.decode_e4m3(q).reshape(d)
+    kx = oracle.decode_e4m3(k).reshape(N, d)
+    assert np.argmax(kx @ qx) == 0          # the premise: key 0 has the top score
+    qq = np.concatenate([q] * N, axis=2)    # N query rows so that q is [1, 1, N, d]
+    o_all, _, _, _ = oracle.attention_fp8(qq, k, v, one, one, one, 0.7, bc=N)
+    for bc in (1, 7, 128, 299, 1000):
+        o_bc, _, _, _ = oracle.attention_fp8(qq, k, v, one, one, one, 0.7, bc=bc)
+        assert np.array_equal(o_bc[0, 0, 0], o_all[0, 0, 0])
+
+
+def test_fp8_tiled_method_stays_within_the_rounding_bound():
+    q, k, v, qd, kd, vd = _fp8_inputs(42, 1, 2, 1, 700, 32, amp=2.0)
+    for bc in (1, 64, 128, 700):
+        om, op, lp, a, b = oracle.attention_fp8_both(q, k, v, qd, kd, vd, 0.2, bc=bc)
+        assert np.all(np.abs(om - op) <= 2.0 ** -4 * a + 2.0 ** -18 * b + 1e-15)
