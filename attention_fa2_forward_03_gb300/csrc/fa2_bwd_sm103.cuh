@@ -1,5 +1,6 @@
-// Backward pass of the attention forward in fa2_fwd_sm103.cu (included by
-// it, so both share the status word and the PTX wrappers).
+// Backward pass of the attention forward (device code). It shares the
+// forward's status word, watchdog and PTX wrappers (fa2_fwd_sm103.cuh);
+// fa2_fwd_sm103.cu holds the host side.
 //
 // The forward pages exclude the backward pass ("FlashAttention-2 from
 // scratch on Ampere, Part 1", Kernel Specification: forward pass only); the
@@ -21,6 +22,8 @@
 // Warps 0-3 elementwise (thread = TMEM lane), warp 4 TMA producer, warp 5
 // TMEM allocator and MMA issuer. TMEM: S | dP | two d-column accumulators.
 #pragma once
+
+#include "fa2_fwd_sm103.cuh"
 
 namespace fa2 {
 namespace bwd {

@@ -1,0 +1,542 @@
+// FP8 (e4m3) attention forward for GB300 (sm_103a). Device code; it shares
+// the 16-bit kernel's work items, parameters, watchdog and roles' constants
+// (fa2_fwd_sm103.cuh). fa2_fwd_sm103.cu holds the host side.
+//
+// What is computed: attention on quantised inputs with the scales applied
+// inside the kernel, the inference variant of "FlashAttention-3 for
+// Inference: INT8 Quantization and Query Head Packing for MQA/GQA" (Colfax
+// Research author page), which names in-kernel pre-processing of the inputs
+// by specialised warps and query-head packing. Q, K, V are e4m3 codes with
+// one fp32 descale per (batch, KV head) and tensor; O is bf16, LSE fp32:
+//   S = (scale * dq * dk) * Q8 K8^T                      (tcgen05 kind::f8f6f4)
+//   P' = exp2(S log2e - m + 8) in (0, 256], rounded to e4m3   (m: exact row max)
+//   O = dv * (P'8 V8) / l',   l' = sum of the unrounded P'
+//   LSE = (m + log2 l' - 8) * ln 2
+// The 2^8 factor moves P's range (0, 1] up to where e4m3 has its precision;
+// it cancels in O / l' and is taken out of the LSE.
+//
+// How: the 16-bit kernel's persistent, warp-specialised pipeline (two query
+// tiles per item, softmax warpgroups 0-1, correction warpgroup 2, TMA
+// producer warp 12, MMA warp 13) with two changes. Both GEMMs run on 8-bit
+// operands, so the P V product needs V with keys contiguous (K-major): warps
+// 14-15, idle in the 16-bit kernel, transpose each V tile in shared memory
+// into a double-buffered V^T tile (the in-kernel pre-processing); the MMA
+// waits on V^T instead of V. And P is packed four per TMEM column.
+// Head dimension 128 (one 128-byte swizzle row per tile row), N % 128 == 0.
+#pragma once
+
+#include "fa2_fwd_sm103.cuh"
+
+namespace fa2 {
+namespace fp8 {
+
+constexpr int kD = 128;              // head dimension = bytes per tile row
+constexpr int kTile = kBM * kD;      // 16 KB: one Q, K, V or V^T tile
+constexpr int kStages = 8;           // K/V ring; K_j in even stages, V_j in odd ones
+constexpr int kXposeWarp0 = 14;      // warps 14, 15
+
+struct Lay {
+    static constexpr int kQOff = 0;
+    static constexpr int kRingOff = kNQ * kTile;
+    static constexpr int kVtOff = kRingOff + kStages * kTile;
+    static constexpr int kBarOff = kVtOff + 2 * kTile;
+    // q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] alpha[2] stats[2]
+    // p_full[2] o_full[2] mma_done vt_full[2] vt_empty[2]
+    static constexpr int kNumBars = 2 * kStages + 19;
+    static constexpr int kRowOff = kBarOff + kNumBars * 8;  // alpha[2][128], m[2][128], l[2][128]
+    static constexpr int kMiscOff = kRowOff + 3 * kNQ * kBM * 4;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+    static constexpr uint32_t kTmemCols = 512;  // S_0 | S_1 | O_0 | O_1
+    static __device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
+    static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + kD * t; }
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(kStages % 2 == 0, "K and V must keep their stage parity");
+};
+
+struct BarsF8 {
+    uint32_t base;
+    static constexpr int S = kStages;
+    __device__ uint32_t q_full(int t) const { return base + 8 * t; }
+    __device__ uint32_t q_empty(int t) const { return base + 8 * (2 + t); }
+    __device__ uint32_t kv_full(int s) const { return base + 8 * (4 + s); }
+    __device__ uint32_t kv_empty(int s) const { return base + 8 * (4 + S + s); }
+    __device__ uint32_t s_full(int t) const { return base + 8 * (4 + 2 * S + t); }
+    __device__ uint32_t alpha_ready(int t) const { return base + 8 * (6 + 2 * S + t); }
+    __device__ uint32_t stats_ready(int t) const { return base + 8 * (8 + 2 * S + t); }
+    __device__ uint32_t p_full(int t) const { return base + 8 * (10 + 2 * S + t); }
+    __device__ uint32_t o_full(int t) const { return base + 8 * (12 + 2 * S + t); }
+    __device__ uint32_t mma_done() const { return base + 8 * (14 + 2 * S); }
+    __device__ uint32_t vt_full(int b) const { return base + 8 * (15 + 2 * S + b); }
+    __device__ uint32_t vt_empty(int b) const { return base + 8 * (17 + 2 * S + b); }
+};
+
+enum WaitSiteF8 : int { kSiteVtFull = 11, kSiteVtEmpty = 12 };
+
+// (batch, KV head) group of a work item: the index of its descales.
+__device__ __forceinline__ int item_group(const Params& p, int item) { return item / p.pairs; }
+
+// ---------------------------------------------------------------- producer
+
+__device__ __forceinline__ void producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                         const Params& p, uint32_t sbase, const BarsF8& bars, const Waiter& w) {
+    constexpr int S = kStages;
+    int ring = 0;
+    int nq[2] = {0, 0};
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+        const Item item = make_item(p, it);
+        for (int t = 0; t < item.n_tiles && ok; ++t) {
+            if (!(ok = w.wait(bars.q_empty(t), (nq[t] & 1) ^ 1, kSiteQEmpty))) break;
+            ptx::mbar_arrive_expect_tx(bars.q_full(t), kTile);
+            ptx::tma_load_2d(sbase + Lay::kQOff + t * kTile, tmQ, 0, item.q_row0 + t * kBM, bars.q_full(t));
+            ++nq[t];
+        }
+        const int nxt = it + gridDim.x;
+        if (ok && nxt < p.total_items) {
+            const Item ni = make_item(p, nxt);
+            for (int t = 0; t < ni.n_tiles; ++t) ptx::tma_prefetch_l2_2d(tmQ, 0, ni.q_row0 + t * kBM);
+        }
+        for (int k = 0; k < 2 * p.n_kv_tiles && ok; ++k) {
+            const int s = ring % S;
+            if (!(ok = w.wait(bars.kv_empty(s), ((ring / S) & 1) ^ 1, kSiteKvEmpty))) break;
+            ptx::mbar_arrive_expect_tx(bars.kv_full(s), kTile);
+            ptx::tma_load_2d(sbase + Lay::kRingOff + s * kTile, (k & 1) ? tmV : tmK, 0,
+                             item.kv_row0 + (k >> 1) * kBN, bars.kv_full(s));
+            ++ring;
+        }
+    }
+    if (!ok) {
+        const int first = ring > S ? ring - S : 0;
+        for (int r = first; r < ring; ++r) w.drain(bars.kv_full(r % S), (r / S) & 1);
+        for (int t = 0; t < 2; ++t)
+            if (nq[t] > 0) w.drain(bars.q_full(t), (nq[t] - 1) & 1);
+    }
+}
+
+// ---------------------------------------------------------------- V transpose
+
+// Warps 14-15 turn each V tile (keys x dims, dims contiguous, 128-byte
+// swizzle as TMA wrote it) into V^T (dims x keys, keys contiguous, the same
+// swizzle), the K-major B operand of O += P V. A 128-byte swizzled row r
+// keeps its 16-byte chunk c at chunk position c ^ (r % 8).
+//
+// Work split: a unit is 4 keys x 16 dims; lane (qi = lane / 8, j = lane % 8)
+// of warp w takes, in round u, key block br = j (keys 16 br + 4 qi + 0..3) and
+// dim block bc = (j + 2u + w) % 8, so 2 warps x 4 rounds cover all 8 dim
+// blocks of every (br, qi). Each unit is four 16-byte loads (conflict-free:
+// the 8 lanes of a load phase share qi and hold 8 different bc), sixteen
+// 4x4 byte transposes' worth of byte permutes, and sixteen 4-byte stores
+// (conflict-free: the 32 lanes hold 32 different (br, qi), so 32 banks).
+__device__ __forceinline__ void transpose_tile(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int xid) {
+    const int lane = xid & 31;
+    const int w = xid >> 5;
+    const int j = lane & 7;
+    const int qi = lane >> 3;
+    const int br = j;
+#pragma unroll 1   // one unit's 16 words live at a time: the warp runs on 56 registers
+    for (int u = 0; u < 4; ++u) {
+        const int bc = (j + 2 * u + w) & 7;
+        uint32_t x[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = 16 * br + 4 * qi + i;
+            const uint4 v = *reinterpret_cast<const uint4*>(src + r * 128 + ((bc ^ (r & 7)) << 4));
+            x[i][0] = v.x;
+            x[i][1] = v.y;
+            x[i][2] = v.z;
+            x[i][3] = v.w;
+        }
+#pragma unroll
+        for (int wq = 0; wq < 4; ++wq) {
+            // x[i][wq] holds dims 16bc + 4wq + 0..3 of key 16br + 4qi + i;
+            // y[b] gathers dim 16bc + 4wq + b of the four keys.
+            const uint32_t t0 = __byte_perm(x[0][wq], x[1][wq], 0x5140);
+            const uint32_t t1 = __byte_perm(x[0][wq], x[1][wq], 0x7362);
+            const uint32_t t2 = __byte_perm(x[2][wq], x[3][wq], 0x5140);
+            const uint32_t t3 = __byte_perm(x[2][wq], x[3][wq], 0x7362);
+            const uint32_t y[4] = {__byte_perm(t0, t2, 0x5410), __byte_perm(t0, t2, 0x7632),
+                                   __byte_perm(t1, t3, 0x5410), __byte_perm(t1, t3, 0x7632)};
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int c = 16 * bc + 4 * wq + b;
+                *reinterpret_cast<uint32_t*>(dst + c * 128 + ((br ^ (c & 7)) << 4) + 4 * qi) = y[b];
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void xpose_role(const Params& p, uint8_t* smem, const BarsF8& bars, const Waiter& w) {
+    constexpr int S = kStages;
+    const int xid = threadIdx.x - kXposeWarp0 * 32;
+    const int lane = xid & 31;
+    int ring = 0;   // K/V ring items (same sequence as the producer's)
+    int nv = 0;     // V tiles transposed
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+        for (int jt = 0; jt < p.n_kv_tiles; ++jt, ++nv) {
+            ++ring;                      // K_jt: not ours
+            const int r = ring++;        // V_jt
+            const int s = r % S;
+            const int b = nv & 1;
+            ok = w.wait(bars.kv_full(s), (r / S) & 1, kSiteKvFull);
+            if (ok) ok = w.wait(bars.vt_empty(b), ((nv >> 1) & 1) ^ 1, kSiteVtEmpty);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            transpose_tile(smem + Lay::kRingOff + s * kTile, smem + Lay::kVtOff + b * kTile, xid);
+            // Make this thread's generic-proxy stores visible to the tensor
+            // core (async proxy) before the warp's arrival publishes them.
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(bars.vt_full(b));
+                ptx::mbar_arrive(bars.kv_empty(s));
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- MMA issuer
+
+__device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint32_t tmem, const BarsF8& bars,
+                                           const Waiter& w) {
+    constexpr int S = kStages;
+    // e4m3 x e4m3 -> f32; both operands K-major (V is transposed in smem)
+    constexpr uint32_t kIdS = ptx::idesc_f16(0u, 0, 0, kBM, kBN);
+    constexpr uint32_t kIdO = ptx::idesc_f16(0u, 0, 0, kBM, kD);
+    auto stage_addr = [&](int r) { return sbase + Lay::kRingOff + (r % S) * kTile; };
+    auto issue_qk = [&](int t, uint32_t kaddr) {
+        const uint64_t qd = ptx::desc_sw128(sbase + Lay::kQOff + t * kTile, 16, 1024);
+        const uint64_t kd = ptx::desc_sw128(kaddr, 16, 1024);
+        ptx::mma_ss_kloop4_f8(tmem + Lay::col_s(t), qd, kd, kIdS, 0u);
+    };
+    auto issue_pv = [&](int t, int vb, bool acc) {
+        const uint64_t vd = ptx::desc_sw128(sbase + Lay::kVtOff + vb * kTile, 16, 1024);
+        ptx::mma_ts_kloop4_f8(tmem + Lay::col_o(t), tmem + Lay::col_s(t), vd, kIdO, acc ? 1u : 0u);
+    };
+    auto wait_u = [&](uint32_t bar, uint32_t parity, int site) {
+        return __shfl_sync(0xffffffffu, w.wait(bar, parity, site) ? 1 : 0, 0) != 0;
+    };
+    auto wait_ring = [&](int r) { return wait_u(bars.kv_full(r % S), (r / S) & 1, kSiteKvFull); };
+
+    const int nkv = p.n_kv_tiles;
+    int ring = 0;
+    int nv = 0;                   // V^T tiles consumed
+    int nq[2] = {0, 0};
+    int np[2] = {0, 0};
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+        const int nt = make_item(p, it).n_tiles;
+        for (int t = 0; t < nt && ok; ++t) ok = wait_u(bars.q_full(t), nq[t] & 1, kSiteQFull);
+        if (!ok || !(ok = wait_ring(ring))) break;
+        ptx::tc_fence_after();
+        for (int t = 0; t < nt; ++t) {
+            issue_qk(t, stage_addr(ring));
+            ptx::tc_commit_elect(bars.s_full(t));
+            if (nkv == 1) ptx::tc_commit_elect(bars.q_empty(t));
+        }
+        ptx::tc_commit_elect(bars.kv_empty(ring % S));
+        int k_ring = ring;
+        ++ring;
+        for (int j = 0; j < nkv; ++j) {
+            const bool more = j + 1 < nkv;
+            ++ring;                       // V_j: released by the transposer
+            const int vb = nv & 1;
+            if (!(ok = wait_u(bars.vt_full(vb), (nv >> 1) & 1, kSiteVtFull))) break;
+            ++nv;
+            if (more) {
+                k_ring = ring++;
+                if (!(ok = wait_ring(k_ring))) break;
+            }
+            for (int t = 0; t < nt; ++t) {
+                if (!(ok = wait_u(bars.p_full(t), np[t] & 1, kSitePFull))) break;
+                ++np[t];
+                ptx::tc_fence_after();
+                issue_pv(t, vb, j > 0);
+                if (t == nt - 1) ptx::tc_commit_elect(bars.vt_empty(vb));
+                if (more) {
+                    issue_qk(t, stage_addr(k_ring));
+                    ptx::tc_commit_elect(bars.s_full(t));
+                    if (j + 2 == nkv) ptx::tc_commit_elect(bars.q_empty(t));
+                    if (t == nt - 1) ptx::tc_commit_elect(bars.kv_empty(k_ring % S));
+                } else {
+                    ptx::tc_commit_elect(bars.o_full(t));
+                }
+            }
+            if (!ok) break;
+        }
+        for (int t = 0; t < nt; ++t) ++nq[t];
+    }
+    ptx::tc_commit_elect(bars.mma_done());
+    w.drain(bars.mma_done(), 0);
+    __syncwarp();
+}
+
+// ---------------------------------------------------------------- softmax
+
+__device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uint8_t* smem, const BarsF8& bars,
+                                             const Waiter& w, int t) {
+    const int row = threadIdx.x & 127;
+    const uint32_t row_addr = tmem + (static_cast<uint32_t>(row & ~31) << 16);
+    const uint32_t colS = Lay::col_s(t);
+    float* alpha_buf = reinterpret_cast<float*>(smem + Lay::kRowOff) + t * kBM;
+    float* m_buf = alpha_buf + kNQ * kBM;
+    float* l_buf = m_buf + kNQ * kBM;
+
+    int n_s = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+        if (t >= make_item(p, it).n_tiles) continue;
+        const int g = item_group(p, it);
+        // log2-domain factor of the raw code products: scale * log2(e) * dq * dk
+        const float c = p.scale_log2 * __ldg(p.q_descale + g) * __ldg(p.k_descale + g);
+        const uint64_t c2 = ptx::f2_pack(c, c);
+        const int nkv = p.n_kv_tiles;
+        float m = -INFINITY;
+        float l = 0.0f;       // sum of the unrounded 2^8-scaled weights
+        for (int j = 0; j < nkv; ++j, ++n_s) {
+            ok = w.wait(bars.s_full(t), n_s & 1, kSiteSFull);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            uint32_t s[kBN];
+            ptx::tmem_ld32_at<0>(row_addr + colS + 0, s);
+            ptx::tmem_ld32_at<32>(row_addr + colS + 32, s);
+            ptx::tmem_ld32_at<64>(row_addr + colS + 64, s);
+            ptx::tmem_ld32_at<96>(row_addr + colS + 96, s);
+            ptx::tmem_wait_ld();
+
+            float mx[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                float a = __uint_as_float(s[k]);
+#pragma unroll
+                for (int i = 1; i < 15; i += 2)
+                    a = ptx::max3(a, __uint_as_float(s[k + 8 * i]), __uint_as_float(s[k + 8 * (i + 1)]));
+                mx[k] = fmaxf(a, __uint_as_float(s[k + 120]));
+            }
+            // c > 0, so the max of c*s is c times the max of s
+            const float m_tile =
+                fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7]))) * c;
+            const float m_new = fmaxf(m, m_tile);
+            const float alpha = (j == 0 || m_new == m) ? 1.0f : ptx::ex2_approx(m - m_new);
+            alpha_buf[row] = alpha;
+            ptx::mbar_arrive(bars.alpha_ready(t));
+            l *= alpha;
+            m = m_new;
+
+            // P' = exp2(S c - m + 8), four at a time into one TMEM column.
+            const uint64_t nm2 = ptx::f2_pack(8.0f - m, 8.0f - m);
+            uint64_t acc[4] = {0, 0, 0, 0};
+            uint32_t pk[kBN / 4];
+#pragma unroll
+            for (int i = 0; i < kBN / 4; ++i) {
+                float pr[4];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int e = 4 * i + 2 * h;
+                    const uint64_t x =
+                        ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), c2, nm2);
+                    if ((i & 3) == 3 && h == 1) {   // one pair in eight on the FMA pipe
+                        ptx::f2_unpack(ptx::ex2_poly_f2(x), pr[2 * h], pr[2 * h + 1]);
+                    } else {
+                        float x0, x1;
+                        ptx::f2_unpack(x, x0, x1);
+                        pr[2 * h] = ptx::ex2_approx(x0);
+                        pr[2 * h + 1] = ptx::ex2_approx(x1);
+                    }
+                    acc[(2 * i + h) & 3] = ptx::f2_add(acc[(2 * i + h) & 3], ptx::f2_pack(pr[2 * h], pr[2 * h + 1]));
+                }
+                pk[i] = ptx::pack4_e4m3(pr[0], pr[1], pr[2], pr[3]);
+            }
+            float a0, a1;
+            ptx::f2_unpack(ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3])), a0, a1);
+            l += a0 + a1;
+            ptx::tmem_st32_at<0>(row_addr + colS, pk);
+            if (j + 1 == nkv) {
+                m_buf[row] = m;
+                l_buf[row] = l;
+                ptx::mbar_arrive(bars.stats_ready(t));
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bars.p_full(t));
+        }
+    }
+}
+
+// ---------------------------------------------------------------- correction + epilogue
+
+__device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, uint8_t* smem, const BarsF8& bars,
+                                                const Waiter& w) {
+    constexpr int kChunk = 32;
+    const int q = (threadIdx.x / 32) & 3;
+    const int lane = threadIdx.x & 31;
+    const int row = 32 * q + lane;
+    const uint32_t row_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    const float* rowbuf = reinterpret_cast<const float*>(smem + Lay::kRowOff);
+
+    int n_s[2] = {0, 0};
+    int n_items[2] = {0, 0};
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+        const Item item = make_item(p, it);
+        const int n_tiles = item.n_tiles;
+        const float dv = __ldg(p.v_descale + item_group(p, it));
+        for (int j = 0; j < p.n_kv_tiles && ok; ++j) {
+            for (int t = 0; t < n_tiles; ++t) {
+                ok = w.wait(bars.alpha_ready(t), n_s[t] & 1, kSiteAlpha);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                ++n_s[t];
+                const float alpha = rowbuf[t * kBM + row];
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+                    ptx::tc_fence_after();
+                    const uint32_t colO = Lay::col_o(t);
+                    const uint64_t a2 = ptx::f2_pack(alpha, alpha);
+#pragma unroll
+                    for (int h = 0; h < kD; h += kChunk) {
+                        uint32_t o[kChunk];
+                        ptx::tmem_ld32_at<0>(row_addr + colO + h, o);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < kChunk / 2; ++i) {
+                            float o0, o1;
+                            ptx::f2_unpack(
+                                ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
+                                            a2),
+                                o0, o1);
+                            o[2 * i] = __float_as_uint(o0);
+                            o[2 * i + 1] = __float_as_uint(o1);
+                        }
+                        ptx::tmem_st32_at<0>(row_addr + colO + h, o);
+                    }
+                    ptx::tmem_wait_st();
+                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bars.p_full(t));
+            }
+        }
+        // Epilogue: O * dv / l' -> bf16, LSE = (m + log2 l' - 8) ln 2.
+        for (int t = 0; t < n_tiles && ok; ++t) {
+            const int grow = item.q_row0 + t * kBM + row;
+            ok = w.wait(bars.stats_ready(t), n_items[t] & 1, kSiteStats);
+            if (ok) ok = w.wait(bars.o_full(t), n_items[t] & 1, kSiteOFull);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            ++n_items[t];
+            ptx::tc_fence_after();
+            const float m = rowbuf[(2 + t) * kBM + row];
+            const float l = rowbuf[(4 + t) * kBM + row];
+            const float f = dv * ptx::rcp_approx(l);
+            const uint32_t colO = Lay::col_o(t);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + static_cast<size_t>(grow) * kD);
+#pragma unroll
+            for (int h = 0; h < kD; h += kChunk) {
+                uint32_t o[kChunk];
+                ptx::tmem_ld32_at<0>(row_addr + colO + h, o);
+                ptx::tmem_wait_ld();
+                uint32_t hv[kChunk / 2];
+#pragma unroll
+                for (int i = 0; i < kChunk / 2; ++i)
+                    hv[i] = ptx::pack2<true>(__uint_as_float(o[2 * i]) * f, __uint_as_float(o[2 * i + 1]) * f);
+#pragma unroll
+                for (int v = 0; v < kChunk / 8; ++v)
+                    dst[h / 8 + v] = make_uint4(hv[4 * v], hv[4 * v + 1], hv[4 * v + 2], hv[4 * v + 3]);
+            }
+            p.lse[grow] = (m + ptx::lg2_approx(l) - 8.0f) * 0.69314718055994530942f;
+        }
+        ptx::tc_fence_before();
+    }
+}
+
+}  // namespace fp8
+
+// ---------------------------------------------------------------- kernel
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fa2_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const Params p) {
+    using L = fp8::Lay;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = ptx::smem_addr(smem);
+    const fp8::BarsF8 bars{sbase + L::kBarOff};
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(bars.q_full(t), 1);
+            ptx::mbar_init(bars.q_empty(t), 1);
+            ptx::mbar_init(bars.s_full(t), 1);
+            ptx::mbar_init(bars.alpha_ready(t), kBM);
+            ptx::mbar_init(bars.stats_ready(t), kBM);
+            ptx::mbar_init(bars.p_full(t), 2 * kBM);
+            ptx::mbar_init(bars.o_full(t), 1);
+            ptx::mbar_init(bars.vt_full(t), 2);    // one arrival per transposer warp
+            ptx::mbar_init(bars.vt_empty(t), 1);   // tcgen05.commit after the P V MMAs
+        }
+        for (int s = 0; s < fp8::kStages; ++s) {
+            ptx::mbar_init(bars.kv_full(s), 1);
+            // K stages are released by the MMA warp's commit, V stages by the
+            // two transposer warps
+            ptx::mbar_init(bars.kv_empty(s), (s & 1) ? 2 : 1);
+        }
+        ptx::mbar_init(bars.mma_done(), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == kLoadWarp && lane == 0) {
+        ptx::tma_prefetch_desc(&tmQ);
+        ptx::tma_prefetch_desc(&tmK);
+        ptx::tma_prefetch_desc(&tmV);
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), L::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Waiter w{abort_flag, p.wait_limit_ns};
+
+    if (warp < kCorrWarp0) {
+        ptx::setmaxnreg_inc<kRegSoftmax>();
+        fp8::softmax_role(p, tmem, smem, bars, w, warp / 4);
+    } else if (warp < kLoadWarp) {
+        ptx::setmaxnreg_dec<kRegCorr>();
+        fp8::correction_role(p, tmem, smem, bars, w);
+    } else {
+        ptx::setmaxnreg_dec<kRegOther>();
+        if (warp == kLoadWarp) {
+            if (lane == 0) fp8::producer(&tmQ, &tmK, &tmV, p, sbase, bars, w);
+            __syncwarp();
+        } else if (warp == kMmaWarp) {
+            fp8::mma_issuer(p, sbase, tmem, bars, w);
+        } else {
+            fp8::xpose_role(p, smem, bars, w);
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+}  // namespace fa2

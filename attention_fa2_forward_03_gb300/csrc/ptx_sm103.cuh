@@ -440,8 +440,8 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo_byte
     return d;
 }
 
-// Instruction descriptor for tcgen05.mma.kind::f16 with fp32 accumulation.
-// ab_type: 0 = fp16, 1 = bf16. a_mn / b_mn: operand is MN-major (1) or
+// Instruction descriptor for tcgen05.mma with fp32 accumulation.
+// ab_type: with kind::f16 0 = fp16, 1 = bf16; with kind::f8f6f4 0 = e4m3. a_mn / b_mn: operand is MN-major (1) or
 // K-major (0). M in {64, 128}, N a multiple of 16 up to 256.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_type, uint32_t a_mn, uint32_t b_mn,
                                                  uint32_t M, uint32_t N) {
@@ -564,6 +564,68 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
         asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     else
         asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// ---------------------------------------------------------------- 8-bit (kind::f8f6f4)
+
+// S (+)= A B^T over one 128-byte K extent of e4m3 operands: 4 MMAs of K = 32,
+// both operands K-major with the 128-byte swizzle; step kk starts 32*kk bytes
+// into the rows (+2 per step in the descriptors' 16-byte units). Step 0
+// accumulates iff `acc`. idesc carries the operand formats (e4m3 = 0).
+__device__ __forceinline__ void mma_ss_kloop4_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred e, p0, pt;\n\t.reg .b32 alo, ahi, blo, bhi, t0, t1;\n\t.reg .b64 a, b;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\t"
+        "setp.eq.b32 pt, %4, %4;\n\t"
+        "mov.b64 {alo, ahi}, %1;\n\t"
+        "mov.b64 {blo, bhi}, %2;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p0;\n\t"
+        "add.u32 t0, alo, 2;\n\tmov.b64 a, {t0, ahi};\n\tadd.u32 t1, blo, 2;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, pt;\n\t"
+        "add.u32 t0, alo, 4;\n\tmov.b64 a, {t0, ahi};\n\tadd.u32 t1, blo, 4;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, pt;\n\t"
+        "add.u32 t0, alo, 6;\n\tmov.b64 a, {t0, ahi};\n\tadd.u32 t1, blo, 6;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, pt;\n\t"
+        "}" ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// O (+)= P B^T with P (e4m3, four per 32-bit column) read from TMEM and B
+// K-major in shared memory: 4 MMAs of K = 32; A advances 8 columns and B 32
+// bytes per step.
+__device__ __forceinline__ void mma_ts_kloop4_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred e, p0, pt;\n\t.reg .b32 blo, bhi, t0, t1;\n\t.reg .b64 b;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\t"
+        "setp.eq.b32 pt, %4, %4;\n\t"
+        "mov.b64 {blo, bhi}, %2;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p0;\n\t"
+        "add.u32 t0, %1, 8;\n\tadd.u32 t1, blo, 2;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [t0], b, %3, pt;\n\t"
+        "add.u32 t0, %1, 16;\n\tadd.u32 t1, blo, 4;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [t0], b, %3, pt;\n\t"
+        "add.u32 t0, %1, 24;\n\tadd.u32 t1, blo, 6;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [t0], b, %3, pt;\n\t"
+        "}" ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// Four fp32 values to four e4m3 bytes, x0 in bits 0..7: round to nearest
+// even, saturating at +-448 (the conversion puts its first source in the
+// upper byte of each 16-bit half).
+__device__ __forceinline__ uint32_t pack4_e4m3(float x0, float x1, float x2, float x3) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
     return r;
 }
 

@@ -53,15 +53,20 @@ UNIT = "TFLOP/s"
 L2_BYTES = 129 * 1024 * 1024
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 CSRC = os.path.join(ROOT, "attention_fa2_forward_03_gb300", "csrc")
-KERNEL_SOURCES = [os.path.join(CSRC, "fa2_fwd_sm103.cu"), os.path.join(CSRC, "ptx_sm103.cuh")]
+# Device code of each kernel (host planning code is not part of it)
+KERNEL_SOURCES = [os.path.join(CSRC, "fa2_fwd_sm103.cuh"), os.path.join(CSRC, "ptx_sm103.cuh")]
 BWD_SOURCES = KERNEL_SOURCES + [os.path.join(CSRC, "fa2_bwd_sm103.cuh")]
+FP8_SOURCES = KERNEL_SOURCES + [os.path.join(CSRC, "fa2_fwd_fp8_sm103.cuh")]
 PASSES = ("fwd", "fwd_causal", "bwd", "bwd_causal")
 REASON_FIELDS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
 
 def kernel_source_hash(which: str = "fwd") -> str:
+    """sha256[:16] of the device code a pass runs: "fwd" (16-bit forward,
+    also fwd_causal), "bwd*" or "fp8"."""
     h = hashlib.sha256()
-    for f in (BWD_SOURCES if which.startswith("bwd") else KERNEL_SOURCES):
+    files = BWD_SOURCES if which.startswith("bwd") else FP8_SOURCES if which == "fp8" else KERNEL_SOURCES
+    for f in files:
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -192,14 +197,19 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ peaks and traffic
 
-def load_peak():
+def load_peak(fp8: bool = False):
+    """Dense tensor peak for the kernel's operand type: the measured bf16
+    burst figure, times the nominal fp8 : bf16 ratio (4.5 : 2.25 PFLOP/s)
+    for FP8 operands."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    ratio, tag = (2.0, " x 2 (nominal fp8:bf16 ratio)") if fp8 else (1.0, "")
     try:
         with open(path) as fh:
             peaks = json.load(fh)
-        return float(peaks["bf16_tflops"]), "measured (bf16_tflops burst, MEASURED_PEAKS.json)"
+        return (float(peaks["bf16_tflops"]) * ratio,
+                "measured (bf16_tflops burst, MEASURED_PEAKS.json)" + tag)
     except (OSError, KeyError, ValueError):
-        return 1900.0, "fallback (1.9 PFLOP/s bf16 burst)"
+        return 1900.0 * ratio, "fallback (1.9 PFLOP/s bf16 burst)" + tag
 
 
 def traffic_key(workload: str, which: str) -> str:
@@ -216,7 +226,8 @@ def load_traffic(workload: str, which: str = "fwd"):
     except (OSError, ValueError):
         return None
     entry = rec.get(traffic_key(workload, which))
-    if not entry or entry.get("kernel_source_sha") != kernel_source_hash(which):
+    src = "fp8" if gen.workload(workload).fp8 else which
+    if not entry or entry.get("kernel_source_sha") != kernel_source_hash(src):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -248,7 +259,19 @@ def pass_bytes(w, which: str) -> int:
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def oracle_rows_for(w, seconds: float, q, k, v, causal: bool = False):
+def oracle_forward(w, inputs, rows, causal: bool = False):
+    """The oracle's forward on a row sample of this workload."""
+    import oracle
+
+    if w.fp8:
+        return oracle.attention_fp8(*inputs, w.scale, round_p=True, rows=rows)
+    q, k, v = inputs
+    if causal:
+        return oracle.attention_ex(q, k, v, w.scale, w.dtype, causal=True, rows=rows)
+    return oracle.attention(q, k, v, w.scale, w.dtype, rows=rows)
+
+
+def oracle_rows_for(w, seconds: float, inputs, causal: bool = False):
     """Rows per second of the fp64 oracle on this host, then a seeded row
     sample sized to take about `seconds`."""
     import oracle
@@ -257,10 +280,7 @@ def oracle_rows_for(w, seconds: float, q, k, v, causal: bool = False):
     total = w.B * w.Hq * w.N
     calib = rng.integers(0, total, 64)
     t0 = time.perf_counter()
-    if causal:
-        oracle.attention_ex(q, k, v, w.scale, w.dtype, causal=True, rows=calib)
-    else:
-        oracle.attention(q, k, v, w.scale, w.dtype, rows=calib)
+    oracle_forward(w, inputs, calib, causal)
     rate = 64 / max(time.perf_counter() - t0, 1e-6)
     n = int(max(1, min(total, rate * seconds)))
     return rng.integers(0, total, n), oracle.max_threads()
@@ -274,10 +294,12 @@ class OracleSample:
     head 0 and its query heads, full N): dK and dV need every query row.
     """
 
-    def __init__(self, w, which: str, seconds: float, q, k, v):
+    def __init__(self, w, which: str, seconds: float, inputs):
         import oracle
 
         self.oracle, self.w, self.which = oracle, w, which
+        self.inputs = inputs
+        q, k, v = inputs[:3]
         self.causal = which.endswith("causal")
         self.cores = oracle.max_threads()
         if which.startswith("bwd"):
@@ -290,8 +312,7 @@ class OracleSample:
             self.desc = (f"backward of one KV-head group (b=0, kv head 0, {G} query head(s), "
                          f"N={w.N}) of the {w.B * w.Hkv}-group workload per step; fp64 C oracle, OpenMP")
         else:
-            self.q, self.k, self.v = q, k, v
-            self.rows, _ = oracle_rows_for(w, seconds, q, k, v, self.causal)
+            self.rows, _ = oracle_rows_for(w, seconds, inputs, self.causal)
             i = self.rows % w.N
             keys = (i + 1) if self.causal else np.full(self.rows.shape, w.N)
             self.flops = 4.0 * w.d * float(keys.sum())
@@ -303,14 +324,12 @@ class OracleSample:
         o, w = self.oracle, self.w
         if self.which.startswith("bwd"):
             o.attention_bwd(self.q, self.k, self.v, self.do, w.scale, w.dtype, causal=self.causal)
-        elif self.causal:
-            o.attention_ex(self.q, self.k, self.v, w.scale, w.dtype, causal=True, rows=self.rows)
         else:
-            o.attention(self.q, self.k, self.v, w.scale, w.dtype, rows=self.rows)
+            oracle_forward(w, self.inputs, self.rows, self.causal)
 
 
-def time_oracle(w, which: str, q, k, v, seconds: float):
-    sample = OracleSample(w, which, seconds, q, k, v)
+def time_oracle(w, which: str, inputs, seconds: float):
+    sample = OracleSample(w, which, seconds, inputs)
     t0 = time.perf_counter()
     sample.run()
     dt = time.perf_counter() - t0
@@ -323,10 +342,9 @@ def run_reference(args, dist, w):
     """fp64 CPU oracle as the reference arm: each step a bounded sample."""
     if dist.rank != 0:
         return None
-    q, k, v = w.inputs()
     total_budget = 120.0
     per_step = total_budget / max(1, args.steps + args.warmup)
-    sample = OracleSample(w, args.pass_, per_step, q, k, v)
+    sample = OracleSample(w, args.pass_, per_step, w.inputs())
     for _ in range(args.warmup):
         sample.run()
     t0 = time.perf_counter()
@@ -336,7 +354,7 @@ def run_reference(args, dist, w):
     value = sample.flops * args.steps / dt / 1e12
     return {
         "impl": "reference",
-        "metric": metric_of(args.pass_), "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "metric": metric_of(args.pass_, w), "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -347,7 +365,9 @@ def run_reference(args, dist, w):
     }
 
 
-def metric_of(which: str) -> str:
+def metric_of(which: str, w=None) -> str:
+    if w is not None and w.fp8:
+        return "attention fwd TFLOP/s (4BHN²d) at 1 GB300, FP8 e4m3 inputs; % of dense FP8 tensor peak"
     if which == "fwd":
         return METRIC
     if which == "fwd_causal":
@@ -356,9 +376,14 @@ def metric_of(which: str) -> str:
             (", causal" if which == "bwd_causal" else "") + ") at 1 GB300")
 
 
+def dtype_name(w) -> str:
+    return {gen.BF16: "bf16", gen.FP16: "fp16", gen.E4M3: "e4m3"}[w.dtype]
+
+
 def config_of(w, n_gpus, which: str = "fwd"):
     return {"workload": w.name, "pass": which, "B": w.B, "H_q": w.Hq, "H_kv": w.Hkv, "N": w.N,
-            "d": w.d, "dtype": "bf16" if w.dtype == gen.BF16 else "fp16",
+            "d": w.d, "dtype": dtype_name(w) + (" in, bf16 out, per-(batch, KV head) descales"
+                                                if w.fp8 else ""),
             "causal": which.endswith("causal"), "scale": "1/sqrt(d)",
             "inputs": f"N(0,1)x{w.amp:g} seed {w.seed}"
                       + (f"; dO N(0,1) seed {w.seed + 50000}" if which.startswith("bwd") else ""),
@@ -368,7 +393,7 @@ def config_of(w, n_gpus, which: str = "fwd"):
 
 
 def qkv_bytes(w) -> int:
-    return 2 * w.d * w.N * w.B * (w.Hq + 2 * w.Hkv)
+    return (1 if w.fp8 else 2) * w.d * w.N * w.B * (w.Hq + 2 * w.Hkv)
 
 
 def l2_note(w) -> str:
@@ -381,17 +406,24 @@ def l2_note(w) -> str:
 class Step:
     """Device tensors and the C-ABI call of one step of a pass."""
 
-    def __init__(self, fa2, torch, w, which, dev, stream, q, k, v):
+    def __init__(self, fa2, torch, w, which, dev, stream, inputs):
         self.fa2, self.torch, self.w, self.which, self.stream = fa2, torch, w, which, stream
-        self.tdt = torch.bfloat16 if w.dtype == gen.BF16 else torch.float16
+        self.tdt = torch.bfloat16 if w.dtype in (gen.BF16, gen.E4M3) else torch.float16
         self.causal = which.endswith("causal")
         self.bwd = which.startswith("bwd")
+        self.fp8 = w.fp8
+        if self.fp8 and which != "fwd":
+            raise ValueError("FP8 workloads have the forward pass only")
 
         def up(x):
+            if x.dtype == np.uint8 or x.dtype == np.float32:
+                return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
             return torch.from_numpy(x.view(np.int16)).to(dev).view(self.tdt)
 
-        self.tq, self.tk, self.tv = up(q), up(k), up(v)
-        self.o = torch.empty_like(self.tq)
+        self.tq, self.tk, self.tv = (up(x) for x in inputs[:3])
+        if self.fp8:
+            self.tqd, self.tkd, self.tvd = (up(x) for x in inputs[3:])
+        self.o = torch.empty(self.tq.shape, dtype=self.tdt, device=dev)
         self.lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
         if self.bwd:
             self.tdo = up(w.grad_output())
@@ -405,6 +437,8 @@ class Step:
         self.launches = 3 if self.bwd else 1
         if self.bwd:
             self.kernel = "fa2_bwd (delta + dK/dV + dQ kernels)"
+        elif self.fp8:
+            self.kernel = "fa2_fwd_fp8_kernel"
         else:
             self.kernel = (f"fa2_fwd_kernel<{w.d},{'bf16' if w.dtype == gen.BF16 else 'fp16'}"
                            f"{',general' if self.causal else ''}>")
@@ -418,6 +452,12 @@ class Step:
                                self.delta.data_ptr(), w.B, w.Hq, w.Hkv, w.N, w.d, w.scale,
                                self.causal, w.dtype, s)
             name = "fa2_bwd"
+        elif self.fp8:
+            rc = f.fa2_fwd_fp8_ptr(self.tq.data_ptr(), self.tk.data_ptr(), self.tv.data_ptr(),
+                                   self.tqd.data_ptr(), self.tkd.data_ptr(), self.tvd.data_ptr(),
+                                   self.o.data_ptr(), self.lse.data_ptr(), w.B, w.Hq, w.Hkv, w.N, w.d,
+                                   w.scale, s)
+            name = "fa2_fwd_fp8"
         elif self.causal:
             rc = f.fa2_fwd_ex_ptr(self.tq.data_ptr(), self.tk.data_ptr(), self.tv.data_ptr(),
                                   self.o.data_ptr(), self.lse.data_ptr(), w.B, w.Hq, w.Hkv, w.N,
@@ -445,6 +485,13 @@ class Step:
                       causal=self.causal, dq=self.dq, dk=self.dk, dv=self.dv, delta=self.delta,
                       stream=st)
             dev_out = (self.dq, self.dk, self.dv)
+        elif self.fp8:
+            dev_in = (self.tq, self.tk, self.tv, self.tqd, self.tkd, self.tvd)
+            for d_, h_ in zip(dev_in, ins):
+                d_.copy_(h_, non_blocking=True)
+            f.fa2_fwd_fp8(self.tq, self.tk, self.tv, self.tqd, self.tkd, self.tvd, self.o, self.lse,
+                          scale=self.w.scale, stream=st)
+            dev_out = (self.o, self.lse)
         else:
             for d_, h_ in zip((self.tq, self.tk, self.tv), ins):
                 d_.copy_(h_, non_blocking=True)
@@ -468,7 +515,8 @@ class Step:
             outs = tuple(self.torch.empty(t.shape, dtype=t.dtype).pin_memory()
                          for t in (self.dq, self.dk, self.dv))
         else:
-            ins = tuple(pin(t) for t in (self.tq, self.tk, self.tv))
+            dev_in = (self.tq, self.tk, self.tv) + ((self.tqd, self.tkd, self.tvd) if self.fp8 else ())
+            ins = tuple(pin(t) for t in dev_in)
             outs = tuple(self.torch.empty(t.shape, dtype=t.dtype).pin_memory()
                          for t in (self.o, self.lse))
         nbytes = [sum(t.numel() * t.element_size() for t in x) for x in (ins, outs)]
@@ -486,8 +534,8 @@ def run_ours(args, dist, w):
     dist.init("nccl")
     stream = torch.cuda.current_stream(dev)
 
-    q, k, v = w.inputs()
-    step = Step(fa2, torch, w, args.pass_, dev, stream, q, k, v)
+    inputs = w.inputs()
+    step = Step(fa2, torch, w, args.pass_, dev, stream, inputs)
     flops = pass_flops(w, args.pass_)
     flush = None
     if qkv_bytes(w) <= L2_BYTES:
@@ -526,6 +574,9 @@ def run_ours(args, dist, w):
     clocks.mark(1)
     region_ms = region0.elapsed_time(region1)
     kernel_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
+    # With an L2 flush between steps the flush is not part of the work: the
+    # timed span is then the sum of the steps' own intervals.
+    timed_ms = kernel_ms * args.steps if flush is not None else region_ms
     rc = fa2.fa2_check_status(stream.cuda_stream)
     if rc != fa2.FA2_OK:
         raise RuntimeError(f"kernel status {fa2.status_string(rc)}")
@@ -533,7 +584,7 @@ def run_ours(args, dist, w):
         time.sleep(0.25)
         clocks.stop()
 
-    value, max_region_ms = aggregate_throughput(dist, flops * args.steps, region_ms, dev)
+    value, max_region_ms = aggregate_throughput(dist, flops * args.steps, timed_ms, dev)
 
     # end to end through the public binding, every step: pinned host inputs
     # -> device -> kernels -> device -> pinned host results
@@ -555,15 +606,15 @@ def run_ours(args, dist, w):
 
     result = None
     if dist.rank == 0:
-        peak, peak_src = load_peak()
+        peak, peak_src = load_peak(w.fp8)
         achieved = flops / (kernel_ms * 1e-3) / 1e12
         nbytes = pass_bytes(w, args.pass_)
         result = {
-            "metric": metric_of(args.pass_), "value": value, "unit": UNIT, "n_gpus": dist.world,
+            "metric": metric_of(args.pass_, w), "value": value, "unit": UNIT, "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": max_region_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if w.dtype == gen.BF16 else "fp16", "data": "synthetic",
+            "dtype": dtype_name(w), "data": "synthetic",
             "config": config_of(w, dist.world, args.pass_),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "traffic": load_traffic(w.name, args.pass_),
@@ -577,7 +628,7 @@ def run_ours(args, dist, w):
             "clocks": clocks.summary(),
         }
         if dist.world == 1 and not args.no_cpu_baseline:
-            cv, cores, desc, dt = time_oracle(w, args.pass_, q, k, v, args.cpu_seconds)
+            cv, cores, desc, dt = time_oracle(w, args.pass_, inputs, args.cpu_seconds)
             result["cpu_baseline"] = {"value": cv, "unit": UNIT, "cores": cores, "kind": "oracle",
                                       "sample": f"{desc}, {dt:.1f} s"}
     return result

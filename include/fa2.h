@@ -111,6 +111,35 @@ fa2_status fa2_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
                       int causal, fa2_dtype dtype, cudaStream_t stream);
 
 /*
+ * FP8 attention forward with in-kernel scaling: the inference variant named
+ * by "FlashAttention-3 for Inference: INT8 Quantization and Query Head
+ * Packing for MQA/GQA" (Colfax Research author page: quantised inputs,
+ * in-kernel pre-processing by specialised warps, query-head packing). The
+ * pages give no more than that; the form here:
+ *   q       : [B, H_q, N, d] e4m3 codes (OCP FP8 E4M3, one byte each), device
+ *   k, v    : [B, H_kv, N, d] e4m3 codes, device
+ *   q_descale, k_descale, v_descale : [B * H_kv] fp32, device; the value of
+ *             a code of (batch b, KV head g) -- for q, of the query heads
+ *             that share KV head g -- is code * descale[b * H_kv + g]
+ *   o       : [B, H_q, N, d] bf16, device (output)
+ *   lse     : [B, H_q, N] fp32, device (output, natural-log logsumexp of the
+ *             scaled scores of the dequantised inputs)
+ *   d       : 128 (other values: FA2_ERR_UNSUPPORTED)
+ *   B, H_q, H_kv, N, scale, stream : as fa2_fwd_gqa (N % 128 == 0)
+ * Both products run on e4m3 tensor-core operands: S = Q K^T exactly in fp32
+ * (then scaled by scale * dq * dk), and the softmax weights are scaled by
+ * 2^8 and rounded to e4m3 before P V; l sums the unrounded weights. So O
+ * differs from attention on the dequantised inputs by at most
+ * 2^-4 sum_j p_j |v_j| / l + 2^-18 sum_j |v_j| / l per element (plus the
+ * bf16 rounding of O); the LSE carries no rounding of P.
+ * Alignment: q, k, v, o, lse 16-byte aligned; descales 4-byte aligned.
+ * Errors as fa2_fwd_gqa. Nothing is allocated; all buffers are the caller's.
+ */
+fa2_status fa2_fwd_fp8(const void* q, const void* k, const void* v, const float* q_descale,
+                       const float* k_descale, const float* v_descale, void* o, float* lse,
+                       int B, int H_q, int H_kv, int N, int d, float scale, cudaStream_t stream);
+
+/*
  * Attention backward (gradients of fa2_fwd / fa2_fwd_gqa with optional
  * causal mask, equal lengths N, N % 128 == 0). The forward pages exclude the
  * backward pass ("FlashAttention-2 from scratch on Ampere, Part 1", Kernel

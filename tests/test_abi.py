@@ -100,6 +100,21 @@ def test_backward_host_validation(lib):
     assert f(*ok, 1, 70000, 1, 128, 64, 0.1, 0, 0) == fa2.FA2_ERR_UNSUPPORTED       # B*Hq > 65535
 
 
+def test_fp8_entry_host_validation(lib):
+    f = fa2.fa2_fwd_fp8_ptr
+    ok = [A] * 8            # q, k, v, q/k/v descales, o, lse
+    assert f(*([0] + ok[1:]), 1, 1, 1, 128, 128, 0.1) == fa2.FA2_ERR_INVALID_ARG         # NULL q
+    assert f(*(ok[:4] + [0] + ok[5:]), 1, 1, 1, 128, 128, 0.1) == fa2.FA2_ERR_INVALID_ARG  # NULL k_descale
+    assert f(*(ok[:3] + [A + 2] + ok[4:]), 1, 1, 1, 128, 128, 0.1) == fa2.FA2_ERR_INVALID_ARG  # descale align
+    assert f(*(ok[:7] + [A + 4]), 1, 1, 1, 128, 128, 0.1) == fa2.FA2_ERR_INVALID_ARG      # lse align
+    assert f(*ok, 1, 3, 2, 128, 128, 0.1) == fa2.FA2_ERR_INVALID_ARG                      # Hq % Hkv
+    assert f(*ok, 1, 1, 1, 128, 128, 0.0) == fa2.FA2_ERR_INVALID_ARG                      # scale
+    assert f(*ok, 1, 1, 1, 0, 128, 0.1) == fa2.FA2_ERR_INVALID_ARG                        # N = 0
+    assert f(*ok, 1, 1, 1, 128, 64, 0.1) == fa2.FA2_ERR_UNSUPPORTED                       # d = 64
+    assert f(*ok, 1, 1, 1, 200, 128, 0.1) == fa2.FA2_ERR_UNSUPPORTED                      # N % 128
+    assert f(*ok, 2048, 8, 8, 131072, 128, 0.1) == fa2.FA2_ERR_UNSUPPORTED                # rows >= 2^31
+
+
 def test_mha_entry_forwards_to_gqa(lib):
     assert fa2.fa2_fwd_ptr(0, A, A, A, A, 1, 1, 128, 128, 0.1, 0) == fa2.FA2_ERR_INVALID_ARG
     assert fa2.fa2_fwd_ptr(A, A, A, A, A, 1, 1, 128, 80, 0.1, 0) == fa2.FA2_ERR_UNSUPPORTED

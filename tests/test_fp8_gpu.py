@@ -1,0 +1,136 @@
+"""Parity of the FP8 (e4m3) forward (fa2_fwd_fp8) with the fp64 oracle,
+through the C ABI.
+
+Tolerance, derived from the method's arithmetic (no tolerance is given for
+FP8 inputs). The kernel computes S = Q K^T exactly in fp32 from the e4m3
+codes, then P' = 2^8 p in fp32 and rounds P' to e4m3 before P.V; l sums the
+unrounded P'. Rounding to e4m3 moves each weight by at most 2^-4 p_j (normal
+range) or 2^-10 / 2^8 absolutely (subnormal range), so against attention on
+the dequantised inputs (the oracle with round_p=False):
+    |O - O_plain| <= 2^-4 a + 2^-18 b + 2^-8 |O_plain| + 2^-12 a
+elementwise, with a = sum_j p_j |v_j| / l and b = sum_j |v_j| / l from the
+oracle; 2^-8 |O| is the bf16 rounding of O and 2^-12 a covers the fp32
+arithmetic (exponentials, sums). Against the method itself (the oracle with
+round_p=True, P rounded in double) the outputs differ only by bf16 rounding,
+fp32 arithmetic and the rare weight that sits within fp32 error of an e4m3
+rounding midpoint and rounds the other way, so normwise
+    ||O - O_method||_F <= 2^-7 ||O_method||_F.
+The LSE carries no rounding of P: |LSE - LSE_ref| <= 1e-3 (the 16-bit path's
+bound).
+"""
+import numpy as np
+import pytest
+
+import gen
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fp8(fa2, q, k, v, qd, kd, vd, scale):
+    import torch
+
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to("cuda")
+    o, lse = fa2.fa2_fwd_fp8(dev(q), dev(k), dev(v), dev(qd), dev(kd), dev(vd), scale=scale)
+    assert fa2.fa2_check_status(torch.cuda.current_stream().cuda_stream) == fa2.FA2_OK
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, scale, rows=None, what=""):
+    om, op, lp, a, b = oracle.attention_fp8_both(q, k, v, qd, kd, vd, scale, rows=rows)
+    d = q.shape[-1]
+    if rows is not None:
+        o = o.reshape(-1, d)[rows]
+        lse = lse.reshape(-1)[rows]
+    o, om, op, a, b = (x.reshape(-1, d) for x in (o, om, op, a, b))
+    assert np.isfinite(o).all(), what
+    bound = 2.0 ** -4 * a + 2.0 ** -18 * b + 2.0 ** -8 * np.abs(op) + 2.0 ** -12 * a + 1e-7
+    err = np.abs(o - op)
+    bad = err > bound
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements beyond the rounding bound, worst ratio " \
+                          f"{(err / bound).max():.3g}"
+    rel = np.linalg.norm(o - om) / np.linalg.norm(om)
+    assert rel <= 2.0 ** -7, f"{what}: ||O - O_method|| / ||O_method|| = {rel:.3g}"
+    assert np.max(np.abs(lse.reshape(-1) - lp.reshape(-1))) <= 1e-3, what
+    return rel
+
+
+CASES = [
+    # B, Hq, Hkv, N, amp
+    (1, 1, 1, 128, 1.0),      # one tile, one KV tile
+    (1, 2, 1, 256, 1.0),      # grouped heads, two KV tiles
+    (1, 1, 1, 384, 1.0),      # three query tiles: an item with one tile
+    (2, 4, 2, 1024, 1.0),     # grouped heads, eight KV tiles
+    (1, 4, 4, 1024, 3.0),     # sharp softmax: many rescales, large logits
+    (2, 16, 16, 1024, 1.0),   # 256 items on 152 SMs: CTAs take several items
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,amp", CASES)
+def test_fp8_matches_oracle(gpu_lib, B, Hq, Hkv, N, amp):
+    q, k, v, qd, kd, vd = gen.make_qkv_fp8(7000 + N + Hq + int(amp), B, Hq, Hkv, N, 128, amp)
+    scale = 128 ** -0.5
+    o, lse = run_fp8(gpu_lib, q, k, v, qd, kd, vd, scale)
+    assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, scale, what=f"B{B} Hq{Hq} Hkv{Hkv} N{N} x{amp}")
+
+
+def test_fp8_descales_are_applied(gpu_lib):
+    # A descale changes only its own group, by its own factor: a power of two
+    # on v's descale scales that group's O exactly and leaves its LSE alone.
+    B, Hq, Hkv, N = 2, 2, 1, 256                         # two groups: batch 0 and batch 1
+    q, k, v, qd, kd, vd = gen.make_qkv_fp8(7101, B, Hq, Hkv, N, 128)
+    vd2 = vd * np.array([1.0, 4.0], dtype=np.float32)
+    o1, l1 = run_fp8(gpu_lib, q, k, v, qd, kd, vd, 0.09)
+    o2, l2 = run_fp8(gpu_lib, q, k, v, qd, kd, vd2, 0.09)
+    assert np.array_equal(o1[0], o2[0]) and np.array_equal(l1, l2)
+    assert np.array_equal(o1[1] * 4.0, o2[1])          # power-of-two factor: exact in bf16
+    assert_fp8_parity(o2, l2, q, k, v, qd, kd, vd2, 0.09, what="vd x4")
+    kd2 = kd * np.float32(2.0)
+    o3, l3 = run_fp8(gpu_lib, q, k, v, qd, kd2, vd, 0.09)
+    assert_fp8_parity(o3, l3, q, k, v, qd, kd2, vd, 0.09, what="kd x2")
+
+
+def test_fp8_constant_values(gpu_lib):
+    # V = 2 everywhere: the plain result is exactly 2; the method's is within
+    # 2^-4 of it (P rounding) -- and every row's weights still sum to l.
+    B, Hq, Hkv, N = 1, 2, 1, 512
+    q, k, _, qd, kd, _ = gen.make_qkv_fp8(7102, B, Hq, Hkv, N, 128)
+    v = np.full((B, Hkv, N, 128), 0x40, dtype=np.uint8)
+    vd = np.ones(B * Hkv, dtype=np.float32)
+    o, lse = run_fp8(gpu_lib, q, k, v, qd, kd, vd, 0.1)
+    assert np.max(np.abs(o - 2.0)) <= 2.0 ** -4 * 2.0 + 2.0 ** -7
+    assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, 0.1, what="V = 2")
+
+
+def test_fp8_accepts_torch_float8_tensors(gpu_lib):
+    import torch
+
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    q, k, v, qd, kd, vd = gen.make_qkv_fp8(7103, 1, 2, 2, 256, 128)
+    t = lambda x: torch.from_numpy(x).to("cuda").view(torch.float8_e4m3fn)
+    f = lambda x: torch.from_numpy(x).to("cuda")
+    o, lse = gpu_lib.fa2_fwd_fp8(t(q), t(k), t(v), f(qd), f(kd), f(vd), scale=0.1)
+    o2, lse2 = run_fp8(gpu_lib, q, k, v, qd, kd, vd, 0.1)
+    assert np.array_equal(o.float().cpu().numpy(), o2) and np.array_equal(lse.cpu().numpy(), lse2)
+
+
+def test_fp8_full_size_bench_workload_sampled_rows(gpu_lib):
+    # The workload bench.py times for FP8, in the same launch configuration;
+    # the oracle checks a seeded sample of rows, spread over every batch and
+    # head, plus the first and last row.
+    w = gen.workload("fp8_mha_B4_H16_N4096_d128_e4m3")
+    q, k, v, qd, kd, vd = w.inputs()
+    o, lse = run_fp8(gpu_lib, q, k, v, qd, kd, vd, w.scale)
+    total = w.B * w.Hq * w.N
+    rows = np.unique(np.concatenate([np.random.default_rng(5).integers(0, total, 1500), [0, total - 1]]))
+    assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, w.scale, rows=rows, what=w.name)
+
+
+def test_fp8_rejects_unsupported_head_dim(gpu_lib):
+    import torch
+
+    q = torch.zeros((1, 1, 128, 64), dtype=torch.uint8, device="cuda")
+    ds = torch.ones(1, dtype=torch.float32, device="cuda")
+    with pytest.raises(gpu_lib.FA2Error):
+        gpu_lib.fa2_fwd_fp8(q, q, q, ds, ds, ds)
