@@ -303,24 +303,14 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
             }
             ptx::tc_fence_after();
             uint32_t s[kBN];
-            ptx::tmem_ld32_at<0>(row_addr + colS + 0, s);
-            ptx::tmem_ld32_at<32>(row_addr + colS + 32, s);
-            ptx::tmem_ld32_at<64>(row_addr + colS + 64, s);
-            ptx::tmem_ld32_at<96>(row_addr + colS + 96, s);
+            float mq[4];   // row max of each 32-column load
+            ptx::tmem_ld32_max_at<0>(row_addr + colS + 0, s, mq[0]);
+            ptx::tmem_ld32_max_at<32>(row_addr + colS + 32, s, mq[1]);
+            ptx::tmem_ld32_max_at<64>(row_addr + colS + 64, s, mq[2]);
+            ptx::tmem_ld32_max_at<96>(row_addr + colS + 96, s, mq[3]);
             ptx::tmem_wait_ld();
-
-            float mx[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                float a = __uint_as_float(s[k]);
-#pragma unroll
-                for (int i = 1; i < 15; i += 2)
-                    a = ptx::max3(a, __uint_as_float(s[k + 8 * i]), __uint_as_float(s[k + 8 * (i + 1)]));
-                mx[k] = fmaxf(a, __uint_as_float(s[k + 120]));
-            }
             // c > 0, so the max of c*s is c times the max of s
-            const float m_tile =
-                fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7]))) * c;
+            const float m_tile = fmaxf(ptx::max3(mq[0], mq[1], mq[2]), mq[3]) * c;
             const float m_new = fmaxf(m, m_tile);
             const float alpha = (j == 0 || m_new == m) ? 1.0f : ptx::ex2_approx(m - m_new);
             alpha_buf[row] = alpha;

@@ -575,12 +575,13 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
             }
             ptx::tc_fence_after();
             uint32_t s[kBN];
-            ptx::tmem_ld32_at<0>(row_addr + colS + 0, s);
-            ptx::tmem_ld32_at<32>(row_addr + colS + 32, s);
-            ptx::tmem_ld32_at<64>(row_addr + colS + 64, s);
-            ptx::tmem_ld32_at<96>(row_addr + colS + 96, s);
-            ptx::tmem_wait_ld();
+            float m_tile;
             if constexpr (kGen) {
+                ptx::tmem_ld32_at<0>(row_addr + colS + 0, s);
+                ptx::tmem_ld32_at<32>(row_addr + colS + 32, s);
+                ptx::tmem_ld32_at<64>(row_addr + colS + 64, s);
+                ptx::tmem_ld32_at<96>(row_addr + colS + 96, s);
+                ptx::tmem_wait_ld();
                 // Keys at or past kend(row) (the causal diagonal, the end of
                 // a ragged key sequence, TMA's zero fill) get -inf.
                 if (j >= jmask) {
@@ -588,20 +589,28 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
 #pragma unroll
                     for (int c = 0; c < kBN; ++c) s[c] = c < lim ? s[c] : 0xFF800000u;
                 }
-            }
-
-            // Row max: eight independent chains of 3-input max, then combine.
-            float mx[8];
+                // Row max: eight independent chains of 3-input max, then combine.
+                float mx[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                float a = __uint_as_float(s[k]);
+                for (int k = 0; k < 8; ++k) {
+                    float a = __uint_as_float(s[k]);
 #pragma unroll
-                for (int i = 1; i < 15; i += 2)
-                    a = ptx::max3(a, __uint_as_float(s[k + 8 * i]), __uint_as_float(s[k + 8 * (i + 1)]));
-                mx[k] = fmaxf(a, __uint_as_float(s[k + 120]));
+                    for (int i = 1; i < 15; i += 2)
+                        a = ptx::max3(a, __uint_as_float(s[k + 8 * i]), __uint_as_float(s[k + 8 * (i + 1)]));
+                    mx[k] = fmaxf(a, __uint_as_float(s[k + 120]));
+                }
+                m_tile = fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7]))) *
+                         c;
+            } else {
+                // Row max from the loads themselves (no masking here).
+                float mq[4];
+                ptx::tmem_ld32_max_at<0>(row_addr + colS + 0, s, mq[0]);
+                ptx::tmem_ld32_max_at<32>(row_addr + colS + 32, s, mq[1]);
+                ptx::tmem_ld32_max_at<64>(row_addr + colS + 64, s, mq[2]);
+                ptx::tmem_ld32_max_at<96>(row_addr + colS + 96, s, mq[3]);
+                ptx::tmem_wait_ld();
+                m_tile = fmaxf(ptx::max3(mq[0], mq[1], mq[2]), mq[3]) * c;
             }
-            const float m_tile =
-                fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7]))) * c;
             // Hand the correction warpgroup this row's rescale factor
             // (exactly 1 when the max does not move).
             const float m_new = fmaxf(m, m_tile);

@@ -424,6 +424,28 @@ __device__ __forceinline__ void tmem_st32_at(uint32_t taddr, const uint32_t (&r)
         : "memory");
 }
 
+// The same 32-column load that also returns, per thread, the maximum of the
+// 32 fp32 values it loaded (tcgen05.ld.red, an sm_103a instruction): the
+// row max of a score tile comes out of the TMEM loads instead of a tree of
+// max instructions.
+template <int OFF, int NREG>
+__device__ __forceinline__ void tmem_ld32_max_at(uint32_t taddr, uint32_t (&r)[NREG], float& mx) {
+    static_assert(OFF + 32 <= NREG, "slice out of range");
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, %32, [%33];"
+        : "=r"(r[OFF + 0]), "=r"(r[OFF + 1]), "=r"(r[OFF + 2]), "=r"(r[OFF + 3]), "=r"(r[OFF + 4]),
+          "=r"(r[OFF + 5]), "=r"(r[OFF + 6]), "=r"(r[OFF + 7]), "=r"(r[OFF + 8]), "=r"(r[OFF + 9]),
+          "=r"(r[OFF + 10]), "=r"(r[OFF + 11]), "=r"(r[OFF + 12]), "=r"(r[OFF + 13]),
+          "=r"(r[OFF + 14]), "=r"(r[OFF + 15]), "=r"(r[OFF + 16]), "=r"(r[OFF + 17]),
+          "=r"(r[OFF + 18]), "=r"(r[OFF + 19]), "=r"(r[OFF + 20]), "=r"(r[OFF + 21]),
+          "=r"(r[OFF + 22]), "=r"(r[OFF + 23]), "=r"(r[OFF + 24]), "=r"(r[OFF + 25]),
+          "=r"(r[OFF + 26]), "=r"(r[OFF + 27]), "=r"(r[OFF + 28]), "=r"(r[OFF + 29]),
+          "=r"(r[OFF + 30]), "=r"(r[OFF + 31]), "=f"(mx)
+        : "r"(taddr));
+}
+
 // ------------------------------------------------------------------ descriptors
 
 // Shared-memory matrix descriptor for tcgen05.mma with the 128-byte swizzle:
