@@ -20,7 +20,15 @@
 //   fa2_bwd_dq_kernel     one CTA per 128-query tile: S = Q K^T,
 //                         dP = dO V^T, dS in TMEM, dQ += dS K
 // Warps 0-3 elementwise (thread = TMEM lane), warp 4 TMA producer, warp 5
-// TMEM allocator and MMA issuer. TMEM: S | dP | two d-column accumulators.
+// TMEM allocator and MMA issuer. TMEM: S | dP | two d-column accumulators
+// (dK/dV), S0 | S1 | dP | dQ (dQ).
+//
+// Overlap. The elementwise step of a tile runs in two phases with their own
+// barriers: P as soon as S is in TMEM (while the tensor core computes dP),
+// then dS once dP is (while the tensor core runs the first product that
+// consumes P). dK/dV issues S, dP, dV (after P), dK (after dS) per query
+// tile; dQ double-buffers S, so S of the next key tile is computed during
+// the current tile's elementwise work whenever its K/V stage has arrived.
 #pragma once
 
 #include "fa2_fwd_sm103.cuh"
@@ -60,12 +68,16 @@ struct BwdLayout {
     static constexpr int kRingOff = 2 * kTileBytes;
     static constexpr int kStageBytes = 2 * kTileBytes + 1024;    // two tiles + LSE + D
     static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
-    // fixed_full, stage_full[S], stage_empty[S], s_full, p_full, acc_full
-    static constexpr int kNumBars = 1 + 2 * kStages + 3;
+    // fixed_full, stage_full[S], stage_empty[S], s_full[2], dp_full, p_full, ds_full, acc_full,
+    // lse_ready[S]
+    static constexpr int kNumBars = 1 + 2 * kStages + 6 + kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    // dK/dV kernel: S | dP | dV | dK
     static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
+    // dQ kernel: S0 | S1 | dP | dQ
+    static constexpr uint32_t kQColS0 = 0, kQColDP = 256, kQColAcc = 384;
 };
 
 template <int D>
@@ -74,9 +86,12 @@ struct BwdBars {
     __device__ uint32_t fixed_full() const { return base; }
     __device__ uint32_t stage_full(int s) const { return base + 8 * (1 + s); }
     __device__ uint32_t stage_empty(int s) const { return base + 8 * (1 + kStages + s); }
-    __device__ uint32_t s_full() const { return base + 8 * (1 + 2 * kStages); }
-    __device__ uint32_t p_full() const { return base + 8 * (2 + 2 * kStages); }
-    __device__ uint32_t acc_full() const { return base + 8 * (3 + 2 * kStages); }
+    __device__ uint32_t s_full(int b = 0) const { return base + 8 * (1 + 2 * kStages + b); }
+    __device__ uint32_t dp_full() const { return base + 8 * (3 + 2 * kStages); }
+    __device__ uint32_t p_full() const { return base + 8 * (4 + 2 * kStages); }
+    __device__ uint32_t ds_full() const { return base + 8 * (5 + 2 * kStages); }
+    __device__ uint32_t acc_full() const { return base + 8 * (6 + 2 * kStages); }
+    __device__ uint32_t lse_ready(int s) const { return base + 8 * (7 + 2 * kStages + s); }
 };
 
 // ---------------------------------------------------------------- D = rowsum(dO o O)
@@ -182,9 +197,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bars.stage_full(s), 1);
             ptx::mbar_init(bars.stage_empty(s), 1);
         }
-        ptx::mbar_init(bars.s_full(), 1);
+        ptx::mbar_init(bars.s_full(0), 1);
+        ptx::mbar_init(bars.s_full(1), 1);
+        ptx::mbar_init(bars.dp_full(), 1);
         ptx::mbar_init(bars.p_full(), 128);
+        ptx::mbar_init(bars.ds_full(), 128);
         ptx::mbar_init(bars.acc_full(), 1);
+        for (int s = 0; s < kStages; ++s) ptx::mbar_init(bars.lse_ready(s), 128);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -252,14 +271,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             const uint32_t st = sbase + L::kRingOff + s * L::kStageBytes;
             qk_kloop<D>(tmem + L::kColS, kdesc, ptx::desc_sw128(st, 16, 1024), kIdT);
-            qk_kloop<D>(tmem + L::kColDP, vdesc, ptx::desc_sw128(st + L::kTileBytes, 16, 1024), kIdT);
             ptx::tc_commit_elect(bars.s_full());
+            qk_kloop<D>(tmem + L::kColDP, vdesc, ptx::desc_sw128(st + L::kTileBytes, 16, 1024), kIdT);
+            ptx::tc_commit_elect(bars.dp_full());
+            // dV += P^T dO as soon as P^T is in TMEM (16-bit in the first
+            // half of the S columns; dO as the MN-major B operand) ...
             if (!(ok = wait_u(bars.p_full(), n & 1, kSitePFull))) break;
             ptx::tc_fence_after();
-            // dV += P^T dO, dK += dS^T Q (P^T, dS^T 16-bit in the first half
-            // of their fp32 columns; dO and Q as MN-major B operands)
             pv_kloop(tmem + L::kColAcc0, tmem + L::kColS, ptx::desc_sw128(st + L::kTileBytes, L::kBlkBytes, 1024),
                      kIdA, n > 0 ? 1u : 0u);
+            // ... and dK += dS^T Q once dS^T is
+            if (!(ok = wait_u(bars.ds_full(), n & 1, kSitePFull))) break;
+            ptx::tc_fence_after();
             pv_kloop(tmem + L::kColAcc1, tmem + L::kColDP, ptx::desc_sw128(st, L::kBlkBytes, 1024), kIdA,
                      n > 0 ? 1u : 0u);
             ptx::tc_commit_elect(bars.stage_empty(s));
@@ -286,36 +309,67 @@ __global__ void __launch_bounds__(kThreads, 1)
             int g, i;
             dkdv_step(p, kt, n, g, i);
             const bool diag = p.causal && i == kt;  // query q may see key k only if q >= k
-            const float* lse = reinterpret_cast<const float*>(smem + L::kRingOff + s * L::kStageBytes +
-                                                              2 * L::kTileBytes);
+            float* lse = reinterpret_cast<float*>(smem + L::kRingOff + s * L::kStageBytes + 2 * L::kTileBytes);
             const float* dl = lse + 128;
-#pragma unroll 1
+            // The stage's LSE row, times log2(e) in place (one value per
+            // thread); the stage is reloaded by TMA only after this tile's
+            // MMAs, hence the proxy fence.
+            lse[row] *= kLog2e;
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(bars.lse_ready(s));
+            ok = w.wait(bars.lse_ready(s), (n / kStages) & 1, kSiteStats);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            // P phase: P^T = exp2(S^T c - LSE log2 e) -> 16-bit over S^T
+            float pf[128];
+#pragma unroll
             for (int cc = 0; cc < 128; cc += 32) {
-                uint32_t sv[32], dp[32];
+                uint32_t sv[32];
                 ptx::tmem_ld32(row_addr + L::kColS + cc, sv);
-                ptx::tmem_ld32(row_addr + L::kColDP + cc, dp);
                 ptx::tmem_wait_ld();
-                uint32_t pk[16], dk[16];
+                uint32_t pk[16];
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
-                    float pv[2], ds[2];
 #pragma unroll
                     for (int y = 0; y < 2; ++y) {
                         const int qc = cc + 2 * x + y;
-                        float pp = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * x + y]), c, -lse[qc] * kLog2e));
+                        float pp = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * x + y]), c, -lse[qc]));
                         if (diag && qc < row) pp = 0.0f;
-                        pv[y] = pp;
-                        ds[y] = pp * (__uint_as_float(dp[2 * x + y]) - dl[qc]);
+                        pf[qc] = pp;
                     }
-                    pk[x] = ptx::pack2<kBf16>(pv[0], pv[1]);
-                    dk[x] = ptx::pack2<kBf16>(ds[0], ds[1]);
+                    pk[x] = ptx::pack2<kBf16>(pf[cc + 2 * x], pf[cc + 2 * x + 1]);
                 }
                 ptx::tmem_st16(row_addr + L::kColS + cc / 2, pk);
-                ptx::tmem_st16(row_addr + L::kColDP + cc / 2, dk);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bars.p_full());
+            // dS phase: dS^T = P^T o (dP^T - D) -> 16-bit over dP^T
+            ok = w.wait(bars.dp_full(), n & 1, kSiteSFull);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < 128; cc += 32) {
+                uint32_t dp[32];
+                ptx::tmem_ld32(row_addr + L::kColDP + cc, dp);
+                ptx::tmem_wait_ld();
+                uint32_t dk[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const int qc = cc + 2 * x;
+                    dk[x] = ptx::pack2<kBf16>(pf[qc] * (__uint_as_float(dp[2 * x]) - dl[qc]),
+                                              pf[qc + 1] * (__uint_as_float(dp[2 * x + 1]) - dl[qc + 1]));
+                }
+                ptx::tmem_st16(row_addr + L::kColDP + cc / 2, dk);
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bars.ds_full());
         }
         if (ok) ok = w.wait(bars.acc_full(), 0, kSiteOFull);
         if (__all_sync(0xffffffffu, ok)) {
@@ -365,8 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bars.stage_full(s), 1);
             ptx::mbar_init(bars.stage_empty(s), 1);
         }
-        ptx::mbar_init(bars.s_full(), 1);
-        ptx::mbar_init(bars.p_full(), 128);
+        ptx::mbar_init(bars.s_full(0), 1);
+        ptx::mbar_init(bars.s_full(1), 1);
+        ptx::mbar_init(bars.dp_full(), 1);
+        ptx::mbar_init(bars.ds_full(), 128);
         ptx::mbar_init(bars.acc_full(), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -422,19 +478,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = wait_u(bars.fixed_full(), 0, kSiteQFull);
         const uint64_t qdesc = ptx::desc_sw128(sbase + L::kFixedOff, 16, 1024);
         const uint64_t dodesc = ptx::desc_sw128(sbase + L::kFixedOff + L::kTileBytes, 16, 1024);
+        auto stage_addr = [&](int n) { return sbase + L::kRingOff + (n % kStages) * L::kStageBytes; };
+        // S of key tile n into buffer n % 2, once its stage has landed
+        auto issue_s = [&](int n) {
+            qk_kloop<D>(tmem + L::kQColS0 + 128u * (n & 1), qdesc, ptx::desc_sw128(stage_addr(n), 16, 1024), kIdS);
+            ptx::tc_commit_elect(bars.s_full(n & 1));
+        };
+        int s_issued = 0;   // key tiles whose S has been issued
+        if (steps > 0 && (ok = ok && wait_u(bars.stage_full(0), 0, kSiteKvFull))) {
+            ptx::tc_fence_after();
+            issue_s(0);
+            s_issued = 1;
+        }
         for (int n = 0; n < steps && ok; ++n) {
-            const int s = n % kStages;
-            if (!(ok = wait_u(bars.stage_full(s), (n / kStages) & 1, kSiteKvFull))) break;
+            const uint32_t st = stage_addr(n);
+            // dP (its stage landed before S(n) was issued)
+            qk_kloop<D>(tmem + L::kQColDP, dodesc, ptx::desc_sw128(st + L::kTileBytes, 16, 1024), kIdS);
+            ptx::tc_commit_elect(bars.dp_full());
+            // S of the next key tile now if its stage is already here, so it
+            // is ready when the elementwise warps finish this tile
+            if (s_issued == n + 1 && n + 1 < steps) {
+                const uint32_t bar = bars.stage_full((n + 1) % kStages);
+                const uint32_t par = ((n + 1) / kStages) & 1;
+                if (__shfl_sync(0xffffffffu, ptx::mbar_test_wait(bar, par) ? 1 : 0, 0)) {
+                    ptx::tc_fence_after();
+                    issue_s(n + 1);
+                    ++s_issued;
+                }
+            }
+            // dQ += dS K once dS is in TMEM (16-bit over the dP columns; K as
+            // the MN-major B operand)
+            if (!(ok = wait_u(bars.ds_full(), n & 1, kSitePFull))) break;
             ptx::tc_fence_after();
-            const uint32_t st = sbase + L::kRingOff + s * L::kStageBytes;
-            qk_kloop<D>(tmem + L::kColS, qdesc, ptx::desc_sw128(st, 16, 1024), kIdS);
-            qk_kloop<D>(tmem + L::kColDP, dodesc, ptx::desc_sw128(st + L::kTileBytes, 16, 1024), kIdS);
-            ptx::tc_commit_elect(bars.s_full());
-            if (!(ok = wait_u(bars.p_full(), n & 1, kSitePFull))) break;
-            ptx::tc_fence_after();
-            pv_kloop(tmem + L::kColAcc0, tmem + L::kColDP, ptx::desc_sw128(st, L::kBlkBytes, 1024), kIdQ,
+            pv_kloop(tmem + L::kQColAcc, tmem + L::kQColDP, ptx::desc_sw128(st, L::kBlkBytes, 1024), kIdQ,
                      n > 0 ? 1u : 0u);
-            ptx::tc_commit_elect(bars.stage_empty(s));
+            ptx::tc_commit_elect(bars.stage_empty(n % kStages));
+            if (s_issued == n + 1 && n + 1 < steps) {
+                if (!(ok = wait_u(bars.stage_full((n + 1) % kStages), ((n + 1) / kStages) & 1, kSiteKvFull))) break;
+                ptx::tc_fence_after();
+                issue_s(n + 1);
+                ++s_issued;
+            }
         }
         ptx::tc_commit_elect(bars.acc_full());
         w.drain(bars.acc_full(), 0);
@@ -448,42 +532,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float dl = p.delta[q_row0 + row];
         bool ok = true;
         for (int n = 0; n < steps; ++n) {
-            ok = w.wait(bars.s_full(), n & 1, kSiteSFull);
+            ok = w.wait(bars.s_full(n & 1), (n >> 1) & 1, kSiteSFull);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
             const bool diag = p.causal && n == qt;  // key k visible to query q only if k <= q
-#pragma unroll 1
+            // P phase: P = exp2(S c - LSE log2 e), kept in registers
+            const uint32_t colS = L::kQColS0 + 128u * (n & 1);
+            float pf[128];
+#pragma unroll
             for (int cc = 0; cc < 128; cc += 32) {
-                uint32_t sv[32], dp[32];
-                ptx::tmem_ld32(row_addr + L::kColS + cc, sv);
-                ptx::tmem_ld32(row_addr + L::kColDP + cc, dp);
+                uint32_t sv[32];
+                ptx::tmem_ld32(row_addr + colS + cc, sv);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    const int kc = cc + x;
+                    float pp = ptx::ex2_approx(fmaf(__uint_as_float(sv[x]), c, -lse2));
+                    if (diag && kc > row) pp = 0.0f;
+                    pf[kc] = pp;
+                }
+            }
+            // dS phase: dS = P o (dP - D) -> 16-bit over dP
+            ok = w.wait(bars.dp_full(), n & 1, kSiteSFull);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < 128; cc += 32) {
+                uint32_t dp[32];
+                ptx::tmem_ld32(row_addr + L::kQColDP + cc, dp);
                 ptx::tmem_wait_ld();
                 uint32_t dk[16];
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
-                    float ds[2];
-#pragma unroll
-                    for (int y = 0; y < 2; ++y) {
-                        const int kc = cc + 2 * x + y;
-                        float pp = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * x + y]), c, -lse2));
-                        if (diag && kc > row) pp = 0.0f;
-                        ds[y] = pp * (__uint_as_float(dp[2 * x + y]) - dl);
-                    }
-                    dk[x] = ptx::pack2<kBf16>(ds[0], ds[1]);
+                    const int kc = cc + 2 * x;
+                    dk[x] = ptx::pack2<kBf16>(pf[kc] * (__uint_as_float(dp[2 * x]) - dl),
+                                              pf[kc + 1] * (__uint_as_float(dp[2 * x + 1]) - dl));
                 }
-                ptx::tmem_st16(row_addr + L::kColDP + cc / 2, dk);
+                ptx::tmem_st16(row_addr + L::kQColDP + cc / 2, dk);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bars.p_full());
+            ptx::mbar_arrive(bars.ds_full());
         }
         if (ok) ok = w.wait(bars.acc_full(), 0, kSiteOFull);
         if (__all_sync(0xffffffffu, ok)) {
             ptx::tc_fence_after();
-            store_acc_row<D, kBf16>(row_addr, L::kColAcc0, p.scale, p.dq, q_row0 + row);
+            store_acc_row<D, kBf16>(row_addr, L::kQColAcc, p.scale, p.dq, q_row0 + row);
         }
     }
 
