@@ -19,8 +19,12 @@
 //                         head of a KV head) in TMEM
 //   fa2_bwd_dq_kernel     one CTA per 128-query tile: S = Q K^T,
 //                         dP = dO V^T, dS in TMEM, dQ += dS K
-// Warps 0-3 elementwise (thread = TMEM lane), warp 4 TMA producer, warp 5
-// TMEM allocator and MMA issuer. TMEM: S | dP | two d-column accumulators
+// Warps 0-7 elementwise (warp w: TMEM lanes 32 (w % 4) .. + 31, one row per
+// thread, columns 64 (w / 4) .. + 63 of the tile, so two warps per scheduler
+// hide each other's latency), warp 8 TMA producer, warp 9 TMEM allocator and
+// MMA issuer. Each half's 16-bit results (P^T, dS^T, dS) are packed into the
+// first 32 of its own 64 fp32 columns -- never into the other warp's, which
+// may not have been read yet -- and the MMAs read A in those two halves. TMEM: S | dP | two d-column accumulators
 // (dK/dV), S0 | S1 | dP | dQ (dQ).
 //
 // Overlap. The elementwise step of a tile runs in two phases with their own
@@ -36,9 +40,10 @@
 namespace fa2 {
 namespace bwd {
 
-constexpr int kThreads = 192;
-constexpr int kLoadWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kEwThreads = 256;   // warps 0-7
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr int kStages = 2;
 
 struct Params {
@@ -142,12 +147,13 @@ __device__ __forceinline__ void store_row_16(void* base, long long row, int d, i
     for (int v = 0; v < 4; ++v) dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
 }
 
-// Write a d-column fp32 TMEM accumulator row (times `mul`) as 16-bit.
+// Write columns [c0, c1) of a d-column fp32 TMEM accumulator row (times
+// `mul`) as 16-bit.
 template <int D, bool kBf16>
 __device__ __forceinline__ void store_acc_row(uint32_t row_addr, uint32_t col, float mul, void* out,
-                                              long long grow) {
+                                              long long grow, int c0 = 0, int c1 = D) {
 #pragma unroll 1
-    for (int cc = 0; cc < D; cc += 32) {
+    for (int cc = c0; cc < c1; cc += 32) {
         uint32_t a[32];
         ptx::tmem_ld32(row_addr + col + cc, a);
         ptx::tmem_wait_ld();
@@ -200,8 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bars.s_full(0), 1);
         ptx::mbar_init(bars.s_full(1), 1);
         ptx::mbar_init(bars.dp_full(), 1);
-        ptx::mbar_init(bars.p_full(), 128);
-        ptx::mbar_init(bars.ds_full(), 128);
+        ptx::mbar_init(bars.p_full(), kEwThreads);
+        ptx::mbar_init(bars.ds_full(), kEwThreads);
         ptx::mbar_init(bars.acc_full(), 1);
         for (int s = 0; s < kStages; ++s) ptx::mbar_init(bars.lse_ready(s), 128);
         *abort_flag = 0;
@@ -278,12 +284,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // half of the S columns; dO as the MN-major B operand) ...
             if (!(ok = wait_u(bars.p_full(), n & 1, kSitePFull))) break;
             ptx::tc_fence_after();
-            pv_kloop(tmem + L::kColAcc0, tmem + L::kColS, ptx::desc_sw128(st + L::kTileBytes, L::kBlkBytes, 1024),
+            ptx::mma_ts_kloop8_split(tmem + L::kColAcc0, tmem + L::kColS, ptx::desc_sw128(st + L::kTileBytes, L::kBlkBytes, 1024),
                      kIdA, n > 0 ? 1u : 0u);
             // ... and dK += dS^T Q once dS^T is
             if (!(ok = wait_u(bars.ds_full(), n & 1, kSitePFull))) break;
             ptx::tc_fence_after();
-            pv_kloop(tmem + L::kColAcc1, tmem + L::kColDP, ptx::desc_sw128(st, L::kBlkBytes, 1024), kIdA,
+            ptx::mma_ts_kloop8_split(tmem + L::kColAcc1, tmem + L::kColDP, ptx::desc_sw128(st, L::kBlkBytes, 1024), kIdA,
                      n > 0 ? 1u : 0u);
             ptx::tc_commit_elect(bars.stage_empty(s));
         }
@@ -291,9 +297,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         w.drain(bars.acc_full(), 0);
         __syncwarp();
     } else {
-        // elementwise: thread = key row of the tile = TMEM lane
-        const int row = threadIdx.x;
-        const uint32_t row_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+        // elementwise: thread = key row of the tile = TMEM lane; columns
+        // (query rows) [c0, c0 + 64)
+        const int row = 32 * (warp & 3) + lane;
+        const int c0 = 64 * (warp >> 2);
+        const uint32_t row_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
         const float c = p.scale_log2;
         constexpr float kLog2e = 1.4426950408889634f;
         bool ok = true;
@@ -314,34 +322,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The stage's LSE row, times log2(e) in place (one value per
             // thread); the stage is reloaded by TMA only after this tile's
             // MMAs, hence the proxy fence.
-            lse[row] *= kLog2e;
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(bars.lse_ready(s));
+            if (c0 == 0) {
+                lse[row] *= kLog2e;
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(bars.lse_ready(s));
+            }
             ok = w.wait(bars.lse_ready(s), (n / kStages) & 1, kSiteStats);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
             }
             // P phase: P^T = exp2(S^T c - LSE log2 e) -> 16-bit over S^T
-            float pf[128];
+            float pf[64];
 #pragma unroll
-            for (int cc = 0; cc < 128; cc += 32) {
+            for (int cc = 0; cc < 64; cc += 32) {
                 uint32_t sv[32];
-                ptx::tmem_ld32(row_addr + L::kColS + cc, sv);
+                ptx::tmem_ld32(row_addr + L::kColS + c0 + cc, sv);
                 ptx::tmem_wait_ld();
                 uint32_t pk[16];
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
 #pragma unroll
                     for (int y = 0; y < 2; ++y) {
-                        const int qc = cc + 2 * x + y;
+                        const int qc = c0 + cc + 2 * x + y;
                         float pp = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * x + y]), c, -lse[qc]));
                         if (diag && qc < row) pp = 0.0f;
-                        pf[qc] = pp;
+                        pf[cc + 2 * x + y] = pp;
                     }
                     pk[x] = ptx::pack2<kBf16>(pf[cc + 2 * x], pf[cc + 2 * x + 1]);
                 }
-                ptx::tmem_st16(row_addr + L::kColS + cc / 2, pk);
+                ptx::tmem_st16(row_addr + L::kColS + c0 + cc / 2, pk);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
@@ -354,18 +364,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::tc_fence_after();
 #pragma unroll
-            for (int cc = 0; cc < 128; cc += 32) {
+            for (int cc = 0; cc < 64; cc += 32) {
                 uint32_t dp[32];
-                ptx::tmem_ld32(row_addr + L::kColDP + cc, dp);
+                ptx::tmem_ld32(row_addr + L::kColDP + c0 + cc, dp);
                 ptx::tmem_wait_ld();
                 uint32_t dk[16];
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
-                    const int qc = cc + 2 * x;
-                    dk[x] = ptx::pack2<kBf16>(pf[qc] * (__uint_as_float(dp[2 * x]) - dl[qc]),
-                                              pf[qc + 1] * (__uint_as_float(dp[2 * x + 1]) - dl[qc + 1]));
+                    const int j = cc + 2 * x;
+                    dk[x] = ptx::pack2<kBf16>(pf[j] * (__uint_as_float(dp[2 * x]) - dl[c0 + j]),
+                                              pf[j + 1] * (__uint_as_float(dp[2 * x + 1]) - dl[c0 + j + 1]));
                 }
-                ptx::tmem_st16(row_addr + L::kColDP + cc / 2, dk);
+                ptx::tmem_st16(row_addr + L::kColDP + c0 + cc / 2, dk);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
@@ -375,8 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__all_sync(0xffffffffu, ok)) {
             ptx::tc_fence_after();
             const long long grow = kv_row0 + row;
-            store_acc_row<D, kBf16>(row_addr, L::kColAcc0, 1.0f, p.dv, grow);
-            store_acc_row<D, kBf16>(row_addr, L::kColAcc1, p.scale, p.dk, grow);
+            if (c0 == 0)
+                store_acc_row<D, kBf16>(row_addr, L::kColAcc0, 1.0f, p.dv, grow);
+            else
+                store_acc_row<D, kBf16>(row_addr, L::kColAcc1, p.scale, p.dk, grow);
         }
     }
 
@@ -422,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bars.s_full(0), 1);
         ptx::mbar_init(bars.s_full(1), 1);
         ptx::mbar_init(bars.dp_full(), 1);
-        ptx::mbar_init(bars.ds_full(), 128);
+        ptx::mbar_init(bars.ds_full(), kEwThreads);
         ptx::mbar_init(bars.acc_full(), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -510,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the MN-major B operand)
             if (!(ok = wait_u(bars.ds_full(), n & 1, kSitePFull))) break;
             ptx::tc_fence_after();
-            pv_kloop(tmem + L::kQColAcc, tmem + L::kQColDP, ptx::desc_sw128(st, L::kBlkBytes, 1024), kIdQ,
+            ptx::mma_ts_kloop8_split(tmem + L::kQColAcc, tmem + L::kQColDP, ptx::desc_sw128(st, L::kBlkBytes, 1024), kIdQ,
                      n > 0 ? 1u : 0u);
             ptx::tc_commit_elect(bars.stage_empty(n % kStages));
             if (s_issued == n + 1 && n + 1 < steps) {
@@ -524,9 +536,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         w.drain(bars.acc_full(), 0);
         __syncwarp();
     } else {
-        // elementwise: thread = query row of the tile = TMEM lane
-        const int row = threadIdx.x;
-        const uint32_t row_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+        // elementwise: thread = query row of the tile = TMEM lane; columns
+        // (keys) [c0, c0 + 64)
+        const int row = 32 * (warp & 3) + lane;
+        const int c0 = 64 * (warp >> 2);
+        const uint32_t row_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
         const float c = p.scale_log2;
         const float lse2 = p.lse[q_row0 + row] * 1.4426950408889634f;
         const float dl = p.delta[q_row0 + row];
@@ -541,18 +555,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool diag = p.causal && n == qt;  // key k visible to query q only if k <= q
             // P phase: P = exp2(S c - LSE log2 e), kept in registers
             const uint32_t colS = L::kQColS0 + 128u * (n & 1);
-            float pf[128];
+            float pf[64];
 #pragma unroll
-            for (int cc = 0; cc < 128; cc += 32) {
+            for (int cc = 0; cc < 64; cc += 32) {
                 uint32_t sv[32];
-                ptx::tmem_ld32(row_addr + colS + cc, sv);
+                ptx::tmem_ld32(row_addr + colS + c0 + cc, sv);
                 ptx::tmem_wait_ld();
 #pragma unroll
                 for (int x = 0; x < 32; ++x) {
-                    const int kc = cc + x;
+                    const int kc = c0 + cc + x;
                     float pp = ptx::ex2_approx(fmaf(__uint_as_float(sv[x]), c, -lse2));
                     if (diag && kc > row) pp = 0.0f;
-                    pf[kc] = pp;
+                    pf[cc + x] = pp;
                 }
             }
             // dS phase: dS = P o (dP - D) -> 16-bit over dP
@@ -563,18 +577,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::tc_fence_after();
 #pragma unroll
-            for (int cc = 0; cc < 128; cc += 32) {
+            for (int cc = 0; cc < 64; cc += 32) {
                 uint32_t dp[32];
-                ptx::tmem_ld32(row_addr + L::kQColDP + cc, dp);
+                ptx::tmem_ld32(row_addr + L::kQColDP + c0 + cc, dp);
                 ptx::tmem_wait_ld();
                 uint32_t dk[16];
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
-                    const int kc = cc + 2 * x;
-                    dk[x] = ptx::pack2<kBf16>(pf[kc] * (__uint_as_float(dp[2 * x]) - dl),
-                                              pf[kc + 1] * (__uint_as_float(dp[2 * x + 1]) - dl));
+                    const int j = cc + 2 * x;
+                    dk[x] = ptx::pack2<kBf16>(pf[j] * (__uint_as_float(dp[2 * x]) - dl),
+                                              pf[j + 1] * (__uint_as_float(dp[2 * x + 1]) - dl));
                 }
-                ptx::tmem_st16(row_addr + L::kQColDP + cc / 2, dk);
+                ptx::tmem_st16(row_addr + L::kQColDP + c0 + cc / 2, dk);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
@@ -583,7 +597,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = w.wait(bars.acc_full(), 0, kSiteOFull);
         if (__all_sync(0xffffffffu, ok)) {
             ptx::tc_fence_after();
-            store_acc_row<D, kBf16>(row_addr, L::kQColAcc, p.scale, p.dq, q_row0 + row);
+            store_acc_row<D, kBf16>(row_addr, L::kQColAcc, p.scale, p.dq, q_row0 + row, c0 * D / 128,
+                                    (c0 + 64) * D / 128);
         }
     }
 

@@ -342,6 +342,36 @@ __device__ __forceinline__ void mma_ts_kloop8(uint32_t d_tmem, uint32_t a_tmem, 
         : "memory");
 }
 
+// The same with A in two 32-column halves 64 columns apart: K-steps 0-3
+// read A columns 0..31, steps 4-7 columns 64..95 (each half of a row's
+// 16-bit values packed inside the fp32 columns it was computed from).
+__device__ __forceinline__ void mma_ts_kloop8_split(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                    uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred e, p0, pt;\n\t.reg .b32 blo, bhi, t0, t1;\n\t.reg .b64 b;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\t"
+        "setp.eq.b32 pt, %4, %4;\n\t"
+        "mov.b64 {blo, bhi}, %2;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
+        "add.u32 t0, %1, 8;\n\tadd.u32 t1, blo, 128;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], b, %3, pt;\n\t"
+        "add.u32 t0, %1, 16;\n\tadd.u32 t1, blo, 256;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], b, %3, pt;\n\t"
+        "add.u32 t0, %1, 24;\n\tadd.u32 t1, blo, 384;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], b, %3, pt;\n\t"
+        "add.u32 t0, %1, 64;\n\tadd.u32 t1, blo, 512;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], b, %3, pt;\n\t"
+        "add.u32 t0, %1, 72;\n\tadd.u32 t1, blo, 640;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], b, %3, pt;\n\t"
+        "add.u32 t0, %1, 80;\n\tadd.u32 t1, blo, 768;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], b, %3, pt;\n\t"
+        "add.u32 t0, %1, 88;\n\tadd.u32 t1, blo, 896;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], b, %3, pt;\n\t"
+        "}" ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
 __device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
