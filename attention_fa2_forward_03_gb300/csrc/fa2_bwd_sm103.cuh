@@ -73,9 +73,8 @@ struct BwdLayout {
     static constexpr int kRingOff = 2 * kTileBytes;
     static constexpr int kStageBytes = 2 * kTileBytes + 1024;    // two tiles + LSE + D
     static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
-    // fixed_full, stage_full[S], stage_empty[S], s_full[2], dp_full, p_full, ds_full, acc_full,
-    // lse_ready[S]
-    static constexpr int kNumBars = 1 + 2 * kStages + 6 + kStages;
+    // fixed_full, stage_full[S], stage_empty[S], s_full[2], dp_full, p_full, ds_full, acc_full
+    static constexpr int kNumBars = 1 + 2 * kStages + 6;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -96,7 +95,6 @@ struct BwdBars {
     __device__ uint32_t p_full() const { return base + 8 * (4 + 2 * kStages); }
     __device__ uint32_t ds_full() const { return base + 8 * (5 + 2 * kStages); }
     __device__ uint32_t acc_full() const { return base + 8 * (6 + 2 * kStages); }
-    __device__ uint32_t lse_ready(int s) const { return base + 8 * (7 + 2 * kStages + s); }
 };
 
 // ---------------------------------------------------------------- D = rowsum(dO o O)
@@ -209,7 +207,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bars.p_full(), kEwThreads);
         ptx::mbar_init(bars.ds_full(), kEwThreads);
         ptx::mbar_init(bars.acc_full(), 1);
-        for (int s = 0; s < kStages; ++s) ptx::mbar_init(bars.lse_ready(s), 128);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -305,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float c = p.scale_log2;
         constexpr float kLog2e = 1.4426950408889634f;
         bool ok = true;
+        int qi = p.causal ? kt : 0;   // query tile of the current step
         for (int n = 0; n < steps; ++n) {
             const int s = n % kStages;
             ok = w.wait(bars.s_full(), n & 1, kSiteSFull);
@@ -314,43 +312,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             ptx::tc_fence_after();
-            int g, i;
-            dkdv_step(p, kt, n, g, i);
-            const bool diag = p.causal && i == kt;  // query q may see key k only if q >= k
-            float* lse = reinterpret_cast<float*>(smem + L::kRingOff + s * L::kStageBytes + 2 * L::kTileBytes);
+            // query tile of step n: tiles first .. n_tiles-1 of each query head in turn
+            const bool diag = p.causal && qi == kt;  // query q may see key k only if q >= k
+            if (++qi == p.n_tiles) qi = p.causal ? kt : 0;
+            const float* lse = reinterpret_cast<const float*>(smem + L::kRingOff + s * L::kStageBytes +
+                                                              2 * L::kTileBytes);
             const float* dl = lse + 128;
-            // The stage's LSE row, times log2(e) in place (one value per
-            // thread); the stage is reloaded by TMA only after this tile's
-            // MMAs, hence the proxy fence.
-            if (c0 == 0) {
-                lse[row] *= kLog2e;
-                ptx::fence_proxy_async_smem();
-                ptx::mbar_arrive(bars.lse_ready(s));
-            }
-            ok = w.wait(bars.lse_ready(s), (n / kStages) & 1, kSiteStats);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
+            // This warp's 64 query columns: lane x holds LSE (times log2 e)
+            // and D of columns c0 + x and c0 + 32 + x; the loops below take
+            // them by shuffle, keeping shared memory free for the tensor
+            // core's operand reads while the dP and dV MMAs run.
+            const float l2v[2] = {-lse[c0 + lane] * kLog2e, -lse[c0 + 32 + lane] * kLog2e};
+            const float dv2[2] = {dl[c0 + lane], dl[c0 + 32 + lane]};
             // P phase: P^T = exp2(S^T c - LSE log2 e) -> 16-bit over S^T
             float pf[64];
+            {
+                uint32_t sv[64];
+                ptx::tmem_ld32_at<0>(row_addr + L::kColS + c0, sv);
+                ptx::tmem_ld32_at<32>(row_addr + L::kColS + c0 + 32, sv);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    const float nl = __shfl_sync(0xffffffffu, l2v[j / 32], j % 32);
+                    pf[j] = ptx::ex2_approx(fmaf(__uint_as_float(sv[j]), c, nl));
+                }
+            }
+            if (diag) {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) pf[j] = c0 + j < row ? 0.0f : pf[j];
+            }
 #pragma unroll
             for (int cc = 0; cc < 64; cc += 32) {
-                uint32_t sv[32];
-                ptx::tmem_ld32(row_addr + L::kColS + c0 + cc, sv);
-                ptx::tmem_wait_ld();
                 uint32_t pk[16];
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-#pragma unroll
-                    for (int y = 0; y < 2; ++y) {
-                        const int qc = c0 + cc + 2 * x + y;
-                        float pp = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * x + y]), c, -lse[qc]));
-                        if (diag && qc < row) pp = 0.0f;
-                        pf[cc + 2 * x + y] = pp;
-                    }
-                    pk[x] = ptx::pack2<kBf16>(pf[cc + 2 * x], pf[cc + 2 * x + 1]);
-                }
+                for (int x = 0; x < 16; ++x) pk[x] = ptx::pack2<kBf16>(pf[cc + 2 * x], pf[cc + 2 * x + 1]);
                 ptx::tmem_st16(row_addr + L::kColS + c0 + cc / 2, pk);
             }
             ptx::tmem_wait_st();
@@ -363,19 +358,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             ptx::tc_fence_after();
-#pragma unroll
-            for (int cc = 0; cc < 64; cc += 32) {
-                uint32_t dp[32];
-                ptx::tmem_ld32(row_addr + L::kColDP + c0 + cc, dp);
+            {
+                uint32_t dp[64];
+                ptx::tmem_ld32_at<0>(row_addr + L::kColDP + c0, dp);
+                ptx::tmem_ld32_at<32>(row_addr + L::kColDP + c0 + 32, dp);
                 ptx::tmem_wait_ld();
-                uint32_t dk[16];
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const int j = cc + 2 * x;
-                    dk[x] = ptx::pack2<kBf16>(pf[j] * (__uint_as_float(dp[2 * x]) - dl[c0 + j]),
-                                              pf[j + 1] * (__uint_as_float(dp[2 * x + 1]) - dl[c0 + j + 1]));
+                for (int cc = 0; cc < 64; cc += 32) {
+                    uint32_t dk[16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const int j = cc + 2 * x;
+                        const float d0 = __shfl_sync(0xffffffffu, dv2[cc / 32], 2 * x);
+                        const float d1 = __shfl_sync(0xffffffffu, dv2[cc / 32], 2 * x + 1);
+                        dk[x] = ptx::pack2<kBf16>(pf[j] * (__uint_as_float(dp[j]) - d0),
+                                                  pf[j + 1] * (__uint_as_float(dp[j + 1]) - d1));
+                    }
+                    ptx::tmem_st16(row_addr + L::kColDP + c0 + cc / 2, dk);
                 }
-                ptx::tmem_st16(row_addr + L::kColDP + c0 + cc / 2, dk);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
@@ -556,18 +556,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // P phase: P = exp2(S c - LSE log2 e), kept in registers
             const uint32_t colS = L::kQColS0 + 128u * (n & 1);
             float pf[64];
-#pragma unroll
-            for (int cc = 0; cc < 64; cc += 32) {
-                uint32_t sv[32];
-                ptx::tmem_ld32(row_addr + colS + c0 + cc, sv);
+            {
+                uint32_t sv[64];
+                ptx::tmem_ld32_at<0>(row_addr + colS + c0, sv);
+                ptx::tmem_ld32_at<32>(row_addr + colS + c0 + 32, sv);
                 ptx::tmem_wait_ld();
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    const int kc = c0 + cc + x;
-                    float pp = ptx::ex2_approx(fmaf(__uint_as_float(sv[x]), c, -lse2));
-                    if (diag && kc > row) pp = 0.0f;
-                    pf[cc + x] = pp;
-                }
+                for (int j = 0; j < 64; ++j) pf[j] = ptx::ex2_approx(fmaf(__uint_as_float(sv[j]), c, -lse2));
+            }
+            if (diag) {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) pf[j] = c0 + j > row ? 0.0f : pf[j];
             }
             // dS phase: dS = P o (dP - D) -> 16-bit over dP
             ok = w.wait(bars.dp_full(), n & 1, kSiteSFull);
@@ -576,19 +575,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             ptx::tc_fence_after();
-#pragma unroll
-            for (int cc = 0; cc < 64; cc += 32) {
-                uint32_t dp[32];
-                ptx::tmem_ld32(row_addr + L::kQColDP + c0 + cc, dp);
+            {
+                uint32_t dp[64];
+                ptx::tmem_ld32_at<0>(row_addr + L::kQColDP + c0, dp);
+                ptx::tmem_ld32_at<32>(row_addr + L::kQColDP + c0 + 32, dp);
                 ptx::tmem_wait_ld();
-                uint32_t dk[16];
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const int j = cc + 2 * x;
-                    dk[x] = ptx::pack2<kBf16>(pf[j] * (__uint_as_float(dp[2 * x]) - dl),
-                                              pf[j + 1] * (__uint_as_float(dp[2 * x + 1]) - dl));
+                for (int cc = 0; cc < 64; cc += 32) {
+                    uint32_t dk[16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const int j = cc + 2 * x;
+                        dk[x] = ptx::pack2<kBf16>(pf[j] * (__uint_as_float(dp[j]) - dl),
+                                                  pf[j + 1] * (__uint_as_float(dp[j + 1]) - dl));
+                    }
+                    ptx::tmem_st16(row_addr + L::kQColDP + c0 + cc / 2, dk);
                 }
-                ptx::tmem_st16(row_addr + L::kQColDP + c0 + cc / 2, dk);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
