@@ -268,27 +268,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = wait_u(bars.fixed_full(), 0, kSiteQFull);
         const uint64_t kdesc = ptx::desc_sw128(sbase + L::kFixedOff, 16, 1024);
         const uint64_t vdesc = ptx::desc_sw128(sbase + L::kFixedOff + L::kTileBytes, 16, 1024);
-        for (int n = 0; n < steps && ok; ++n) {
-            const int s = n % kStages;
-            if (!(ok = wait_u(bars.stage_full(s), (n / kStages) & 1, kSiteKvFull))) break;
-            ptx::tc_fence_after();
-            const uint32_t st = sbase + L::kRingOff + s * L::kStageBytes;
-            qk_kloop<D>(tmem + L::kColS, kdesc, ptx::desc_sw128(st, 16, 1024), kIdT);
+        auto stage_addr = [&](int n) { return sbase + L::kRingOff + (n % kStages) * L::kStageBytes; };
+        auto issue_s = [&](int n) {   // S^T of step n, once its stage has landed
+            qk_kloop<D>(tmem + L::kColS, kdesc, ptx::desc_sw128(stage_addr(n), 16, 1024), kIdT);
             ptx::tc_commit_elect(bars.s_full());
+        };
+        int s_issued = 0;   // steps whose S^T has been issued
+        if (steps > 0 && (ok = ok && wait_u(bars.stage_full(0), 0, kSiteKvFull))) {
+            ptx::tc_fence_after();
+            issue_s(0);
+            s_issued = 1;
+        }
+        for (int n = 0; n < steps && ok; ++n) {
+            const uint32_t st = stage_addr(n);
+            // dP^T (the stage landed before S^T(n) was issued)
             qk_kloop<D>(tmem + L::kColDP, vdesc, ptx::desc_sw128(st + L::kTileBytes, 16, 1024), kIdT);
             ptx::tc_commit_elect(bars.dp_full());
-            // dV += P^T dO as soon as P^T is in TMEM (16-bit in the first
-            // half of the S columns; dO as the MN-major B operand) ...
+            // dV += P^T dO as soon as P^T is in TMEM (16-bit over the S
+            // columns; dO as the MN-major B operand) ...
             if (!(ok = wait_u(bars.p_full(), n & 1, kSitePFull))) break;
             ptx::tc_fence_after();
-            ptx::mma_ts_kloop8_split(tmem + L::kColAcc0, tmem + L::kColS, ptx::desc_sw128(st + L::kTileBytes, L::kBlkBytes, 1024),
-                     kIdA, n > 0 ? 1u : 0u);
+            ptx::mma_ts_kloop8_split(tmem + L::kColAcc0, tmem + L::kColS,
+                                     ptx::desc_sw128(st + L::kTileBytes, L::kBlkBytes, 1024), kIdA, n > 0 ? 1u : 0u);
+            // ... then S^T of the next step, if its stage is already here,
+            // so the elementwise warps find it when they finish dS^T(n)
+            // (it overwrites P^T(n) only after dV has read it: in order) ...
+            if (s_issued == n + 1 && n + 1 < steps) {
+                const uint32_t bar = bars.stage_full((n + 1) % kStages);
+                const uint32_t par = ((n + 1) / kStages) & 1;
+                if (__shfl_sync(0xffffffffu, ptx::mbar_test_wait(bar, par) ? 1 : 0, 0)) {
+                    ptx::tc_fence_after();
+                    issue_s(n + 1);
+                    ++s_issued;
+                }
+            }
             // ... and dK += dS^T Q once dS^T is
             if (!(ok = wait_u(bars.ds_full(), n & 1, kSitePFull))) break;
             ptx::tc_fence_after();
-            ptx::mma_ts_kloop8_split(tmem + L::kColAcc1, tmem + L::kColDP, ptx::desc_sw128(st, L::kBlkBytes, 1024), kIdA,
-                     n > 0 ? 1u : 0u);
-            ptx::tc_commit_elect(bars.stage_empty(s));
+            ptx::mma_ts_kloop8_split(tmem + L::kColAcc1, tmem + L::kColDP, ptx::desc_sw128(st, L::kBlkBytes, 1024),
+                                     kIdA, n > 0 ? 1u : 0u);
+            ptx::tc_commit_elect(bars.stage_empty(n % kStages));
+            if (s_issued == n + 1 && n + 1 < steps) {
+                if (!(ok = wait_u(bars.stage_full((n + 1) % kStages), ((n + 1) / kStages) & 1, kSiteKvFull))) break;
+                ptx::tc_fence_after();
+                issue_s(n + 1);
+                ++s_issued;
+            }
         }
         ptx::tc_commit_elect(bars.acc_full());
         w.drain(bars.acc_full(), 0);
