@@ -165,25 +165,56 @@ __device__ __forceinline__ void store_acc_row(uint32_t row_addr, uint32_t col, f
 
 // ---------------------------------------------------------------- dK, dV
 
-// Step n of a dK/dV CTA: query head g (of the KV head's group), query tile i.
-__device__ __forceinline__ void dkdv_step(const Params& p, int kt, int n, int& g, int& i) {
-    const int first = p.causal ? kt : 0;
-    const int per = p.n_tiles - first;
-    g = n / per;
-    i = first + n % per;
-}
+
+// dK/dV kernel layout: K and V once, then separate rings for the query
+// tiles (3 stages: Q(n) is read by S^T(n), issued as early as mid-step n-1,
+// and by dK(n) at the end of step n) and the upstream-gradient tiles (2
+// stages: dO(n) is read by dP^T(n) and dV(n) only). LSE and D are read by
+// the elementwise warps from global memory, one step ahead.
+template <int D>
+struct DkdvLayout {
+    static constexpr int kBlkBytes = 128 * 128;
+    static constexpr int kTileBytes = 128 * D * 2;
+    static constexpr int kQStages = 3, kDoStages = 2;
+    static constexpr int kFixedOff = 0;                               // K | V
+    static constexpr int kQOff = 2 * kTileBytes;
+    static constexpr int kDoOff = kQOff + kQStages * kTileBytes;
+    static constexpr int kBarOff = kDoOff + kDoStages * kTileBytes;
+    // fixed_full, q_full[3], q_empty[3], do_full[2], do_empty[2], s_full, dp_full, p_full, ds_full, acc_full
+    static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDoStages + 5;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
+};
+
+struct DkdvBars {
+    uint32_t base;
+    static constexpr int QS = 3, DS = 2;
+    __device__ uint32_t fixed_full() const { return base; }
+    __device__ uint32_t q_full(int s) const { return base + 8 * (1 + s); }
+    __device__ uint32_t q_empty(int s) const { return base + 8 * (1 + QS + s); }
+    __device__ uint32_t do_full(int s) const { return base + 8 * (1 + 2 * QS + s); }
+    __device__ uint32_t do_empty(int s) const { return base + 8 * (1 + 2 * QS + DS + s); }
+    __device__ uint32_t s_full() const { return base + 8 * (1 + 2 * QS + 2 * DS); }
+    __device__ uint32_t dp_full() const { return base + 8 * (2 + 2 * QS + 2 * DS); }
+    __device__ uint32_t p_full() const { return base + 8 * (3 + 2 * QS + 2 * DS); }
+    __device__ uint32_t ds_full() const { return base + 8 * (4 + 2 * QS + 2 * DS); }
+    __device__ uint32_t acc_full() const { return base + 8 * (5 + 2 * QS + 2 * DS); }
+};
 
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa2_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                         const Params p) {
-    using L = BwdLayout<D>;
+    using L = DkdvLayout<D>;
+    constexpr int QS = L::kQStages, DS = L::kDoStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = ptx::smem_addr(smem);
-    const BwdBars<D> bars{sbase + L::kBarOff};
+    const DkdvBars bars{sbase + L::kBarOff};
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
     const int warp = threadIdx.x / 32;
@@ -192,17 +223,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kvh = blockIdx.y;                // b * Hkv + kv head
     const int b = kvh / (p.hq / p.group);
     const int hk = kvh - b * (p.hq / p.group);
-    const int steps = p.group * (p.n_tiles - (p.causal ? kt : 0));
+    const int first = p.causal ? kt : 0;       // first query tile that sees this key tile
+    const int steps = p.group * (p.n_tiles - first);
     const long long kv_row0 = static_cast<long long>(kvh) * p.n_tiles * 128 + kt * 128;
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(bars.fixed_full(), 1);
-        for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(bars.stage_full(s), 1);
-            ptx::mbar_init(bars.stage_empty(s), 1);
+        for (int s = 0; s < QS; ++s) {
+            ptx::mbar_init(bars.q_full(s), 1);
+            ptx::mbar_init(bars.q_empty(s), 1);
         }
-        ptx::mbar_init(bars.s_full(0), 1);
-        ptx::mbar_init(bars.s_full(1), 1);
+        for (int s = 0; s < DS; ++s) {
+            ptx::mbar_init(bars.do_full(s), 1);
+            ptx::mbar_init(bars.do_empty(s), 1);
+        }
+        ptx::mbar_init(bars.s_full(), 1);
         ptx::mbar_init(bars.dp_full(), 1);
         ptx::mbar_init(bars.p_full(), kEwThreads);
         ptx::mbar_init(bars.ds_full(), kEwThreads);
@@ -219,9 +254,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Waiter w{abort_flag, p.wait_limit_ns};
+    // First row of step n's query tile: query heads of the group in turn,
+    // tiles first .. n_tiles - 1 of each.
     auto q_row = [&](int g, int i) {
         return (static_cast<long long>(b) * p.hq + hk * p.group + g) * p.n_tiles * 128 + i * 128;
     };
+    auto q_addr = [&](int n) { return sbase + L::kQOff + (n % QS) * L::kTileBytes; };
+    auto do_addr = [&](int n) { return sbase + L::kDoOff + (n % DS) * L::kTileBytes; };
 
     if (warp == kLoadWarp) {
         if (lane == 0) {
@@ -233,27 +272,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tma_load_2d(sbase + L::kFixedOff + L::kTileBytes + blk * L::kBlkBytes, &tmV, blk * 64,
                                  static_cast<int>(kv_row0), bars.fixed_full());
             }
-            int n = 0;
-            for (; n < steps; ++n) {
-                const int s = n % kStages;
-                if (!w.wait(bars.stage_empty(s), ((n / kStages) & 1) ^ 1, kSiteKvEmpty)) break;
-                int g, i;
-                dkdv_step(p, kt, n, g, i);
-                const long long qr = q_row(g, i);
-                const uint32_t st = sbase + L::kRingOff + s * L::kStageBytes;
-                ptx::mbar_arrive_expect_tx(bars.stage_full(s), 2 * L::kTileBytes + 1024);
+            int nq = 0, nd = 0;   // Q and dO tiles issued
+            int g = 0, i = first;
+            bool ok = true;
+            for (int n = 0; n < steps && ok; ++n) {
+                const int qr = static_cast<int>(q_row(g, i));
+                if (!(ok = w.wait(bars.q_empty(n % QS), ((n / QS) & 1) ^ 1, kSiteKvEmpty))) break;
+                ptx::mbar_arrive_expect_tx(bars.q_full(n % QS), L::kTileBytes);
 #pragma unroll
-                for (int blk = 0; blk < D / 64; ++blk) {
-                    ptx::tma_load_2d(st + blk * L::kBlkBytes, &tmQ, blk * 64, static_cast<int>(qr), bars.stage_full(s));
-                    ptx::tma_load_2d(st + L::kTileBytes + blk * L::kBlkBytes, &tmDO, blk * 64, static_cast<int>(qr),
-                                     bars.stage_full(s));
+                for (int blk = 0; blk < D / 64; ++blk)
+                    ptx::tma_load_2d(q_addr(n) + blk * L::kBlkBytes, &tmQ, blk * 64, qr, bars.q_full(n % QS));
+                ++nq;
+                if (!(ok = w.wait(bars.do_empty(n % DS), ((n / DS) & 1) ^ 1, kSiteKvEmpty))) break;
+                ptx::mbar_arrive_expect_tx(bars.do_full(n % DS), L::kTileBytes);
+#pragma unroll
+                for (int blk = 0; blk < D / 64; ++blk)
+                    ptx::tma_load_2d(do_addr(n) + blk * L::kBlkBytes, &tmDO, blk * 64, qr, bars.do_full(n % DS));
+                ++nd;
+                if (++i == p.n_tiles) {
+                    i = first;
+                    ++g;
                 }
-                ptx::bulk_load(st + 2 * L::kTileBytes, p.lse + qr, 512, bars.stage_full(s));
-                ptx::bulk_load(st + 2 * L::kTileBytes + 512, p.delta + qr, 512, bars.stage_full(s));
             }
-            if (n < steps) {
-                const int first = n > kStages ? n - kStages : 0;
-                for (int r = first; r < n; ++r) w.drain(bars.stage_full(r % kStages), (r / kStages) & 1);
+            if (!ok) {
+                // let every copy this CTA started land before it exits
+                for (int r = nq > QS ? nq - QS : 0; r < nq; ++r) w.drain(bars.q_full(r % QS), (r / QS) & 1);
+                for (int r = nd > DS ? nd - DS : 0; r < nd; ++r) w.drain(bars.do_full(r % DS), (r / DS) & 1);
             }
             w.drain(bars.fixed_full(), 0);
         }
@@ -268,48 +312,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = wait_u(bars.fixed_full(), 0, kSiteQFull);
         const uint64_t kdesc = ptx::desc_sw128(sbase + L::kFixedOff, 16, 1024);
         const uint64_t vdesc = ptx::desc_sw128(sbase + L::kFixedOff + L::kTileBytes, 16, 1024);
-        auto stage_addr = [&](int n) { return sbase + L::kRingOff + (n % kStages) * L::kStageBytes; };
-        auto issue_s = [&](int n) {   // S^T of step n, once its stage has landed
-            qk_kloop<D>(tmem + L::kColS, kdesc, ptx::desc_sw128(stage_addr(n), 16, 1024), kIdT);
+        auto issue_s = [&](int n) {   // S^T of step n, once Q(n) has landed
+            qk_kloop<D>(tmem + L::kColS, kdesc, ptx::desc_sw128(q_addr(n), 16, 1024), kIdT);
             ptx::tc_commit_elect(bars.s_full());
         };
         int s_issued = 0;   // steps whose S^T has been issued
-        if (steps > 0 && (ok = ok && wait_u(bars.stage_full(0), 0, kSiteKvFull))) {
+        if (steps > 0 && (ok = ok && wait_u(bars.q_full(0), 0, kSiteKvFull))) {
             ptx::tc_fence_after();
             issue_s(0);
             s_issued = 1;
         }
         for (int n = 0; n < steps && ok; ++n) {
-            const uint32_t st = stage_addr(n);
-            // dP^T (the stage landed before S^T(n) was issued)
-            qk_kloop<D>(tmem + L::kColDP, vdesc, ptx::desc_sw128(st + L::kTileBytes, 16, 1024), kIdT);
+            // dP^T = V dO(n)^T
+            if (!(ok = wait_u(bars.do_full(n % DS), (n / DS) & 1, kSiteKvFull))) break;
+            ptx::tc_fence_after();
+            qk_kloop<D>(tmem + L::kColDP, vdesc, ptx::desc_sw128(do_addr(n), 16, 1024), kIdT);
             ptx::tc_commit_elect(bars.dp_full());
             // dV += P^T dO as soon as P^T is in TMEM (16-bit over the S
-            // columns; dO as the MN-major B operand) ...
+            // columns; dO as the MN-major B operand); dO(n) is then free
             if (!(ok = wait_u(bars.p_full(), n & 1, kSitePFull))) break;
             ptx::tc_fence_after();
             ptx::mma_ts_kloop8_split(tmem + L::kColAcc0, tmem + L::kColS,
-                                     ptx::desc_sw128(st + L::kTileBytes, L::kBlkBytes, 1024), kIdA, n > 0 ? 1u : 0u);
-            // ... then S^T of the next step, if its stage is already here,
-            // so the elementwise warps find it when they finish dS^T(n)
-            // (it overwrites P^T(n) only after dV has read it: in order) ...
+                                     ptx::desc_sw128(do_addr(n), L::kBlkBytes, 1024), kIdA, n > 0 ? 1u : 0u);
+            ptx::tc_commit_elect(bars.do_empty(n % DS));
+            // S^T of the next step if Q(n+1) is here (it overwrites P^T(n)
+            // only after dV has read it: in order), so the elementwise warps
+            // go from dS^T(n) straight to P^T(n+1)
             if (s_issued == n + 1 && n + 1 < steps) {
-                const uint32_t bar = bars.stage_full((n + 1) % kStages);
-                const uint32_t par = ((n + 1) / kStages) & 1;
+                const uint32_t bar = bars.q_full((n + 1) % QS);
+                const uint32_t par = ((n + 1) / QS) & 1;
                 if (__shfl_sync(0xffffffffu, ptx::mbar_test_wait(bar, par) ? 1 : 0, 0)) {
                     ptx::tc_fence_after();
                     issue_s(n + 1);
                     ++s_issued;
                 }
             }
-            // ... and dK += dS^T Q once dS^T is
+            // dK += dS^T Q once dS^T is; Q(n) is then free
             if (!(ok = wait_u(bars.ds_full(), n & 1, kSitePFull))) break;
             ptx::tc_fence_after();
-            ptx::mma_ts_kloop8_split(tmem + L::kColAcc1, tmem + L::kColDP, ptx::desc_sw128(st, L::kBlkBytes, 1024),
+            ptx::mma_ts_kloop8_split(tmem + L::kColAcc1, tmem + L::kColDP, ptx::desc_sw128(q_addr(n), L::kBlkBytes, 1024),
                                      kIdA, n > 0 ? 1u : 0u);
-            ptx::tc_commit_elect(bars.stage_empty(n % kStages));
+            ptx::tc_commit_elect(bars.q_empty(n % QS));
             if (s_issued == n + 1 && n + 1 < steps) {
-                if (!(ok = wait_u(bars.stage_full((n + 1) % kStages), ((n + 1) / kStages) & 1, kSiteKvFull))) break;
+                if (!(ok = wait_u(bars.q_full((n + 1) % QS), ((n + 1) / QS) & 1, kSiteKvFull))) break;
                 ptx::tc_fence_after();
                 issue_s(n + 1);
                 ++s_issued;
@@ -326,29 +371,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t row_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
         const float c = p.scale_log2;
         constexpr float kLog2e = 1.4426950408889634f;
+        // This warp's 64 query columns of a step: lane x holds -LSE log2 e
+        // and D of columns c0 + x and c0 + 32 + x (from global memory, one
+        // step ahead); the loops take them by shuffle.
+        int g = 0, qi = first;
+        float nl_nx[2] = {0.0f, 0.0f}, d_nx[2] = {0.0f, 0.0f};
+        auto fetch = [&](int gg, int ii) {
+            const long long qr = q_row(gg, ii);
+            nl_nx[0] = -__ldg(p.lse + qr + c0 + lane) * kLog2e;
+            nl_nx[1] = -__ldg(p.lse + qr + c0 + 32 + lane) * kLog2e;
+            d_nx[0] = __ldg(p.delta + qr + c0 + lane);
+            d_nx[1] = __ldg(p.delta + qr + c0 + 32 + lane);
+        };
+        if (steps > 0) fetch(g, qi);
         bool ok = true;
-        int qi = p.causal ? kt : 0;   // query tile of the current step
         for (int n = 0; n < steps; ++n) {
-            const int s = n % kStages;
+            const float l2v[2] = {nl_nx[0], nl_nx[1]};
+            const float dv2[2] = {d_nx[0], d_nx[1]};
+            const bool diag = p.causal && qi == kt;  // query q may see key k only if q >= k
+            if (++qi == p.n_tiles) {
+                qi = first;
+                ++g;
+            }
+            if (n + 1 < steps) fetch(g, qi);
             ok = w.wait(bars.s_full(), n & 1, kSiteSFull);
-            if (ok) ok = w.wait(bars.stage_full(s), (n / kStages) & 1, kSiteKvFull);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-            // query tile of step n: tiles first .. n_tiles-1 of each query head in turn
-            const bool diag = p.causal && qi == kt;  // query q may see key k only if q >= k
-            if (++qi == p.n_tiles) qi = p.causal ? kt : 0;
-            const float* lse = reinterpret_cast<const float*>(smem + L::kRingOff + s * L::kStageBytes +
-                                                              2 * L::kTileBytes);
-            const float* dl = lse + 128;
-            // This warp's 64 query columns: lane x holds LSE (times log2 e)
-            // and D of columns c0 + x and c0 + 32 + x; the loops below take
-            // them by shuffle, keeping shared memory free for the tensor
-            // core's operand reads while the dP and dV MMAs run.
-            const float l2v[2] = {-lse[c0 + lane] * kLog2e, -lse[c0 + 32 + lane] * kLog2e};
-            const float dv2[2] = {dl[c0 + lane], dl[c0 + 32 + lane]};
             // P phase: P^T = exp2(S^T c - LSE log2 e) -> 16-bit over S^T
             float pf[64];
             {

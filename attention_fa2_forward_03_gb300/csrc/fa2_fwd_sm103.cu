@@ -354,28 +354,28 @@ fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, c
     const dim3 gkv(static_cast<unsigned>(p.n_tiles), static_cast<unsigned>(B * H_kv));
     const dim3 gq(static_cast<unsigned>(p.n_tiles), static_cast<unsigned>(B * H_q));
 
-    auto run = [&](auto delta_k, auto dkdv_k, auto dq_k, int smem, int slot) -> fa2_status {
+    auto run = [&](auto delta_k, auto dkdv_k, auto dq_k, int smem_kv, int smem_q, int slot) -> fa2_status {
         if (!g_dev[dev].smem_set[slot]) {
-            if (cudaFuncSetAttribute(dkdv_k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-                cudaFuncSetAttribute(dq_k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            if (cudaFuncSetAttribute(dkdv_k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kv) != cudaSuccess ||
+                cudaFuncSetAttribute(dq_k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q) != cudaSuccess)
                 return FA2_ERR_CUDA;
             std::lock_guard<std::mutex> lk(g_mu);
             g_dev[dev].smem_set[slot] = true;
         }
         delta_k<<<gdelta, 256, 0, stream>>>(o, dout, delta, rows_q);
-        dkdv_k<<<gkv, fa2::bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
-        dq_k<<<gq, fa2::bwd::kThreads, smem, stream>>>(mq, mk, mv, mdo, p);
+        dkdv_k<<<gkv, fa2::bwd::kThreads, smem_kv, stream>>>(mq, mk, mv, mdo, p);
+        dq_k<<<gq, fa2::bwd::kThreads, smem_q, stream>>>(mq, mk, mv, mdo, p);
         return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
     };
     if (d == 128)
         return bf ? run(fa2::bwd::fa2_bwd_delta_kernel<128, true>, fa2::bwd::fa2_bwd_dkdv_kernel<128, true>,
-                        fa2::bwd::fa2_bwd_dq_kernel<128, true>, fa2::bwd::BwdLayout<128>::kSmemBytes, 8)
+                        fa2::bwd::fa2_bwd_dq_kernel<128, true>, fa2::bwd::DkdvLayout<128>::kSmemBytes, fa2::bwd::BwdLayout<128>::kSmemBytes, 8)
                   : run(fa2::bwd::fa2_bwd_delta_kernel<128, false>, fa2::bwd::fa2_bwd_dkdv_kernel<128, false>,
-                        fa2::bwd::fa2_bwd_dq_kernel<128, false>, fa2::bwd::BwdLayout<128>::kSmemBytes, 9);
+                        fa2::bwd::fa2_bwd_dq_kernel<128, false>, fa2::bwd::DkdvLayout<128>::kSmemBytes, fa2::bwd::BwdLayout<128>::kSmemBytes, 9);
     return bf ? run(fa2::bwd::fa2_bwd_delta_kernel<64, true>, fa2::bwd::fa2_bwd_dkdv_kernel<64, true>,
-                    fa2::bwd::fa2_bwd_dq_kernel<64, true>, fa2::bwd::BwdLayout<64>::kSmemBytes, 10)
+                    fa2::bwd::fa2_bwd_dq_kernel<64, true>, fa2::bwd::DkdvLayout<64>::kSmemBytes, fa2::bwd::BwdLayout<64>::kSmemBytes, 10)
               : run(fa2::bwd::fa2_bwd_delta_kernel<64, false>, fa2::bwd::fa2_bwd_dkdv_kernel<64, false>,
-                    fa2::bwd::fa2_bwd_dq_kernel<64, false>, fa2::bwd::BwdLayout<64>::kSmemBytes, 11);
+                    fa2::bwd::fa2_bwd_dq_kernel<64, false>, fa2::bwd::DkdvLayout<64>::kSmemBytes, fa2::bwd::BwdLayout<64>::kSmemBytes, 11);
 }
 
 }  // extern "C"
