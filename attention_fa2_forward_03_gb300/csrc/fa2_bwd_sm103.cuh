@@ -44,7 +44,6 @@ constexpr int kEwThreads = 256;   // warps 0-7
 constexpr int kThreads = 320;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kStages = 2;
 
 struct Params {
     const void* o;        // forward output [rows, D]
@@ -60,41 +59,6 @@ struct Params {
     int causal;
     float scale;          // softmax scale
     float scale_log2;     // scale * log2(e)
-};
-
-// Shared memory (1024-aligned). dK/dV kernel: K, V tiles once, then a ring of
-// stages each holding one Q tile, one dO tile and their 128 LSE and D values.
-// dQ kernel: Q and dO tiles once, then a ring of stages each holding K and V.
-template <int D>
-struct BwdLayout {
-    static constexpr int kBlkBytes = 128 * 128;
-    static constexpr int kTileBytes = 128 * D * 2;
-    static constexpr int kFixedOff = 0;                          // two fixed tiles
-    static constexpr int kRingOff = 2 * kTileBytes;
-    static constexpr int kStageBytes = 2 * kTileBytes + 1024;    // two tiles + LSE + D
-    static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
-    // fixed_full, stage_full[S], stage_empty[S], s_full[2], dp_full, p_full, ds_full, acc_full
-    static constexpr int kNumBars = 1 + 2 * kStages + 6;
-    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
-    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-    // dK/dV kernel: S | dP | dV | dK
-    static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
-    // dQ kernel: S0 | S1 | dP | dQ
-    static constexpr uint32_t kQColS0 = 0, kQColDP = 256, kQColAcc = 384;
-};
-
-template <int D>
-struct BwdBars {
-    uint32_t base;
-    __device__ uint32_t fixed_full() const { return base; }
-    __device__ uint32_t stage_full(int s) const { return base + 8 * (1 + s); }
-    __device__ uint32_t stage_empty(int s) const { return base + 8 * (1 + kStages + s); }
-    __device__ uint32_t s_full(int b = 0) const { return base + 8 * (1 + 2 * kStages + b); }
-    __device__ uint32_t dp_full() const { return base + 8 * (3 + 2 * kStages); }
-    __device__ uint32_t p_full() const { return base + 8 * (4 + 2 * kStages); }
-    __device__ uint32_t ds_full() const { return base + 8 * (5 + 2 * kStages); }
-    __device__ uint32_t acc_full() const { return base + 8 * (6 + 2 * kStages); }
 };
 
 // ---------------------------------------------------------------- D = rowsum(dO o O)
@@ -478,17 +442,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- dQ
 
+// dQ kernel layout: Q and dO once, then separate rings for the key tiles
+// (3 stages: K(j) is read by S(j), issued as early as mid-step j-1, and by
+// dQ(j)) and the value tiles (2 stages: V(j) is read by dP(j) only).
+template <int D>
+struct DqLayout {
+    static constexpr int kBlkBytes = 128 * 128;
+    static constexpr int kTileBytes = 128 * D * 2;
+    static constexpr int kKStages = 3, kVStages = 2;
+    static constexpr int kFixedOff = 0;                               // Q | dO
+    static constexpr int kKOff = 2 * kTileBytes;
+    static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+    static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+    // fixed_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], dp_full, ds_full, acc_full
+    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 5;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    // TMEM: S0 | S1 | dP | dQ
+    static constexpr uint32_t kColS0 = 0, kColDP = 256, kColAcc = 384;
+};
+
+struct DqBars {
+    uint32_t base;
+    static constexpr int KS = 3, VS = 2;
+    __device__ uint32_t fixed_full() const { return base; }
+    __device__ uint32_t k_full(int s) const { return base + 8 * (1 + s); }
+    __device__ uint32_t k_empty(int s) const { return base + 8 * (1 + KS + s); }
+    __device__ uint32_t v_full(int s) const { return base + 8 * (1 + 2 * KS + s); }
+    __device__ uint32_t v_empty(int s) const { return base + 8 * (1 + 2 * KS + VS + s); }
+    __device__ uint32_t s_full(int b) const { return base + 8 * (1 + 2 * KS + 2 * VS + b); }
+    __device__ uint32_t dp_full() const { return base + 8 * (3 + 2 * KS + 2 * VS); }
+    __device__ uint32_t ds_full() const { return base + 8 * (4 + 2 * KS + 2 * VS); }
+    __device__ uint32_t acc_full() const { return base + 8 * (5 + 2 * KS + 2 * VS); }
+};
+
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa2_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                       const Params p) {
-    using L = BwdLayout<D>;
+    using L = DqLayout<D>;
+    constexpr int KS = L::kKStages, VS = L::kVStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = ptx::smem_addr(smem);
-    const BwdBars<D> bars{sbase + L::kBarOff};
+    const DqBars bars{sbase + L::kBarOff};
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
     const int warp = threadIdx.x / 32;
@@ -503,9 +503,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(bars.fixed_full(), 1);
-        for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(bars.stage_full(s), 1);
-            ptx::mbar_init(bars.stage_empty(s), 1);
+        for (int s = 0; s < KS; ++s) {
+            ptx::mbar_init(bars.k_full(s), 1);
+            ptx::mbar_init(bars.k_empty(s), 1);
+        }
+        for (int s = 0; s < VS; ++s) {
+            ptx::mbar_init(bars.v_full(s), 1);
+            ptx::mbar_init(bars.v_empty(s), 1);
         }
         ptx::mbar_init(bars.s_full(0), 1);
         ptx::mbar_init(bars.s_full(1), 1);
@@ -524,6 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Waiter w{abort_flag, p.wait_limit_ns};
+    auto k_addr = [&](int n) { return sbase + L::kKOff + (n % KS) * L::kTileBytes; };
+    auto v_addr = [&](int n) { return sbase + L::kVOff + (n % VS) * L::kTileBytes; };
 
     if (warp == kLoadWarp) {
         if (lane == 0) {
@@ -535,23 +541,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tma_load_2d(sbase + L::kFixedOff + L::kTileBytes + blk * L::kBlkBytes, &tmDO, blk * 64,
                                  static_cast<int>(q_row0), bars.fixed_full());
             }
-            int n = 0;
-            for (; n < steps; ++n) {
-                const int s = n % kStages;
-                if (!w.wait(bars.stage_empty(s), ((n / kStages) & 1) ^ 1, kSiteKvEmpty)) break;
-                const long long kr = kv_base + n * 128;
-                const uint32_t st = sbase + L::kRingOff + s * L::kStageBytes;
-                ptx::mbar_arrive_expect_tx(bars.stage_full(s), 2 * L::kTileBytes);
+            int nk = 0, nv = 0;
+            bool ok = true;
+            for (int n = 0; n < steps && ok; ++n) {
+                const int kr = static_cast<int>(kv_base + n * 128);
+                if (!(ok = w.wait(bars.k_empty(n % KS), ((n / KS) & 1) ^ 1, kSiteKvEmpty))) break;
+                ptx::mbar_arrive_expect_tx(bars.k_full(n % KS), L::kTileBytes);
 #pragma unroll
-                for (int blk = 0; blk < D / 64; ++blk) {
-                    ptx::tma_load_2d(st + blk * L::kBlkBytes, &tmK, blk * 64, static_cast<int>(kr), bars.stage_full(s));
-                    ptx::tma_load_2d(st + L::kTileBytes + blk * L::kBlkBytes, &tmV, blk * 64, static_cast<int>(kr),
-                                     bars.stage_full(s));
-                }
+                for (int blk = 0; blk < D / 64; ++blk)
+                    ptx::tma_load_2d(k_addr(n) + blk * L::kBlkBytes, &tmK, blk * 64, kr, bars.k_full(n % KS));
+                ++nk;
+                if (!(ok = w.wait(bars.v_empty(n % VS), ((n / VS) & 1) ^ 1, kSiteKvEmpty))) break;
+                ptx::mbar_arrive_expect_tx(bars.v_full(n % VS), L::kTileBytes);
+#pragma unroll
+                for (int blk = 0; blk < D / 64; ++blk)
+                    ptx::tma_load_2d(v_addr(n) + blk * L::kBlkBytes, &tmV, blk * 64, kr, bars.v_full(n % VS));
+                ++nv;
             }
-            if (n < steps) {
-                const int first = n > kStages ? n - kStages : 0;
-                for (int r = first; r < n; ++r) w.drain(bars.stage_full(r % kStages), (r / kStages) & 1);
+            if (!ok) {
+                for (int r = nk > KS ? nk - KS : 0; r < nk; ++r) w.drain(bars.k_full(r % KS), (r / KS) & 1);
+                for (int r = nv > VS ? nv - VS : 0; r < nv; ++r) w.drain(bars.v_full(r % VS), (r / VS) & 1);
             }
             w.drain(bars.fixed_full(), 0);
         }
@@ -566,28 +575,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = wait_u(bars.fixed_full(), 0, kSiteQFull);
         const uint64_t qdesc = ptx::desc_sw128(sbase + L::kFixedOff, 16, 1024);
         const uint64_t dodesc = ptx::desc_sw128(sbase + L::kFixedOff + L::kTileBytes, 16, 1024);
-        auto stage_addr = [&](int n) { return sbase + L::kRingOff + (n % kStages) * L::kStageBytes; };
-        // S of key tile n into buffer n % 2, once its stage has landed
+        // S of key tile n into buffer n % 2, once K(n) has landed
         auto issue_s = [&](int n) {
-            qk_kloop<D>(tmem + L::kQColS0 + 128u * (n & 1), qdesc, ptx::desc_sw128(stage_addr(n), 16, 1024), kIdS);
+            qk_kloop<D>(tmem + L::kColS0 + 128u * (n & 1), qdesc, ptx::desc_sw128(k_addr(n), 16, 1024), kIdS);
             ptx::tc_commit_elect(bars.s_full(n & 1));
         };
         int s_issued = 0;   // key tiles whose S has been issued
-        if (steps > 0 && (ok = ok && wait_u(bars.stage_full(0), 0, kSiteKvFull))) {
+        if (steps > 0 && (ok = ok && wait_u(bars.k_full(0), 0, kSiteKvFull))) {
             ptx::tc_fence_after();
             issue_s(0);
             s_issued = 1;
         }
         for (int n = 0; n < steps && ok; ++n) {
-            const uint32_t st = stage_addr(n);
-            // dP (its stage landed before S(n) was issued)
-            qk_kloop<D>(tmem + L::kQColDP, dodesc, ptx::desc_sw128(st + L::kTileBytes, 16, 1024), kIdS);
+            // dP = dO V(n)^T; V(n) is then free
+            if (!(ok = wait_u(bars.v_full(n % VS), (n / VS) & 1, kSiteKvFull))) break;
+            ptx::tc_fence_after();
+            qk_kloop<D>(tmem + L::kColDP, dodesc, ptx::desc_sw128(v_addr(n), 16, 1024), kIdS);
             ptx::tc_commit_elect(bars.dp_full());
-            // S of the next key tile now if its stage is already here, so it
-            // is ready when the elementwise warps finish this tile
+            ptx::tc_commit_elect(bars.v_empty(n % VS));
+            // S of the next key tile now if K(n+1) is here, so it is ready
+            // when the elementwise warps finish this tile
             if (s_issued == n + 1 && n + 1 < steps) {
-                const uint32_t bar = bars.stage_full((n + 1) % kStages);
-                const uint32_t par = ((n + 1) / kStages) & 1;
+                const uint32_t bar = bars.k_full((n + 1) % KS);
+                const uint32_t par = ((n + 1) / KS) & 1;
                 if (__shfl_sync(0xffffffffu, ptx::mbar_test_wait(bar, par) ? 1 : 0, 0)) {
                     ptx::tc_fence_after();
                     issue_s(n + 1);
@@ -595,14 +605,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // dQ += dS K once dS is in TMEM (16-bit over the dP columns; K as
-            // the MN-major B operand)
+            // the MN-major B operand); K(n) is then free
             if (!(ok = wait_u(bars.ds_full(), n & 1, kSitePFull))) break;
             ptx::tc_fence_after();
-            ptx::mma_ts_kloop8_split(tmem + L::kQColAcc, tmem + L::kQColDP, ptx::desc_sw128(st, L::kBlkBytes, 1024), kIdQ,
-                     n > 0 ? 1u : 0u);
-            ptx::tc_commit_elect(bars.stage_empty(n % kStages));
+            ptx::mma_ts_kloop8_split(tmem + L::kColAcc, tmem + L::kColDP, ptx::desc_sw128(k_addr(n), L::kBlkBytes, 1024),
+                                     kIdQ, n > 0 ? 1u : 0u);
+            ptx::tc_commit_elect(bars.k_empty(n % KS));
             if (s_issued == n + 1 && n + 1 < steps) {
-                if (!(ok = wait_u(bars.stage_full((n + 1) % kStages), ((n + 1) / kStages) & 1, kSiteKvFull))) break;
+                if (!(ok = wait_u(bars.k_full((n + 1) % KS), ((n + 1) / KS) & 1, kSiteKvFull))) break;
                 ptx::tc_fence_after();
                 issue_s(n + 1);
                 ++s_issued;
@@ -630,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             const bool diag = p.causal && n == qt;  // key k visible to query q only if k <= q
             // P phase: P = exp2(S c - LSE log2 e), kept in registers
-            const uint32_t colS = L::kQColS0 + 128u * (n & 1);
+            const uint32_t colS = L::kColS0 + 128u * (n & 1);
             float pf[64];
             {
                 uint32_t sv[64];
@@ -653,8 +663,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             {
                 uint32_t dp[64];
-                ptx::tmem_ld32_at<0>(row_addr + L::kQColDP + c0, dp);
-                ptx::tmem_ld32_at<32>(row_addr + L::kQColDP + c0 + 32, dp);
+                ptx::tmem_ld32_at<0>(row_addr + L::kColDP + c0, dp);
+                ptx::tmem_ld32_at<32>(row_addr + L::kColDP + c0 + 32, dp);
                 ptx::tmem_wait_ld();
 #pragma unroll
                 for (int cc = 0; cc < 64; cc += 32) {
@@ -665,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dk[x] = ptx::pack2<kBf16>(pf[j] * (__uint_as_float(dp[j]) - dl),
                                                   pf[j + 1] * (__uint_as_float(dp[j + 1]) - dl));
                     }
-                    ptx::tmem_st16(row_addr + L::kQColDP + c0 + cc / 2, dk);
+                    ptx::tmem_st16(row_addr + L::kColDP + c0 + cc / 2, dk);
                 }
             }
             ptx::tmem_wait_st();
@@ -675,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = w.wait(bars.acc_full(), 0, kSiteOFull);
         if (__all_sync(0xffffffffu, ok)) {
             ptx::tc_fence_after();
-            store_acc_row<D, kBf16>(row_addr, L::kQColAcc, p.scale, p.dq, q_row0 + row, c0 * D / 128,
+            store_acc_row<D, kBf16>(row_addr, L::kColAcc, p.scale, p.dq, q_row0 + row, c0 * D / 128,
                                     (c0 + 64) * D / 128);
         }
     }

@@ -369,13 +369,13 @@ fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, c
     };
     if (d == 128)
         return bf ? run(fa2::bwd::fa2_bwd_delta_kernel<128, true>, fa2::bwd::fa2_bwd_dkdv_kernel<128, true>,
-                        fa2::bwd::fa2_bwd_dq_kernel<128, true>, fa2::bwd::DkdvLayout<128>::kSmemBytes, fa2::bwd::BwdLayout<128>::kSmemBytes, 8)
+                        fa2::bwd::fa2_bwd_dq_kernel<128, true>, fa2::bwd::DkdvLayout<128>::kSmemBytes, fa2::bwd::DqLayout<128>::kSmemBytes, 8)
                   : run(fa2::bwd::fa2_bwd_delta_kernel<128, false>, fa2::bwd::fa2_bwd_dkdv_kernel<128, false>,
-                        fa2::bwd::fa2_bwd_dq_kernel<128, false>, fa2::bwd::DkdvLayout<128>::kSmemBytes, fa2::bwd::BwdLayout<128>::kSmemBytes, 9);
+                        fa2::bwd::fa2_bwd_dq_kernel<128, false>, fa2::bwd::DkdvLayout<128>::kSmemBytes, fa2::bwd::DqLayout<128>::kSmemBytes, 9);
     return bf ? run(fa2::bwd::fa2_bwd_delta_kernel<64, true>, fa2::bwd::fa2_bwd_dkdv_kernel<64, true>,
-                    fa2::bwd::fa2_bwd_dq_kernel<64, true>, fa2::bwd::DkdvLayout<64>::kSmemBytes, fa2::bwd::BwdLayout<64>::kSmemBytes, 10)
+                    fa2::bwd::fa2_bwd_dq_kernel<64, true>, fa2::bwd::DkdvLayout<64>::kSmemBytes, fa2::bwd::DqLayout<64>::kSmemBytes, 10)
               : run(fa2::bwd::fa2_bwd_delta_kernel<64, false>, fa2::bwd::fa2_bwd_dkdv_kernel<64, false>,
-                    fa2::bwd::fa2_bwd_dq_kernel<64, false>, fa2::bwd::DkdvLayout<64>::kSmemBytes, fa2::bwd::BwdLayout<64>::kSmemBytes, 11);
+                    fa2::bwd::fa2_bwd_dq_kernel<64, false>, fa2::bwd::DkdvLayout<64>::kSmemBytes, fa2::bwd::DqLayout<64>::kSmemBytes, 11);
 }
 
 }  // extern "C"
