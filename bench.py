@@ -328,6 +328,21 @@ class OracleSample:
             oracle_forward(w, self.inputs, self.rows, self.causal)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (from /proc/cpuinfo; Arm hosts may list none)."""
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                key, _, val = line.partition(":")
+                if key.strip().lower() in ("model name", "cpu model", "hardware"):
+                    return val.strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.processor() or platform.machine()
+
+
 def time_oracle(w, which: str, inputs, seconds: float):
     sample = OracleSample(w, which, seconds, inputs)
     t0 = time.perf_counter()
@@ -342,8 +357,7 @@ def run_reference(args, dist, w):
     """fp64 CPU oracle as the reference arm: each step a bounded sample."""
     if dist.rank != 0:
         return None
-    total_budget = 120.0
-    per_step = total_budget / max(1, args.steps + args.warmup)
+    per_step = args.ref_seconds / max(1, args.steps + args.warmup)
     sample = OracleSample(w, args.pass_, per_step, w.inputs())
     for _ in range(args.warmup):
         sample.run()
@@ -360,7 +374,7 @@ def run_reference(args, dist, w):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w, args.gpus, args.pass_),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": sample.cores, "kind": "oracle",
-                         "sample": sample.desc},
+                         "sample": sample.desc, "cpu": cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -630,7 +644,7 @@ def run_ours(args, dist, w):
         if dist.world == 1 and not args.no_cpu_baseline:
             cv, cores, desc, dt = time_oracle(w, args.pass_, inputs, args.cpu_seconds)
             result["cpu_baseline"] = {"value": cv, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                      "sample": f"{desc}, {dt:.1f} s"}
+                                      "sample": f"{desc}, {dt:.1f} s", "cpu": cpu_model()}
     return result
 
 
@@ -644,6 +658,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="oracle time budget of a whole --impl reference run (warm-up + timed steps)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

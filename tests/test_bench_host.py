@@ -1,0 +1,62 @@
+"""bench.py's host side on the CPU: the reference arm (the fp64 oracle timed
+on a bounded sample) for every pass and for an FP8 workload, the JSON line's
+keys, and the FLOP and byte counts of each pass."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+import bench
+import gen
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def run_reference(*args):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "3", "--ref-seconds", "4", *args],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    return json.loads(lines[0])
+
+
+@pytest.mark.parametrize("pass_", ["fwd", "fwd_causal", "bwd", "bwd_causal"])
+def test_reference_arm_every_pass(pass_):
+    d = run_reference("--workload", "tiny_B1_H1_N128_d128_bf16", "--pass", pass_)
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
+    assert d["config"]["pass"] == pass_ and d["config"]["causal"] == pass_.endswith("causal")
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["cpu"]
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_fp8_workload():
+    d = run_reference("--workload", "fp8_mha_B4_H16_N4096_d128_e4m3")
+    assert d["value"] > 0 and d["config"]["dtype"].startswith("e4m3")
+    assert "FP8" in d["metric"]
+
+
+def test_pass_flop_and_byte_counts():
+    w = gen.workload("mha_B4_H16_N4096_d128_bf16")
+    assert bench.pass_flops(w, "fwd") == 4.0 * 4 * 16 * 4096 * 4096 * 128
+    assert bench.pass_flops(w, "fwd_causal") == 4.0 * 4 * 16 * (4096 * 4097 // 2) * 128
+    assert bench.pass_flops(w, "bwd") == 2.5 * bench.pass_flops(w, "fwd")
+    assert bench.pass_flops(w, "bwd_causal") == 2.5 * bench.pass_flops(w, "fwd_causal")
+    assert bench.pass_bytes(w, "fwd") == w.alg_bytes == 269484032
+    q = 4 * 16 * 4096 * 128 * 2
+    # reads q, k, v, o, dO (5 tensors) + lse; writes dq, dk, dv; delta written and read
+    assert bench.pass_bytes(w, "bwd") == 8 * q + 4 * 4 * 16 * 4096 + 8 * 4 * 16 * 4096
+    f = gen.workload("fp8_mha_B4_H16_N4096_d128_e4m3")
+    # Q, K, V one byte each, O bf16, LSE fp32, 3 descales per KV head
+    assert f.alg_bytes == 3 * q // 2 + q + 4 * 4 * 16 * 4096 + 12 * 4 * 16
+
+
+def test_fp8_peak_is_twice_the_bf16_peak():
+    bf, _ = bench.load_peak(False)
+    f8, src = bench.load_peak(True)
+    assert f8 == 2 * bf and "x 2" in src
