@@ -48,6 +48,8 @@ CASES = [
     (1, 4, 2, 256, 128, gen.BF16, False),   # grouped heads: dK, dV summed over 2 query heads
     (1, 4, 1, 384, 64, gen.BF16, True),
     (1, 2, 2, 512, 128, gen.FP16, True),
+    (1, 2, 2, 2048, 128, gen.BF16, False),  # 16 steps: every ring wraps several times
+    (1, 4, 2, 2048, 128, gen.BF16, True),   # grouped heads, causal, up to 32 dK/dV steps
 ]
 
 
@@ -91,3 +93,24 @@ def test_backward_key_gradient_sums_to_zero(gpu_lib):
     dq, dk, dv = gpu_lib.fa2_bwd(tq, tk, tv, o, lse, tdo)
     s = dk.double().sum(dim=2)
     assert float(s.abs().max()) <= 2.0 ** -6 * float(dk.double().abs().sum(dim=2).max())
+
+
+def test_backward_full_size_bench_workload_slices(gpu_lib):
+    """The backward bench workload (B4 H16 N4096 d128 bf16, dO from the
+    workload's generator), in the bench's launch configuration; two (batch,
+    head) slices are checked against the oracle run on that slice alone (with
+    equal head counts a head's gradients depend on its own Q, K, V, dO only)."""
+    import torch
+
+    w = gen.workload("mha_B4_H16_N4096_d128_bf16")
+    q, k, v = w.inputs()
+    do = w.grad_output()
+    tq, tk, tv, tdo = (to_dev(x, w.dtype) for x in (q, k, v, do))
+    o, lse = gpu_lib.fa2_fwd_gqa(tq, tk, tv, scale=w.scale)
+    dq, dk, dv = gpu_lib.fa2_bwd(tq, tk, tv, o, lse, tdo, scale=w.scale)
+    assert gpu_lib.fa2_check_status(torch.cuda.current_stream().cuda_stream) == gpu_lib.FA2_OK
+    for b, h in ((0, 0), (3, 15)):
+        sl = lambda x: np.ascontiguousarray(x[b:b + 1, h:h + 1])
+        rq, rk, rv = oracle.attention_bwd(sl(q), sl(k), sl(v), sl(do), w.scale, w.dtype)
+        for name, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+            check(f"{name}[{b},{h}]", g[b:b + 1, h:h + 1].float().cpu().numpy(), r, w.dtype)
