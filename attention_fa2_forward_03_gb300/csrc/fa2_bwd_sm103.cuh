@@ -54,7 +54,8 @@ struct Params {
     void* dk;             // [B*Hkv*N, D]
     void* dv;             // [B*Hkv*N, D]
     long long wait_limit_ns;
-    int n_tiles;          // N / 128
+    int n;                // N: rows per head (any positive length)
+    int n_tiles;          // ceil(N / 128)
     int hq, group;        // Hq, Hq / Hkv
     int causal;
     float scale;          // softmax scale
@@ -110,10 +111,12 @@ __device__ __forceinline__ void store_row_16(void* base, long long row, int d, i
 }
 
 // Write columns [c0, c1) of a d-column fp32 TMEM accumulator row (times
-// `mul`) as 16-bit.
+// `mul`) as 16-bit; `store` false skips the global stores (a row past a
+// ragged end). The whole warp must call this together: the TMEM loads are
+// warp-collective (.sync.aligned) and may not sit in a divergent branch.
 template <int D, bool kBf16>
 __device__ __forceinline__ void store_acc_row(uint32_t row_addr, uint32_t col, float mul, void* out,
-                                              long long grow, int c0 = 0, int c1 = D) {
+                                              long long grow, int c0, int c1, bool store) {
 #pragma unroll 1
     for (int cc = c0; cc < c1; cc += 32) {
         uint32_t a[32];
@@ -123,7 +126,7 @@ __device__ __forceinline__ void store_acc_row(uint32_t row_addr, uint32_t col, f
 #pragma unroll
         for (int i = 0; i < 16; ++i)
             h[i] = ptx::pack2<kBf16>(__uint_as_float(a[2 * i]) * mul, __uint_as_float(a[2 * i + 1]) * mul);
-        store_row_16(out, grow, D, cc, h);
+        if (store) store_row_16(out, grow, D, cc, h);
     }
 }
 
@@ -189,7 +192,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hk = kvh - b * (p.hq / p.group);
     const int first = p.causal ? kt : 0;       // first query tile that sees this key tile
     const int steps = p.group * (p.n_tiles - first);
-    const long long kv_row0 = static_cast<long long>(kvh) * p.n_tiles * 128 + kt * 128;
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(bars.fixed_full(), 1);
@@ -218,11 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Waiter w{abort_flag, p.wait_limit_ns};
-    // First row of step n's query tile: query heads of the group in turn,
-    // tiles first .. n_tiles - 1 of each.
-    auto q_row = [&](int g, int i) {
-        return (static_cast<long long>(b) * p.hq + hk * p.group + g) * p.n_tiles * 128 + i * 128;
-    };
+    // Query head of step n's tile: the group's query heads in turn, tiles
+    // first .. n_tiles - 1 of each. Tensor maps are [heads, N, d]: a tile never
+    // crosses heads and rows past N read as zero.
+    auto q_head = [&](int g) { return b * p.hq + hk * p.group + g; };
     auto q_addr = [&](int n) { return sbase + L::kQOff + (n % QS) * L::kTileBytes; };
     auto do_addr = [&](int n) { return sbase + L::kDoOff + (n % DS) * L::kTileBytes; };
 
@@ -231,27 +232,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive_expect_tx(bars.fixed_full(), 2 * L::kTileBytes);
 #pragma unroll
             for (int blk = 0; blk < D / 64; ++blk) {
-                ptx::tma_load_2d(sbase + L::kFixedOff + blk * L::kBlkBytes, &tmK, blk * 64,
-                                 static_cast<int>(kv_row0), bars.fixed_full());
-                ptx::tma_load_2d(sbase + L::kFixedOff + L::kTileBytes + blk * L::kBlkBytes, &tmV, blk * 64,
-                                 static_cast<int>(kv_row0), bars.fixed_full());
+                ptx::tma_load_3d(sbase + L::kFixedOff + blk * L::kBlkBytes, &tmK, blk * 64, kt * 128, kvh,
+                                 bars.fixed_full());
+                ptx::tma_load_3d(sbase + L::kFixedOff + L::kTileBytes + blk * L::kBlkBytes, &tmV, blk * 64, kt * 128,
+                                 kvh, bars.fixed_full());
             }
             int nq = 0, nd = 0;   // Q and dO tiles issued
             int g = 0, i = first;
             bool ok = true;
             for (int n = 0; n < steps && ok; ++n) {
-                const int qr = static_cast<int>(q_row(g, i));
+                const int qh = q_head(g);
                 if (!(ok = w.wait(bars.q_empty(n % QS), ((n / QS) & 1) ^ 1, kSiteKvEmpty))) break;
                 ptx::mbar_arrive_expect_tx(bars.q_full(n % QS), L::kTileBytes);
 #pragma unroll
                 for (int blk = 0; blk < D / 64; ++blk)
-                    ptx::tma_load_2d(q_addr(n) + blk * L::kBlkBytes, &tmQ, blk * 64, qr, bars.q_full(n % QS));
+                    ptx::tma_load_3d(q_addr(n) + blk * L::kBlkBytes, &tmQ, blk * 64, i * 128, qh, bars.q_full(n % QS));
                 ++nq;
                 if (!(ok = w.wait(bars.do_empty(n % DS), ((n / DS) & 1) ^ 1, kSiteKvEmpty))) break;
                 ptx::mbar_arrive_expect_tx(bars.do_full(n % DS), L::kTileBytes);
 #pragma unroll
                 for (int blk = 0; blk < D / 64; ++blk)
-                    ptx::tma_load_2d(do_addr(n) + blk * L::kBlkBytes, &tmDO, blk * 64, qr, bars.do_full(n % DS));
+                    ptx::tma_load_3d(do_addr(n) + blk * L::kBlkBytes, &tmDO, blk * 64, i * 128, qh,
+                                     bars.do_full(n % DS));
                 ++nd;
                 if (++i == p.n_tiles) {
                     i = first;
@@ -337,15 +339,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr float kLog2e = 1.4426950408889634f;
         // This warp's 64 query columns of a step: lane x holds -LSE log2 e
         // and D of columns c0 + x and c0 + 32 + x (from global memory, one
-        // step ahead); the loops take them by shuffle.
+        // step ahead); the loops take them by shuffle. A query past N (a
+        // ragged last tile) gets -LSE = -inf and D = 0: its P^T and dS^T
+        // columns are exactly 0.
         int g = 0, qi = first;
         float nl_nx[2] = {0.0f, 0.0f}, d_nx[2] = {0.0f, 0.0f};
         auto fetch = [&](int gg, int ii) {
-            const long long qr = q_row(gg, ii);
-            nl_nx[0] = -__ldg(p.lse + qr + c0 + lane) * kLog2e;
-            nl_nx[1] = -__ldg(p.lse + qr + c0 + 32 + lane) * kLog2e;
-            d_nx[0] = __ldg(p.delta + qr + c0 + lane);
-            d_nx[1] = __ldg(p.delta + qr + c0 + 32 + lane);
+            const long long base = static_cast<long long>(q_head(gg)) * p.n;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int q = ii * 128 + c0 + 32 * h + lane;
+                nl_nx[h] = q < p.n ? -__ldg(p.lse + base + q) * kLog2e : -INFINITY;
+                d_nx[h] = q < p.n ? __ldg(p.delta + base + q) : 0.0f;
+            }
         };
         if (steps > 0) fetch(g, qi);
         bool ok = true;
@@ -424,11 +430,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = w.wait(bars.acc_full(), 0, kSiteOFull);
         if (__all_sync(0xffffffffu, ok)) {
             ptx::tc_fence_after();
-            const long long grow = kv_row0 + row;
-            if (c0 == 0)
-                store_acc_row<D, kBf16>(row_addr, L::kColAcc0, 1.0f, p.dv, grow);
+            // key rows past N (a ragged last tile) are not stored
+            const long long grow = static_cast<long long>(kvh) * p.n + kt * 128 + row;
+            const bool valid = kt * 128 + row < p.n;
+            if (c0 == 0)   // warp-uniform: warps 0-3 write dV, warps 4-7 dK
+                store_acc_row<D, kBf16>(row_addr, L::kColAcc0, 1.0f, p.dv, grow, 0, D, valid);
             else
-                store_acc_row<D, kBf16>(row_addr, L::kColAcc1, p.scale, p.dk, grow);
+                store_acc_row<D, kBf16>(row_addr, L::kColAcc1, p.scale, p.dk, grow, 0, D, valid);
         }
     }
 
@@ -497,8 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qh = blockIdx.y;                 // b * Hq + query head
     const int b = qh / p.hq;
     const int hkv = (qh - b * p.hq) / p.group;
-    const long long q_row0 = static_cast<long long>(qh) * p.n_tiles * 128 + qt * 128;
-    const long long kv_base = (static_cast<long long>(b) * (p.hq / p.group) + hkv) * p.n_tiles * 128;
+    const int kvh = b * (p.hq / p.group) + hkv;
     const int steps = p.causal ? qt + 1 : p.n_tiles;
 
     if (threadIdx.x == 0) {
@@ -536,26 +543,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive_expect_tx(bars.fixed_full(), 2 * L::kTileBytes);
 #pragma unroll
             for (int blk = 0; blk < D / 64; ++blk) {
-                ptx::tma_load_2d(sbase + L::kFixedOff + blk * L::kBlkBytes, &tmQ, blk * 64,
-                                 static_cast<int>(q_row0), bars.fixed_full());
-                ptx::tma_load_2d(sbase + L::kFixedOff + L::kTileBytes + blk * L::kBlkBytes, &tmDO, blk * 64,
-                                 static_cast<int>(q_row0), bars.fixed_full());
+                ptx::tma_load_3d(sbase + L::kFixedOff + blk * L::kBlkBytes, &tmQ, blk * 64, qt * 128, qh,
+                                 bars.fixed_full());
+                ptx::tma_load_3d(sbase + L::kFixedOff + L::kTileBytes + blk * L::kBlkBytes, &tmDO, blk * 64, qt * 128,
+                                 qh, bars.fixed_full());
             }
             int nk = 0, nv = 0;
             bool ok = true;
             for (int n = 0; n < steps && ok; ++n) {
-                const int kr = static_cast<int>(kv_base + n * 128);
                 if (!(ok = w.wait(bars.k_empty(n % KS), ((n / KS) & 1) ^ 1, kSiteKvEmpty))) break;
                 ptx::mbar_arrive_expect_tx(bars.k_full(n % KS), L::kTileBytes);
 #pragma unroll
                 for (int blk = 0; blk < D / 64; ++blk)
-                    ptx::tma_load_2d(k_addr(n) + blk * L::kBlkBytes, &tmK, blk * 64, kr, bars.k_full(n % KS));
+                    ptx::tma_load_3d(k_addr(n) + blk * L::kBlkBytes, &tmK, blk * 64, n * 128, kvh, bars.k_full(n % KS));
                 ++nk;
                 if (!(ok = w.wait(bars.v_empty(n % VS), ((n / VS) & 1) ^ 1, kSiteKvEmpty))) break;
                 ptx::mbar_arrive_expect_tx(bars.v_full(n % VS), L::kTileBytes);
 #pragma unroll
                 for (int blk = 0; blk < D / 64; ++blk)
-                    ptx::tma_load_2d(v_addr(n) + blk * L::kBlkBytes, &tmV, blk * 64, kr, bars.v_full(n % VS));
+                    ptx::tma_load_3d(v_addr(n) + blk * L::kBlkBytes, &tmV, blk * 64, n * 128, kvh, bars.v_full(n % VS));
                 ++nv;
             }
             if (!ok) {
@@ -628,8 +634,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c0 = 64 * (warp >> 2);
         const uint32_t row_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
         const float c = p.scale_log2;
-        const float lse2 = p.lse[q_row0 + row] * 1.4426950408889634f;
-        const float dl = p.delta[q_row0 + row];
+        // A query row past N (a ragged last tile) gets LSE = +inf and D = 0:
+        // its P and dS are exactly 0 and it is not stored.
+        const bool row_valid = qt * 128 + row < p.n;
+        const long long grow = static_cast<long long>(qh) * p.n + qt * 128 + row;
+        const float lse2 = row_valid ? p.lse[grow] * 1.4426950408889634f : INFINITY;
+        const float dl = row_valid ? p.delta[grow] : 0.0f;
+        const int key_end = p.n - (p.n_tiles - 1) * 128;   // keys of the last key tile (1..128)
         bool ok = true;
         for (int n = 0; n < steps; ++n) {
             ok = w.wait(bars.s_full(n & 1), (n >> 1) & 1, kSiteSFull);
@@ -653,6 +664,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (diag) {
 #pragma unroll
                 for (int j = 0; j < 64; ++j) pf[j] = c0 + j > row ? 0.0f : pf[j];
+            }
+            if (n == p.n_tiles - 1 && key_end < 128) {   // keys past N (zero-filled K) get no weight
+#pragma unroll
+                for (int j = 0; j < 64; ++j) pf[j] = c0 + j >= key_end ? 0.0f : pf[j];
             }
             // dS phase: dS = P o (dP - D) -> 16-bit over dP
             ok = w.wait(bars.dp_full(), n & 1, kSiteSFull);
@@ -685,8 +700,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = w.wait(bars.acc_full(), 0, kSiteOFull);
         if (__all_sync(0xffffffffu, ok)) {
             ptx::tc_fence_after();
-            store_acc_row<D, kBf16>(row_addr, L::kColAcc, p.scale, p.dq, q_row0 + row, c0 * D / 128,
-                                    (c0 + 64) * D / 128);
+            store_acc_row<D, kBf16>(row_addr, L::kColAcc, p.scale, p.dq, grow, c0 * D / 128, (c0 + 64) * D / 128,
+                                    row_valid);
         }
     }
 

@@ -320,7 +320,6 @@ fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, c
     if (dtype != FA2_BF16 && dtype != FA2_FP16) return FA2_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA2_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return FA2_ERR_UNSUPPORTED;
-    if (N % fa2::kBM != 0) return FA2_ERR_UNSUPPORTED;
     const long long rows_q = static_cast<long long>(B) * H_q * N;
     if (rows_q > 0x7FFFFFFFLL || static_cast<long long>(B) * H_q > 65535) return FA2_ERR_UNSUPPORTED;
 
@@ -328,10 +327,12 @@ fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, c
     fa2_status st = check_device(&dev);
     if (st != FA2_OK) return st;
     if ((st = get_encoder()) != FA2_OK) return st;
+    // [heads, N, d] views: tiles never cross heads; rows past a ragged N read as 0
     CUtensorMap mq, mk, mv, mdo;
-    const uint64_t rows_kv = static_cast<uint64_t>(B) * H_kv * N;
-    if (encode_map(&mq, q, static_cast<uint64_t>(rows_q), d) != FA2_OK || encode_map(&mk, k, rows_kv, d) != FA2_OK ||
-        encode_map(&mv, v, rows_kv, d) != FA2_OK || encode_map(&mdo, dout, static_cast<uint64_t>(rows_q), d) != FA2_OK)
+    const uint64_t hq = static_cast<uint64_t>(B) * H_q, hkv = static_cast<uint64_t>(B) * H_kv;
+    const uint64_t n = static_cast<uint64_t>(N);
+    if (encode_map_3d(&mq, q, hq, n, d) != FA2_OK || encode_map_3d(&mk, k, hkv, n, d) != FA2_OK ||
+        encode_map_3d(&mv, v, hkv, n, d) != FA2_OK || encode_map_3d(&mdo, dout, hq, n, d) != FA2_OK)
         return FA2_ERR_CUDA;
 
     fa2::bwd::Params p{};
@@ -343,7 +344,8 @@ fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, c
     p.dk = dk;
     p.dv = dv;
     p.wait_limit_ns = g_wait_limit_ns.load();
-    p.n_tiles = N / fa2::kBM;
+    p.n = N;
+    p.n_tiles = (N + fa2::kBM - 1) / fa2::kBM;
     p.hq = H_q;
     p.group = H_q / H_kv;
     p.causal = causal;

@@ -140,8 +140,8 @@ fa2_status fa2_fwd_fp8(const void* q, const void* k, const void* v, const float*
                        int B, int H_q, int H_kv, int N, int d, float scale, cudaStream_t stream);
 
 /*
- * Attention backward (gradients of fa2_fwd / fa2_fwd_gqa with optional
- * causal mask, equal lengths N, N % 128 == 0). The forward pages exclude the
+ * Attention backward (gradients of the forward with optional causal mask and
+ * equal query/key lengths N; any N >= 1, like fa2_fwd_ex). The forward pages exclude the
  * backward pass ("FlashAttention-2 from scratch on Ampere, Part 1", Kernel
  * Specification: forward pass only); it is built here as an extension and
  * recomputes P = exp(scale*S - LSE) from the forward's logsumexp:
@@ -156,7 +156,8 @@ fa2_status fa2_fwd_fp8(const void* q, const void* k, const void* v, const float*
  *   causal         : 0 or 1 (same mask as the forward with N_q == N_k)
  * All pointers device memory, 16-byte aligned. Launches three kernels on
  * `stream` (D, then dK/dV, then dQ); allocates nothing. Errors as
- * fa2_fwd_gqa; B*H_q > 65535 is FA2_ERR_UNSUPPORTED.
+ * fa2_fwd_gqa except that N need not be a multiple of 128; B*H_q > 65535
+ * is FA2_ERR_UNSUPPORTED.
  */
 fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                    const void* dout, void* dq, void* dk, void* dv, float* delta,

@@ -95,7 +95,6 @@ def test_backward_host_validation(lib):
     assert f(*(ok[:9] + [A + 4]), 1, 1, 1, 128, 128, 0.1, 0, 0) == fa2.FA2_ERR_INVALID_ARG  # delta align
     assert f(*ok, 1, 1, 1, 128, 128, 0.1, 3, 0) == fa2.FA2_ERR_INVALID_ARG          # causal
     assert f(*ok, 1, 3, 2, 128, 128, 0.1, 0, 0) == fa2.FA2_ERR_INVALID_ARG          # Hq % Hkv
-    assert f(*ok, 1, 1, 1, 100, 128, 0.1, 0, 0) == fa2.FA2_ERR_UNSUPPORTED          # N % 128
     assert f(*ok, 1, 1, 1, 128, 80, 0.1, 0, 0) == fa2.FA2_ERR_UNSUPPORTED           # d
     assert f(*ok, 1, 70000, 1, 128, 64, 0.1, 0, 0) == fa2.FA2_ERR_UNSUPPORTED       # B*Hq > 65535
 
