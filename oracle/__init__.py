@@ -68,8 +68,9 @@ def _load():
         lib.oracle_decode_e4m3.restype = None
         lib.oracle_round_e4m3.argtypes = [p, i64, p]
         lib.oracle_round_e4m3.restype = None
-        lib.oracle_attention_fp8_rows.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64,
-                                                  ctypes.c_double, i64, p, i64, p, p, p, p, p, ctypes.c_int]
+        lib.oracle_attention_fp8_rows.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64, i64,
+                                                  ctypes.c_double, ctypes.c_int, i64, p, i64, p, p, p, p, p,
+                                                  ctypes.c_int]
         lib.oracle_attention_fp8_rows.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -209,22 +210,24 @@ def round_e4m3(x) -> np.ndarray:
 
 
 def attention_fp8_both(q, k, v, q_descale, k_descale, v_descale, scale: float, rows=None,
-                       threads: int = 0, bc: int = 128):
+                       threads: int = 0, bc: int = 128, causal: bool = False):
     """Attention forward on e4m3 inputs with per-(batch, KV head) descales,
     in one pass: returns (o_method, o_plain, lse, a, b).
 
-    q: uint8 [B, Hq, N, d]; k, v: uint8 [B, Hkv, N, d]; descales: [B*Hkv].
-    o_method follows the FP8 method: the online softmax over key tiles of bc
-    keys, with each tile's weights scaled by 2^8 and rounded to e4m3 (against
-    the tile's running max) before the P.V product; o_plain is the plain
-    definition on the dequantised inputs. o_*, a, b: [B, Hq, N, d] (or [len(rows), d]); lse:
+    q: uint8 [B, Hq, Nq, d]; k, v: uint8 [B, Hkv, Nk, d]; descales: [B*Hkv].
+    causal: query row i sees keys j < min(Nk, i + 1 + Nk - Nq) (rows that
+    see none: o = 0, lse = -inf). o_method follows the FP8 method: the
+    online softmax over key tiles of bc keys (from key 0), with each tile's
+    weights scaled by 2^8 and rounded to e4m3 (against the tile's running
+    max) before the P.V product; o_plain is the plain definition on the
+    dequantised inputs. o_*, a, b: [B, Hq, Nq, d] (or [len(rows), d]); lse:
     [B, Hq, N] (or [len(rows)]); a = sum_j p_j |v_j| / l and
     b = sum_j |v_j| / l elementwise.
     """
     q, k, v = (np.ascontiguousarray(x, dtype=np.uint8) for x in (q, k, v))
     B, Hq, N, d = q.shape
-    Hkv = k.shape[1]
-    if k.shape != (B, Hkv, N, d) or v.shape != k.shape:
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if k.shape != (B, Hkv, Nk, d) or v.shape != k.shape:
         raise ValueError("shape mismatch between q, k and v")
     qd, kd, vd = (np.ascontiguousarray(x, dtype=np.float64).reshape(-1) for x in
                   (q_descale, k_descale, v_descale))
@@ -238,9 +241,9 @@ def attention_fp8_both(q, k, v, q_descale, k_descale, v_descale, scale: float, r
     om, op, a, b = (np.empty((nrows, d), dtype=np.float64) for _ in range(4))
     lse = np.empty(nrows, dtype=np.float64)
     rc = _load().oracle_attention_fp8_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, qd.ctypes.data,
-                                           kd.ctypes.data, vd.ctypes.data, B, Hq, Hkv, N, d, float(scale),
-                                           int(bc), rptr, nrows, om.ctypes.data, op.ctypes.data, lse.ctypes.data,
-                                           a.ctypes.data, b.ctypes.data, int(threads))
+                                           kd.ctypes.data, vd.ctypes.data, B, Hq, Hkv, N, Nk, d, float(scale),
+                                           int(bool(causal)), int(bc), rptr, nrows, om.ctypes.data, op.ctypes.data,
+                                           lse.ctypes.data, a.ctypes.data, b.ctypes.data, int(threads))
     if rc != 0:
         raise ValueError("oracle rejected the sizes")
     if rows is None:
@@ -250,10 +253,11 @@ def attention_fp8_both(q, k, v, q_descale, k_descale, v_descale, scale: float, r
 
 
 def attention_fp8(q, k, v, q_descale, k_descale, v_descale, scale: float, round_p: bool = True,
-                  rows=None, threads: int = 0, bc: int = 128):
+                  rows=None, threads: int = 0, bc: int = 128, causal: bool = False):
     """(o, lse, a, b) of :func:`attention_fp8_both`, with o the method's
     output (round_p=True) or the plain definition's (round_p=False)."""
-    om, op, lse, a, b = attention_fp8_both(q, k, v, q_descale, k_descale, v_descale, scale, rows, threads, bc)
+    om, op, lse, a, b = attention_fp8_both(q, k, v, q_descale, k_descale, v_descale, scale, rows, threads, bc,
+                                           causal)
     return (om if round_p else op), lse, a, b
 
 

@@ -468,18 +468,21 @@ void oracle_round_e4m3(const double* x, int64_t n, double* out) {
 }
 
 /*
- * q: [B, Hq, N, d] e4m3 codes; k, v: [B, Hkv, N, d] codes; qd, kd, vd:
- * [B*Hkv] descales. bc: key tile of the method (>= 1). rows: flat query rows
- * (b*Hq + h)*N + i or NULL for all. o_method, o_plain, a_out, b_out:
+ * q: [B, Hq, Nq, d] e4m3 codes; k, v: [B, Hkv, Nk, d] codes; qd, kd, vd:
+ * [B*Hkv] descales. causal: query row i sees keys j < kend(i) =
+ * min(Nk, i + 1 + Nk - Nq) (the mask of oracle_attention_ex_rows), else all
+ * Nk keys; a row that sees no key gets o = 0, lse = -inf. bc: key tile of the
+ * method (>= 1), tiles start at key 0. rows: flat query rows
+ * (b*Hq + h)*Nq + i or NULL for all. o_method, o_plain, a_out, b_out:
  * [nrows, d], each may be NULL; lse: [nrows] (the plain definition's).
  */
 int oracle_attention_fp8_rows(const uint8_t* q, const uint8_t* k, const uint8_t* v, const double* qd,
                               const double* kd, const double* vd, int64_t B, int64_t Hq, int64_t Hkv,
-                              int64_t N, int64_t d, double scale, int64_t bc, const int64_t* rows,
-                              int64_t nrows, double* o_method, double* o_plain, double* lse_out,
-                              double* a_out, double* b_out, int nthreads) {
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || Hq % Hkv || bc <= 0) return -1;
-    if (!rows && nrows != B * Hq * N) return -1;
+                              int64_t Nq, int64_t Nk, int64_t d, double scale, int causal, int64_t bc,
+                              const int64_t* rows, int64_t nrows, double* o_method, double* o_plain,
+                              double* lse_out, double* a_out, double* b_out, int nthreads) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || Hq % Hkv || bc <= 0) return -1;
+    if (!rows && nrows != B * Hq * Nq) return -1;
     const int64_t G = Hq / Hkv;
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
@@ -493,7 +496,7 @@ int oracle_attention_fp8_rows(const uint8_t* q, const uint8_t* k, const uint8_t*
 #pragma omp parallel
     {
         double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
-        double* s = (double*)malloc(sizeof(double) * (size_t)N);
+        double* s = (double*)malloc(sizeof(double) * (size_t)Nk);
         double* acc = (double*)malloc(sizeof(double) * (size_t)d);
         double* accp = (double*)malloc(sizeof(double) * (size_t)d);
         double* aa = (double*)malloc(sizeof(double) * (size_t)d);
@@ -501,18 +504,30 @@ int oracle_attention_fp8_rows(const uint8_t* q, const uint8_t* k, const uint8_t*
 #pragma omp for schedule(dynamic, 4)
         for (int64_t r = 0; r < nrows; ++r) {
             const int64_t flat = rows ? rows[r] : r;
-            const int64_t i = flat % N;
-            const int64_t h = (flat / N) % Hq;
-            const int64_t b = flat / (N * Hq);
+            const int64_t i = flat % Nq;
+            const int64_t h = (flat / Nq) % Hq;
+            const int64_t b = flat / (Nq * Hq);
             const int64_t g = b * Hkv + h / G;      /* the (batch, KV head) group */
-            const uint8_t* qp = q + ((b * Hq + h) * N + i) * d;
-            const uint8_t* kp = k + g * N * d;
-            const uint8_t* vp = v + g * N * d;
+            const uint8_t* qp = q + ((b * Hq + h) * Nq + i) * d;
+            const uint8_t* kp = k + g * Nk * d;
+            const uint8_t* vp = v + g * Nk * d;
+            int64_t kend = Nk;                      /* keys j < kend are allowed */
+            if (causal && i + 1 + Nk - Nq < kend) kend = i + 1 + Nk - Nq;
+            if (kend <= 0) {                        /* no allowed key */
+                for (int64_t t = 0; t < d; ++t) {
+                    if (o_method) o_method[r * d + t] = 0.0;
+                    if (o_plain) o_plain[r * d + t] = 0.0;
+                    if (a_out) a_out[r * d + t] = 0.0;
+                    if (b_out) b_out[r * d + t] = 0.0;
+                }
+                lse_out[r] = -INFINITY;
+                continue;
+            }
 
             /* dequantised inputs: code * descale */
             for (int64_t t = 0; t < d; ++t) qrow[t] = tab[qp[t]] * qd[g];
             double m = -INFINITY;
-            for (int64_t j = 0; j < N; ++j) {
+            for (int64_t j = 0; j < kend; ++j) {
                 double dot = 0.0;
                 for (int64_t t = 0; t < d; ++t) dot += qrow[t] * (tab[kp[j * d + t]] * kd[g]);
                 s[j] = scale * dot;
@@ -521,7 +536,7 @@ int oracle_attention_fp8_rows(const uint8_t* q, const uint8_t* k, const uint8_t*
             /* plain definition and the two bounding sums */
             double l = 0.0;
             for (int64_t t = 0; t < d; ++t) accp[t] = aa[t] = bb[t] = 0.0;
-            for (int64_t j = 0; j < N; ++j) {
+            for (int64_t j = 0; j < kend; ++j) {
                 const double pj = exp(s[j] - m);
                 l += pj;
                 for (int64_t t = 0; t < d; ++t) {
@@ -534,8 +549,8 @@ int oracle_attention_fp8_rows(const uint8_t* q, const uint8_t* k, const uint8_t*
             /* the method: online softmax over key tiles, P rounded per tile */
             double mt = -INFINITY, lt = 0.0;
             for (int64_t t = 0; t < d; ++t) acc[t] = 0.0;
-            for (int64_t j0 = 0; j0 < N; j0 += bc) {
-                const int64_t j1 = j0 + bc < N ? j0 + bc : N;
+            for (int64_t j0 = 0; j0 < kend; j0 += bc) {
+                const int64_t j1 = j0 + bc < kend ? j0 + bc : kend;
                 double mnew = mt;
                 for (int64_t j = j0; j < j1; ++j)
                     if (s[j] > mnew) mnew = s[j];

@@ -600,3 +600,76 @@ def test_fp8_tiled_method_stays_within_the_rounding_bound():
     for bc in (1, 64, 128, 700):
         om, op, lp, a, b = oracle.attention_fp8_both(q, k, v, qd, kd, vd, 0.2, bc=bc)
         assert np.all(np.abs(om - op) <= 2.0 ** -4 * a + 2.0 ** -18 * b + 1e-15)
+
+
+def _fp8_general_inputs(seed, B, Hq, Hkv, nq, nk, d, amp=1.0):
+    q, _, _, qd, _, _ = gen.make_qkv_fp8(seed, B, Hq, Hkv, nq, d, amp)
+    _, k, v, _, kd, vd = gen.make_qkv_fp8(seed + 1, B, Hq, Hkv, nk, d, amp)
+    return q, k, v, qd, kd, vd
+
+
+@pytest.mark.parametrize("nq,nk,causal", [(70, 70, True), (50, 90, True), (90, 50, True), (33, 100, False),
+                                          (100, 33, False)])
+def test_fp8_general_plain_mode_library_crosscheck(nq, nk, causal):
+    # Plain mode with unequal lengths and the bottom-right causal mask is
+    # masked softmax attention on the dequantised inputs; rows that see no key
+    # (causal, nq > nk) give o = 0 and lse = -inf.
+    torch = pytest.importorskip("torch")
+    B, Hq, Hkv, d = 2, 4, 2, 32
+    q, k, v, qd, kd, vd = _fp8_general_inputs(51, B, Hq, Hkv, nq, nk, d)
+    o, lse, _, _ = oracle.attention_fp8(q, k, v, qd, kd, vd, 0.25, round_p=False, causal=causal)
+    G = Hq // Hkv
+    qx = torch.from_numpy(_dequant(q, qd, G))
+    kx = torch.from_numpy(np.repeat(_dequant(k, kd, 1), G, axis=1))
+    vx = torch.from_numpy(np.repeat(_dequant(v, vd, 1), G, axis=1))
+    s = 0.25 * qx @ kx.transpose(-1, -2)
+    if causal:
+        i = torch.arange(nq)[:, None]
+        j = torch.arange(nk)[None, :]
+        s = s.masked_fill(j > i + (nk - nq), float("-inf"))
+    ref_o = torch.nan_to_num(torch.softmax(s, dim=-1)) @ vx
+    np.testing.assert_allclose(o, ref_o.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), rtol=0, atol=1e-12)
+    if causal and nq > nk:
+        assert np.all(np.isneginf(lse[:, :, : nq - nk])) and np.all(o[:, :, : nq - nk] == 0)
+        assert np.all(np.isfinite(lse[:, :, nq - nk:]))
+
+
+def test_fp8_causal_first_row_is_its_first_value():
+    # Equal lengths, causal: row 0 sees key 0 alone, so p = 1, 2^8 p = 256 is
+    # exact in e4m3 and both modes return v_0 dequantised, exactly.
+    q, k, v, qd, kd, vd = _fp8_inputs(52, 1, 2, 1, 64, 32)
+    for round_p in (True, False):
+        o, lse, _, _ = oracle.attention_fp8(q, k, v, qd, kd, vd, 0.3, round_p=round_p, causal=True)
+        v0 = oracle.decode_e4m3(v[0, 0, 0]) * np.float64(vd[0])
+        for h in range(2):
+            assert np.array_equal(o[0, h, 0], v0)
+            s0 = 0.3 * np.dot(oracle.decode_e4m3(q[0, h, 0]) * np.float64(qd[0]),
+                              oracle.decode_e4m3(k[0, 0, 0]) * np.float64(kd[0]))
+            assert lse[0, h, 0] == pytest.approx(s0, abs=1e-12)
+
+
+@pytest.mark.parametrize("nq,nk", [(40, 40), (30, 75), (75, 30)])
+def test_fp8_causal_method_equals_the_method_on_the_visible_keys(nq, nk):
+    # The mask only removes keys: with key tiles starting at key 0, causal row
+    # i is the non-causal method on keys [0, kend(i)) -- for every tile width,
+    # so the rounding against the running max is the same too.
+    q, k, v, qd, kd, vd = _fp8_general_inputs(53, 1, 1, 1, nq, nk, 16, amp=2.0)
+    for bc in (1, 8, 128):
+        o, lse, a, b = oracle.attention_fp8(q, k, v, qd, kd, vd, 0.4, causal=True, bc=bc)
+        for i in range(nq):
+            kend = min(nk, i + 1 + nk - nq)
+            if kend <= 0:
+                assert np.isneginf(lse[0, 0, i]) and not o[0, 0, i].any()
+                continue
+            oi, li, ai, bi = oracle.attention_fp8(q[:, :, i:i + 1], k[:, :, :kend], v[:, :, :kend], qd, kd, vd,
+                                                  0.4, bc=bc)
+            assert np.array_equal(o[0, 0, i], oi[0, 0, 0]) and lse[0, 0, i] == li[0, 0, 0]
+            assert np.array_equal(a[0, 0, i], ai[0, 0, 0]) and np.array_equal(b[0, 0, i], bi[0, 0, 0])
+
+
+def test_fp8_general_method_stays_within_the_rounding_bound():
+    q, k, v, qd, kd, vd = _fp8_general_inputs(54, 1, 2, 1, 300, 500, 32, amp=2.0)
+    for causal in (False, True):
+        om, op, lp, a, b = oracle.attention_fp8_both(q, k, v, qd, kd, vd, 0.2, causal=causal)
+        assert np.all(np.abs(om - op) <= 2.0 ** -4 * a + 2.0 ** -18 * b + 1e-15)
