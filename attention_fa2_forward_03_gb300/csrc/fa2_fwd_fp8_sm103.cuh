@@ -22,7 +22,15 @@
 // 14-15, idle in the 16-bit kernel, transpose each V tile in shared memory
 // into a double-buffered V^T tile (the in-kernel pre-processing); the MMA
 // waits on V^T instead of V. And P is packed four per TMEM column.
-// Head dimension 128 (one 128-byte swizzle row per tile row), N % 128 == 0.
+// Head dimension 128 (one 128-byte swizzle row per tile row).
+//
+// Two modes, as in the 16-bit kernel: equal lengths N % 128 == 0 without a
+// mask (kGen = false: query-head packing, 2-D tensor maps), and the general
+// mode (kGen = true: unequal and ragged lengths, the bottom-right causal
+// mask; one query head per item, 3-D maps whose rows past a head's end read
+// as zero, masked keys set to -inf before the row max). Key tiles start at
+// key 0 in both, so each tile's weights are rounded against the same running
+// max as without the mask.
 #pragma once
 
 #include "fa2_fwd_sm103.cuh"
@@ -113,6 +121,42 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmQ, const CUtensorM
     }
 }
 
+// General mode: one query head per item (make_item_gen), 3-D maps; only
+// tiles with keys to attend load Q, and an item loads K_j, V_j for
+// j < max(nkv[0], nkv[1]).
+__device__ __forceinline__ void producer_gen(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                             const Params& p, uint32_t sbase, const BarsF8& bars, const Waiter& w) {
+    constexpr int S = kStages;
+    int ring = 0;
+    int nq[2] = {0, 0};
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+        const ItemG g = make_item_gen(p, it);
+        for (int t = 0; t < g.n_tiles && ok; ++t) {
+            if (g.nkv[t] == 0) continue;
+            if (!(ok = w.wait(bars.q_empty(t), (nq[t] & 1) ^ 1, kSiteQEmpty))) break;
+            ptx::mbar_arrive_expect_tx(bars.q_full(t), kTile);
+            ptx::tma_load_3d(sbase + Lay::kQOff + t * kTile, tmQ, 0, g.q0 + t * kBM, g.head, bars.q_full(t));
+            ++nq[t];
+        }
+        const int nmax = max(g.nkv[0], g.nkv[1]);
+        for (int k = 0; k < 2 * nmax && ok; ++k) {
+            const int s = ring % S;
+            if (!(ok = w.wait(bars.kv_empty(s), ((ring / S) & 1) ^ 1, kSiteKvEmpty))) break;
+            ptx::mbar_arrive_expect_tx(bars.kv_full(s), kTile);
+            ptx::tma_load_3d(sbase + Lay::kRingOff + s * kTile, (k & 1) ? tmV : tmK, 0, (k >> 1) * kBN, g.kvhead,
+                             bars.kv_full(s));
+            ++ring;
+        }
+    }
+    if (!ok) {
+        const int first = ring > S ? ring - S : 0;
+        for (int r = first; r < ring; ++r) w.drain(bars.kv_full(r % S), (r / S) & 1);
+        for (int t = 0; t < 2; ++t)
+            if (nq[t] > 0) w.drain(bars.q_full(t), (nq[t] - 1) & 1);
+    }
+}
+
 // ---------------------------------------------------------------- V transpose
 
 // Warps 14-15 turn each V tile (keys x dims, dims contiguous, 128-byte
@@ -165,6 +209,7 @@ __device__ __forceinline__ void transpose_tile(const uint8_t* __restrict__ src, 
     }
 }
 
+template <bool kGen>
 __device__ __forceinline__ void xpose_role(const Params& p, uint8_t* smem, const BarsF8& bars, const Waiter& w) {
     constexpr int S = kStages;
     const int xid = threadIdx.x - kXposeWarp0 * 32;
@@ -173,7 +218,12 @@ __device__ __forceinline__ void xpose_role(const Params& p, uint8_t* smem, const
     int nv = 0;     // V tiles transposed
     bool ok = true;
     for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
-        for (int jt = 0; jt < p.n_kv_tiles; ++jt, ++nv) {
+        int nkv = p.n_kv_tiles;   // KV tiles the item loads
+        if constexpr (kGen) {
+            const ItemG g = make_item_gen(p, it);
+            nkv = max(g.nkv[0], g.nkv[1]);
+        }
+        for (int jt = 0; jt < nkv; ++jt, ++nv) {
             ++ring;                      // K_jt: not ours
             const int r = ring++;        // V_jt
             const int s = r % S;
@@ -273,8 +323,93 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint
     __syncwarp();
 }
 
+// General mode: mma_issuer's order with a KV tile count per query tile (as
+// the 16-bit kernel's general issuer): at KV tile j only tiles with
+// j < nkv[t] take part; V^T_j's buffer and K_{j+1}'s stage are released
+// after their last user.
+__device__ __forceinline__ void mma_issuer_gen(const Params& p, uint32_t sbase, uint32_t tmem, const BarsF8& bars,
+                                               const Waiter& w) {
+    constexpr int S = kStages;
+    constexpr uint32_t kIdS = ptx::idesc_f16(0u, 0, 0, kBM, kBN);
+    constexpr uint32_t kIdO = ptx::idesc_f16(0u, 0, 0, kBM, kD);
+    auto stage_addr = [&](int r) { return sbase + Lay::kRingOff + (r % S) * kTile; };
+    auto issue_qk = [&](int t, uint32_t kaddr) {
+        const uint64_t qd = ptx::desc_sw128(sbase + Lay::kQOff + t * kTile, 16, 1024);
+        const uint64_t kd = ptx::desc_sw128(kaddr, 16, 1024);
+        ptx::mma_ss_kloop4_f8(tmem + Lay::col_s(t), qd, kd, kIdS, 0u);
+    };
+    auto issue_pv = [&](int t, int vb, bool acc) {
+        const uint64_t vd = ptx::desc_sw128(sbase + Lay::kVtOff + vb * kTile, 16, 1024);
+        ptx::mma_ts_kloop4_f8(tmem + Lay::col_o(t), tmem + Lay::col_s(t), vd, kIdO, acc ? 1u : 0u);
+    };
+    auto wait_u = [&](uint32_t bar, uint32_t parity, int site) {
+        return __shfl_sync(0xffffffffu, w.wait(bar, parity, site) ? 1 : 0, 0) != 0;
+    };
+    auto wait_ring = [&](int r) { return wait_u(bars.kv_full(r % S), (r / S) & 1, kSiteKvFull); };
+
+    int ring = 0;
+    int nv = 0;
+    int nq[2] = {0, 0};
+    int np[2] = {0, 0};
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+        const ItemG g = make_item_gen(p, it);
+        const int nmax = max(g.nkv[0], g.nkv[1]);
+        if (nmax == 0) continue;
+        for (int t = 0; t < 2 && ok; ++t)
+            if (g.nkv[t] > 0) ok = wait_u(bars.q_full(t), nq[t] & 1, kSiteQFull);
+        if (!ok || !(ok = wait_ring(ring))) break;
+        ptx::tc_fence_after();
+        for (int t = 0; t < 2; ++t) {
+            if (g.nkv[t] == 0) continue;
+            issue_qk(t, stage_addr(ring));
+            ptx::tc_commit_elect(bars.s_full(t));
+            if (g.nkv[t] == 1) ptx::tc_commit_elect(bars.q_empty(t));
+        }
+        ptx::tc_commit_elect(bars.kv_empty(ring % S));
+        int k_ring = ring;
+        ++ring;
+        for (int j = 0; j < nmax; ++j) {
+            const bool more = j + 1 < nmax;
+            ++ring;                       // V_j: released by the transposer
+            const int vb = nv & 1;
+            if (!(ok = wait_u(bars.vt_full(vb), (nv >> 1) & 1, kSiteVtFull))) break;
+            ++nv;
+            if (more) {
+                k_ring = ring++;
+                if (!(ok = wait_ring(k_ring))) break;
+            }
+            const int last_v = j < g.nkv[1] ? 1 : 0;                 // last tile reading V^T_j
+            const int last_k = (more && j + 1 < g.nkv[1]) ? 1 : 0;   // last tile reading K_{j+1}
+            for (int t = 0; t < 2; ++t) {
+                if (j >= g.nkv[t]) continue;
+                if (!(ok = wait_u(bars.p_full(t), np[t] & 1, kSitePFull))) break;
+                ++np[t];
+                ptx::tc_fence_after();
+                issue_pv(t, vb, j > 0);
+                if (t == last_v) ptx::tc_commit_elect(bars.vt_empty(vb));
+                if (j + 1 < g.nkv[t]) {
+                    issue_qk(t, stage_addr(k_ring));
+                    ptx::tc_commit_elect(bars.s_full(t));
+                    if (j + 2 == g.nkv[t]) ptx::tc_commit_elect(bars.q_empty(t));
+                    if (t == last_k) ptx::tc_commit_elect(bars.kv_empty(k_ring % S));
+                } else {
+                    ptx::tc_commit_elect(bars.o_full(t));
+                }
+            }
+            if (!ok) break;
+        }
+        for (int t = 0; t < 2; ++t)
+            if (g.nkv[t] > 0) ++nq[t];
+    }
+    ptx::tc_commit_elect(bars.mma_done());
+    w.drain(bars.mma_done(), 0);
+    __syncwarp();
+}
+
 // ---------------------------------------------------------------- softmax
 
+template <bool kGen>
 __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uint8_t* smem, const BarsF8& bars,
                                              const Waiter& w, int t) {
     const int row = threadIdx.x & 127;
@@ -287,12 +422,26 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
     int n_s = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
-        if (t >= make_item(p, it).n_tiles) continue;
-        const int g = item_group(p, it);
+        int nkv, grp, jmask = 0x7fffffff, kend_row = 0;
+        if constexpr (kGen) {
+            const ItemG g = make_item_gen(p, it);
+            if (t >= g.n_tiles || g.nkv[t] == 0) continue;
+            nkv = g.nkv[t];
+            jmask = g.jmask[t];
+            kend_row = kend_of(p, g.q0 + t * kBM + row);
+            grp = g.kvhead;
+        } else {
+            if (t >= make_item(p, it).n_tiles) continue;
+            nkv = p.n_kv_tiles;
+            grp = item_group(p, it);
+        }
         // log2-domain factor of the raw code products: scale * log2(e) * dq * dk
-        const float c = p.scale_log2 * __ldg(p.q_descale + g) * __ldg(p.k_descale + g);
+        float c = p.scale_log2 * __ldg(p.q_descale + grp) * __ldg(p.k_descale + grp);
+        // A zero descale makes every score 0; c = FLT_MIN gives the same
+        // weights (exp2 of |s c| < 2^-90 is 1) and keeps masked keys at
+        // -inf * c = -inf instead of NaN.
+        if constexpr (kGen) c = fmaxf(c, 1.17549435e-38f);
         const uint64_t c2 = ptx::f2_pack(c, c);
-        const int nkv = p.n_kv_tiles;
         float m = -INFINITY;
         float l = 0.0f;       // sum of the unrounded 2^8-scaled weights
         for (int j = 0; j < nkv; ++j, ++n_s) {
@@ -303,23 +452,53 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
             }
             ptx::tc_fence_after();
             uint32_t s[kBN];
-            float mq[4];   // row max of each 32-column load
-            ptx::tmem_ld32_max_at<0>(row_addr + colS + 0, s, mq[0]);
-            ptx::tmem_ld32_max_at<32>(row_addr + colS + 32, s, mq[1]);
-            ptx::tmem_ld32_max_at<64>(row_addr + colS + 64, s, mq[2]);
-            ptx::tmem_ld32_max_at<96>(row_addr + colS + 96, s, mq[3]);
-            ptx::tmem_wait_ld();
+            float m_tile;
+            if constexpr (kGen) {
+                ptx::tmem_ld32_at<0>(row_addr + colS + 0, s);
+                ptx::tmem_ld32_at<32>(row_addr + colS + 32, s);
+                ptx::tmem_ld32_at<64>(row_addr + colS + 64, s);
+                ptx::tmem_ld32_at<96>(row_addr + colS + 96, s);
+                ptx::tmem_wait_ld();
+                // Keys at or past kend(row) (the causal diagonal, the end of
+                // a ragged key sequence, TMA's zero fill) get -inf.
+                if (j >= jmask) {
+                    const int lim = kend_row - j * kBN;
+#pragma unroll
+                    for (int e = 0; e < kBN; ++e) s[e] = e < lim ? s[e] : 0xFF800000u;
+                }
+                float mx[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    float a = __uint_as_float(s[k]);
+#pragma unroll
+                    for (int i = 1; i < 15; i += 2)
+                        a = ptx::max3(a, __uint_as_float(s[k + 8 * i]), __uint_as_float(s[k + 8 * (i + 1)]));
+                    mx[k] = fmaxf(a, __uint_as_float(s[k + 120]));
+                }
+                m_tile = fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7]))) *
+                         c;
+            } else {
+                float mq[4];   // row max of each 32-column load
+                ptx::tmem_ld32_max_at<0>(row_addr + colS + 0, s, mq[0]);
+                ptx::tmem_ld32_max_at<32>(row_addr + colS + 32, s, mq[1]);
+                ptx::tmem_ld32_max_at<64>(row_addr + colS + 64, s, mq[2]);
+                ptx::tmem_ld32_max_at<96>(row_addr + colS + 96, s, mq[3]);
+                ptx::tmem_wait_ld();
+                m_tile = fmaxf(ptx::max3(mq[0], mq[1], mq[2]), mq[3]) * c;
+            }
             // c > 0, so the max of c*s is c times the max of s
-            const float m_tile = fmaxf(ptx::max3(mq[0], mq[1], mq[2]), mq[3]) * c;
             const float m_new = fmaxf(m, m_tile);
             const float alpha = (j == 0 || m_new == m) ? 1.0f : ptx::ex2_approx(m - m_new);
             alpha_buf[row] = alpha;
             ptx::mbar_arrive(bars.alpha_ready(t));
             l *= alpha;
             m = m_new;
+            // A row with no allowed key so far keeps m = -inf; exponentiate
+            // against 0 then, so its weights are exp2(-inf) = 0.
+            const float m_use = (kGen && m == -INFINITY) ? 0.0f : m;
 
             // P' = exp2(S c - m + 8), four at a time into one TMEM column.
-            const uint64_t nm2 = ptx::f2_pack(8.0f - m, 8.0f - m);
+            const uint64_t nm2 = ptx::f2_pack(8.0f - m_use, 8.0f - m_use);
             uint64_t acc[4] = {0, 0, 0, 0};
             uint32_t pk[kBN / 4];
 #pragma unroll
@@ -330,7 +509,9 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
                     const int e = 4 * i + 2 * h;
                     const uint64_t x =
                         ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), c2, nm2);
-                    if ((i & 3) == 3 && h == 1) {   // one pair in eight on the FMA pipe
+                    // one pair in eight on the FMA pipe (equal-length mode:
+                    // masked -inf keys need the MUFU's exact 0)
+                    if (!kGen && (i & 3) == 3 && h == 1) {
                         ptx::f2_unpack(ptx::ex2_poly_f2(x), pr[2 * h], pr[2 * h + 1]);
                     } else {
                         float x0, x1;
@@ -360,6 +541,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
 
 // ---------------------------------------------------------------- correction + epilogue
 
+template <bool kGen>
 __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, uint8_t* smem, const BarsF8& bars,
                                                 const Waiter& w) {
     constexpr int kChunk = 32;
@@ -373,11 +555,29 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
     int n_items[2] = {0, 0};
     bool ok = true;
     for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
-        const Item item = make_item(p, it);
-        const int n_tiles = item.n_tiles;
-        const float dv = __ldg(p.v_descale + item_group(p, it));
-        for (int j = 0; j < p.n_kv_tiles && ok; ++j) {
+        // row0: first row of tile 0 in the output view; q0: the same row's
+        // index within its head (general mode, for the ragged-end check).
+        int n_tiles, nkv[2], row0, q0 = 0, grp;
+        if constexpr (kGen) {
+            const ItemG g = make_item_gen(p, it);
+            n_tiles = g.n_tiles;
+            nkv[0] = g.nkv[0];
+            nkv[1] = g.nkv[1];
+            row0 = g.head * p.nq + g.q0;
+            q0 = g.q0;
+            grp = g.kvhead;
+        } else {
+            const Item item = make_item(p, it);
+            n_tiles = item.n_tiles;
+            nkv[0] = nkv[1] = p.n_kv_tiles;
+            row0 = item.q_row0;
+            grp = item_group(p, it);
+        }
+        const float dv = __ldg(p.v_descale + grp);
+        const int nmax = max(nkv[0], n_tiles > 1 ? nkv[1] : 0);
+        for (int j = 0; j < nmax && ok; ++j) {
             for (int t = 0; t < n_tiles; ++t) {
+                if (j >= nkv[t]) continue;
                 ok = w.wait(bars.alpha_ready(t), n_s[t] & 1, kSiteAlpha);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
@@ -414,7 +614,19 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
         }
         // Epilogue: O * dv / l' -> bf16, LSE = (m + log2 l' - 8) ln 2.
         for (int t = 0; t < n_tiles && ok; ++t) {
-            const int grow = item.q_row0 + t * kBM + row;
+            const int grow = row0 + t * kBM + row;
+            // Rows past a ragged query end are computed but not stored.
+            const bool valid = !kGen || q0 + t * kBM + row < p.nq;
+            if (kGen && nkv[t] == 0) {
+                // No row of this tile may attend any key: O = 0, LSE = -inf.
+                if (valid) {
+                    uint4* z = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + static_cast<size_t>(grow) * kD);
+#pragma unroll
+                    for (int v = 0; v < kD / 8; ++v) z[v] = make_uint4(0, 0, 0, 0);
+                    p.lse[grow] = -INFINITY;
+                }
+                continue;
+            }
             ok = w.wait(bars.stats_ready(t), n_items[t] & 1, kSiteStats);
             if (ok) ok = w.wait(bars.o_full(t), n_items[t] & 1, kSiteOFull);
             if (!__all_sync(0xffffffffu, ok)) {
@@ -425,7 +637,8 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
             ptx::tc_fence_after();
             const float m = rowbuf[(2 + t) * kBM + row];
             const float l = rowbuf[(4 + t) * kBM + row];
-            const float f = dv * ptx::rcp_approx(l);
+            // l' = 0 only for a row with no allowed key: O = 0, LSE = -inf.
+            const float f = (!kGen || l > 0.0f) ? dv * ptx::rcp_approx(l) : 0.0f;
             const uint32_t colO = Lay::col_o(t);
             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + static_cast<size_t>(grow) * kD);
 #pragma unroll
@@ -437,11 +650,15 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
 #pragma unroll
                 for (int i = 0; i < kChunk / 2; ++i)
                     hv[i] = ptx::pack2<true>(__uint_as_float(o[2 * i]) * f, __uint_as_float(o[2 * i + 1]) * f);
+                if (valid) {
 #pragma unroll
-                for (int v = 0; v < kChunk / 8; ++v)
-                    dst[h / 8 + v] = make_uint4(hv[4 * v], hv[4 * v + 1], hv[4 * v + 2], hv[4 * v + 3]);
+                    for (int v = 0; v < kChunk / 8; ++v)
+                        dst[h / 8 + v] = make_uint4(hv[4 * v], hv[4 * v + 1], hv[4 * v + 2], hv[4 * v + 3]);
+                }
             }
-            p.lse[grow] = (m + ptx::lg2_approx(l) - 8.0f) * 0.69314718055994530942f;
+            if (valid)
+                p.lse[grow] = (!kGen || l > 0.0f) ? (m + ptx::lg2_approx(l) - 8.0f) * 0.69314718055994530942f
+                                                  : -INFINITY;
         }
         ptx::tc_fence_before();
     }
@@ -451,6 +668,7 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
 
 // ---------------------------------------------------------------- kernel
 
+template <bool kGen>
 __global__ void __launch_bounds__(kThreads, 1)
     fa2_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -505,19 +723,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < kCorrWarp0) {
         ptx::setmaxnreg_inc<kRegSoftmax>();
-        fp8::softmax_role(p, tmem, smem, bars, w, warp / 4);
+        fp8::softmax_role<kGen>(p, tmem, smem, bars, w, warp / 4);
     } else if (warp < kLoadWarp) {
         ptx::setmaxnreg_dec<kRegCorr>();
-        fp8::correction_role(p, tmem, smem, bars, w);
+        fp8::correction_role<kGen>(p, tmem, smem, bars, w);
     } else {
         ptx::setmaxnreg_dec<kRegOther>();
         if (warp == kLoadWarp) {
-            if (lane == 0) fp8::producer(&tmQ, &tmK, &tmV, p, sbase, bars, w);
+            if (lane == 0) {
+                if constexpr (kGen)
+                    fp8::producer_gen(&tmQ, &tmK, &tmV, p, sbase, bars, w);
+                else
+                    fp8::producer(&tmQ, &tmK, &tmV, p, sbase, bars, w);
+            }
             __syncwarp();
         } else if (warp == kMmaWarp) {
-            fp8::mma_issuer(p, sbase, tmem, bars, w);
+            if constexpr (kGen)
+                fp8::mma_issuer_gen(p, sbase, tmem, bars, w);
+            else
+                fp8::mma_issuer(p, sbase, tmem, bars, w);
         } else {
-            fp8::xpose_role(p, smem, bars, w);
+            fp8::xpose_role<kGen>(p, smem, bars, w);
         }
     }
 

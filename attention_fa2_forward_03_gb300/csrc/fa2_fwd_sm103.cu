@@ -37,7 +37,7 @@ struct DeviceState {
     bool probed = false;
     bool supported = false;
     int sm_count = 0;
-    bool smem_set[13] = {};
+    bool smem_set[14] = {};
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -129,18 +129,32 @@ fa2_status encode_map_u8(CUtensorMap* m, const void* ptr, uint64_t rows) {
     return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
 }
 
+// 3-D view [mats, rows, 128] of an 8-bit tensor (FP8 general mode): a box
+// never crosses into the next head, and rows past `rows` read as zero.
+fa2_status encode_map_u8_3d(CUtensorMap* m, const void* ptr, uint64_t mats, uint64_t rows) {
+    cuuint64_t dims[3] = {128, rows, mats};
+    cuuint64_t strides[2] = {128, rows * 128};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
+}
+
+template <bool kGen>
 fa2_status launch_fp8(int dev, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                       const Params& p, dim3 grid, cudaStream_t stream) {
     constexpr int kSmem = fa2::fp8::Lay::kSmemBytes;
-    constexpr int kSlot = 12;
+    constexpr int kSlot = kGen ? 13 : 12;
+    auto kern = fa2::fa2_fwd_fp8_kernel<kGen>;
     if (!g_dev[dev].smem_set[kSlot]) {
-        if (cudaFuncSetAttribute(fa2::fa2_fwd_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
             return FA2_ERR_CUDA;
         std::lock_guard<std::mutex> lk(g_mu);
         g_dev[dev].smem_set[kSlot] = true;
     }
-    fa2::fa2_fwd_fp8_kernel<<<grid, fa2::kThreads, kSmem, stream>>>(mq, mk, mv, p);
+    kern<<<grid, fa2::kThreads, kSmem, stream>>>(mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 
@@ -242,7 +256,63 @@ fa2_status fa2_fwd_fp8(const void* q, const void* k, const void* v, const float*
     p.k_descale = k_descale;
     p.v_descale = v_descale;
     const dim3 grid(static_cast<unsigned>(std::min<long long>(p.total_items, g_dev[dev].sm_count)));
-    return launch_fp8(dev, mq, mk, mv, p, grid, stream);
+    return launch_fp8<false>(dev, mq, mk, mv, p, grid, stream);
+}
+
+fa2_status fa2_fwd_fp8_ex(const void* q, const void* k, const void* v, const float* q_descale,
+                          const float* k_descale, const float* v_descale, void* o, float* lse, int B, int H_q,
+                          int H_kv, int N_q, int N_k, int d, float scale, int causal, cudaStream_t stream) {
+    if (!q || !k || !v || !o || !lse || !q_descale || !k_descale || !v_descale) return FA2_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA2_ERR_INVALID_ARG;
+    if (!aligned4(q_descale) || !aligned4(k_descale) || !aligned4(v_descale)) return FA2_ERR_INVALID_ARG;
+    if (B <= 0 || H_q <= 0 || H_kv <= 0 || N_q <= 0 || N_k <= 0 || d <= 0) return FA2_ERR_INVALID_ARG;
+    if (H_q % H_kv != 0) return FA2_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.0f)) return FA2_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA2_ERR_INVALID_ARG;
+    if (d != fa2::fp8::kD) return FA2_ERR_UNSUPPORTED;
+    // The plain case is the multiple-of-128 kernel.
+    if (!causal && N_q == N_k && N_q % fa2::kBM == 0)
+        return fa2_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, o, lse, B, H_q, H_kv, N_q, d, scale, stream);
+    const long long heads_q = static_cast<long long>(B) * H_q;
+    const long long rows_q = heads_q * N_q;
+    const long long rows_kv = static_cast<long long>(B) * H_kv * N_k;
+    const long long tq = (N_q + fa2::kBM - 1) / fa2::kBM;
+    const long long items = heads_q * ((tq + fa2::kNQ - 1) / fa2::kNQ);
+    if (rows_q > 0x7FFFFFFFLL || rows_kv > 0x7FFFFFFFLL || items > 0x7FFFFFFFLL) return FA2_ERR_UNSUPPORTED;
+
+    int dev = 0;
+    fa2_status st = check_device(&dev);
+    if (st != FA2_OK) return st;
+    if ((st = get_encoder()) != FA2_OK) return st;
+
+    CUtensorMap mq, mk, mv;
+    const uint64_t hkv = static_cast<uint64_t>(B) * H_kv;
+    if (encode_map_u8_3d(&mq, q, static_cast<uint64_t>(heads_q), static_cast<uint64_t>(N_q)) != FA2_OK ||
+        encode_map_u8_3d(&mk, k, hkv, static_cast<uint64_t>(N_k)) != FA2_OK ||
+        encode_map_u8_3d(&mv, v, hkv, static_cast<uint64_t>(N_k)) != FA2_OK)
+        return FA2_ERR_CUDA;
+
+    Params p{};
+    p.o = o;
+    p.lse = lse;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    p.debug_flags = g_debug_flags.load();
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.nq = N_q;
+    p.nk = N_k;
+    p.causal = causal;
+    p.heads_q = static_cast<int>(heads_q);
+    p.hq = H_q;
+    p.group = H_q / H_kv;
+    p.tq = static_cast<int>(tq);
+    p.pairs = static_cast<int>((tq + fa2::kNQ - 1) / fa2::kNQ);
+    p.total_items = static_cast<int>(items);
+    p.q_descale = q_descale;
+    p.k_descale = k_descale;
+    p.v_descale = v_descale;
+    const dim3 grid(static_cast<unsigned>(std::min<long long>(items, g_dev[dev].sm_count)));
+    return launch_fp8<true>(dev, mq, mk, mv, p, grid, stream);
 }
 
 fa2_status fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,

@@ -22,7 +22,7 @@ FA2_ERR_CUDA = 3
 FA2_ERR_TIMEOUT = 4
 
 # symbols declared in include/fa2.h
-EXPORTS = ("fa2_fwd", "fa2_fwd_gqa", "fa2_fwd_ex", "fa2_fwd_fp8", "fa2_bwd", "fa2_bwd_noalloc", "fa2_check_status",
+EXPORTS = ("fa2_fwd", "fa2_fwd_gqa", "fa2_fwd_ex", "fa2_fwd_fp8", "fa2_fwd_fp8_ex", "fa2_bwd", "fa2_bwd_noalloc", "fa2_check_status",
            "fa2_status_string",
            "fa2_set_wait_limit_ns", "fa2_set_debug_flags", "fa2_version")
 
@@ -53,6 +53,8 @@ def load(path: str = LIB_PATH):
     lib.fa2_fwd_ex.restype = i
     lib.fa2_fwd_fp8.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, f, p]
     lib.fa2_fwd_fp8.restype = i
+    lib.fa2_fwd_fp8_ex.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, f, i, p]
+    lib.fa2_fwd_fp8_ex.restype = i
     lib.fa2_bwd.argtypes = [p, p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, i, i, p]
     lib.fa2_bwd.restype = i
     lib.fa2_bwd_noalloc.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, i, i, p]
@@ -99,6 +101,13 @@ def fa2_fwd_fp8_ptr(q, k, v, q_descale, k_descale, v_descale, o, lse, B, H_q, H_
     """fa2_fwd_fp8 on raw device addresses (ints); returns the status code."""
     return load().fa2_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, o, lse, B, H_q, H_kv, N, d,
                               float(scale), stream or None)
+
+
+def fa2_fwd_fp8_ex_ptr(q, k, v, q_descale, k_descale, v_descale, o, lse, B, H_q, H_kv, N_q, N_k, d, scale,
+                       causal, stream=0) -> int:
+    """fa2_fwd_fp8_ex on raw device addresses (ints); returns the status code."""
+    return load().fa2_fwd_fp8_ex(q, k, v, q_descale, k_descale, v_descale, o, lse, B, H_q, H_kv, N_q, N_k, d,
+                                 float(scale), int(causal), stream or None)
 
 
 def fa2_bwd_ptr(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H_q, H_kv, N, d, scale, causal, dtype,
@@ -254,18 +263,19 @@ def fa2_bwd(q, k, v, o, lse, dout, scale=None, causal=False, dq=None, dk=None, d
     return dq, dk, dv
 
 
-def fa2_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, o=None, lse=None, scale=None, stream=None):
-    """FP8 attention forward: q [B,Hq,N,d], k/v [B,Hkv,N,d] e4m3 codes as
-    uint8 (or torch.float8_e4m3fn) CUDA tensors, descales fp32 [B*Hkv] CUDA
-    tensors. Returns (o, lse) with o bf16 [B,Hq,N,d] and lse fp32 [B,Hq,N]."""
+def _fp8_prepare(q, k, v, q_descale, k_descale, v_descale, o, lse, same_len):
+    """Check the FP8 arguments and allocate missing outputs; returns
+    (o, lse, B, Hq, Hkv, Nq, Nk, d)."""
     import torch
 
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be 4-D [B, H, N, d]")
     B, Hq, N, d = q.shape
-    Hkv = k.shape[1]
-    if tuple(k.shape) != (B, Hkv, N, d) or v.shape != k.shape:
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if same_len and Nk != N:
         raise ValueError("k and v must be [B, Hkv, N, d] with q's B, N and d")
+    if tuple(k.shape) != (B, Hkv, Nk, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, Nk, d] with q's B and d")
     for t in (q, k, v):
         if t.element_size() != 1 or not t.is_cuda or not t.is_contiguous():
             raise ValueError("q, k and v must be contiguous one-byte (e4m3) CUDA tensors")
@@ -280,6 +290,14 @@ def fa2_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, o=None, lse=None, scal
         raise ValueError("o must be a contiguous bf16 tensor [B, Hq, N, d]")
     if tuple(lse.shape) != (B, Hq, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 tensor [B, Hq, N]")
+    return o, lse, B, Hq, Hkv, N, Nk, d
+
+
+def fa2_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, o=None, lse=None, scale=None, stream=None):
+    """FP8 attention forward: q [B,Hq,N,d], k/v [B,Hkv,N,d] e4m3 codes as
+    uint8 (or torch.float8_e4m3fn) CUDA tensors, descales fp32 [B*Hkv] CUDA
+    tensors. Returns (o, lse) with o bf16 [B,Hq,N,d] and lse fp32 [B,Hq,N]."""
+    o, lse, B, Hq, Hkv, N, _, d = _fp8_prepare(q, k, v, q_descale, k_descale, v_descale, o, lse, True)
     if scale is None:
         scale = d ** -0.5
     rc = fa2_fwd_fp8_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), q_descale.data_ptr(), k_descale.data_ptr(),
@@ -287,6 +305,22 @@ def fa2_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, o=None, lse=None, scal
                          _stream_handle(stream, q.device))
     if rc != FA2_OK:
         raise FA2Error(rc, "fa2_fwd_fp8")
+    return o, lse
+
+
+def fa2_fwd_fp8_ex(q, k, v, q_descale, k_descale, v_descale, o=None, lse=None, scale=None, causal=False,
+                   stream=None):
+    """General FP8 attention forward: q [B,Hq,Nq,d], k/v [B,Hkv,Nk,d] e4m3
+    codes, any Nq, Nk, optional causal mask (end-aligned). Returns (o, lse)
+    with o bf16 [B,Hq,Nq,d] and lse fp32 [B,Hq,Nq]."""
+    o, lse, B, Hq, Hkv, Nq, Nk, d = _fp8_prepare(q, k, v, q_descale, k_descale, v_descale, o, lse, False)
+    if scale is None:
+        scale = d ** -0.5
+    rc = fa2_fwd_fp8_ex_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), q_descale.data_ptr(), k_descale.data_ptr(),
+                            v_descale.data_ptr(), o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Nq, Nk, d, scale,
+                            bool(causal), _stream_handle(stream, q.device))
+    if rc != FA2_OK:
+        raise FA2Error(rc, "fa2_fwd_fp8_ex")
     return o, lse
 
 

@@ -11,8 +11,9 @@ per step. Prints ONE JSON line (rank 0).
                     [--impl ours|reference] [--no-cpu-baseline]
 
 --pass picks what one step runs (default fwd, the line above):
-  fwd_causal  fa2_fwd_ex with the causal mask; FLOPs counted over the
-              unmasked (query, key) pairs only, 4*d*sum_i(i+1) per head
+  fwd_causal  fa2_fwd_ex (fa2_fwd_fp8_ex for an FP8 workload) with the
+              causal mask; FLOPs counted over the unmasked (query, key)
+              pairs only, 4*d*sum_i(i+1) per head
   bwd         fa2_bwd (D = rowsum(dO*O), then dK/dV, then dQ: three
               launches); FLOPs counted as 2.5x the forward's (the five
               GEMMs of the backward), inputs from one forward call
@@ -264,7 +265,7 @@ def oracle_forward(w, inputs, rows, causal: bool = False):
     import oracle
 
     if w.fp8:
-        return oracle.attention_fp8(*inputs, w.scale, round_p=True, rows=rows)
+        return oracle.attention_fp8(*inputs, w.scale, round_p=True, rows=rows, causal=causal)
     q, k, v = inputs
     if causal:
         return oracle.attention_ex(q, k, v, w.scale, w.dtype, causal=True, rows=rows)
@@ -381,6 +382,9 @@ def run_reference(args, dist, w):
 
 def metric_of(which: str, w=None) -> str:
     if w is not None and w.fp8:
+        if which == "fwd_causal":
+            return ("attention fwd causal TFLOP/s (4d per unmasked pair) at 1 GB300, FP8 e4m3 inputs; "
+                    "% of dense FP8 tensor peak")
         return "attention fwd TFLOP/s (4BHN²d) at 1 GB300, FP8 e4m3 inputs; % of dense FP8 tensor peak"
     if which == "fwd":
         return METRIC
@@ -426,8 +430,8 @@ class Step:
         self.causal = which.endswith("causal")
         self.bwd = which.startswith("bwd")
         self.fp8 = w.fp8
-        if self.fp8 and which != "fwd":
-            raise ValueError("FP8 workloads have the forward pass only")
+        if self.fp8 and self.bwd:
+            raise ValueError("FP8 workloads have the forward passes only")
 
         def up(x):
             if x.dtype == np.uint8 or x.dtype == np.float32:
@@ -452,7 +456,7 @@ class Step:
         if self.bwd:
             self.kernel = "fa2_bwd (delta + dK/dV + dQ kernels)"
         elif self.fp8:
-            self.kernel = "fa2_fwd_fp8_kernel"
+            self.kernel = "fa2_fwd_fp8_kernel" + ("<general>" if self.causal else "")
         else:
             self.kernel = (f"fa2_fwd_kernel<{w.d},{'bf16' if w.dtype == gen.BF16 else 'fp16'}"
                            f"{',general' if self.causal else ''}>")
@@ -466,6 +470,12 @@ class Step:
                                self.delta.data_ptr(), w.B, w.Hq, w.Hkv, w.N, w.d, w.scale,
                                self.causal, w.dtype, s)
             name = "fa2_bwd"
+        elif self.fp8 and self.causal:
+            rc = f.fa2_fwd_fp8_ex_ptr(self.tq.data_ptr(), self.tk.data_ptr(), self.tv.data_ptr(),
+                                      self.tqd.data_ptr(), self.tkd.data_ptr(), self.tvd.data_ptr(),
+                                      self.o.data_ptr(), self.lse.data_ptr(), w.B, w.Hq, w.Hkv, w.N, w.N,
+                                      w.d, w.scale, True, s)
+            name = "fa2_fwd_fp8_ex"
         elif self.fp8:
             rc = f.fa2_fwd_fp8_ptr(self.tq.data_ptr(), self.tk.data_ptr(), self.tv.data_ptr(),
                                    self.tqd.data_ptr(), self.tkd.data_ptr(), self.tvd.data_ptr(),
@@ -501,6 +511,9 @@ class Step:
             dq, dk, dv = outs
             f.fa2_bwd(q, k, v, o, lse, do, scale=w.scale, causal=self.causal, dq=dq, dk=dk, dv=dv,
                       delta=self.delta, stream=stream)
+        elif self.fp8 and self.causal:
+            q, k, v, qd, kd, vd = ins
+            f.fa2_fwd_fp8_ex(q, k, v, qd, kd, vd, outs[0], outs[1], scale=w.scale, causal=True, stream=stream)
         elif self.fp8:
             q, k, v, qd, kd, vd = ins
             f.fa2_fwd_fp8(q, k, v, qd, kd, vd, outs[0], outs[1], scale=w.scale, stream=stream)

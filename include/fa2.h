@@ -120,7 +120,8 @@ fa2_status fa2_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
  *   k, v    : [B, H_kv, N, d] e4m3 codes, device
  *   q_descale, k_descale, v_descale : [B * H_kv] fp32, device; the value of
  *             a code of (batch b, KV head g) -- for q, of the query heads
- *             that share KV head g -- is code * descale[b * H_kv + g]
+ *             that share KV head g -- is code * descale[b * H_kv + g];
+ *             each finite and >= 0 (negative descales: results undefined)
  *   o       : [B, H_q, N, d] bf16, device (output)
  *   lse     : [B, H_q, N] fp32, device (output, natural-log logsumexp of the
  *             scaled scores of the dequantised inputs)
@@ -138,6 +139,29 @@ fa2_status fa2_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
 fa2_status fa2_fwd_fp8(const void* q, const void* k, const void* v, const float* q_descale,
                        const float* k_descale, const float* v_descale, void* o, float* lse,
                        int B, int H_q, int H_kv, int N, int d, float scale, cudaStream_t stream);
+
+/*
+ * fa2_fwd_fp8 generalised as fa2_fwd_ex generalises fa2_fwd_gqa: separate
+ * query and key lengths, any N_q, N_k >= 1, and the optional bottom-right
+ * causal mask (query row i attends keys j < min(N_k, i + 1 + N_k - N_q),
+ * "FlashAttention-2 from scratch on Ampere, Part 1", Kernel Specification,
+ * lists both as left out of its kernel; the reading is that of fa2_fwd_ex).
+ *   q       : [B, H_q, N_q, d] e4m3 codes; o : [B, H_q, N_q, d] bf16;
+ *   lse     : [B, H_q, N_q] fp32 (a row with no allowed key: o = 0,
+ *             lse = -inf)
+ *   k, v    : [B, H_kv, N_k, d] e4m3 codes
+ *   descales, d, alignment, numerics: as fa2_fwd_fp8. Key tiles of 128
+ *             start at key 0, so a masked row rounds its weights exactly as
+ *             the unmasked method on its visible keys.
+ *   causal  : 0 or 1 (other values FA2_ERR_INVALID_ARG)
+ * Non-causal calls with N_q == N_k and N_q % 128 == 0 run fa2_fwd_fp8.
+ * More than 2^31 - 1 query or key rows: FA2_ERR_UNSUPPORTED. Errors
+ * otherwise as fa2_fwd_fp8. Nothing is allocated.
+ */
+fa2_status fa2_fwd_fp8_ex(const void* q, const void* k, const void* v, const float* q_descale,
+                          const float* k_descale, const float* v_descale, void* o, float* lse,
+                          int B, int H_q, int H_kv, int N_q, int N_k, int d, float scale, int causal,
+                          cudaStream_t stream);
 
 /*
  * Attention backward (gradients of the forward with optional causal mask and

@@ -114,6 +114,24 @@ def test_fp8_entry_host_validation(lib):
     assert f(*ok, 2048, 8, 8, 131072, 128, 0.1) == fa2.FA2_ERR_UNSUPPORTED                # rows >= 2^31
 
 
+def test_fp8_general_entry_host_validation(lib):
+    f = fa2.fa2_fwd_fp8_ex_ptr
+    ok = [A] * 8
+    assert f(*([0] + ok[1:]), 1, 1, 1, 100, 100, 128, 0.1, 1) == fa2.FA2_ERR_INVALID_ARG        # NULL q
+    assert f(*(ok[:5] + [0] + ok[6:]), 1, 1, 1, 100, 100, 128, 0.1, 1) == fa2.FA2_ERR_INVALID_ARG  # NULL v_descale
+    assert f(*(ok[:5] + [A + 1] + ok[6:]), 1, 1, 1, 100, 100, 128, 0.1, 1) == fa2.FA2_ERR_INVALID_ARG  # align
+    assert f(*(ok[:6] + [A + 8, A]), 1, 1, 1, 100, 100, 128, 0.1, 1) == fa2.FA2_ERR_INVALID_ARG  # o align
+    assert f(*ok, 1, 4, 3, 100, 100, 128, 0.1, 1) == fa2.FA2_ERR_INVALID_ARG                    # Hq % Hkv
+    assert f(*ok, 1, 1, 1, 0, 100, 128, 0.1, 1) == fa2.FA2_ERR_INVALID_ARG                      # N_q = 0
+    assert f(*ok, 1, 1, 1, 100, 0, 128, 0.1, 0) == fa2.FA2_ERR_INVALID_ARG                      # N_k = 0
+    assert f(*ok, 1, 1, 1, 100, 100, 128, 0.1, 2) == fa2.FA2_ERR_INVALID_ARG                    # causal = 2
+    assert f(*ok, 1, 1, 1, 100, 100, 128, float("nan"), 1) == fa2.FA2_ERR_INVALID_ARG           # scale
+    assert f(*ok, 1, 1, 1, 100, 100, 64, 0.1, 1) == fa2.FA2_ERR_UNSUPPORTED                     # d = 64
+    assert f(*ok, 4096, 8, 8, 65536, 100, 128, 0.1, 1) == fa2.FA2_ERR_UNSUPPORTED               # rows >= 2^31
+    # equal lengths, multiple of 128, no mask: forwarded to fa2_fwd_fp8 and its checks
+    assert f(*ok, 2048, 8, 8, 131072, 131072, 128, 0.1, 0) == fa2.FA2_ERR_UNSUPPORTED
+
+
 def test_mha_entry_forwards_to_gqa(lib):
     assert fa2.fa2_fwd_ptr(0, A, A, A, A, 1, 1, 128, 128, 0.1, 0) == fa2.FA2_ERR_INVALID_ARG
     assert fa2.fa2_fwd_ptr(A, A, A, A, A, 1, 1, 128, 80, 0.1, 0) == fa2.FA2_ERR_UNSUPPORTED

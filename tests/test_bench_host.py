@@ -41,6 +41,12 @@ def test_reference_arm_fp8_workload():
     assert "FP8" in d["metric"]
 
 
+def test_reference_arm_fp8_causal_workload():
+    d = run_reference("--workload", "fp8_mha_B4_H16_N4096_d128_e4m3", "--pass", "fwd_causal")
+    assert d["value"] > 0 and d["config"]["causal"] is True
+    assert "FP8" in d["metric"] and "causal" in d["metric"]
+
+
 def test_pass_flop_and_byte_counts():
     w = gen.workload("mha_B4_H16_N4096_d128_bf16")
     assert bench.pass_flops(w, "fwd") == 4.0 * 4 * 16 * 4096 * 4096 * 128

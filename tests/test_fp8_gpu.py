@@ -1,4 +1,4 @@
-"""Parity of the FP8 (e4m3) forward (fa2_fwd_fp8) with the fp64 oracle,
+"""Parity of the FP8 (e4m3) forward (fa2_fwd_fp8, fa2_fwd_fp8_ex) with the fp64 oracle,
 through the C ABI.
 
 Tolerance, derived from the method's arithmetic (no tolerance is given for
@@ -36,8 +36,17 @@ def run_fp8(fa2, q, k, v, qd, kd, vd, scale):
     return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
 
-def assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, scale, rows=None, what=""):
-    om, op, lp, a, b = oracle.attention_fp8_both(q, k, v, qd, kd, vd, scale, rows=rows)
+def run_fp8_ex(fa2, q, k, v, qd, kd, vd, scale, causal):
+    import torch
+
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to("cuda")
+    o, lse = fa2.fa2_fwd_fp8_ex(dev(q), dev(k), dev(v), dev(qd), dev(kd), dev(vd), scale=scale, causal=causal)
+    assert fa2.fa2_check_status(torch.cuda.current_stream().cuda_stream) == fa2.FA2_OK
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, scale, rows=None, what="", causal=False):
+    om, op, lp, a, b = oracle.attention_fp8_both(q, k, v, qd, kd, vd, scale, rows=rows, causal=causal)
     d = q.shape[-1]
     if rows is not None:
         o = o.reshape(-1, d)[rows]
@@ -49,9 +58,14 @@ def assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, scale, rows=None, what=""):
     bad = err > bound
     assert not bad.any(), f"{what}: {int(bad.sum())} elements beyond the rounding bound, worst ratio " \
                           f"{(err / bound).max():.3g}"
-    rel = np.linalg.norm(o - om) / np.linalg.norm(om)
+    nrm = np.linalg.norm(om)
+    rel = np.linalg.norm(o - om) / nrm if nrm > 0 else np.linalg.norm(o)
     assert rel <= 2.0 ** -7, f"{what}: ||O - O_method|| / ||O_method|| = {rel:.3g}"
-    assert np.max(np.abs(lse.reshape(-1) - lp.reshape(-1))) <= 1e-3, what
+    lse, lp = lse.reshape(-1), lp.reshape(-1)
+    empty = np.isneginf(lp)                 # rows that see no key: o = 0, lse = -inf
+    assert np.array_equal(np.isneginf(lse), empty), what
+    assert not o[empty].any(), what
+    assert np.max(np.abs(lse[~empty] - lp[~empty]), initial=0.0) <= 1e-3, what
     return rel
 
 
@@ -134,3 +148,68 @@ def test_fp8_rejects_unsupported_head_dim(gpu_lib):
     ds = torch.ones(1, dtype=torch.float32, device="cuda")
     with pytest.raises(gpu_lib.FA2Error):
         gpu_lib.fa2_fwd_fp8(q, q, q, ds, ds, ds)
+
+
+# ------------------------------------------------------------ general mode
+
+def fp8_general_inputs(seed, B, Hq, Hkv, nq, nk, amp=1.0):
+    q, _, _, qd, _, _ = gen.make_qkv_fp8(seed, B, Hq, Hkv, nq, 128, amp)
+    _, k, v, _, kd, vd = gen.make_qkv_fp8(seed + 1, B, Hq, Hkv, nk, 128, amp)
+    return q, k, v, qd, kd, vd
+
+
+GEN_CASES = [
+    # B, Hq, Hkv, Nq, Nk, causal
+    (1, 2, 1, 128, 128, True),      # one tile: the diagonal tile only
+    (1, 2, 2, 200, 200, True),      # ragged, causal, two query tiles in one item
+    (2, 4, 2, 300, 500, False),     # unequal lengths, ragged key tail
+    (1, 2, 1, 500, 300, True),      # Nq > Nk: the first 200 rows see no key
+    (1, 1, 1, 1, 1, False),         # one query, one key
+    (1, 2, 1, 1, 700, True),        # one query row (decode) over 700 keys
+    (1, 4, 1, 1000, 1000, True),    # causal over eight key tiles, grouped heads
+    (2, 2, 1, 129, 129, False),     # one row past a tile
+    (1, 2, 1, 640, 384, True),      # items with different KV tile counts per tile
+    (2, 8, 8, 1024, 1024, True),    # 64 items of unequal work on the persistent grid
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,causal", GEN_CASES)
+def test_fp8_general_matches_oracle(gpu_lib, B, Hq, Hkv, Nq, Nk, causal):
+    q, k, v, qd, kd, vd = fp8_general_inputs(7200 + Nq + 3 * Nk + Hq, B, Hq, Hkv, Nq, Nk)
+    scale = 128 ** -0.5
+    o, lse = run_fp8_ex(gpu_lib, q, k, v, qd, kd, vd, scale, causal)
+    assert o.shape == (B, Hq, Nq, 128) and lse.shape == (B, Hq, Nq)
+    assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, scale, causal=causal,
+                      what=f"B{B} Hq{Hq} Hkv{Hkv} Nq{Nq} Nk{Nk} causal{causal}")
+
+
+def test_fp8_general_sharp_softmax_and_zero_descale(gpu_lib):
+    # amp 3: large logits and many rescales under the mask; then a zero k
+    # descale: every score is 0, so each row averages its visible values.
+    q, k, v, qd, kd, vd = fp8_general_inputs(7301, 1, 2, 1, 384, 384, amp=3.0)
+    o, lse = run_fp8_ex(gpu_lib, q, k, v, qd, kd, vd, 0.09, True)
+    assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, 0.09, causal=True, what="causal x3")
+    kd0 = np.zeros_like(kd)
+    o, lse = run_fp8_ex(gpu_lib, q, k, v, qd, kd0, vd, 0.09, True)
+    assert_fp8_parity(o, lse, q, k, v, qd, kd0, vd, 0.09, causal=True, what="k descale 0")
+    assert np.allclose(lse[0, 0], np.log(np.arange(1, 385)), atol=1e-3)
+
+
+def test_fp8_general_equal_lengths_route_to_the_packed_kernel(gpu_lib):
+    # Non-causal, N_q == N_k, N % 128 == 0: fa2_fwd_fp8_ex gives fa2_fwd_fp8's
+    # result bit for bit.
+    q, k, v, qd, kd, vd = gen.make_qkv_fp8(7302, 1, 4, 2, 256, 128)
+    o1, l1 = run_fp8(gpu_lib, q, k, v, qd, kd, vd, 0.1)
+    o2, l2 = run_fp8_ex(gpu_lib, q, k, v, qd, kd, vd, 0.1, False)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_fp8_general_causal_full_size_sampled_rows(gpu_lib):
+    # The FP8 bench workload (B 4, H 16, N 4096) with the causal mask; the
+    # oracle checks a seeded sample of rows plus the first and last row.
+    w = gen.workload("fp8_mha_B4_H16_N4096_d128_e4m3")
+    q, k, v, qd, kd, vd = w.inputs()
+    o, lse = run_fp8_ex(gpu_lib, q, k, v, qd, kd, vd, w.scale, True)
+    total = w.B * w.Hq * w.N
+    rows = np.unique(np.concatenate([np.random.default_rng(6).integers(0, total, 1500), [0, total - 1]]))
+    assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, w.scale, rows=rows, causal=True, what=w.name + " causal")
