@@ -49,8 +49,8 @@ struct Lay {
     static constexpr int kVtOff = kRingOff + kStages * kTile;
     static constexpr int kBarOff = kVtOff + 2 * kTile;
     // q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] alpha[2] stats[2]
-    // p_full[2] o_full[2] mma_done vt_full[2] vt_empty[2]
-    static constexpr int kNumBars = 2 * kStages + 19;
+    // p_full[2] o_full[2] mma_done vt_full[2] vt_empty[2] stats_free[2]
+    static constexpr int kNumBars = 2 * kStages + 21;
     static constexpr int kRowOff = kBarOff + kNumBars * 8;  // alpha[2][128], m[2][128], l[2][128]
     static constexpr int kMiscOff = kRowOff + 3 * kNQ * kBM * 4;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
@@ -76,6 +76,7 @@ struct BarsF8 {
     __device__ uint32_t mma_done() const { return base + 8 * (14 + 2 * S); }
     __device__ uint32_t vt_full(int b) const { return base + 8 * (15 + 2 * S + b); }
     __device__ uint32_t vt_empty(int b) const { return base + 8 * (17 + 2 * S + b); }
+    __device__ uint32_t stats_free(int t) const { return base + 8 * (19 + 2 * S + t); }
 };
 
 enum WaitSiteF8 : int { kSiteVtFull = 11, kSiteVtEmpty = 12 };
@@ -419,7 +420,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
     float* m_buf = alpha_buf + kNQ * kBM;
     float* l_buf = m_buf + kNQ * kBM;
 
-    int n_s = 0;
+    int n_s = 0;      // S tiles consumed; bit 30: item parity (general mode)
     bool ok = true;
     for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
         int nkv, grp, jmask = 0x7fffffff, kend_row = 0;
@@ -442,6 +443,20 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
         // -inf * c = -inf instead of NaN.
         if constexpr (kGen) c = fmaxf(c, 1.17549435e-38f);
         const uint64_t c2 = ptx::f2_pack(c, c);
+        // m and l of the previous item must have been read by the epilogue
+        // before this item's last step overwrites them. With two or more
+        // steps that is already so: S(t, 1) follows PV(t, 0), which waits
+        // for the correction warpgroup's p_full arrival of step 0, which
+        // follows its epilogue of the previous item. A one-step item
+        // (general mode only: the host sends N = 128 there) waits for the
+        // epilogue's stats_free arrival (at once for the first item: a fresh
+        // barrier's preceding phase).
+        if constexpr (kGen) {
+            if (nkv == 1) {
+                ok = w.wait(bars.stats_free(t), ((n_s >> 30) & 1) ^ 1, kSiteStats);
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
+        }
         float m = -INFINITY;
         float l = 0.0f;       // sum of the unrounded 2^8-scaled weights
         for (int j = 0; j < nkv; ++j, ++n_s) {
@@ -536,6 +551,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
             ptx::tc_fence_before();
             ptx::mbar_arrive(bars.p_full(t));
         }
+        if constexpr (kGen) n_s ^= 1 << 30;    // item parity (stats_free phase)
     }
 }
 
@@ -637,6 +653,7 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
             ptx::tc_fence_after();
             const float m = rowbuf[(2 + t) * kBM + row];
             const float l = rowbuf[(4 + t) * kBM + row];
+            if constexpr (kGen) ptx::mbar_arrive(bars.stats_free(t));   // m, l read: may be overwritten
             // l' = 0 only for a row with no allowed key: O = 0, LSE = -inf.
             const float f = (!kGen || l > 0.0f) ? dv * ptx::rcp_approx(l) : 0.0f;
             const uint32_t colO = Lay::col_o(t);
@@ -691,6 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bars.s_full(t), 1);
             ptx::mbar_init(bars.alpha_ready(t), kBM);
             ptx::mbar_init(bars.stats_ready(t), kBM);
+            ptx::mbar_init(bars.stats_free(t), kBM);   // the epilogue's threads have read m, l
             ptx::mbar_init(bars.p_full(t), 2 * kBM);
             ptx::mbar_init(bars.o_full(t), 1);
             ptx::mbar_init(bars.vt_full(t), 2);    // one arrival per transposer warp

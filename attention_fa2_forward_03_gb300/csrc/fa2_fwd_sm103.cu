@@ -161,6 +161,100 @@ fa2_status launch_fp8(int dev, const CUtensorMap& mq, const CUtensorMap& mk, con
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
+// The general-mode kernel (any lengths, optional causal mask) on checked
+// arguments. Also takes equal-length calls with N = 128, whose items have a
+// single KV tile: the kernels' equal-length mode relies on every item
+// having two or more.
+fa2_status fwd_general(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q, int H_kv,
+                       int N_q, int N_k, int d, float scale, int causal, fa2_dtype dtype, cudaStream_t stream) {
+    const long long heads_q = static_cast<long long>(B) * H_q;
+    const long long rows_q = heads_q * N_q;
+    const long long rows_kv = static_cast<long long>(B) * H_kv * N_k;
+    const long long tq = (N_q + fa2::kBM - 1) / fa2::kBM;
+    const long long items = heads_q * ((tq + fa2::kNQ - 1) / fa2::kNQ);
+    if (rows_q > 0x7FFFFFFFLL || rows_kv > 0x7FFFFFFFLL || items > 0x7FFFFFFFLL) return FA2_ERR_UNSUPPORTED;
+
+    int dev = 0;
+    fa2_status st = check_device(&dev);
+    if (st != FA2_OK) return st;
+    if ((st = get_encoder()) != FA2_OK) return st;
+
+    CUtensorMap mq, mk, mv;
+    if (encode_map_3d(&mq, q, static_cast<uint64_t>(heads_q), static_cast<uint64_t>(N_q), d) != FA2_OK ||
+        encode_map_3d(&mk, k, static_cast<uint64_t>(B) * H_kv, static_cast<uint64_t>(N_k), d) != FA2_OK ||
+        encode_map_3d(&mv, v, static_cast<uint64_t>(B) * H_kv, static_cast<uint64_t>(N_k), d) != FA2_OK)
+        return FA2_ERR_CUDA;
+
+    Params p{};
+    p.o = o;
+    p.lse = lse;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    p.debug_flags = g_debug_flags.load();
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.nq = N_q;
+    p.nk = N_k;
+    p.causal = causal;
+    p.heads_q = static_cast<int>(heads_q);
+    p.hq = H_q;
+    p.group = H_q / H_kv;
+    p.tq = static_cast<int>(tq);
+    p.pairs = static_cast<int>((tq + fa2::kNQ - 1) / fa2::kNQ);
+    p.total_items = static_cast<int>(items);
+    const dim3 grid(static_cast<unsigned>(std::min<long long>(items, g_dev[dev].sm_count)));
+
+    const bool bf = dtype == FA2_BF16;
+    if (d == 128)
+        return bf ? launch<128, true, true>(dev, mq, mk, mv, p, grid, stream)
+                  : launch<128, false, true>(dev, mq, mk, mv, p, grid, stream);
+    return bf ? launch<64, true, true>(dev, mq, mk, mv, p, grid, stream)
+              : launch<64, false, true>(dev, mq, mk, mv, p, grid, stream);
+}
+
+// FP8 counterpart of fwd_general (d = 128).
+fa2_status fwd_fp8_general(const void* q, const void* k, const void* v, const float* q_descale,
+                           const float* k_descale, const float* v_descale, void* o, float* lse, int B, int H_q,
+                           int H_kv, int N_q, int N_k, float scale, int causal, cudaStream_t stream) {
+    const long long heads_q = static_cast<long long>(B) * H_q;
+    const long long rows_q = heads_q * N_q;
+    const long long rows_kv = static_cast<long long>(B) * H_kv * N_k;
+    const long long tq = (N_q + fa2::kBM - 1) / fa2::kBM;
+    const long long items = heads_q * ((tq + fa2::kNQ - 1) / fa2::kNQ);
+    if (rows_q > 0x7FFFFFFFLL || rows_kv > 0x7FFFFFFFLL || items > 0x7FFFFFFFLL) return FA2_ERR_UNSUPPORTED;
+
+    int dev = 0;
+    fa2_status st = check_device(&dev);
+    if (st != FA2_OK) return st;
+    if ((st = get_encoder()) != FA2_OK) return st;
+
+    CUtensorMap mq, mk, mv;
+    const uint64_t hkv = static_cast<uint64_t>(B) * H_kv;
+    if (encode_map_u8_3d(&mq, q, static_cast<uint64_t>(heads_q), static_cast<uint64_t>(N_q)) != FA2_OK ||
+        encode_map_u8_3d(&mk, k, hkv, static_cast<uint64_t>(N_k)) != FA2_OK ||
+        encode_map_u8_3d(&mv, v, hkv, static_cast<uint64_t>(N_k)) != FA2_OK)
+        return FA2_ERR_CUDA;
+
+    Params p{};
+    p.o = o;
+    p.lse = lse;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    p.debug_flags = g_debug_flags.load();
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.nq = N_q;
+    p.nk = N_k;
+    p.causal = causal;
+    p.heads_q = static_cast<int>(heads_q);
+    p.hq = H_q;
+    p.group = H_q / H_kv;
+    p.tq = static_cast<int>(tq);
+    p.pairs = static_cast<int>((tq + fa2::kNQ - 1) / fa2::kNQ);
+    p.total_items = static_cast<int>(items);
+    p.q_descale = q_descale;
+    p.k_descale = k_descale;
+    p.v_descale = v_descale;
+    const dim3 grid(static_cast<unsigned>(std::min<long long>(items, g_dev[dev].sm_count)));
+    return launch_fp8<true>(dev, mq, mk, mv, p, grid, stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -176,6 +270,7 @@ fa2_status fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, flo
     if (dtype != FA2_BF16 && dtype != FA2_FP16) return FA2_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return FA2_ERR_UNSUPPORTED;
     if (N % fa2::kBM != 0) return FA2_ERR_UNSUPPORTED;
+    if (N == fa2::kBN) return fwd_general(q, k, v, o, lse, B, H_q, H_kv, N, N, d, scale, 0, dtype, stream);
     // TMA coordinates and row indices are 32-bit.
     const long long rows_q = static_cast<long long>(B) * H_q * N;
     const long long groups = static_cast<long long>(B) * H_kv;
@@ -226,6 +321,8 @@ fa2_status fa2_fwd_fp8(const void* q, const void* k, const void* v, const float*
     if (!std::isfinite(scale) || !(scale > 0.0f)) return FA2_ERR_INVALID_ARG;
     if (d != fa2::fp8::kD) return FA2_ERR_UNSUPPORTED;
     if (N % fa2::kBM != 0) return FA2_ERR_UNSUPPORTED;
+    if (N == fa2::kBN)
+        return fwd_fp8_general(q, k, v, q_descale, k_descale, v_descale, o, lse, B, H_q, H_kv, N, N, scale, 0, stream);
     const long long rows_q = static_cast<long long>(B) * H_q * N;
     const long long groups = static_cast<long long>(B) * H_kv;
     if (rows_q > 0x7FFFFFFFLL) return FA2_ERR_UNSUPPORTED;
@@ -274,45 +371,8 @@ fa2_status fa2_fwd_fp8_ex(const void* q, const void* k, const void* v, const flo
     // The plain case is the multiple-of-128 kernel.
     if (!causal && N_q == N_k && N_q % fa2::kBM == 0)
         return fa2_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, o, lse, B, H_q, H_kv, N_q, d, scale, stream);
-    const long long heads_q = static_cast<long long>(B) * H_q;
-    const long long rows_q = heads_q * N_q;
-    const long long rows_kv = static_cast<long long>(B) * H_kv * N_k;
-    const long long tq = (N_q + fa2::kBM - 1) / fa2::kBM;
-    const long long items = heads_q * ((tq + fa2::kNQ - 1) / fa2::kNQ);
-    if (rows_q > 0x7FFFFFFFLL || rows_kv > 0x7FFFFFFFLL || items > 0x7FFFFFFFLL) return FA2_ERR_UNSUPPORTED;
-
-    int dev = 0;
-    fa2_status st = check_device(&dev);
-    if (st != FA2_OK) return st;
-    if ((st = get_encoder()) != FA2_OK) return st;
-
-    CUtensorMap mq, mk, mv;
-    const uint64_t hkv = static_cast<uint64_t>(B) * H_kv;
-    if (encode_map_u8_3d(&mq, q, static_cast<uint64_t>(heads_q), static_cast<uint64_t>(N_q)) != FA2_OK ||
-        encode_map_u8_3d(&mk, k, hkv, static_cast<uint64_t>(N_k)) != FA2_OK ||
-        encode_map_u8_3d(&mv, v, hkv, static_cast<uint64_t>(N_k)) != FA2_OK)
-        return FA2_ERR_CUDA;
-
-    Params p{};
-    p.o = o;
-    p.lse = lse;
-    p.wait_limit_ns = g_wait_limit_ns.load();
-    p.debug_flags = g_debug_flags.load();
-    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
-    p.nq = N_q;
-    p.nk = N_k;
-    p.causal = causal;
-    p.heads_q = static_cast<int>(heads_q);
-    p.hq = H_q;
-    p.group = H_q / H_kv;
-    p.tq = static_cast<int>(tq);
-    p.pairs = static_cast<int>((tq + fa2::kNQ - 1) / fa2::kNQ);
-    p.total_items = static_cast<int>(items);
-    p.q_descale = q_descale;
-    p.k_descale = k_descale;
-    p.v_descale = v_descale;
-    const dim3 grid(static_cast<unsigned>(std::min<long long>(items, g_dev[dev].sm_count)));
-    return launch_fp8<true>(dev, mq, mk, mv, p, grid, stream);
+    return fwd_fp8_general(q, k, v, q_descale, k_descale, v_descale, o, lse, B, H_q, H_kv, N_q, N_k, scale, causal,
+                           stream);
 }
 
 fa2_status fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
@@ -335,47 +395,7 @@ fa2_status fa2_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
     // The plain case is the multiple-of-128 kernel.
     if (!causal && N_q == N_k && N_q % fa2::kBM == 0)
         return fa2_fwd_gqa(q, k, v, o, lse, B, H_q, H_kv, N_q, d, scale, dtype, stream);
-    const long long heads_q = static_cast<long long>(B) * H_q;
-    const long long rows_q = heads_q * N_q;
-    const long long rows_kv = static_cast<long long>(B) * H_kv * N_k;
-    const long long tq = (N_q + fa2::kBM - 1) / fa2::kBM;
-    const long long items = heads_q * ((tq + fa2::kNQ - 1) / fa2::kNQ);
-    if (rows_q > 0x7FFFFFFFLL || rows_kv > 0x7FFFFFFFLL || items > 0x7FFFFFFFLL) return FA2_ERR_UNSUPPORTED;
-
-    int dev = 0;
-    fa2_status st = check_device(&dev);
-    if (st != FA2_OK) return st;
-    if ((st = get_encoder()) != FA2_OK) return st;
-
-    CUtensorMap mq, mk, mv;
-    if (encode_map_3d(&mq, q, static_cast<uint64_t>(heads_q), static_cast<uint64_t>(N_q), d) != FA2_OK ||
-        encode_map_3d(&mk, k, static_cast<uint64_t>(B) * H_kv, static_cast<uint64_t>(N_k), d) != FA2_OK ||
-        encode_map_3d(&mv, v, static_cast<uint64_t>(B) * H_kv, static_cast<uint64_t>(N_k), d) != FA2_OK)
-        return FA2_ERR_CUDA;
-
-    Params p{};
-    p.o = o;
-    p.lse = lse;
-    p.wait_limit_ns = g_wait_limit_ns.load();
-    p.debug_flags = g_debug_flags.load();
-    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
-    p.nq = N_q;
-    p.nk = N_k;
-    p.causal = causal;
-    p.heads_q = static_cast<int>(heads_q);
-    p.hq = H_q;
-    p.group = H_q / H_kv;
-    p.tq = static_cast<int>(tq);
-    p.pairs = static_cast<int>((tq + fa2::kNQ - 1) / fa2::kNQ);
-    p.total_items = static_cast<int>(items);
-    const dim3 grid(static_cast<unsigned>(std::min<long long>(items, g_dev[dev].sm_count)));
-
-    const bool bf = dtype == FA2_BF16;
-    if (d == 128)
-        return bf ? launch<128, true, true>(dev, mq, mk, mv, p, grid, stream)
-                  : launch<128, false, true>(dev, mq, mk, mv, p, grid, stream);
-    return bf ? launch<64, true, true>(dev, mq, mk, mv, p, grid, stream)
-              : launch<64, false, true>(dev, mq, mk, mv, p, grid, stream);
+    return fwd_general(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, scale, causal, dtype, stream);
 }
 
 fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

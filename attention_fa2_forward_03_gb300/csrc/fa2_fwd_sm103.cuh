@@ -104,8 +104,8 @@ struct Layout {
     static constexpr int kRingOff = kNQ * kTileBytes;
     static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
     // q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] alpha[2] stats[2]
-    // p_full[2] o_full[2] mma_done
-    static constexpr int kNumBars = 2 * kStages + 15;
+    // p_full[2] o_full[2] mma_done stats_free[2]
+    static constexpr int kNumBars = 2 * kStages + 17;
     static constexpr int kRowOff = kBarOff + kNumBars * 8;   // per-row floats
     // alpha[2][128], m[2][128], l[2][128]
     static constexpr int kMiscOff = kRowOff + 3 * kNQ * kBM * 4;
@@ -168,6 +168,7 @@ struct Bars {
     __device__ uint32_t p_full(int t) const { return base + 8 * (10 + 2 * S + t); }
     __device__ uint32_t o_full(int t) const { return base + 8 * (12 + 2 * S + t); }
     __device__ uint32_t mma_done() const { return base + 8 * (14 + 2 * S); }
+    __device__ uint32_t stats_free(int t) const { return base + 8 * (15 + 2 * S + t); }
 };
 
 // One work item: two packed query tiles of one KV head.
@@ -551,7 +552,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
     const float c = p.scale_log2;
     const uint64_t c2 = ptx::f2_pack(c, c);
 
-    int n_s = 0;       // S tiles consumed (s_full / alpha / p_full phases)
+    int n_s = 0;       // S tiles consumed (s_full / alpha / p_full phases); bit 30: item parity (general mode)
     bool ok = true;
     for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
         int nkv, jmask = 0x7fffffff, kend_row = 0;
@@ -564,6 +565,20 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
         } else {
             if (t >= make_item(p, it).n_tiles) continue;
             nkv = p.n_kv_tiles;
+        }
+        // m and l of the previous item must have been read by the epilogue
+        // before this item's last step overwrites them. With two or more
+        // steps that is already so: S(t, 1) follows PV(t, 0), which waits
+        // for the correction warpgroup's p_full arrival of step 0, which
+        // follows its epilogue of the previous item. A one-step item
+        // (general mode only: the host sends N = 128 there) waits for the
+        // epilogue's stats_free arrival (at once for the first item: a fresh
+        // barrier's preceding phase).
+        if constexpr (kGen) {
+            if (nkv == 1) {
+                ok = w.wait(bars.stats_free(t), ((n_s >> 30) & 1) ^ 1, kSiteStats);
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
         }
         float m = -INFINITY;  // running row max of the scaled scores, log2 units
         float l = 0.0f;       // running sum of exp2(s*c - m)
@@ -661,6 +676,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
             ptx::tc_fence_before();
             ptx::mbar_arrive(bars.p_full(t));
         }
+        if constexpr (kGen) n_s ^= 1 << 30;    // item parity (stats_free phase)
     }
 }
 
@@ -765,6 +781,7 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
             ptx::tc_fence_after();
             const float m = rowbuf[(2 + t) * kBM + row];
             const float l = rowbuf[(4 + t) * kBM + row];
+            if constexpr (kGen) ptx::mbar_arrive(bars.stats_free(t));   // m, l read: may be overwritten
             // l = 0 only for a row with no allowed key: O = 0, LSE = -inf.
             const float inv_l = (!kGen || l > 0.0f) ? ptx::rcp_approx(l) : 0.0f;
             const uint32_t colO = L::col_o(t);
@@ -816,6 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bars.s_full(t), 1);
             ptx::mbar_init(bars.alpha_ready(t), kBM);
             ptx::mbar_init(bars.stats_ready(t), kBM);
+            ptx::mbar_init(bars.stats_free(t), kBM);   // the epilogue's threads have read m, l
             ptx::mbar_init(bars.p_full(t), 2 * kBM);  // softmax + correction warpgroups
             ptx::mbar_init(bars.o_full(t), 1);
         }

@@ -213,3 +213,18 @@ def test_fp8_general_causal_full_size_sampled_rows(gpu_lib):
     total = w.B * w.Hq * w.N
     rows = np.unique(np.concatenate([np.random.default_rng(6).integers(0, total, 1500), [0, total - 1]]))
     assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, w.scale, rows=rows, causal=True, what=w.name + " causal")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_many_short_items_per_cta(gpu_lib, causal):
+    # 512 short items (one or two KV tiles) on at most 152 CTAs: several items
+    # per CTA, so the epilogue's statistics slots alternate every item. Five
+    # launches agree bit for bit and with the oracle.
+    B, Hq, Hkv, N = (4, 128, 128, 256) if causal else (4, 256, 128, 128)
+    q, k, v, qd, kd, vd = gen.make_qkv_fp8(7400 + int(causal), B, Hq, Hkv, N, 128)
+    scale = 128 ** -0.5
+    o, lse = run_fp8_ex(gpu_lib, q, k, v, qd, kd, vd, scale, causal)
+    assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, scale, causal=causal, what=f"512 short items causal={causal}")
+    for _ in range(4):
+        o2, l2 = run_fp8_ex(gpu_lib, q, k, v, qd, kd, vd, scale, causal)
+        assert np.array_equal(o2, o) and np.array_equal(l2, lse)

@@ -292,3 +292,19 @@ def test_full_size_workloads(gpu_lib, w):
     rows = sample_rows(w.B, w.Hq, w.N, 160, seed=w.seed)
     check_rows(o, lse, q, k, v, w.dtype, w.scale, rows, w.name)
     check_convex_hull(o, v, w.Hq)
+
+
+def test_many_single_tile_items_per_cta(gpu_lib):
+    # 512 items of one KV tile each (two packed query tiles per item) on at
+    # most 152 CTAs: every CTA runs several items back to back, so the
+    # per-row statistics handed to the epilogue alternate between their two
+    # slots every item. Five launches must agree bit for bit and with the
+    # oracle.
+    B, Hq, Hkv, N, d = 4, 256, 128, 128, 128
+    q, k, v = gen.make_qkv(1401, B, Hq, Hkv, N, d, gen.BF16)
+    scale = d ** -0.5
+    o, lse = full_check(gpu_lib, q, k, v, gen.BF16, scale, what="512 one-tile items")
+    o0, l0 = o.float().cpu().numpy(), lse.cpu().numpy()
+    for _ in range(4):
+        o, lse = run_gpu(gpu_lib, q, k, v, gen.BF16, scale)
+        assert np.array_equal(o.float().cpu().numpy(), o0) and np.array_equal(lse.cpu().numpy(), l0)
