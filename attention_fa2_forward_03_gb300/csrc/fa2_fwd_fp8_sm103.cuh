@@ -131,7 +131,7 @@ __device__ __forceinline__ void producer_gen(const CUtensorMap* tmQ, const CUten
     int ring = 0;
     int nq[2] = {0, 0};
     bool ok = true;
-    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+    for (int it = blockIdx.x; it < p.total_items && ok; it = next_item<true>(it)) {
         const ItemG g = make_item_gen(p, it);
         for (int t = 0; t < g.n_tiles && ok; ++t) {
             if (g.nkv[t] == 0) continue;
@@ -218,7 +218,7 @@ __device__ __forceinline__ void xpose_role(const Params& p, uint8_t* smem, const
     int ring = 0;   // K/V ring items (same sequence as the producer's)
     int nv = 0;     // V tiles transposed
     bool ok = true;
-    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+    for (int it = blockIdx.x; it < p.total_items && ok; it = next_item<kGen>(it)) {
         int nkv = p.n_kv_tiles;   // KV tiles the item loads
         if constexpr (kGen) {
             const ItemG g = make_item_gen(p, it);
@@ -353,7 +353,7 @@ __device__ __forceinline__ void mma_issuer_gen(const Params& p, uint32_t sbase, 
     int nq[2] = {0, 0};
     int np[2] = {0, 0};
     bool ok = true;
-    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+    for (int it = blockIdx.x; it < p.total_items && ok; it = next_item<true>(it)) {
         const ItemG g = make_item_gen(p, it);
         const int nmax = max(g.nkv[0], g.nkv[1]);
         if (nmax == 0) continue;
@@ -422,7 +422,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
 
     int n_s = 0;      // S tiles consumed; bit 30: item parity (general mode)
     bool ok = true;
-    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+    for (int it = blockIdx.x; it < p.total_items && ok; it = next_item<kGen>(it)) {
         int nkv, grp, jmask = 0x7fffffff, kend_row = 0;
         if constexpr (kGen) {
             const ItemG g = make_item_gen(p, it);
@@ -570,7 +570,7 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
     int n_s[2] = {0, 0};
     int n_items[2] = {0, 0};
     bool ok = true;
-    for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
+    for (int it = blockIdx.x; it < p.total_items && ok; it = next_item<kGen>(it)) {
         // row0: first row of tile 0 in the output view; q0: the same row's
         // index within its head (general mode, for the ragged-end check).
         int n_tiles, nkv[2], row0, q0 = 0, grp;

@@ -172,7 +172,9 @@ fa2_status fwd_general(const void* q, const void* k, const void* v, void* o, flo
     const long long rows_kv = static_cast<long long>(B) * H_kv * N_k;
     const long long tq = (N_q + fa2::kBM - 1) / fa2::kBM;
     const long long items = heads_q * ((tq + fa2::kNQ - 1) / fa2::kNQ);
-    if (rows_q > 0x7FFFFFFFLL || rows_kv > 0x7FFFFFFFLL || items > 0x7FFFFFFFLL) return FA2_ERR_UNSUPPORTED;
+    // Item indices stay below 2^31 - 4096 so that a CTA's next index (at most
+    // two grids further) never overflows.
+    if (rows_q > 0x7FFFFFFFLL || rows_kv > 0x7FFFFFFFLL || items > 0x7FFFFFFFLL - 4096) return FA2_ERR_UNSUPPORTED;
 
     int dev = 0;
     fa2_status st = check_device(&dev);
@@ -219,7 +221,9 @@ fa2_status fwd_fp8_general(const void* q, const void* k, const void* v, const fl
     const long long rows_kv = static_cast<long long>(B) * H_kv * N_k;
     const long long tq = (N_q + fa2::kBM - 1) / fa2::kBM;
     const long long items = heads_q * ((tq + fa2::kNQ - 1) / fa2::kNQ);
-    if (rows_q > 0x7FFFFFFFLL || rows_kv > 0x7FFFFFFFLL || items > 0x7FFFFFFFLL) return FA2_ERR_UNSUPPORTED;
+    // Item indices stay below 2^31 - 4096 so that a CTA's next index (at most
+    // two grids further) never overflows.
+    if (rows_q > 0x7FFFFFFFLL || rows_kv > 0x7FFFFFFFLL || items > 0x7FFFFFFFLL - 4096) return FA2_ERR_UNSUPPORTED;
 
     int dev = 0;
     fa2_status st = check_device(&dev);
