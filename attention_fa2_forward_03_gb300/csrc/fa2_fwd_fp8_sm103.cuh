@@ -294,14 +294,16 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint
             const bool more = j + 1 < nkv;
             ++ring;                       // V_j: released by the transposer
             const int vb = nv & 1;
-            if (!(ok = wait_u(bars.vt_full(vb), (nv >> 1) & 1, kSiteVtFull))) break;
+            if (more) k_ring = ring++;
+            // V^T_j, K_{j+1} and P(0, j) are waited for together.
+            const uint32_t wb[3] = {bars.vt_full(vb), more ? bars.kv_full(k_ring % S) : bars.vt_full(vb), bars.p_full(0)};
+            const uint32_t wp[3] = {static_cast<uint32_t>((nv >> 1) & 1),
+                                    static_cast<uint32_t>(more ? (k_ring / S) & 1 : (nv >> 1) & 1),
+                                    static_cast<uint32_t>(np[0] & 1)};
+            if (!(ok = __shfl_sync(0xffffffffu, w.wait_all<3>(wb, wp, kSiteVtFull) ? 1 : 0, 0) != 0)) break;
             ++nv;
-            if (more) {
-                k_ring = ring++;
-                if (!(ok = wait_ring(k_ring))) break;
-            }
             for (int t = 0; t < nt; ++t) {
-                if (!(ok = wait_u(bars.p_full(t), np[t] & 1, kSitePFull))) break;
+                if (t > 0 && !(ok = wait_u(bars.p_full(t), np[t] & 1, kSitePFull))) break;
                 ++np[t];
                 ptx::tc_fence_after();
                 issue_pv(t, vb, j > 0);
@@ -374,17 +376,20 @@ __device__ __forceinline__ void mma_issuer_gen(const Params& p, uint32_t sbase, 
             const bool more = j + 1 < nmax;
             ++ring;                       // V_j: released by the transposer
             const int vb = nv & 1;
-            if (!(ok = wait_u(bars.vt_full(vb), (nv >> 1) & 1, kSiteVtFull))) break;
+            if (more) k_ring = ring++;
+            // V^T_j, K_{j+1} and P of the first tile taking part, together.
+            const int t0 = j < g.nkv[0] ? 0 : 1;
+            const uint32_t wb[3] = {bars.vt_full(vb), more ? bars.kv_full(k_ring % S) : bars.vt_full(vb), bars.p_full(t0)};
+            const uint32_t wp[3] = {static_cast<uint32_t>((nv >> 1) & 1),
+                                    static_cast<uint32_t>(more ? (k_ring / S) & 1 : (nv >> 1) & 1),
+                                    static_cast<uint32_t>(np[t0] & 1)};
+            if (!(ok = __shfl_sync(0xffffffffu, w.wait_all<3>(wb, wp, kSiteVtFull) ? 1 : 0, 0) != 0)) break;
             ++nv;
-            if (more) {
-                k_ring = ring++;
-                if (!(ok = wait_ring(k_ring))) break;
-            }
             const int last_v = j < g.nkv[1] ? 1 : 0;                 // last tile reading V^T_j
             const int last_k = (more && j + 1 < g.nkv[1]) ? 1 : 0;   // last tile reading K_{j+1}
             for (int t = 0; t < 2; ++t) {
                 if (j >= g.nkv[t]) continue;
-                if (!(ok = wait_u(bars.p_full(t), np[t] & 1, kSitePFull))) break;
+                if (t != t0 && !(ok = wait_u(bars.p_full(t), np[t] & 1, kSitePFull))) break;
                 ++np[t];
                 ptx::tc_fence_after();
                 issue_pv(t, vb, j > 0);

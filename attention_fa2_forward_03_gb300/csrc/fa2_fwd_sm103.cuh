@@ -140,6 +140,38 @@ struct Waiter {
         }
     }
 
+    // Waits for N phases at once: the N tests are in flight together, so a
+    // slow test of one barrier does not delay the others (a test issued
+    // while the tensor core streams its operands from shared memory can
+    // take hundreds of cycles).
+    template <int N>
+    __device__ __forceinline__ bool wait_all(const uint32_t (&bar)[N], const uint32_t (&parity)[N], int site) const {
+        bool d[N];
+        bool all = true;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            d[i] = ptx::mbar_try_wait(bar[i], parity[i]);
+            all = all && d[i];
+        }
+        if (all) return true;
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (true) {
+            all = true;
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                if (!d[i]) d[i] = ptx::mbar_try_wait(bar[i], parity[i]);
+                all = all && d[i];
+            }
+            if (all) return true;
+            if (*abort_flag) return false;
+            if (static_cast<long long>(ptx::globaltimer_ns() - t0) > limit_ns) {
+                *abort_flag = 1;
+                atomicCAS(&g_fa2_status, 0, FA2_ERR_TIMEOUT | (site << 8));
+                return false;
+            }
+        }
+    }
+
     // Same, ignoring the abort flag: used to let in-flight copies land
     // before an aborting CTA exits.
     __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
@@ -374,15 +406,16 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint
         for (int j = 0; j < nkv; ++j) {
             const bool more = j + 1 < nkv;
             const int v_ring = ring++;
-            if (!(ok = wait_ring(v_ring))) break;
-            // K_{j+1} is waited for here, before P, so nothing but the MMAs
-            // sits between P becoming ready and the next QK being issued.
-            if (more) {
-                k_ring = ring++;
-                if (!(ok = wait_ring(k_ring))) break;
-            }
+            if (more) k_ring = ring++;
+            // V_j, K_{j+1} and P(0, j) are waited for together, so nothing
+            // but the MMAs sits between P becoming ready and the next QK.
+            const int kr = more ? k_ring : v_ring;
+            const uint32_t wb[3] = {bars.kv_full(v_ring % S), bars.kv_full(kr % S), bars.p_full(0)};
+            const uint32_t wp[3] = {static_cast<uint32_t>((v_ring / S) & 1), static_cast<uint32_t>((kr / S) & 1),
+                                    static_cast<uint32_t>(np[0] & 1)};
+            if (!(ok = __shfl_sync(0xffffffffu, w.wait_all<3>(wb, wp, kSiteKvFull) ? 1 : 0, 0) != 0)) break;
             for (int t = 0; t < nt; ++t) {
-                if (!(ok = wait_u(bars.p_full(t), np[t] & 1, kSitePFull))) break;
+                if (t > 0 && !(ok = wait_u(bars.p_full(t), np[t] & 1, kSitePFull))) break;
                 ++np[t];
                 ptx::tc_fence_after();
                 issue_pv(t, stage_addr(v_ring), j > 0);
@@ -504,16 +537,19 @@ __device__ __forceinline__ void mma_issuer_gen(const Params& p, uint32_t sbase, 
         for (int j = 0; j < nmax; ++j) {
             const bool more = j + 1 < nmax;
             const int v_ring = ring++;
-            if (!(ok = wait_ring(v_ring))) break;
-            if (more) {
-                k_ring = ring++;
-                if (!(ok = wait_ring(k_ring))) break;
-            }
+            if (more) k_ring = ring++;
+            // V_j, K_{j+1} and P of the first tile taking part, together.
+            const int t0 = j < g.nkv[0] ? 0 : 1;
+            const int kr = more ? k_ring : v_ring;
+            const uint32_t wb[3] = {bars.kv_full(v_ring % S), bars.kv_full(kr % S), bars.p_full(t0)};
+            const uint32_t wp[3] = {static_cast<uint32_t>((v_ring / S) & 1), static_cast<uint32_t>((kr / S) & 1),
+                                    static_cast<uint32_t>(np[t0] & 1)};
+            if (!(ok = __shfl_sync(0xffffffffu, w.wait_all<3>(wb, wp, kSiteKvFull) ? 1 : 0, 0) != 0)) break;
             const int last_v = j < g.nkv[1] ? 1 : 0;                 // last tile reading V_j
             const int last_k = (more && j + 1 < g.nkv[1]) ? 1 : 0;   // last tile reading K_{j+1}
             for (int t = 0; t < 2; ++t) {
                 if (j >= g.nkv[t]) continue;
-                if (!(ok = wait_u(bars.p_full(t), np[t] & 1, kSitePFull))) break;
+                if (t != t0 && !(ok = wait_u(bars.p_full(t), np[t] & 1, kSitePFull))) break;
                 ++np[t];
                 ptx::tc_fence_after();
                 issue_pv(t, stage_addr(v_ring), j > 0);
