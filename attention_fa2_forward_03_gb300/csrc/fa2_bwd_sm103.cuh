@@ -288,9 +288,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_s(0);
             s_issued = 1;
         }
+        bool do_seen = false;   // dO(n) observed landed while waiting for dS^T(n-1)
         for (int n = 0; n < steps && ok; ++n) {
             // dP^T = V dO(n)^T
-            if (!(ok = wait_u(bars.do_full(n % DS), (n / DS) & 1, kSiteKvFull))) break;
+            if (!do_seen && !(ok = wait_u(bars.do_full(n % DS), (n / DS) & 1, kSiteKvFull))) break;
             ptx::tc_fence_after();
             qk_kloop<D>(tmem + L::kColDP, vdesc, ptx::desc_sw128(do_addr(n), 16, 1024), kIdT);
             ptx::tc_commit_elect(bars.dp_full());
@@ -313,8 +314,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++s_issued;
                 }
             }
-            // dK += dS^T Q once dS^T is; Q(n) is then free
-            if (!(ok = wait_u(bars.ds_full(), n & 1, kSitePFull))) break;
+            // dK += dS^T Q once dS^T is; Q(n) is then free. The wait also
+            // tests whether dO(n+1) has landed, so that the next step's
+            // dP^T needs no separate wait.
+            do_seen = n + 1 >= steps;
+            ok = __shfl_sync(0xffffffffu,
+                             w.wait_and_test(bars.ds_full(), n & 1, kSitePFull, bars.do_full((n + 1) % DS),
+                                             ((n + 1) / DS) & 1, do_seen) ? 1 : 0, 0) != 0;
+            do_seen = __all_sync(0xffffffffu, do_seen);
+            if (!ok) break;
             ptx::tc_fence_after();
             ptx::mma_ts_kloop8_split(tmem + L::kColAcc1, tmem + L::kColDP, ptx::desc_sw128(q_addr(n), L::kBlkBytes, 1024),
                                      kIdA, n > 0 ? 1u : 0u);
@@ -592,9 +600,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_s(0);
             s_issued = 1;
         }
+        bool v_seen = false;   // V(n) observed landed while waiting for dS(n-1)
         for (int n = 0; n < steps && ok; ++n) {
             // dP = dO V(n)^T; V(n) is then free
-            if (!(ok = wait_u(bars.v_full(n % VS), (n / VS) & 1, kSiteKvFull))) break;
+            if (!v_seen && !(ok = wait_u(bars.v_full(n % VS), (n / VS) & 1, kSiteKvFull))) break;
             ptx::tc_fence_after();
             qk_kloop<D>(tmem + L::kColDP, dodesc, ptx::desc_sw128(v_addr(n), 16, 1024), kIdS);
             ptx::tc_commit_elect(bars.dp_full());
@@ -611,8 +620,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // dQ += dS K once dS is in TMEM (16-bit over the dP columns; K as
-            // the MN-major B operand); K(n) is then free
-            if (!(ok = wait_u(bars.ds_full(), n & 1, kSitePFull))) break;
+            // the MN-major B operand); K(n) is then free. The wait also tests
+            // whether V(n+1) has landed (see the dK/dV kernel).
+            v_seen = n + 1 >= steps;
+            ok = __shfl_sync(0xffffffffu,
+                             w.wait_and_test(bars.ds_full(), n & 1, kSitePFull, bars.v_full((n + 1) % VS),
+                                             ((n + 1) / VS) & 1, v_seen) ? 1 : 0, 0) != 0;
+            v_seen = __all_sync(0xffffffffu, v_seen);
+            if (!ok) break;
             ptx::tc_fence_after();
             ptx::mma_ts_kloop8_split(tmem + L::kColAcc, tmem + L::kColDP, ptx::desc_sw128(k_addr(n), L::kBlkBytes, 1024),
                                      kIdQ, n > 0 ? 1u : 0u);

@@ -172,6 +172,27 @@ struct Waiter {
         }
     }
 
+    // Waits for phase `parity` of `bar`; meanwhile tests phase `tparity` of
+    // `tbar` too, without waiting for it, and sets `seen` once it is
+    // complete (so a later wait for it can be skipped).
+    __device__ __forceinline__ bool wait_and_test(uint32_t bar, uint32_t parity, int site, uint32_t tbar,
+                                                  uint32_t tparity, bool& seen) const {
+        bool done = ptx::mbar_try_wait(bar, parity);
+        if (!seen) seen = ptx::mbar_test_wait(tbar, tparity);
+        if (done) return true;
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (true) {
+            if (ptx::mbar_try_wait(bar, parity)) return true;
+            if (!seen) seen = ptx::mbar_test_wait(tbar, tparity);
+            if (*abort_flag) return false;
+            if (static_cast<long long>(ptx::globaltimer_ns() - t0) > limit_ns) {
+                *abort_flag = 1;
+                atomicCAS(&g_fa2_status, 0, FA2_ERR_TIMEOUT | (site << 8));
+                return false;
+            }
+        }
+    }
+
     // Same, ignoring the abort flag: used to let in-flight copies land
     // before an aborting CTA exits.
     __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
