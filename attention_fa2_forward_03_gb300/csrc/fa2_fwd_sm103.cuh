@@ -140,10 +140,11 @@ struct Waiter {
         }
     }
 
-    // Waits for N phases at once: the N tests are in flight together, so a
-    // slow test of one barrier does not delay the others (a test issued
-    // while the tensor core streams its operands from shared memory can
-    // take hundreds of cycles).
+    // Waits for N phases at once, the N tests in flight together, instead of
+    // N waits one after the other. In the MMA warps this shortens the time
+    // from the last of the N barriers completing to the next MMA issue
+    // (measured: +4.5% for the forward), although a single test of a
+    // completed barrier takes only ~20 cycles, with or without MMAs running.
     template <int N>
     __device__ __forceinline__ bool wait_all(const uint32_t (&bar)[N], const uint32_t (&parity)[N], int site) const {
         bool d[N];
