@@ -66,3 +66,31 @@ def test_fp8_peak_is_twice_the_bf16_peak():
     bf, _ = bench.load_peak(False)
     f8, src = bench.load_peak(True)
     assert f8 == 2 * bf and "x 2" in src
+
+
+def test_traffic_record_in_bytes_and_only_current_entries_reported():
+    # Each entry of the committed DRAM-traffic record names the kernel source
+    # hash it was captured on. An entry whose hash matches the current
+    # sources is what bench.py reports as `traffic`: bytes per launch, read
+    # + write, of the order of the algorithmic bytes (never MB); a stale one
+    # is reported as null.
+    import json
+
+    with open(bench.TRAFFIC_FILE) as fh:
+        rec = json.load(fh)
+    assert rec
+    for key, entry in rec.items():
+        name, _, pass_ = key.partition(":")
+        pass_ = pass_ or "fwd"
+        w = gen.workload(name)
+        assert entry["dram_bytes_per_launch"] == entry["dram_bytes_read"] + entry["dram_bytes_write"]
+        assert 0.5 * bench.pass_bytes(w, pass_) < entry["dram_bytes_per_launch"] < 10 * bench.pass_bytes(w, pass_)
+        src = "fp8" if w.fp8 else pass_
+        current = entry["kernel_source_sha"] == bench.kernel_source_hash(src)
+        expect = entry["dram_bytes_per_launch"] if current else None
+        assert bench.load_traffic(name, pass_) == expect, key
+
+
+def test_traffic_is_null_for_uncaptured_passes():
+    assert bench.load_traffic("mha_B4_H16_N4096_d128_bf16", "bwd") is None
+    assert bench.load_traffic("tiny_B1_H1_N128_d128_bf16", "fwd") is None
