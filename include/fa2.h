@@ -28,8 +28,9 @@
  *     lse  : [B, Hq,  N]      fp32
  * Every pointer must be 16-byte aligned. Outputs are fully overwritten.
  *
- * Execution. Calls are asynchronous on `stream` (0 = legacy default stream)
- * and launch exactly one kernel. The library allocates no memory per call;
+ * Execution. Calls are asynchronous on `stream` (0 = legacy default stream);
+ * each forward call launches exactly one kernel, fa2_bwd three (in stream
+ * order). The library allocates no memory per call;
  * it owns one status word per device (a __device__ variable), which the
  * kernel sets if one of its bounded waits gives up.
  *
