@@ -673,3 +673,19 @@ def test_fp8_general_method_stays_within_the_rounding_bound():
     for causal in (False, True):
         om, op, lp, a, b = oracle.attention_fp8_both(q, k, v, qd, kd, vd, 0.2, causal=causal)
         assert np.all(np.abs(om - op) <= 2.0 ** -4 * a + 2.0 ** -18 * b + 1e-15)
+
+
+def test_results_do_not_depend_on_the_thread_count():
+    # Query rows are independent, so the OpenMP thread count must not change
+    # a single bit of the forward oracles' results.
+    q, k, v = rand_inputs(61, 1, 4, 2, 192, 32)
+    o1, l1 = oracle.attention(q, k, v, 0.2, gen.BF16, threads=1)
+    o4, l4 = oracle.attention(q, k, v, 0.2, gen.BF16, threads=4)
+    assert np.array_equal(o1, o4) and np.array_equal(l1, l4)
+    e1 = oracle.attention_ex(q[:, :, :150], k, v, 0.2, gen.BF16, causal=True, threads=1)
+    e4 = oracle.attention_ex(q[:, :, :150], k, v, 0.2, gen.BF16, causal=True, threads=3)
+    assert all(np.array_equal(a, b) for a, b in zip(e1, e4))
+    q8, k8, v8, qd, kd, vd = gen.make_qkv_fp8(62, 1, 2, 1, 200, 32)
+    f1 = oracle.attention_fp8_both(q8, k8, v8, qd, kd, vd, 0.3, threads=1, causal=True)
+    f4 = oracle.attention_fp8_both(q8, k8, v8, qd, kd, vd, 0.3, threads=4, causal=True)
+    assert all(np.array_equal(a, b) for a, b in zip(f1, f4))
