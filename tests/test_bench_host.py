@@ -94,3 +94,24 @@ def test_traffic_record_in_bytes_and_only_current_entries_reported():
 def test_traffic_is_null_for_uncaptured_passes():
     assert bench.load_traffic("mha_B4_H16_N4096_d128_bf16", "bwd") is None
     assert bench.load_traffic("tiny_B1_H1_N128_d128_bf16", "fwd") is None
+
+
+def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
+    # The driver launches both arms the same way for N > 1: one process per
+    # rank under torchrun. For the reference arm rank 0 alone works and
+    # prints; the other ranks exit 0 without output.
+    import socket
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    out = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                          "--master-addr", "127.0.0.1", "--master-port", str(port),
+                          os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                          "--steps", "1", "--warmup", "3", "--ref-seconds", "4"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
