@@ -83,6 +83,21 @@ void oracle_decode16(const uint16_t* bits, int64_t n, int dtype, double* out) {
 }
 
 /*
+ * Step 1 of the definition for a whole K or V tensor: every 16-bit pattern
+ * widened to its exact double value once, before any row uses it, so that
+ * the per-row loops below read doubles. (Decoding is exact, so doing it
+ * here rather than inside the loops changes no result.) Returns NULL if the
+ * memory is not available.
+ */
+static double* decode_all(const uint16_t* bits, int64_t n, int dtype) {
+    double* out = (double*)malloc(sizeof(double) * (size_t)n);
+    if (!out) return NULL;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) out[i] = decode16(bits[i], dtype);
+    return out;
+}
+
+/*
  * Attention forward for a list of query rows.
  *
  * q:   [B, Hq, N, d]   16-bit patterns, contiguous
@@ -107,6 +122,14 @@ int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* 
 #else
     (void)nthreads;
 #endif
+    /* step 1: exact double values of K and V */
+    double* kall = decode_all(k, B * Hkv * N * d, dtype);
+    double* vall = decode_all(v, B * Hkv * N * d, dtype);
+    if (!kall || !vall) {
+        free(kall);
+        free(vall);
+        return -2;
+    }
 
 #pragma omp parallel
     {
@@ -121,8 +144,8 @@ int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* 
             const int64_t b = flat / (N * Hq);
             const int64_t hk = h / G;
             const uint16_t* qp = q + ((b * Hq + h) * N + i) * d;
-            const uint16_t* kp = k + (b * Hkv + hk) * N * d;
-            const uint16_t* vp = v + (b * Hkv + hk) * N * d;
+            const double* kp = kall + (b * Hkv + hk) * N * d;
+            const double* vp = vall + (b * Hkv + hk) * N * d;
 
             for (int64_t t = 0; t < d; ++t) qrow[t] = decode16(qp[t], dtype);
 
@@ -130,7 +153,7 @@ int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* 
             double m = -INFINITY;
             for (int64_t j = 0; j < N; ++j) {
                 double dot = 0.0;
-                for (int64_t t = 0; t < d; ++t) dot += qrow[t] * decode16(kp[j * d + t], dtype);
+                for (int64_t t = 0; t < d; ++t) dot += qrow[t] * kp[j * d + t];
                 s[j] = scale * dot;
                 if (s[j] > m) m = s[j];
             }
@@ -140,7 +163,7 @@ int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* 
             for (int64_t j = 0; j < N; ++j) {
                 const double p = exp(s[j] - m);
                 l += p;
-                for (int64_t t = 0; t < d; ++t) acc[t] += p * decode16(vp[j * d + t], dtype);
+                for (int64_t t = 0; t < d; ++t) acc[t] += p * vp[j * d + t];
             }
             for (int64_t t = 0; t < d; ++t) o_out[r * d + t] = acc[t] / l;
             lse_out[r] = m + log(l);
@@ -149,6 +172,8 @@ int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* 
         free(s);
         free(acc);
     }
+    free(kall);
+    free(vall);
     return 0;
 }
 
@@ -206,6 +231,14 @@ int oracle_attention_ex_rows(const uint16_t* q, const uint16_t* k, const uint16_
 #else
     (void)nthreads;
 #endif
+    /* step 1: exact double values of K and V */
+    double* kall = decode_all(k, B * Hkv * Nk * d, dtype);
+    double* vall = decode_all(v, B * Hkv * Nk * d, dtype);
+    if (!kall || !vall) {
+        free(kall);
+        free(vall);
+        return -2;
+    }
 
 #pragma omp parallel
     {
@@ -220,8 +253,8 @@ int oracle_attention_ex_rows(const uint16_t* q, const uint16_t* k, const uint16_
             const int64_t b = flat / (Nq * Hq);
             const int64_t hk = h / G;
             const uint16_t* qp = q + ((b * Hq + h) * Nq + i) * d;
-            const uint16_t* kp = k + (b * Hkv + hk) * Nk * d;
-            const uint16_t* vp = v + (b * Hkv + hk) * Nk * d;
+            const double* kp = kall + (b * Hkv + hk) * Nk * d;
+            const double* vp = vall + (b * Hkv + hk) * Nk * d;
             int64_t kend = Nk;
             if (causal) {
                 const int64_t lim = i + 1 + Nk - Nq;
@@ -236,7 +269,7 @@ int oracle_attention_ex_rows(const uint16_t* q, const uint16_t* k, const uint16_
             double m = -INFINITY;
             for (int64_t j = 0; j < kend; ++j) {
                 double dot = 0.0;
-                for (int64_t t = 0; t < d; ++t) dot += qrow[t] * decode16(kp[j * d + t], dtype);
+                for (int64_t t = 0; t < d; ++t) dot += qrow[t] * kp[j * d + t];
                 s[j] = scale * dot;
                 if (s[j] > m) m = s[j];
             }
@@ -245,7 +278,7 @@ int oracle_attention_ex_rows(const uint16_t* q, const uint16_t* k, const uint16_
             for (int64_t j = 0; j < kend; ++j) {
                 const double p = exp(s[j] - m);
                 l += p;
-                for (int64_t t = 0; t < d; ++t) acc[t] += p * decode16(vp[j * d + t], dtype);
+                for (int64_t t = 0; t < d; ++t) acc[t] += p * vp[j * d + t];
             }
             for (int64_t t = 0; t < d; ++t) o_out[r * d + t] = acc[t] / l;
             lse_out[r] = m + log(l);
@@ -254,6 +287,8 @@ int oracle_attention_ex_rows(const uint16_t* q, const uint16_t* k, const uint16_
         free(s);
         free(acc);
     }
+    free(kall);
+    free(vall);
     return 0;
 }
 
