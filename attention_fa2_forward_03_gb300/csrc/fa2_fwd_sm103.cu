@@ -33,13 +33,25 @@ std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 constexpr int kMaxDevices = 64;
+// Kernel slots: 16-bit forward 0-7, backward dK/dV 8-11, FP8 forward 12-13,
+// backward dQ 14-17.
+constexpr int kKernelSlots = 18;
+// Per-device facts, read without a lock: every field is an atomic written
+// with release and read with acquire, and two threads that probe the same
+// device at once store the same values.
 struct DeviceState {
-    bool probed = false;
-    bool supported = false;
-    int sm_count = 0;
-    bool smem_set[14] = {};
+    std::atomic<int> state;     // 0 = not probed, 1 = compute capability 10.3, 2 = other
+    std::atomic<int> sm_count;
+    std::atomic<bool> smem_set[kKernelSlots];  // dynamic shared-memory limit raised for kernel slot i
 };
-DeviceState g_dev[kMaxDevices];
+DeviceState g_dev[kMaxDevices];  // static storage: zero-initialised
+
+// A CUDA call of this library failed: return FA2_ERR_CUDA and leave no
+// (non-sticky) error of ours pending for the caller's next cudaGetLastError.
+fa2_status cuda_fail() {
+    (void)cudaGetLastError();
+    return FA2_ERR_CUDA;
+}
 
 fa2_status get_encoder() {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -49,29 +61,55 @@ fa2_status get_encoder() {
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
             cudaSuccess ||
         q != cudaDriverEntryPointSuccess || !fn)
-        return FA2_ERR_CUDA;
+        return cuda_fail();
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     return FA2_OK;
 }
 
 fa2_status check_device(int* dev_out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return FA2_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail();
     if (dev < 0 || dev >= kMaxDevices) return FA2_ERR_UNSUPPORTED;
     DeviceState& st = g_dev[dev];
-    if (!st.probed) {
+    int s = st.state.load(std::memory_order_acquire);
+    if (s == 0) {
         int major = 0, minor = 0, sms = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return FA2_ERR_CUDA;
-        std::lock_guard<std::mutex> lk(g_mu);
-        st.supported = (major == 10 && minor == 3);
-        st.sm_count = sms;
-        st.probed = true;
+            return cuda_fail();
+        st.sm_count.store(sms, std::memory_order_relaxed);
+        s = (major == 10 && minor == 3) ? 1 : 2;
+        st.state.store(s, std::memory_order_release);
     }
     *dev_out = dev;
-    return st.supported ? FA2_OK : FA2_ERR_UNSUPPORTED;
+    return s == 1 ? FA2_OK : FA2_ERR_UNSUPPORTED;
+}
+
+int sm_count(int dev) { return g_dev[dev].sm_count.load(std::memory_order_relaxed); }
+
+// Raises the dynamic shared-memory limit of `kern` on device `dev` once.
+template <typename K>
+fa2_status set_smem(int dev, int slot, K kern, int bytes) {
+    std::atomic<bool>& done = g_dev[dev].smem_set[slot];
+    if (done.load(std::memory_order_acquire)) return FA2_OK;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return cuda_fail();
+    done.store(true, std::memory_order_release);
+    return FA2_OK;
+}
+
+// Queues one kernel and judges the launch by its own return code (not by
+// cudaGetLastError, which would also report an error left pending earlier).
+template <typename... Exp, typename... Act>
+fa2_status launch_kernel(void (*kern)(Exp...), dim3 grid, int threads, int smem, cudaStream_t stream,
+                         Act&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Act>(args)...) == cudaSuccess ? FA2_OK : cuda_fail();
 }
 
 // 2-D view [rows, d] of a 16-bit tensor, boxes of 128 rows x 64 elements
@@ -106,14 +144,9 @@ fa2_status launch(int dev, const CUtensorMap& mq, const CUtensorMap& mk, const C
     constexpr int kSmem = Layout<D>::kSmemBytes;
     auto kern = fa2::fa2_fwd_kernel<D, kBf16, kGen>;
     const int slot = (D == 128 ? 0 : 2) + (kBf16 ? 0 : 1) + (kGen ? 4 : 0);
-    if (!g_dev[dev].smem_set[slot]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
-            return FA2_ERR_CUDA;
-        std::lock_guard<std::mutex> lk(g_mu);
-        g_dev[dev].smem_set[slot] = true;
-    }
-    kern<<<grid, fa2::kThreads, kSmem, stream>>>(mq, mk, mv, p);
-    return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+    const fa2_status st = set_smem(dev, slot, kern, kSmem);
+    if (st != FA2_OK) return st;
+    return launch_kernel(kern, grid, fa2::kThreads, kSmem, stream, mq, mk, mv, p);
 }
 
 // 2-D view [rows, 128] of an 8-bit tensor (FP8 kernel): boxes of 128 rows x
@@ -148,14 +181,9 @@ fa2_status launch_fp8(int dev, const CUtensorMap& mq, const CUtensorMap& mk, con
     constexpr int kSmem = fa2::fp8::Lay::kSmemBytes;
     constexpr int kSlot = kGen ? 13 : 12;
     auto kern = fa2::fa2_fwd_fp8_kernel<kGen>;
-    if (!g_dev[dev].smem_set[kSlot]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
-            return FA2_ERR_CUDA;
-        std::lock_guard<std::mutex> lk(g_mu);
-        g_dev[dev].smem_set[kSlot] = true;
-    }
-    kern<<<grid, fa2::kThreads, kSmem, stream>>>(mq, mk, mv, p);
-    return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+    const fa2_status st = set_smem(dev, kSlot, kern, kSmem);
+    if (st != FA2_OK) return st;
+    return launch_kernel(kern, grid, fa2::kThreads, kSmem, stream, mq, mk, mv, p);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -185,7 +213,7 @@ fa2_status fwd_general(const void* q, const void* k, const void* v, void* o, flo
     if (encode_map_3d(&mq, q, static_cast<uint64_t>(heads_q), static_cast<uint64_t>(N_q), d) != FA2_OK ||
         encode_map_3d(&mk, k, static_cast<uint64_t>(B) * H_kv, static_cast<uint64_t>(N_k), d) != FA2_OK ||
         encode_map_3d(&mv, v, static_cast<uint64_t>(B) * H_kv, static_cast<uint64_t>(N_k), d) != FA2_OK)
-        return FA2_ERR_CUDA;
+        return cuda_fail();
 
     Params p{};
     p.o = o;
@@ -202,7 +230,7 @@ fa2_status fwd_general(const void* q, const void* k, const void* v, void* o, flo
     p.tq = static_cast<int>(tq);
     p.pairs = static_cast<int>((tq + fa2::kNQ - 1) / fa2::kNQ);
     p.total_items = static_cast<int>(items);
-    const dim3 grid(static_cast<unsigned>(std::min<long long>(items, g_dev[dev].sm_count)));
+    const dim3 grid(static_cast<unsigned>(std::min<long long>(items, sm_count(dev))));
 
     const bool bf = dtype == FA2_BF16;
     if (d == 128)
@@ -235,7 +263,7 @@ fa2_status fwd_fp8_general(const void* q, const void* k, const void* v, const fl
     if (encode_map_u8_3d(&mq, q, static_cast<uint64_t>(heads_q), static_cast<uint64_t>(N_q)) != FA2_OK ||
         encode_map_u8_3d(&mk, k, hkv, static_cast<uint64_t>(N_k)) != FA2_OK ||
         encode_map_u8_3d(&mv, v, hkv, static_cast<uint64_t>(N_k)) != FA2_OK)
-        return FA2_ERR_CUDA;
+        return cuda_fail();
 
     Params p{};
     p.o = o;
@@ -255,7 +283,7 @@ fa2_status fwd_fp8_general(const void* q, const void* k, const void* v, const fl
     p.q_descale = q_descale;
     p.k_descale = k_descale;
     p.v_descale = v_descale;
-    const dim3 grid(static_cast<unsigned>(std::min<long long>(items, g_dev[dev].sm_count)));
+    const dim3 grid(static_cast<unsigned>(std::min<long long>(items, sm_count(dev))));
     return launch_fp8<true>(dev, mq, mk, mv, p, grid, stream);
 }
 
@@ -289,7 +317,7 @@ fa2_status fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, flo
     const uint64_t rows_kv = static_cast<uint64_t>(B) * H_kv * N;
     if (encode_map(&mq, q, static_cast<uint64_t>(rows_q), d) != FA2_OK ||
         encode_map(&mk, k, rows_kv, d) != FA2_OK || encode_map(&mv, v, rows_kv, d) != FA2_OK)
-        return FA2_ERR_CUDA;
+        return cuda_fail();
 
     Params p{};
     p.o = o;
@@ -303,7 +331,7 @@ fa2_status fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, flo
     p.debug_flags = g_debug_flags.load();
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     // Persistent grid: one CTA per SM (shared memory and TMEM admit one).
-    const dim3 grid(static_cast<unsigned>(std::min<long long>(p.total_items, g_dev[dev].sm_count)));
+    const dim3 grid(static_cast<unsigned>(std::min<long long>(p.total_items, sm_count(dev))));
 
     const bool bf = dtype == FA2_BF16;
     if (d == 128)
@@ -340,7 +368,7 @@ fa2_status fa2_fwd_fp8(const void* q, const void* k, const void* v, const float*
     const uint64_t rows_kv = static_cast<uint64_t>(B) * H_kv * N;
     if (encode_map_u8(&mq, q, static_cast<uint64_t>(rows_q)) != FA2_OK || encode_map_u8(&mk, k, rows_kv) != FA2_OK ||
         encode_map_u8(&mv, v, rows_kv) != FA2_OK)
-        return FA2_ERR_CUDA;
+        return cuda_fail();
 
     Params p{};
     p.o = o;
@@ -356,7 +384,7 @@ fa2_status fa2_fwd_fp8(const void* q, const void* k, const void* v, const float*
     p.q_descale = q_descale;
     p.k_descale = k_descale;
     p.v_descale = v_descale;
-    const dim3 grid(static_cast<unsigned>(std::min<long long>(p.total_items, g_dev[dev].sm_count)));
+    const dim3 grid(static_cast<unsigned>(std::min<long long>(p.total_items, sm_count(dev))));
     return launch_fp8<false>(dev, mq, mk, mv, p, grid, stream);
 }
 
@@ -402,10 +430,17 @@ fa2_status fa2_fwd_ex(const void* q, const void* k, const void* v, void* o, floa
     return fwd_general(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, scale, causal, dtype, stream);
 }
 
-fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                   const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H_q, int H_kv,
-                   int N, int d, float scale, int causal, fa2_dtype dtype, cudaStream_t stream) {
-    const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv, delta};
+}  // extern "C"
+
+namespace {
+
+// The argument and size checks that fa2_bwd and fa2_bwd_noalloc share (every
+// pointer but fa2_bwd's `delta`), in the order the header documents:
+// FA2_ERR_INVALID_ARG before FA2_ERR_UNSUPPORTED.
+fa2_status bwd_check_args(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                          const void* dout, void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int N, int d,
+                          float scale, int causal, fa2_dtype dtype) {
+    const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
     for (const void* x : ptrs)
         if (!x || !aligned16(x)) return FA2_ERR_INVALID_ARG;
     if (B <= 0 || H_q <= 0 || H_kv <= 0 || N <= 0 || d <= 0) return FA2_ERR_INVALID_ARG;
@@ -416,11 +451,16 @@ fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, c
     if (d != 64 && d != 128) return FA2_ERR_UNSUPPORTED;
     const long long rows_q = static_cast<long long>(B) * H_q * N;
     if (rows_q > 0x7FFFFFFFLL || static_cast<long long>(B) * H_q > 65535) return FA2_ERR_UNSUPPORTED;
+    return FA2_OK;
+}
 
-    int dev = 0;
-    fa2_status st = check_device(&dev);
+// The backward's three launches on checked arguments and a checked device.
+fa2_status bwd_launch(int dev, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H_q, int H_kv,
+                      int N, int d, float scale, int causal, fa2_dtype dtype, cudaStream_t stream) {
+    fa2_status st = get_encoder();
     if (st != FA2_OK) return st;
-    if ((st = get_encoder()) != FA2_OK) return st;
+    const long long rows_q = static_cast<long long>(B) * H_q * N;
     // [heads, N, d] views: tiles never cross heads; rows past a ragged N read as 0
     CUtensorMap mq, mk, mv, mdo;
     const uint64_t hq = static_cast<uint64_t>(B) * H_q, hkv = static_cast<uint64_t>(B) * H_kv;
@@ -451,27 +491,39 @@ fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, c
     const dim3 gq(static_cast<unsigned>(p.n_tiles), static_cast<unsigned>(B * H_q));
 
     auto run = [&](auto delta_k, auto dkdv_k, auto dq_k, int smem_kv, int smem_q, int slot) -> fa2_status {
-        if (!g_dev[dev].smem_set[slot]) {
-            if (cudaFuncSetAttribute(dkdv_k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kv) != cudaSuccess ||
-                cudaFuncSetAttribute(dq_k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q) != cudaSuccess)
-                return FA2_ERR_CUDA;
-            std::lock_guard<std::mutex> lk(g_mu);
-            g_dev[dev].smem_set[slot] = true;
-        }
-        delta_k<<<gdelta, 256, 0, stream>>>(o, dout, delta, rows_q);
-        dkdv_k<<<gkv, fa2::bwd::kThreads, smem_kv, stream>>>(mq, mk, mv, mdo, p);
-        dq_k<<<gq, fa2::bwd::kThreads, smem_q, stream>>>(mq, mk, mv, mdo, p);
-        return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+        fa2_status s = set_smem(dev, slot, dkdv_k, smem_kv);
+        if (s == FA2_OK) s = set_smem(dev, slot + 6, dq_k, smem_q);
+        if (s == FA2_OK) s = launch_kernel(delta_k, gdelta, 256, 0, stream, o, dout, delta, rows_q);
+        if (s == FA2_OK) s = launch_kernel(dkdv_k, gkv, fa2::bwd::kThreads, smem_kv, stream, mq, mk, mv, mdo, p);
+        if (s == FA2_OK) s = launch_kernel(dq_k, gq, fa2::bwd::kThreads, smem_q, stream, mq, mk, mv, mdo, p);
+        return s;
     };
+    using namespace fa2::bwd;
     if (d == 128)
-        return bf ? run(fa2::bwd::fa2_bwd_delta_kernel<128, true>, fa2::bwd::fa2_bwd_dkdv_kernel<128, true>,
-                        fa2::bwd::fa2_bwd_dq_kernel<128, true>, fa2::bwd::DkdvLayout<128>::kSmemBytes, fa2::bwd::DqLayout<128>::kSmemBytes, 8)
-                  : run(fa2::bwd::fa2_bwd_delta_kernel<128, false>, fa2::bwd::fa2_bwd_dkdv_kernel<128, false>,
-                        fa2::bwd::fa2_bwd_dq_kernel<128, false>, fa2::bwd::DkdvLayout<128>::kSmemBytes, fa2::bwd::DqLayout<128>::kSmemBytes, 9);
-    return bf ? run(fa2::bwd::fa2_bwd_delta_kernel<64, true>, fa2::bwd::fa2_bwd_dkdv_kernel<64, true>,
-                    fa2::bwd::fa2_bwd_dq_kernel<64, true>, fa2::bwd::DkdvLayout<64>::kSmemBytes, fa2::bwd::DqLayout<64>::kSmemBytes, 10)
-              : run(fa2::bwd::fa2_bwd_delta_kernel<64, false>, fa2::bwd::fa2_bwd_dkdv_kernel<64, false>,
-                    fa2::bwd::fa2_bwd_dq_kernel<64, false>, fa2::bwd::DkdvLayout<64>::kSmemBytes, fa2::bwd::DqLayout<64>::kSmemBytes, 11);
+        return bf ? run(fa2_bwd_delta_kernel<128, true>, fa2_bwd_dkdv_kernel<128, true>, fa2_bwd_dq_kernel<128, true>,
+                        DkdvLayout<128>::kSmemBytes, DqLayout<128>::kSmemBytes, 8)
+                  : run(fa2_bwd_delta_kernel<128, false>, fa2_bwd_dkdv_kernel<128, false>,
+                        fa2_bwd_dq_kernel<128, false>, DkdvLayout<128>::kSmemBytes, DqLayout<128>::kSmemBytes, 9);
+    return bf ? run(fa2_bwd_delta_kernel<64, true>, fa2_bwd_dkdv_kernel<64, true>, fa2_bwd_dq_kernel<64, true>,
+                    DkdvLayout<64>::kSmemBytes, DqLayout<64>::kSmemBytes, 10)
+              : run(fa2_bwd_delta_kernel<64, false>, fa2_bwd_dkdv_kernel<64, false>, fa2_bwd_dq_kernel<64, false>,
+                    DkdvLayout<64>::kSmemBytes, DqLayout<64>::kSmemBytes, 11);
+}
+
+}  // namespace
+
+extern "C" {
+
+fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H_q, int H_kv,
+                   int N, int d, float scale, int causal, fa2_dtype dtype, cudaStream_t stream) {
+    if (!delta || !aligned16(delta)) return FA2_ERR_INVALID_ARG;
+    fa2_status st = bwd_check_args(q, k, v, o, lse, dout, dq, dk, dv, B, H_q, H_kv, N, d, scale, causal, dtype);
+    if (st != FA2_OK) return st;
+    int dev = 0;
+    if ((st = check_device(&dev)) != FA2_OK) return st;
+    return bwd_launch(dev, q, k, v, o, lse, dout, dq, dk, dv, delta, B, H_q, H_kv, N, d, scale, causal, dtype,
+                      stream);
 }
 
 }  // extern "C"
@@ -480,50 +532,57 @@ fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, c
 
 // Scratch for fa2_bwd_noalloc: the per-row D = rowsum(dO o O) of the
 // backward, for at most kNoAllocMaxRows query rows (4 MiB of fp32). Every GPU
-// that loads this library keeps this array until the process exits. On the
-// host the name only stands for the array: its device address comes from
-// cudaGetSymbolAddress, once per device.
+// that loads this library keeps this array until the process exits. In host
+// code the name stands for the array but is not its device address: that
+// comes from cudaGetSymbolAddress, asked on every call with the caller's
+// device current, so the address always belongs to the context the kernels
+// run in (after cudaDeviceReset, or under another context, the array may
+// live elsewhere).
 static constexpr long long kNoAllocMaxRows = 1LL << 20;
 static __device__ __align__(256) float fa2_noalloc_delta[kNoAllocMaxRows];
-
-namespace {
-float* g_noalloc_delta_ptr[kMaxDevices] = {};
-}  // namespace
 
 extern "C" {
 
 fa2_status fa2_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                            const void* dout, void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int N,
                            int d, float scale, int causal, fa2_dtype dtype, cudaStream_t stream) {
-    if (B <= 0 || H_q <= 0 || N <= 0) return FA2_ERR_INVALID_ARG;
-    if (static_cast<long long>(B) * H_q * N > kNoAllocMaxRows) return FA2_ERR_UNSUPPORTED;
+    // fa2_bwd's checks first, so the same arguments give the same errors.
+    fa2_status st = bwd_check_args(q, k, v, o, lse, dout, dq, dk, dv, B, H_q, H_kv, N, d, scale, causal, dtype);
+    if (st != FA2_OK) return st;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return FA2_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return FA2_ERR_UNSUPPORTED;
-    if (!g_noalloc_delta_ptr[dev]) {
-        // First call on this device (which is current): find the array's
-        // device address.
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, fa2_noalloc_delta) != cudaSuccess || !ptr) return FA2_ERR_CUDA;
-        std::lock_guard<std::mutex> lk(g_mu);
-        g_noalloc_delta_ptr[dev] = static_cast<float*>(ptr);
-    }
+    if ((st = check_device(&dev)) != FA2_OK) return st;
+    if (static_cast<long long>(B) * H_q * N > kNoAllocMaxRows) return FA2_ERR_UNSUPPORTED;
+    // The array's address in the current context (a host-side lookup; the
+    // first one on a device may load this library's device code there).
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, fa2_noalloc_delta) != cudaSuccess || !ptr) return cuda_fail();
     // D is written in full by the first kernel of the backward before it is
     // read, so nothing left from an earlier call needs clearing.
-    return fa2_bwd(q, k, v, o, lse, dout, dq, dk, dv, g_noalloc_delta_ptr[dev], B, H_q, H_kv, N, d, scale, causal,
-                   dtype, stream);
+    return bwd_launch(dev, q, k, v, o, lse, dout, dq, dk, dv, static_cast<float*>(ptr), B, H_q, H_kv, N, d, scale,
+                      causal, dtype, stream);
 }
 
 fa2_status fa2_check_status(cudaStream_t stream) {
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return FA2_ERR_CUDA;
+    // The status word read is that of the stream's device; the current
+    // device is switched to it for the read and then restored.
+    int sdev = 0, cur = 0;
+    if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) return cuda_fail();
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return cuda_fail();
+    if (cudaGetDevice(&cur) != cudaSuccess) return cuda_fail();
+    if (sdev != cur && cudaSetDevice(sdev) != cudaSuccess) return cuda_fail();
+    fa2_status result = FA2_OK;
     int v = 0;
-    if (cudaMemcpyFromSymbol(&v, fa2::g_fa2_status, sizeof(int)) != cudaSuccess) return FA2_ERR_CUDA;
-    if (v != 0) {
+    if (cudaMemcpyFromSymbol(&v, fa2::g_fa2_status, sizeof(int)) != cudaSuccess) {
+        result = cuda_fail();
+    } else if (v != 0) {
         const int zero = 0;
-        if (cudaMemcpyToSymbol(fa2::g_fa2_status, &zero, sizeof(int)) != cudaSuccess) return FA2_ERR_CUDA;
-        return (v & 0xFF) == FA2_ERR_TIMEOUT ? FA2_ERR_TIMEOUT : FA2_ERR_CUDA;
+        if (cudaMemcpyToSymbol(fa2::g_fa2_status, &zero, sizeof(int)) != cudaSuccess)
+            result = cuda_fail();
+        else
+            result = (v & 0xFF) == FA2_ERR_TIMEOUT ? FA2_ERR_TIMEOUT : FA2_ERR_CUDA;
     }
-    return FA2_OK;
+    if (sdev != cur && cudaSetDevice(cur) != cudaSuccess) return cuda_fail();
+    return result;
 }
 
 const char* fa2_status_string(fa2_status s) {

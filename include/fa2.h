@@ -34,8 +34,13 @@
  * it owns one status word per device (a __device__ variable), which the
  * kernel sets if one of its bounded waits gives up.
  *
- * Errors. Argument errors are detected on the host before anything is
- * launched; no entry point exits the process or throws.
+ * Errors. Argument errors (FA2_ERR_INVALID_ARG) and unsupported sizes or
+ * devices (FA2_ERR_UNSUPPORTED) are detected on the host before anything is
+ * launched. FA2_ERR_CUDA means a CUDA call of the library failed; each launch
+ * is judged by its own return code, so an error the caller left pending does
+ * not turn a successful call into a failure, and a failed call leaves none
+ * of its own (non-sticky) errors pending. No entry point exits the process
+ * or throws.
  */
 #ifndef FA2_H_
 #define FA2_H_
@@ -182,7 +187,9 @@ fa2_status fa2_fwd_fp8_ex(const void* q, const void* k, const void* v, const flo
  * All pointers device memory, 16-byte aligned. Launches three kernels on
  * `stream` (D, then dK/dV, then dQ); allocates nothing. Errors as
  * fa2_fwd_gqa except that N need not be a multiple of 128; B*H_q > 65535
- * is FA2_ERR_UNSUPPORTED.
+ * is FA2_ERR_UNSUPPORTED. If one of the three launches fails
+ * (FA2_ERR_CUDA), the kernels before it may already be queued and the
+ * gradients are undefined.
  */
 fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                    const void* dout, void* dq, void* dk, void* dv, float* delta,
@@ -200,14 +207,20 @@ fa2_status fa2_bwd(const void* q, const void* k, const void* v, const void* o, c
  * Same arguments and results as fa2_bwd minus `delta`. D = rowsum(dO o O)
  * lives instead in a fixed device array inside this library, sized for
  * B * H_q * N <= 1048576 query rows (4 MiB of fp32, held on every GPU that
- * loads the library until the process exits); larger problems return
- * FA2_ERR_UNSUPPORTED and launch nothing. Nothing is allocated by the call.
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) and caches it; make that first call before any
- * stream capture. Every call uses the same array: calls that may overlap on
- * the GPU (other streams, other host threads) race on it and must be
- * ordered by the caller. The array keeps the last call's D; each call
- * rewrites the rows it uses before reading them.
+ * loads the library until the process exits). Errors: first those of
+ * fa2_bwd for the same arguments (so a NULL pointer is FA2_ERR_INVALID_ARG
+ * whatever the size, and a device that is not compute capability 10.3 is
+ * FA2_ERR_UNSUPPORTED), then more than 1048576 query rows is
+ * FA2_ERR_UNSUPPORTED; nothing is launched in those cases. Nothing is
+ * allocated by the call.
+ * Each call looks up the array's device address in the current device's
+ * context (cudaGetSymbolAddress, a host-side lookup), so the address stays
+ * right after cudaDeviceReset or under another context. The first call on a
+ * device may load this library's device code on it; make that first call
+ * before any stream capture. Every call uses the same array: calls that may
+ * overlap on the GPU (other streams, other host threads) race on it and
+ * must be ordered by the caller. The array keeps the last call's D; each
+ * call rewrites the rows it uses before reading them.
  */
 fa2_status fa2_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                            const void* dout, void* dq, void* dk, void* dv,
@@ -215,10 +228,17 @@ fa2_status fa2_bwd_noalloc(const void* q, const void* k, const void* v, const vo
                            fa2_dtype dtype, cudaStream_t stream);
 
 /*
- * Synchronises `stream`, then reads and clears the current device's status
- * word. Returns FA2_ERR_TIMEOUT if a kernel since the last check abandoned a
- * wait (its outputs are then undefined), FA2_ERR_CUDA if the stream reported
- * an error, FA2_OK otherwise.
+ * Synchronises `stream`, then reads and clears the status word of the device
+ * that `stream` belongs to (the current device is switched to it for the
+ * read and restored afterwards). Returns FA2_ERR_TIMEOUT if a kernel since
+ * the last check abandoned a wait (its outputs are then undefined),
+ * FA2_ERR_CUDA if the stream reported an error, FA2_OK otherwise.
+ * There is one status word per device, shared by every stream and host
+ * thread that uses the device: a timeout of a kernel on another stream is
+ * reported to whichever caller checks first (and then cleared), and a kernel
+ * still running on another stream may set the word after this call read it.
+ * Callers that need per-stream attribution check after synchronising all
+ * streams that ran the library's kernels.
  */
 fa2_status fa2_check_status(cudaStream_t stream);
 

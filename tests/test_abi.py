@@ -99,6 +99,29 @@ def test_backward_host_validation(lib):
     assert f(*ok, 1, 70000, 1, 128, 64, 0.1, 0, 0) == fa2.FA2_ERR_UNSUPPORTED       # B*Hq > 65535
 
 
+def test_backward_noalloc_checks_arguments_before_size_and_device(lib):
+    """fa2_bwd_noalloc runs fa2_bwd's argument checks before its own row limit
+    and before any device call, so the same bad argument gives the same
+    error, whatever the size (no GPU is touched on these paths)."""
+    f = fa2.fa2_bwd_noalloc_ptr
+    ok = [A] * 9
+    big = (64, 32, 32, 1024)     # B*H_q*N = 2^21 query rows: past the fixed array
+    assert f(*([0] + ok[1:]), *big, 128, 0.1, 0, 0) == fa2.FA2_ERR_INVALID_ARG     # NULL q, too many rows
+    assert f(*(ok[:8] + [0]), *big, 128, 0.1, 0, 0) == fa2.FA2_ERR_INVALID_ARG     # NULL dv, too many rows
+    assert f(*(ok[:4] + [A + 4] + ok[5:]), *big, 128, 0.1, 0, 0) == fa2.FA2_ERR_INVALID_ARG  # lse misaligned
+    assert f(*ok, 64, 32, 24, 1024, 128, 0.1, 0, 0) == fa2.FA2_ERR_INVALID_ARG     # H_q % H_kv, too many rows
+    assert f(*ok, 1, 3, 2, 128, 128, 0.1, 0, 0) == fa2.FA2_ERR_INVALID_ARG         # H_q % H_kv
+    assert f(*ok, *big, 128, 0.1, 2, 0) == fa2.FA2_ERR_INVALID_ARG                 # causal = 2
+    assert f(*ok, *big, 128, float("inf"), 0, 0) == fa2.FA2_ERR_INVALID_ARG        # scale
+    assert f(*ok, *big, 128, 0.1, 0, 7) == fa2.FA2_ERR_INVALID_ARG                 # dtype
+    assert f(*ok, *big, 96, 0.1, 0, 0) == fa2.FA2_ERR_UNSUPPORTED                  # d, before the row limit
+    assert f(*ok, 1, 70000, 1, 128, 64, 0.1, 0, 0) == fa2.FA2_ERR_UNSUPPORTED      # B*H_q > 65535
+    # and every one of them matches fa2_bwd with a valid workspace pointer
+    for args in (([0] + ok[1:], big), (ok, (64, 32, 24, 1024))):
+        assert (fa2.fa2_bwd_ptr(*args[0], A, *args[1], 128, 0.1, 0, 0)
+                == f(*args[0], *args[1], 128, 0.1, 0, 0))
+
+
 def test_fp8_entry_host_validation(lib):
     f = fa2.fa2_fwd_fp8_ptr
     ok = [A] * 8            # q, k, v, q/k/v descales, o, lse
