@@ -59,7 +59,7 @@ def _load():
                                                  ctypes.c_int]
         lib.oracle_attention_ex_rows.restype = ctypes.c_int
         lib.oracle_attention_bwd.argtypes = [p, p, p, p, ctypes.c_int, i64, i64, i64, i64, i64,
-                                             ctypes.c_double, ctypes.c_int, p, p, p]
+                                             ctypes.c_double, ctypes.c_int, p, p, p, p, p, p]
         lib.oracle_attention_bwd.restype = ctypes.c_int
         lib.oracle_attention_f64.argtypes = [p, p, p, i64, i64, i64, i64, i64, ctypes.c_double,
                                              ctypes.c_int, p]
@@ -159,11 +159,16 @@ def attention_ex(q, k, v, scale: float, dtype: int, causal: bool = False, rows=N
     return o, lse
 
 
-def attention_bwd(q, k, v, dout, scale: float, dtype: int, causal: bool = False):
+def attention_bwd(q, k, v, dout, scale: float, dtype: int, causal: bool = False, bounds: bool = False):
     """Gradients (dq, dk, dv) of attention for upstream gradient dout, fp64.
 
     q, dout: uint16 [B, Hq, N, d]; k, v: uint16 [B, Hkv, N, d]. With grouped
     heads dk and dv sum over the query heads of each KV head.
+
+    bounds=True also returns a dict of the absolute sums that bound the
+    error of a computation rounding P, dS and O to 16 bits (see oracle.c):
+    ``q`` and ``k`` are [3, ...] arrays (A, BE, BF) shaped like dq and dk,
+    ``v`` is A shaped like dv.
     """
     q, k, v, dout = _u16(q), _u16(k), _u16(v), _u16(dout)
     B, Hq, N, d = q.shape
@@ -173,11 +178,18 @@ def attention_bwd(q, k, v, dout, scale: float, dtype: int, causal: bool = False)
     dq = np.empty(q.shape, dtype=np.float64)
     dk = np.empty(k.shape, dtype=np.float64)
     dv = np.empty(v.shape, dtype=np.float64)
+    bq = np.empty((3,) + q.shape, dtype=np.float64) if bounds else None
+    bk = np.empty((3,) + k.shape, dtype=np.float64) if bounds else None
+    bv = np.empty(v.shape, dtype=np.float64) if bounds else None
+    ptr = lambda a: None if a is None else a.ctypes.data
     rc = _load().oracle_attention_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data,
                                       dtype, B, Hq, Hkv, N, d, float(scale), int(bool(causal)),
-                                      dq.ctypes.data, dk.ctypes.data, dv.ctypes.data)
+                                      dq.ctypes.data, dk.ctypes.data, dv.ctypes.data,
+                                      ptr(bq), ptr(bk), ptr(bv))
     if rc != 0:
         raise ValueError("oracle rejected the sizes")
+    if bounds:
+        return dq, dk, dv, {"q": bq, "k": bk, "v": bv}
     return dq, dk, dv
 
 
@@ -210,7 +222,7 @@ def round_e4m3(x) -> np.ndarray:
 
 
 def attention_fp8_both(q, k, v, q_descale, k_descale, v_descale, scale: float, rows=None,
-                       threads: int = 0, bc: int = 128, causal: bool = False):
+                       threads: int = 0, bc: int = 128, causal: bool = False, method: bool = True):
     """Attention forward on e4m3 inputs with per-(batch, KV head) descales,
     in one pass: returns (o_method, o_plain, lse, a, b).
 
@@ -222,7 +234,8 @@ def attention_fp8_both(q, k, v, q_descale, k_descale, v_descale, scale: float, r
     max) before the P.V product; o_plain is the plain definition on the
     dequantised inputs. o_*, a, b: [B, Hq, Nq, d] (or [len(rows), d]); lse:
     [B, Hq, N] (or [len(rows)]); a = sum_j p_j |v_j| / l and
-    b = sum_j |v_j| / l elementwise.
+    b = sum_j |v_j| / l elementwise. method=False skips the method (o_method
+    is then None).
     """
     q, k, v = (np.ascontiguousarray(x, dtype=np.uint8) for x in (q, k, v))
     B, Hq, N, d = q.shape
@@ -238,17 +251,20 @@ def attention_fp8_both(q, k, v, q_descale, k_descale, v_descale, scale: float, r
     else:
         rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
         nrows, rptr = rows_arr.size, rows_arr.ctypes.data
-    om, op, a, b = (np.empty((nrows, d), dtype=np.float64) for _ in range(4))
+    om = np.empty((nrows, d), dtype=np.float64) if method else None
+    op, a, b = (np.empty((nrows, d), dtype=np.float64) for _ in range(3))
     lse = np.empty(nrows, dtype=np.float64)
     rc = _load().oracle_attention_fp8_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, qd.ctypes.data,
                                            kd.ctypes.data, vd.ctypes.data, B, Hq, Hkv, N, Nk, d, float(scale),
-                                           int(bool(causal)), int(bc), rptr, nrows, om.ctypes.data, op.ctypes.data,
+                                           int(bool(causal)), int(bc), rptr, nrows,
+                                           None if om is None else om.ctypes.data, op.ctypes.data,
                                            lse.ctypes.data, a.ctypes.data, b.ctypes.data, int(threads))
     if rc != 0:
         raise ValueError("oracle rejected the sizes")
     if rows is None:
         shp = (B, Hq, N, d)
-        return om.reshape(shp), op.reshape(shp), lse.reshape(B, Hq, N), a.reshape(shp), b.reshape(shp)
+        return (None if om is None else om.reshape(shp)), op.reshape(shp), lse.reshape(B, Hq, N), \
+            a.reshape(shp), b.reshape(shp)
     return om, op, lse, a, b
 
 
@@ -257,7 +273,7 @@ def attention_fp8(q, k, v, q_descale, k_descale, v_descale, scale: float, round_
     """(o, lse, a, b) of :func:`attention_fp8_both`, with o the method's
     output (round_p=True) or the plain definition's (round_p=False)."""
     om, op, lse, a, b = attention_fp8_both(q, k, v, q_descale, k_descale, v_descale, scale, rows, threads, bc,
-                                           causal)
+                                           causal, method=round_p)
     return (om if round_p else op), lse, a, b
 
 

@@ -302,44 +302,77 @@ int oracle_attention_ex_rows(const uint16_t* q, const uint16_t* k, const uint16_
  * Inputs q, k, v, dout are 16-bit patterns ([B,Hq,N,d], [B,Hkv,N,d],
  * [B,Hkv,N,d], [B,Hq,N,d]); outputs are doubles of the same shapes as q, k, v.
  * Equal query/key lengths N. Rows with no allowed key contribute nothing.
+ *
+ * Optional bound sums (each pointer may be NULL). They are not part of the
+ * gradient: they are the absolute sums that bound, element by element, how
+ * far a computation that rounds P, dS and O to 16 bits and accumulates in
+ * fp32 can land from the exact gradient. With a_it = sum_j P_ij |V_jt|,
+ * E_i = sum_t |dO_it| (|O_it| + a_it) and F_ij = sum_t |dO_it| |V_jt|:
+ *   bq [3, B,Hq,N,d]:  A = scale sum_j |dS_ij| |K_jt|,
+ *                      BE = scale E_i sum_j P_ij |K_jt|,
+ *                      BF = scale sum_j P_ij F_ij |K_jt|
+ *   bk [3, B,Hkv,N,d]: the same three sums over the query rows i (and the
+ *                      query heads of the KV head) with |Q_it| for |K_jt|
+ *   bv [B,Hkv,N,d]:    A = sum_i P_ij |dO_it|
  */
 int oracle_attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
                          int dtype, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
-                         double scale, int causal, double* dq, double* dk, double* dv) {
+                         double scale, int causal, double* dq, double* dk, double* dv,
+                         double* bq, double* bk, double* bv) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || Hq % Hkv) return -1;
     const int64_t G = Hq / Hkv;
-    for (int64_t i = 0; i < B * Hkv * N * d; ++i) {
+    const int64_t nq = B * Hq * N * d, nkv = B * Hkv * N * d;
+    /* the 16-bit inputs as exact doubles */
+    double* Q = decode_all(q, nq, dtype);
+    double* K = decode_all(k, nkv, dtype);
+    double* V = decode_all(v, nkv, dtype);
+    double* dO = decode_all(dout, nq, dtype);
+    if (!Q || !K || !V || !dO) {
+        free(Q);
+        free(K);
+        free(V);
+        free(dO);
+        return -2;
+    }
+    for (int64_t i = 0; i < nkv; ++i) {
         dk[i] = 0.0;
         dv[i] = 0.0;
+        if (bk) bk[i] = bk[nkv + i] = bk[2 * nkv + i] = 0.0;
+        if (bv) bv[i] = 0.0;
     }
     for (int64_t b = 0; b < B; ++b) {
         for (int64_t hk = 0; hk < Hkv; ++hk) {
-            const uint16_t* kp = k + (b * Hkv + hk) * N * d;
-            const uint16_t* vp = v + (b * Hkv + hk) * N * d;
-            double* dkp = dk + (b * Hkv + hk) * N * d;
-            double* dvp = dv + (b * Hkv + hk) * N * d;
+            const int64_t kvoff = (b * Hkv + hk) * N * d;
+            const double* kp = K + kvoff;
+            const double* vp = V + kvoff;
             for (int64_t g = 0; g < G; ++g) {
                 const int64_t h = hk * G + g;
-                const uint16_t* qp = q + (b * Hq + h) * N * d;
-                const uint16_t* dop = dout + (b * Hq + h) * N * d;
-                double* dqp = dq + (b * Hq + h) * N * d;
+                const int64_t qoff = (b * Hq + h) * N * d;
+                const double* qp = Q + qoff;
+                const double* dop = dO + qoff;
 #pragma omp parallel
                 {
                     double* P = (double*)malloc(sizeof(double) * (size_t)N);
                     double* dS = (double*)malloc(sizeof(double) * (size_t)N);
+                    double* F = (double*)malloc(sizeof(double) * (size_t)N);
                     double* o = (double*)malloc(sizeof(double) * (size_t)d);
-                    /* per query row: P, D, dS and dQ; dK and dV rows are
-                       accumulated under a lock-free reduction per thread */
-                    double* dkl = (double*)calloc((size_t)(N * d), sizeof(double));
-                    double* dvl = (double*)calloc((size_t)(N * d), sizeof(double));
+                    double* a = (double*)malloc(sizeof(double) * (size_t)d);
+                    /* per-thread dK, dV (and bound) rows, added up at the end */
+                    const int nloc = 2 + (bk ? 3 : 0) + (bv ? 1 : 0);
+                    double* loc = (double*)calloc((size_t)(nloc * N * d), sizeof(double));
+                    double* dkl = loc;
+                    double* dvl = loc + N * d;
+                    double* bkl = bk ? loc + 2 * N * d : NULL;
+                    double* bvl = bv ? loc + (2 + (bk ? 3 : 0)) * N * d : NULL;
 #pragma omp for schedule(dynamic, 4)
                     for (int64_t i = 0; i < N; ++i) {
                         const int64_t kend = causal ? (i + 1 < N ? i + 1 : N) : N;
+                        const double* qi = qp + i * d;
+                        const double* doi = dop + i * d;
                         double m = -INFINITY;
                         for (int64_t j = 0; j < kend; ++j) {
                             double dot = 0.0;
-                            for (int64_t t = 0; t < d; ++t)
-                                dot += decode16(qp[i * d + t], dtype) * decode16(kp[j * d + t], dtype);
+                            for (int64_t t = 0; t < d; ++t) dot += qi[t] * kp[j * d + t];
                             P[j] = scale * dot;
                             if (P[j] > m) m = P[j];
                         }
@@ -348,46 +381,83 @@ int oracle_attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v
                             P[j] = exp(P[j] - m);
                             l += P[j];
                         }
-                        for (int64_t t = 0; t < d; ++t) o[t] = 0.0;
+                        for (int64_t t = 0; t < d; ++t) o[t] = a[t] = 0.0;
                         for (int64_t j = 0; j < kend; ++j) {
                             P[j] /= l;
-                            for (int64_t t = 0; t < d; ++t) o[t] += P[j] * decode16(vp[j * d + t], dtype);
+                            for (int64_t t = 0; t < d; ++t) {
+                                o[t] += P[j] * vp[j * d + t];
+                                a[t] += P[j] * fabs(vp[j * d + t]);
+                            }
                         }
-                        double Di = 0.0;
-                        for (int64_t t = 0; t < d; ++t) Di += decode16(dop[i * d + t], dtype) * o[t];
+                        double Di = 0.0, Ei = 0.0;
+                        for (int64_t t = 0; t < d; ++t) {
+                            Di += doi[t] * o[t];
+                            Ei += fabs(doi[t]) * (fabs(o[t]) + a[t]);
+                        }
                         for (int64_t j = 0; j < kend; ++j) {
-                            double dp = 0.0;
-                            for (int64_t t = 0; t < d; ++t)
-                                dp += decode16(dop[i * d + t], dtype) * decode16(vp[j * d + t], dtype);
+                            double dp = 0.0, f = 0.0;
+                            for (int64_t t = 0; t < d; ++t) {
+                                dp += doi[t] * vp[j * d + t];
+                                f += fabs(doi[t]) * fabs(vp[j * d + t]);
+                            }
                             dS[j] = P[j] * (dp - Di);
+                            F[j] = f;
                         }
                         for (int64_t t = 0; t < d; ++t) {
-                            double acc = 0.0;
-                            for (int64_t j = 0; j < kend; ++j) acc += dS[j] * decode16(kp[j * d + t], dtype);
-                            dqp[i * d + t] = scale * acc;
+                            double acc = 0.0, sa = 0.0, se = 0.0, sf = 0.0;
+                            for (int64_t j = 0; j < kend; ++j) {
+                                const double kk = kp[j * d + t];
+                                acc += dS[j] * kk;
+                                sa += fabs(dS[j]) * fabs(kk);
+                                se += P[j] * fabs(kk);
+                                sf += P[j] * F[j] * fabs(kk);
+                            }
+                            dq[qoff + i * d + t] = scale * acc;
+                            if (bq) {
+                                bq[qoff + i * d + t] = scale * sa;
+                                bq[nq + qoff + i * d + t] = scale * Ei * se;
+                                bq[2 * nq + qoff + i * d + t] = scale * sf;
+                            }
                         }
                         for (int64_t j = 0; j < kend; ++j)
                             for (int64_t t = 0; t < d; ++t) {
-                                dkl[j * d + t] += scale * dS[j] * decode16(qp[i * d + t], dtype);
-                                dvl[j * d + t] += P[j] * decode16(dop[i * d + t], dtype);
+                                dkl[j * d + t] += scale * dS[j] * qi[t];
+                                dvl[j * d + t] += P[j] * doi[t];
+                                if (bkl) {
+                                    bkl[j * d + t] += scale * fabs(dS[j]) * fabs(qi[t]);
+                                    bkl[N * d + j * d + t] += scale * P[j] * Ei * fabs(qi[t]);
+                                    bkl[2 * N * d + j * d + t] += scale * P[j] * F[j] * fabs(qi[t]);
+                                }
+                                if (bvl) bvl[j * d + t] += P[j] * fabs(doi[t]);
                             }
                     }
 #pragma omp critical
                     {
                         for (int64_t x = 0; x < N * d; ++x) {
-                            dkp[x] += dkl[x];
-                            dvp[x] += dvl[x];
+                            dk[kvoff + x] += dkl[x];
+                            dv[kvoff + x] += dvl[x];
+                            if (bkl) {
+                                bk[kvoff + x] += bkl[x];
+                                bk[nkv + kvoff + x] += bkl[N * d + x];
+                                bk[2 * nkv + kvoff + x] += bkl[2 * N * d + x];
+                            }
+                            if (bvl) bv[kvoff + x] += bvl[x];
                         }
                     }
                     free(P);
                     free(dS);
+                    free(F);
                     free(o);
-                    free(dkl);
-                    free(dvl);
+                    free(a);
+                    free(loc);
                 }
             }
         }
     }
+    free(Q);
+    free(K);
+    free(V);
+    free(dO);
     return 0;
 }
 

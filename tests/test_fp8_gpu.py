@@ -10,13 +10,10 @@ the dequantised inputs (the oracle with round_p=False):
     |O - O_plain| <= 2^-4 a + 2^-18 b + 2^-8 |O_plain| + 2^-12 a
 elementwise, with a = sum_j p_j |v_j| / l and b = sum_j |v_j| / l from the
 oracle; 2^-8 |O| is the bf16 rounding of O and 2^-12 a covers the fp32
-arithmetic (exponentials, sums). Against the method itself (the oracle with
-round_p=True, P rounded in double) the outputs differ only by bf16 rounding,
-fp32 arithmetic and the rare weight that sits within fp32 error of an e4m3
-rounding midpoint and rounds the other way, so normwise
-    ||O - O_method||_F <= 2^-7 ||O_method||_F.
-The LSE carries no rounding of P: |LSE - LSE_ref| <= 1e-3 (the 16-bit path's
-bound).
+arithmetic (exponentials, sums). The bound holds whatever running max each
+weight is rounded against, so it does not depend on the kernel's tiling:
+the GPU is judged against the plain definition only. The LSE carries no
+rounding of P: |LSE - LSE_ref| <= 1e-3 (the 16-bit path's bound).
 """
 import numpy as np
 import pytest
@@ -46,27 +43,24 @@ def run_fp8_ex(fa2, q, k, v, qd, kd, vd, scale, causal):
 
 
 def assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, scale, rows=None, what="", causal=False):
-    om, op, lp, a, b = oracle.attention_fp8_both(q, k, v, qd, kd, vd, scale, rows=rows, causal=causal)
+    op, lp, a, b = oracle.attention_fp8(q, k, v, qd, kd, vd, scale, round_p=False, rows=rows, causal=causal)
     d = q.shape[-1]
     if rows is not None:
         o = o.reshape(-1, d)[rows]
         lse = lse.reshape(-1)[rows]
-    o, om, op, a, b = (x.reshape(-1, d) for x in (o, om, op, a, b))
+    o, op, a, b = (x.reshape(-1, d) for x in (o, op, a, b))
     assert np.isfinite(o).all(), what
     bound = 2.0 ** -4 * a + 2.0 ** -18 * b + 2.0 ** -8 * np.abs(op) + 2.0 ** -12 * a + 1e-7
     err = np.abs(o - op)
     bad = err > bound
-    assert not bad.any(), f"{what}: {int(bad.sum())} elements beyond the rounding bound, worst ratio " \
-                          f"{(err / bound).max():.3g}"
-    nrm = np.linalg.norm(om)
-    rel = np.linalg.norm(o - om) / nrm if nrm > 0 else np.linalg.norm(o)
-    assert rel <= 2.0 ** -7, f"{what}: ||O - O_method|| / ||O_method|| = {rel:.3g}"
+    worst = float((err / bound).max()) if err.size else 0.0
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements beyond the rounding bound, worst ratio {worst:.3g}"
     lse, lp = lse.reshape(-1), lp.reshape(-1)
     empty = np.isneginf(lp)                 # rows that see no key: o = 0, lse = -inf
     assert np.array_equal(np.isneginf(lse), empty), what
     assert not o[empty].any(), what
     assert np.max(np.abs(lse[~empty] - lp[~empty]), initial=0.0) <= 1e-3, what
-    return rel
+    return worst
 
 
 CASES = [
@@ -129,16 +123,13 @@ def test_fp8_accepts_torch_float8_tensors(gpu_lib):
     assert np.array_equal(o.float().cpu().numpy(), o2) and np.array_equal(lse.cpu().numpy(), lse2)
 
 
-def test_fp8_full_size_bench_workload_sampled_rows(gpu_lib):
-    # The workload bench.py times for FP8, in the same launch configuration;
-    # the oracle checks a seeded sample of rows, spread over every batch and
-    # head, plus the first and last row.
+def test_fp8_full_size_bench_workload(gpu_lib):
+    # The workload bench.py times for FP8, in the same launch configuration:
+    # every element against the oracle's plain definition.
     w = gen.workload("fp8_mha_B4_H16_N4096_d128_e4m3")
     q, k, v, qd, kd, vd = w.inputs()
     o, lse = run_fp8(gpu_lib, q, k, v, qd, kd, vd, w.scale)
-    total = w.B * w.Hq * w.N
-    rows = np.unique(np.concatenate([np.random.default_rng(5).integers(0, total, 1500), [0, total - 1]]))
-    assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, w.scale, rows=rows, what=w.name)
+    assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, w.scale, what=w.name)
 
 
 def test_fp8_rejects_unsupported_head_dim(gpu_lib):
@@ -204,15 +195,13 @@ def test_fp8_general_equal_lengths_route_to_the_packed_kernel(gpu_lib):
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
-def test_fp8_general_causal_full_size_sampled_rows(gpu_lib):
-    # The FP8 bench workload (B 4, H 16, N 4096) with the causal mask; the
-    # oracle checks a seeded sample of rows plus the first and last row.
+def test_fp8_general_causal_full_size(gpu_lib):
+    # The FP8 bench workload (B 4, H 16, N 4096) with the causal mask: every
+    # element against the oracle's plain definition.
     w = gen.workload("fp8_mha_B4_H16_N4096_d128_e4m3")
     q, k, v, qd, kd, vd = w.inputs()
     o, lse = run_fp8_ex(gpu_lib, q, k, v, qd, kd, vd, w.scale, True)
-    total = w.B * w.Hq * w.N
-    rows = np.unique(np.concatenate([np.random.default_rng(6).integers(0, total, 1500), [0, total - 1]]))
-    assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, w.scale, rows=rows, causal=True, what=w.name + " causal")
+    assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, w.scale, causal=True, what=w.name + " causal")
 
 
 @pytest.mark.parametrize("causal", [False, True])

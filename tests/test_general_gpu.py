@@ -108,23 +108,19 @@ def test_general_path_on_multiple_of_128_agrees_with_fast_path(gpu_lib):
     assert_parity(o, lse, o_ref, lse_ref, gen.BF16, "general 256x384")
 
 
-def test_causal_full_size_sampled_rows(gpu_lib):
-    """B=4, H=16, N=4096, d=128, causal: sampled rows against the oracle."""
+def test_causal_full_size(gpu_lib):
+    """B=4, H=16, N=4096, d=128, causal (the causal benchmark's workload and
+    launch): every element against the oracle."""
     import torch
 
-    B, H, N, d = 4, 16, 4096, 128
-    q, k, v = gen.make_qkv(3400, B, H, H, N, d, gen.BF16)
-    o, lse = gpu_lib.fa2_fwd_ex(to_dev(q, gen.BF16), to_dev(k, gen.BF16), to_dev(v, gen.BF16),
-                                scale=d ** -0.5, causal=True)
+    w = gen.workload("mha_B4_H16_N4096_d128_bf16")
+    q, k, v = w.inputs()
+    o, lse = gpu_lib.fa2_fwd_ex(to_dev(q, w.dtype), to_dev(k, w.dtype), to_dev(v, w.dtype),
+                                scale=w.scale, causal=True)
     assert gpu_lib.fa2_check_status(torch.cuda.current_stream().cuda_stream) == gpu_lib.FA2_OK
-    rng = np.random.default_rng(7)
-    rows = np.unique(np.concatenate([rng.integers(0, B * H * N, 160),
-                                     [0, 1, 127, 128, N - 1, N, 5 * N + 4095, B * H * N - 1]]))
-    idx = torch.from_numpy(rows).cuda()
-    o_s = o.reshape(-1, d).index_select(0, idx).float().cpu().numpy().astype(np.float64)
-    l_s = lse.reshape(-1).index_select(0, idx).cpu().numpy().astype(np.float64)
-    o_ref, lse_ref = oracle.attention_ex(q, k, v, d ** -0.5, gen.BF16, causal=True, rows=rows)
-    assert_parity(o_s, l_s, o_ref, lse_ref, gen.BF16, "causal B4 H16 N4096")
+    o_ref, lse_ref = oracle.attention_ex(q, k, v, w.scale, w.dtype, causal=True)
+    assert_parity(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+                  o_ref, lse_ref, w.dtype, "causal B4 H16 N4096")
     assert bool(torch.isfinite(o.float()).all())
 
 

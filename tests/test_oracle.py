@@ -425,6 +425,45 @@ def test_backward_closed_forms():
     assert not dq0.any() and not dk0.any() and not dv0.any()
 
 
+@pytest.mark.parametrize("causal,Hq,Hkv", [(False, 2, 2), (True, 4, 2)])
+def test_backward_bound_sums_follow_their_definitions(causal, Hq, Hkv):
+    """The absolute sums the GPU backward's elementwise bound is built from,
+    recomputed here with dense float64 numpy arrays from their definitions
+    (P, dS, O, a, E and F as matrices; grouped heads by repetition)."""
+    B, N, d, scale = 2, 33, 8, 0.3
+    q, k, v, do = bwd_inputs(54, B, Hq, Hkv, N, d)
+    dq, dk, dv, bnd = oracle.attention_bwd(q, k, v, do, scale, gen.BF16, causal=causal, bounds=True)
+    G = Hq // Hkv
+    Q, dO = (oracle.decode16(x, gen.BF16) for x in (q, do))
+    K, V = (np.repeat(oracle.decode16(x, gen.BF16), G, axis=1) for x in (k, v))
+    s = scale * np.einsum("bhid,bhjd->bhij", Q, K)
+    if causal:
+        s = np.where(np.triu(np.ones((N, N), bool), 1), -np.inf, s)
+    P = np.exp(s - s.max(-1, keepdims=True))
+    P /= P.sum(-1, keepdims=True)
+    O = P @ V
+    a = P @ np.abs(V)
+    E = np.sum(np.abs(dO) * (np.abs(O) + a), -1)                       # [b,h,i]
+    F = np.einsum("bhid,bhjd->bhij", np.abs(dO), np.abs(V))           # [b,h,i,j]
+    dS = P * (dO @ np.swapaxes(V, -1, -2) - np.sum(dO * O, -1)[..., None])
+    np.testing.assert_allclose(dq, scale * dS @ K, rtol=1e-10, atol=1e-12)
+    want_q = [scale * np.abs(dS) @ np.abs(K), scale * E[..., None] * (P @ np.abs(K)),
+              scale * (P * F) @ np.abs(K)]
+    kv = lambda x: x.reshape(B, Hkv, G, N, d).sum(axis=2)              # sum over a KV head's query heads
+    tr = lambda x: np.swapaxes(x, -1, -2)
+    want_k = [kv(scale * tr(np.abs(dS)) @ np.abs(Q)), kv(scale * tr(P * E[..., None]) @ np.abs(Q)),
+              kv(scale * tr(P * F) @ np.abs(Q))]
+    for got, want in zip(bnd["q"], want_q):
+        np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-13)
+    for got, want in zip(bnd["k"], want_k):
+        np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(bnd["v"], kv(tr(P) @ np.abs(dO)), rtol=1e-10, atol=1e-13)
+    # the bound sums dominate the gradients they bound
+    assert np.all(np.abs(dq) <= bnd["q"][0] * (1 + 1e-12) + 1e-15)
+    assert np.all(np.abs(dk) <= bnd["k"][0] * (1 + 1e-12) + 1e-15)
+    assert np.all(np.abs(dv) <= bnd["v"] * (1 + 1e-12) + 1e-15)
+
+
 # ---------------------------------------------------------------- FP8 (e4m3) inputs
 
 def _torch_e4m3():
