@@ -8,7 +8,13 @@ per step. Prints ONE JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--pass fwd|fwd_causal|bwd|bwd_causal]
-                    [--impl ours|reference] [--no-cpu-baseline]
+                    [--impl ours|reference] [--no-cpu-baseline] [--all-configs]
+
+--all-configs runs every forward workload configuration in turn (the tiny
+case, the B4 H16 N4096 headline, the twelve sequence-sweep points, the
+sharper-softmax d=64 case and the grouped-KV case) and prints one JSON line
+for each, then one line per sweep dtype with the harmonic mean of its six
+points (the averaging the Ampere series' Performance section uses).
 
 --pass picks what one step runs (default fwd, the line above):
   fwd_causal  fa2_fwd_ex (fa2_fwd_fp8_ex for an FP8 workload) with the
@@ -83,7 +89,7 @@ class Dist:
         self.pg = None
 
     def init(self, backend: str):
-        if self.world > 1:
+        if self.world > 1 and self.pg is None:
             import torch.distributed as dist
 
             dist.init_process_group(backend=backend)
@@ -213,6 +219,20 @@ def load_peak(fp8: bool = False):
         return 1900.0 * ratio, "fallback (1.9 PFLOP/s bf16 burst)" + tag
 
 
+def load_hbm_peak():
+    """Measured HBM copy bandwidth (GB/s), else the stated fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured (hbm_gbs, MEASURED_PEAKS.json)"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback (6.8 TB/s)"
+
+
+def ridge_flop_per_byte(tensor_peak_tflops: float) -> float:
+    """FLOP per byte where the tensor and HBM roofs meet."""
+    return tensor_peak_tflops * 1e12 / (load_hbm_peak()[0] * 1e9)
+
+
 def traffic_key(workload: str, which: str) -> str:
     return workload if which == "fwd" else f"{workload}:{which}"
 
@@ -265,7 +285,7 @@ def oracle_forward(w, inputs, rows, causal: bool = False):
     import oracle
 
     if w.fp8:
-        return oracle.attention_fp8(*inputs, w.scale, round_p=True, rows=rows, causal=causal)
+        return oracle.attention_fp8(*inputs, w.scale, round_p=False, rows=rows, causal=causal)
     q, k, v = inputs
     if causal:
         return oracle.attention_ex(q, k, v, w.scale, w.dtype, causal=True, rows=rows)
@@ -594,6 +614,33 @@ class Step:
         return (ins, outs), nbytes[0], nbytes[1]
 
 
+ALL_CONFIGS = (["tiny_B1_H1_N128_d128_bf16", "mha_B4_H16_N4096_d128_bf16"]
+               + [f"sweep_N{n}_{t}" for t in ("bf16", "fp16") for n in (512, 1024, 2048, 4096, 8192, 16384)]
+               + ["sharp_B8_H32_N2048_d64_bf16_x3", "gqa_B2_Hq32_Hkv8_N8192_d128_bf16"])
+
+
+def harmonic_mean_line(lines, tag, n_gpus):
+    """One line for the harmonic mean over the sweep points of one dtype."""
+    pts = [ln for ln in lines if ln["config"]["workload"].startswith("sweep_") and
+           ln["config"]["workload"].endswith(tag)]
+    if not pts:
+        return None
+    hm = len(pts) / sum(1.0 / ln["value"] for ln in pts)
+    hk = len(pts) / sum(1.0 / ln["roofline"]["achieved"] for ln in pts)
+    peak = pts[0]["roofline"]["peak"]
+    return {"metric": METRIC + "; harmonic mean over N in {512..16384}", "value": hm, "unit": UNIT,
+            "n_gpus": n_gpus, "steps": pts[0]["steps"], "warmup": pts[0]["warmup"],
+            "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": tag, "data": "synthetic",
+            "config": {"workload": f"sweep_{tag}_harmonic_mean", "points": {
+                ln["config"]["workload"]: round(ln["value"], 1) for ln in pts},
+                "B*N": 16384, "H": 16, "d": 128},
+            "roofline": {"bound": "tensor", "achieved": hk, "peak": peak, "unit": UNIT, "frac": hk / peak,
+                         "traffic": None, "peak_source": pts[0]["roofline"]["peak_source"],
+                         "kernel": pts[0]["roofline"]["kernel"],
+                         "note": "harmonic mean of the points' per-launch kernel rates"}}
+
+
 def run_ours(args, dist, w):
     import torch
 
@@ -671,6 +718,17 @@ def run_ours(args, dist, w):
         peak, peak_src = load_peak(w.fp8)
         achieved = flops / (kernel_ms * 1e-3) / 1e12
         nbytes = pass_bytes(w, args.pass_)
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                "frac": achieved / peak, "traffic": load_traffic(w.name, args.pass_),
+                "peak_source": peak_src, "kernel": step.kernel, "kernel_ms": kernel_ms,
+                "alg_flops_per_launch": flops, "alg_bytes_per_launch": nbytes,
+                "hbm_gbs_alg": nbytes / (kernel_ms * 1e-3) / 1e9}
+        if flops / nbytes < ridge_flop_per_byte(peak):
+            # left of the ridge (the one-tile case, N = 512): judged by bytes moved
+            hbm, hbm_src = load_hbm_peak()
+            roof.update({"bound": "hbm", "achieved": roof["hbm_gbs_alg"], "peak": hbm, "unit": "GB/s",
+                         "frac": roof["hbm_gbs_alg"] / hbm, "peak_source": hbm_src,
+                         "tflops": achieved})
         result = {
             "metric": metric_of(args.pass_, w), "value": value, "unit": UNIT, "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup,
@@ -678,11 +736,7 @@ def run_ours(args, dist, w):
             "scaling": "weak", "vs_baseline": None,
             "dtype": dtype_name(w), "data": "synthetic",
             "config": config_of(w, dist.world, args.pass_),
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                         "frac": achieved / peak, "traffic": load_traffic(w.name, args.pass_),
-                         "peak_source": peak_src, "kernel": step.kernel, "kernel_ms": kernel_ms,
-                         "alg_flops_per_launch": flops, "alg_bytes_per_launch": nbytes,
-                         "hbm_gbs_alg": nbytes / (kernel_ms * 1e-3) / 1e9},
+            "roofline": roof,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                     "ms_per_step": e2e_ms / e2e_steps,
@@ -709,17 +763,36 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="oracle time budget of a whole --impl reference run (warm-up + timed steps)")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="one line per forward workload configuration plus the sweep's harmonic means")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.all_configs and args.pass_ != "fwd":
+        ap.error("--all-configs runs the forward pass")
     dist = Dist()
-    w = gen.workload(args.workload)
-    if args.impl == "reference":
-        res = run_reference(args, dist, w)
-    else:
-        res = run_ours(args, dist, w)
-    if res is not None and dist.rank == 0:
-        print(json.dumps(res), flush=True)
+    names = ALL_CONFIGS if args.all_configs else [args.workload]
+    if args.all_configs and args.cpu_seconds == ap.get_default("cpu_seconds"):
+        args.cpu_seconds = 3.0        # 16 configurations: keep the oracle legs short
+    lines = []
+    for name in names:
+        w = gen.workload(name)
+        if args.impl == "reference":
+            res = run_reference(args, dist, w)
+        else:
+            res = run_ours(args, dist, w)
+        if res is not None and dist.rank == 0:
+            print(json.dumps(res), flush=True)
+            lines.append(res)
+        if args.impl != "reference" and args.all_configs:
+            import torch
+
+            torch.cuda.empty_cache()
+    if args.all_configs and args.impl != "reference" and dist.rank == 0:
+        for tag in ("bf16", "fp16"):
+            hm = harmonic_mean_line(lines, tag, dist.world)
+            if hm is not None:
+                print(json.dumps(hm), flush=True)
     dist.done()
 
 

@@ -115,3 +115,39 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+
+
+def test_all_configs_cover_every_forward_configuration():
+    names = bench.ALL_CONFIGS
+    assert len(names) == len(set(names)) == 16
+    ws = [gen.workload(n) for n in names]
+    assert not any(w.fp8 for w in ws)
+    sweep = [w for w in ws if w.name.startswith("sweep_")]
+    assert sorted({w.N for w in sweep}) == [512, 1024, 2048, 4096, 8192, 16384]
+    assert all(w.B * w.N == 16384 and w.Hq == 16 and w.d == 128 for w in sweep)
+    assert {w.dtype for w in sweep} == {gen.BF16, gen.FP16}
+
+
+def test_harmonic_mean_line():
+    def line(name, v, a):
+        return {"value": v, "steps": 10, "warmup": 3, "config": {"workload": name},
+                "roofline": {"achieved": a, "peak": 2000.0, "peak_source": "x", "kernel": "k"}}
+    lines = [line("sweep_N512_bf16", 1000.0, 1100.0), line("sweep_N1024_bf16", 2000.0, 2200.0),
+             line("sweep_N512_fp16", 5.0, 5.0), line("mha_B4_H16_N4096_d128_bf16", 7.0, 7.0)]
+    hm = bench.harmonic_mean_line(lines, "bf16", 1)
+    assert abs(hm["value"] - 2 / (1 / 1000 + 1 / 2000)) < 1e-9
+    assert abs(hm["roofline"]["achieved"] - 2 / (1 / 1100 + 1 / 2200)) < 1e-9
+    assert abs(hm["roofline"]["frac"] - hm["roofline"]["achieved"] / 2000.0) < 1e-12
+    assert set(hm["config"]["points"]) == {"sweep_N512_bf16", "sweep_N1024_bf16"}
+    assert bench.harmonic_mean_line(lines, "e4m3", 1) is None
+
+
+def test_left_of_the_ridge_are_the_one_tile_case_and_the_shortest_sweep_point():
+    # 64 and 255 FLOP/B against a ridge of ~281 (1901.5 TFLOP/s / 6759 GB/s)
+    peak, _ = bench.load_peak()
+    ridge = bench.ridge_flop_per_byte(peak)
+    left_names = {"tiny_B1_H1_N128_d128_bf16", "sweep_N512_bf16", "sweep_N512_fp16"}
+    for name in bench.ALL_CONFIGS:
+        w = gen.workload(name)
+        left = bench.pass_flops(w, "fwd") / bench.pass_bytes(w, "fwd") < ridge
+        assert left == (name in left_names), name
