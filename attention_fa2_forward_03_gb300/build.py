@@ -13,6 +13,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libfa2.so")
+# The same sources with FA2_DEBUG: device-side bounds checks that report
+# FA2_ERR_BOUNDS instead of touching memory outside the planned extents.
+DEBUG_LIB = os.path.join(PKG, "libfa2_debug.so")
 SOURCES = [os.path.join(CSRC, "fa2_fwd_sm103.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "ptx_sm103.cuh"), os.path.join(CSRC, "fa2_fwd_sm103.cuh"), os.path.join(CSRC, "fa2_bwd_sm103.cuh"), os.path.join(CSRC, "fa2_fwd_fp8_sm103.cuh"),
                      os.path.join(INCLUDE, "fa2.h")]
@@ -24,24 +27,30 @@ def nvcc() -> str:
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB):
+def needs_build(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in DEPENDS)
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile libfa2.so next to this file if it is missing or stale."""
-    if not force and not needs_build():
-        return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-           "-I", INCLUDE, "-o", tmp, *SOURCES]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    """Compile libfa2.so and libfa2_debug.so next to this file (in parallel)
+    if they are missing or stale; returns the release library's path."""
+    jobs = []
+    for lib, extra in ((LIB, []), (DEBUG_LIB, ["-DFA2_DEBUG"])):
+        if not force and not needs_build(lib):
+            continue
+        tmp = lib + f".tmp{os.getpid()}"
+        cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
+               *extra, "-I", INCLUDE, "-o", tmp, *SOURCES]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        jobs.append((subprocess.Popen(cmd), tmp, lib, cmd))
+    for proc, tmp, lib, cmd in jobs:
+        if proc.wait() != 0:
+            raise subprocess.CalledProcessError(proc.returncode, cmd)
+        os.replace(tmp, lib)
     return LIB
 
 

@@ -60,6 +60,9 @@ struct Params {
     int causal;
     float scale;          // softmax scale
     float scale_log2;     // scale * log2(e)
+    // Extents for the debug build's checks.
+    int heads_q, heads_kv;        // B * Hq, B * Hkv
+    long long rows_q, rows_kv;    // B * Hq * N, B * Hkv * N
 };
 
 // ---------------------------------------------------------------- D = rowsum(dO o O)
@@ -116,7 +119,7 @@ __device__ __forceinline__ void store_row_16(void* base, long long row, int d, i
 // warp-collective (.sync.aligned) and may not sit in a divergent branch.
 template <int D, bool kBf16>
 __device__ __forceinline__ void store_acc_row(uint32_t row_addr, uint32_t col, float mul, void* out,
-                                              long long grow, int c0, int c1, bool store) {
+                                              long long grow, long long rows, int c0, int c1, bool store) {
 #pragma unroll 1
     for (int cc = c0; cc < c1; cc += 32) {
         uint32_t a[32];
@@ -126,7 +129,7 @@ __device__ __forceinline__ void store_acc_row(uint32_t row_addr, uint32_t col, f
 #pragma unroll
         for (int i = 0; i < 16; ++i)
             h[i] = ptx::pack2<kBf16>(__uint_as_float(a[2 * i]) * mul, __uint_as_float(a[2 * i + 1]) * mul);
-        if (store) store_row_16(out, grow, D, cc, h);
+        if (store && FA2_DBG_OK(grow < rows, kDbgBwdRow)) store_row_16(out, grow, D, cc, h);
     }
 }
 
@@ -232,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive_expect_tx(bars.fixed_full(), 2 * L::kTileBytes);
 #pragma unroll
             for (int blk = 0; blk < D / 64; ++blk) {
+                if (!FA2_DBG_OK(kvh < p.heads_kv && kt * 128 < p.n, kDbgKvTile)) break;
                 ptx::tma_load_3d(sbase + L::kFixedOff + blk * L::kBlkBytes, &tmK, blk * 64, kt * 128, kvh,
                                  bars.fixed_full());
                 ptx::tma_load_3d(sbase + L::kFixedOff + L::kTileBytes + blk * L::kBlkBytes, &tmV, blk * 64, kt * 128,
@@ -244,16 +248,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int qh = q_head(g);
                 if (!(ok = w.wait(bars.q_empty(n % QS), ((n / QS) & 1) ^ 1, kSiteKvEmpty))) break;
                 ptx::mbar_arrive_expect_tx(bars.q_full(n % QS), L::kTileBytes);
+                if (FA2_DBG_OK(qh < p.heads_q && i * 128 < p.n, kDbgQTile))
 #pragma unroll
-                for (int blk = 0; blk < D / 64; ++blk)
-                    ptx::tma_load_3d(q_addr(n) + blk * L::kBlkBytes, &tmQ, blk * 64, i * 128, qh, bars.q_full(n % QS));
+                    for (int blk = 0; blk < D / 64; ++blk)
+                        ptx::tma_load_3d(q_addr(n) + blk * L::kBlkBytes, &tmQ, blk * 64, i * 128, qh,
+                                         bars.q_full(n % QS));
                 ++nq;
                 if (!(ok = w.wait(bars.do_empty(n % DS), ((n / DS) & 1) ^ 1, kSiteKvEmpty))) break;
                 ptx::mbar_arrive_expect_tx(bars.do_full(n % DS), L::kTileBytes);
+                if (FA2_DBG_OK(qh < p.heads_q && i * 128 < p.n, kDbgQTile))
 #pragma unroll
-                for (int blk = 0; blk < D / 64; ++blk)
-                    ptx::tma_load_3d(do_addr(n) + blk * L::kBlkBytes, &tmDO, blk * 64, i * 128, qh,
-                                     bars.do_full(n % DS));
+                    for (int blk = 0; blk < D / 64; ++blk)
+                        ptx::tma_load_3d(do_addr(n) + blk * L::kBlkBytes, &tmDO, blk * 64, i * 128, qh,
+                                         bars.do_full(n % DS));
                 ++nd;
                 if (++i == p.n_tiles) {
                     i = first;
@@ -357,8 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int q = ii * 128 + c0 + 32 * h + lane;
-                nl_nx[h] = q < p.n ? -__ldg(p.lse + base + q) * kLog2e : -INFINITY;
-                d_nx[h] = q < p.n ? __ldg(p.delta + base + q) : 0.0f;
+                const bool in = q < p.n && FA2_DBG_OK(base + q < p.rows_q, kDbgBwdRow);
+                nl_nx[h] = in ? -__ldg(p.lse + base + q) * kLog2e : -INFINITY;
+                d_nx[h] = in ? __ldg(p.delta + base + q) : 0.0f;
             }
         };
         if (steps > 0) fetch(g, qi);
@@ -442,9 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long grow = static_cast<long long>(kvh) * p.n + kt * 128 + row;
             const bool valid = kt * 128 + row < p.n;
             if (c0 == 0)   // warp-uniform: warps 0-3 write dV, warps 4-7 dK
-                store_acc_row<D, kBf16>(row_addr, L::kColAcc0, 1.0f, p.dv, grow, 0, D, valid);
+                store_acc_row<D, kBf16>(row_addr, L::kColAcc0, 1.0f, p.dv, grow, p.rows_kv, 0, D, valid);
             else
-                store_acc_row<D, kBf16>(row_addr, L::kColAcc1, p.scale, p.dk, grow, 0, D, valid);
+                store_acc_row<D, kBf16>(row_addr, L::kColAcc1, p.scale, p.dk, grow, p.rows_kv, 0, D, valid);
         }
     }
 
@@ -551,6 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive_expect_tx(bars.fixed_full(), 2 * L::kTileBytes);
 #pragma unroll
             for (int blk = 0; blk < D / 64; ++blk) {
+                if (!FA2_DBG_OK(qh < p.heads_q && qt * 128 < p.n, kDbgQTile)) break;
                 ptx::tma_load_3d(sbase + L::kFixedOff + blk * L::kBlkBytes, &tmQ, blk * 64, qt * 128, qh,
                                  bars.fixed_full());
                 ptx::tma_load_3d(sbase + L::kFixedOff + L::kTileBytes + blk * L::kBlkBytes, &tmDO, blk * 64, qt * 128,
@@ -561,15 +570,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int n = 0; n < steps && ok; ++n) {
                 if (!(ok = w.wait(bars.k_empty(n % KS), ((n / KS) & 1) ^ 1, kSiteKvEmpty))) break;
                 ptx::mbar_arrive_expect_tx(bars.k_full(n % KS), L::kTileBytes);
+                if (FA2_DBG_OK(kvh < p.heads_kv && n * 128 < p.n, kDbgKvTile))
 #pragma unroll
-                for (int blk = 0; blk < D / 64; ++blk)
-                    ptx::tma_load_3d(k_addr(n) + blk * L::kBlkBytes, &tmK, blk * 64, n * 128, kvh, bars.k_full(n % KS));
+                    for (int blk = 0; blk < D / 64; ++blk)
+                        ptx::tma_load_3d(k_addr(n) + blk * L::kBlkBytes, &tmK, blk * 64, n * 128, kvh,
+                                         bars.k_full(n % KS));
                 ++nk;
                 if (!(ok = w.wait(bars.v_empty(n % VS), ((n / VS) & 1) ^ 1, kSiteKvEmpty))) break;
                 ptx::mbar_arrive_expect_tx(bars.v_full(n % VS), L::kTileBytes);
+                if (FA2_DBG_OK(kvh < p.heads_kv && n * 128 < p.n, kDbgKvTile))
 #pragma unroll
-                for (int blk = 0; blk < D / 64; ++blk)
-                    ptx::tma_load_3d(v_addr(n) + blk * L::kBlkBytes, &tmV, blk * 64, n * 128, kvh, bars.v_full(n % VS));
+                    for (int blk = 0; blk < D / 64; ++blk)
+                        ptx::tma_load_3d(v_addr(n) + blk * L::kBlkBytes, &tmV, blk * 64, n * 128, kvh,
+                                         bars.v_full(n % VS));
                 ++nv;
             }
             if (!ok) {
@@ -653,8 +666,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // its P and dS are exactly 0 and it is not stored.
         const bool row_valid = qt * 128 + row < p.n;
         const long long grow = static_cast<long long>(qh) * p.n + qt * 128 + row;
-        const float lse2 = row_valid ? p.lse[grow] * 1.4426950408889634f : INFINITY;
-        const float dl = row_valid ? p.delta[grow] : 0.0f;
+        const bool in = row_valid && FA2_DBG_OK(grow < p.rows_q, kDbgBwdRow);
+        const float lse2 = in ? p.lse[grow] * 1.4426950408889634f : INFINITY;
+        const float dl = in ? p.delta[grow] : 0.0f;
         const int key_end = p.n - (p.n_tiles - 1) * 128;   // keys of the last key tile (1..128)
         bool ok = true;
         for (int n = 0; n < steps; ++n) {
@@ -715,8 +729,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = w.wait(bars.acc_full(), 0, kSiteOFull);
         if (__all_sync(0xffffffffu, ok)) {
             ptx::tc_fence_after();
-            store_acc_row<D, kBf16>(row_addr, L::kColAcc, p.scale, p.dq, grow, c0 * D / 128, (c0 + 64) * D / 128,
-                                    row_valid);
+            store_acc_row<D, kBf16>(row_addr, L::kColAcc, p.scale, p.dq, grow, p.rows_q, c0 * D / 128,
+                                    (c0 + 64) * D / 128, row_valid);
         }
     }
 

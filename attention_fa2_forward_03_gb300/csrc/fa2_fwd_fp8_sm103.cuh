@@ -47,7 +47,10 @@ struct Lay {
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = kNQ * kTile;
     static constexpr int kVtOff = kRingOff + kStages * kTile;
-    static constexpr int kBarOff = kVtOff + 2 * kTile;
+    // Epilogue staging: 128 rows x 64 bf16 columns (the 16-bit kernel's form)
+    static constexpr int kStageOff = kVtOff + 2 * kTile;
+    static constexpr int kStageBytes = kBM * 128;
+    static constexpr int kBarOff = kStageOff + kStageBytes;
     // q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] alpha[2] stats[2]
     // p_full[2] o_full[2] mma_done vt_full[2] vt_empty[2] stats_free[2]
     static constexpr int kNumBars = 2 * kStages + 21;
@@ -97,7 +100,8 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmQ, const CUtensorM
         for (int t = 0; t < item.n_tiles && ok; ++t) {
             if (!(ok = w.wait(bars.q_empty(t), (nq[t] & 1) ^ 1, kSiteQEmpty))) break;
             ptx::mbar_arrive_expect_tx(bars.q_full(t), kTile);
-            ptx::tma_load_2d(sbase + Lay::kQOff + t * kTile, tmQ, 0, item.q_row0 + t * kBM, bars.q_full(t));
+            if (FA2_DBG_OK(item.q_row0 + t * kBM + kBM <= p.rows_q, kDbgQTile))
+                ptx::tma_load_2d(sbase + Lay::kQOff + t * kTile, tmQ, 0, item.q_row0 + t * kBM, bars.q_full(t));
             ++nq[t];
         }
         const int nxt = it + gridDim.x;
@@ -109,8 +113,9 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmQ, const CUtensorM
             const int s = ring % S;
             if (!(ok = w.wait(bars.kv_empty(s), ((ring / S) & 1) ^ 1, kSiteKvEmpty))) break;
             ptx::mbar_arrive_expect_tx(bars.kv_full(s), kTile);
-            ptx::tma_load_2d(sbase + Lay::kRingOff + s * kTile, (k & 1) ? tmV : tmK, 0,
-                             item.kv_row0 + (k >> 1) * kBN, bars.kv_full(s));
+            if (FA2_DBG_OK(item.kv_row0 + (k >> 1) * kBN + kBN <= p.rows_kv, kDbgKvTile))
+                ptx::tma_load_2d(sbase + Lay::kRingOff + s * kTile, (k & 1) ? tmV : tmK, 0,
+                                 item.kv_row0 + (k >> 1) * kBN, bars.kv_full(s));
             ++ring;
         }
     }
@@ -137,7 +142,8 @@ __device__ __forceinline__ void producer_gen(const CUtensorMap* tmQ, const CUten
             if (g.nkv[t] == 0) continue;
             if (!(ok = w.wait(bars.q_empty(t), (nq[t] & 1) ^ 1, kSiteQEmpty))) break;
             ptx::mbar_arrive_expect_tx(bars.q_full(t), kTile);
-            ptx::tma_load_3d(sbase + Lay::kQOff + t * kTile, tmQ, 0, g.q0 + t * kBM, g.head, bars.q_full(t));
+            if (FA2_DBG_OK(g.head < p.heads_q && g.q0 + t * kBM < p.nq, kDbgQTile))
+                ptx::tma_load_3d(sbase + Lay::kQOff + t * kTile, tmQ, 0, g.q0 + t * kBM, g.head, bars.q_full(t));
             ++nq[t];
         }
         const int nmax = max(g.nkv[0], g.nkv[1]);
@@ -145,8 +151,9 @@ __device__ __forceinline__ void producer_gen(const CUtensorMap* tmQ, const CUten
             const int s = ring % S;
             if (!(ok = w.wait(bars.kv_empty(s), ((ring / S) & 1) ^ 1, kSiteKvEmpty))) break;
             ptx::mbar_arrive_expect_tx(bars.kv_full(s), kTile);
-            ptx::tma_load_3d(sbase + Lay::kRingOff + s * kTile, (k & 1) ? tmV : tmK, 0, (k >> 1) * kBN, g.kvhead,
-                             bars.kv_full(s));
+            if (FA2_DBG_OK(g.kvhead < p.heads_kv && (k >> 1) * kBN < p.nk, kDbgKvTile))
+                ptx::tma_load_3d(sbase + Lay::kRingOff + s * kTile, (k & 1) ? tmV : tmK, 0, (k >> 1) * kBN, g.kvhead,
+                                 bars.kv_full(s));
             ++ring;
         }
     }
@@ -560,132 +567,6 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
     }
 }
 
-// ---------------------------------------------------------------- correction + epilogue
-
-template <bool kGen>
-__device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, uint8_t* smem, const BarsF8& bars,
-                                                const Waiter& w) {
-    constexpr int kChunk = 32;
-    const int q = (threadIdx.x / 32) & 3;
-    const int lane = threadIdx.x & 31;
-    const int row = 32 * q + lane;
-    const uint32_t row_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
-    const float* rowbuf = reinterpret_cast<const float*>(smem + Lay::kRowOff);
-
-    int n_s[2] = {0, 0};
-    int n_items[2] = {0, 0};
-    bool ok = true;
-    for (int it = blockIdx.x; it < p.total_items && ok; it = next_item<kGen>(it)) {
-        // row0: first row of tile 0 in the output view; q0: the same row's
-        // index within its head (general mode, for the ragged-end check).
-        int n_tiles, nkv[2], row0, q0 = 0, grp;
-        if constexpr (kGen) {
-            const ItemG g = make_item_gen(p, it);
-            n_tiles = g.n_tiles;
-            nkv[0] = g.nkv[0];
-            nkv[1] = g.nkv[1];
-            row0 = g.head * p.nq + g.q0;
-            q0 = g.q0;
-            grp = g.kvhead;
-        } else {
-            const Item item = make_item(p, it);
-            n_tiles = item.n_tiles;
-            nkv[0] = nkv[1] = p.n_kv_tiles;
-            row0 = item.q_row0;
-            grp = item_group(p, it);
-        }
-        const float dv = __ldg(p.v_descale + grp);
-        const int nmax = max(nkv[0], n_tiles > 1 ? nkv[1] : 0);
-        for (int j = 0; j < nmax && ok; ++j) {
-            for (int t = 0; t < n_tiles; ++t) {
-                if (j >= nkv[t]) continue;
-                ok = w.wait(bars.alpha_ready(t), n_s[t] & 1, kSiteAlpha);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
-                ++n_s[t];
-                const float alpha = rowbuf[t * kBM + row];
-                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-                    ptx::tc_fence_after();
-                    const uint32_t colO = Lay::col_o(t);
-                    const uint64_t a2 = ptx::f2_pack(alpha, alpha);
-#pragma unroll
-                    for (int h = 0; h < kD; h += kChunk) {
-                        uint32_t o[kChunk];
-                        ptx::tmem_ld32_at<0>(row_addr + colO + h, o);
-                        ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < kChunk / 2; ++i) {
-                            float o0, o1;
-                            ptx::f2_unpack(
-                                ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
-                                            a2),
-                                o0, o1);
-                            o[2 * i] = __float_as_uint(o0);
-                            o[2 * i + 1] = __float_as_uint(o1);
-                        }
-                        ptx::tmem_st32_at<0>(row_addr + colO + h, o);
-                    }
-                    ptx::tmem_wait_st();
-                }
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(bars.p_full(t));
-            }
-        }
-        // Epilogue: O * dv / l' -> bf16, LSE = (m + log2 l' - 8) ln 2.
-        for (int t = 0; t < n_tiles && ok; ++t) {
-            const int grow = row0 + t * kBM + row;
-            // Rows past a ragged query end are computed but not stored.
-            const bool valid = !kGen || q0 + t * kBM + row < p.nq;
-            if (kGen && nkv[t] == 0) {
-                // No row of this tile may attend any key: O = 0, LSE = -inf.
-                if (valid) {
-                    uint4* z = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + static_cast<size_t>(grow) * kD);
-#pragma unroll
-                    for (int v = 0; v < kD / 8; ++v) z[v] = make_uint4(0, 0, 0, 0);
-                    p.lse[grow] = -INFINITY;
-                }
-                continue;
-            }
-            ok = w.wait(bars.stats_ready(t), n_items[t] & 1, kSiteStats);
-            if (ok) ok = w.wait(bars.o_full(t), n_items[t] & 1, kSiteOFull);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
-            ++n_items[t];
-            ptx::tc_fence_after();
-            const float m = rowbuf[(2 + t) * kBM + row];
-            const float l = rowbuf[(4 + t) * kBM + row];
-            if constexpr (kGen) ptx::mbar_arrive(bars.stats_free(t));   // m, l read: may be overwritten
-            // l' = 0 only for a row with no allowed key: O = 0, LSE = -inf.
-            const float f = (!kGen || l > 0.0f) ? dv * ptx::rcp_approx(l) : 0.0f;
-            const uint32_t colO = Lay::col_o(t);
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + static_cast<size_t>(grow) * kD);
-#pragma unroll
-            for (int h = 0; h < kD; h += kChunk) {
-                uint32_t o[kChunk];
-                ptx::tmem_ld32_at<0>(row_addr + colO + h, o);
-                ptx::tmem_wait_ld();
-                uint32_t hv[kChunk / 2];
-#pragma unroll
-                for (int i = 0; i < kChunk / 2; ++i)
-                    hv[i] = ptx::pack2<true>(__uint_as_float(o[2 * i]) * f, __uint_as_float(o[2 * i + 1]) * f);
-                if (valid) {
-#pragma unroll
-                    for (int v = 0; v < kChunk / 8; ++v)
-                        dst[h / 8 + v] = make_uint4(hv[4 * v], hv[4 * v + 1], hv[4 * v + 2], hv[4 * v + 3]);
-                }
-            }
-            if (valid)
-                p.lse[grow] = (!kGen || l > 0.0f) ? (m + ptx::lg2_approx(l) - 8.0f) * 0.69314718055994530942f
-                                                  : -INFINITY;
-        }
-        ptx::tc_fence_before();
-    }
-}
-
 }  // namespace fp8
 
 // ---------------------------------------------------------------- kernel
@@ -749,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fp8::softmax_role<kGen>(p, tmem, smem, bars, w, warp / 4);
     } else if (warp < kLoadWarp) {
         ptx::setmaxnreg_dec<kRegCorr>();
-        fp8::correction_role<kGen>(p, tmem, smem, bars, w);
+        correction_role<L, fp8::BarsF8, fp8::kD, true, kGen, true>(p, tmem, smem, sbase, bars, w);
     } else {
         ptx::setmaxnreg_dec<kRegOther>();
         if (warp == kLoadWarp) {

@@ -230,6 +230,9 @@ fa2_status fwd_general(const void* q, const void* k, const void* v, void* o, flo
     p.tq = static_cast<int>(tq);
     p.pairs = static_cast<int>((tq + fa2::kNQ - 1) / fa2::kNQ);
     p.total_items = static_cast<int>(items);
+    p.heads_kv = B * H_kv;
+    p.rows_q = rows_q;
+    p.rows_kv = rows_kv;
     const dim3 grid(static_cast<unsigned>(std::min<long long>(items, sm_count(dev))));
 
     const bool bf = dtype == FA2_BF16;
@@ -280,6 +283,9 @@ fa2_status fwd_fp8_general(const void* q, const void* k, const void* v, const fl
     p.tq = static_cast<int>(tq);
     p.pairs = static_cast<int>((tq + fa2::kNQ - 1) / fa2::kNQ);
     p.total_items = static_cast<int>(items);
+    p.heads_kv = B * H_kv;
+    p.rows_q = rows_q;
+    p.rows_kv = rows_kv;
     p.q_descale = q_descale;
     p.k_descale = k_descale;
     p.v_descale = v_descale;
@@ -328,6 +334,9 @@ fa2_status fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, flo
     p.pairs = (p.q_tiles + fa2::kNQ - 1) / fa2::kNQ;
     p.total_items = static_cast<int>(p.pairs * groups);
     p.kv_rows = N;
+    p.heads_kv = B * H_kv;
+    p.rows_q = rows_q;
+    p.rows_kv = static_cast<long long>(rows_kv);
     p.debug_flags = g_debug_flags.load();
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     // Persistent grid: one CTA per SM (shared memory and TMEM admit one).
@@ -379,6 +388,9 @@ fa2_status fa2_fwd_fp8(const void* q, const void* k, const void* v, const float*
     p.pairs = (p.q_tiles + fa2::kNQ - 1) / fa2::kNQ;
     p.total_items = static_cast<int>(p.pairs * groups);
     p.kv_rows = N;
+    p.heads_kv = B * H_kv;
+    p.rows_q = rows_q;
+    p.rows_kv = static_cast<long long>(rows_kv);
     p.debug_flags = g_debug_flags.load();
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     p.q_descale = q_descale;
@@ -485,6 +497,10 @@ fa2_status bwd_launch(int dev, const void* q, const void* k, const void* v, cons
     p.causal = causal;
     p.scale = scale;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.heads_q = B * H_q;
+    p.heads_kv = B * H_kv;
+    p.rows_q = rows_q;
+    p.rows_kv = static_cast<long long>(B) * H_kv * N;
     const bool bf = dtype == FA2_BF16;
     const dim3 gdelta(static_cast<unsigned>((rows_q + 15) / 16));
     const dim3 gkv(static_cast<unsigned>(p.n_tiles), static_cast<unsigned>(B * H_kv));
@@ -579,7 +595,8 @@ fa2_status fa2_check_status(cudaStream_t stream) {
         if (cudaMemcpyToSymbol(fa2::g_fa2_status, &zero, sizeof(int)) != cudaSuccess)
             result = cuda_fail();
         else
-            result = (v & 0xFF) == FA2_ERR_TIMEOUT ? FA2_ERR_TIMEOUT : FA2_ERR_CUDA;
+            result = (v & 0xFF) == FA2_ERR_TIMEOUT || (v & 0xFF) == FA2_ERR_BOUNDS ? static_cast<fa2_status>(v & 0xFF)
+                                                                                   : FA2_ERR_CUDA;
     }
     if (sdev != cur && cudaSetDevice(cur) != cudaSuccess) return cuda_fail();
     return result;
@@ -592,6 +609,7 @@ const char* fa2_status_string(fa2_status s) {
         case FA2_ERR_UNSUPPORTED: return "FA2_ERR_UNSUPPORTED";
         case FA2_ERR_CUDA: return "FA2_ERR_CUDA";
         case FA2_ERR_TIMEOUT: return "FA2_ERR_TIMEOUT";
+        case FA2_ERR_BOUNDS: return "FA2_ERR_BOUNDS";
     }
     return "FA2_ERR_UNKNOWN";
 }
@@ -603,6 +621,10 @@ int64_t fa2_set_wait_limit_ns(int64_t limit_ns) {
 
 int fa2_set_debug_flags(int flags) { return g_debug_flags.exchange(flags); }
 
-const char* fa2_version(void) { return "fa2-sm103a 0.1.0"; }
+#ifdef FA2_DEBUG
+const char* fa2_version(void) { return "fa2-sm103a 0.2.0 debug"; }
+#else
+const char* fa2_version(void) { return "fa2-sm103a 0.2.0"; }
+#endif
 
 }  // extern "C"

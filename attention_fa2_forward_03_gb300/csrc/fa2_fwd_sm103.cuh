@@ -89,6 +89,10 @@ struct Params {
     int hq;              // Hq
     int group;           // Hq / Hkv
     int tq;              // ceil(nq / 128): query tiles per head
+    int heads_kv;        // B * Hkv
+    // Extents for the debug build's checks: rows of the [rows, D] views of
+    // Q / O / LSE and of K / V (equal-length mode), or per head (nq, nk).
+    long long rows_q, rows_kv;
     // FP8 kernel only: fp32 descales per (batch, KV head) group.
     const float* q_descale;
     const float* k_descale;
@@ -102,7 +106,11 @@ struct Layout {
     static constexpr int kStages = D == 128 ? 4 : 8;   // K/V ring stages
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = kNQ * kTileBytes;
-    static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
+    // Epilogue staging: 128 rows x 64 columns of 16-bit O (128 bytes a row),
+    // one 32-row slice per correction warp, which reads it back transposed.
+    static constexpr int kStageOff = kRingOff + kStages * kTileBytes;
+    static constexpr int kStageBytes = kBM * 128;
+    static constexpr int kBarOff = kStageOff + kStageBytes;
     // q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] alpha[2] stats[2]
     // p_full[2] o_full[2] mma_done stats_free[2]
     static constexpr int kNumBars = 2 * kStages + 17;
@@ -118,6 +126,28 @@ struct Layout {
 };
 
 __device__ int g_fa2_status;  // per device; 0 = OK
+
+// Debug builds (compiled with FA2_DEBUG: libfa2_debug.so) check every tile
+// start a TMA copy is given and every global row a thread stores or loads
+// outside TMA against the extents the host planned with. A failed check
+// records FA2_ERR_BOUNDS and its site in the status word and skips the
+// access (it never traps). Release builds compile the checks away: the
+// condition is not even evaluated.
+enum DbgSite : int {
+    kDbgQTile = 32,     // a query tile's first row
+    kDbgKvTile = 33,    // a K/V tile's first row
+    kDbgORow = 34,      // an O / LSE row stored by the epilogue
+    kDbgBwdRow = 35,    // a row the backward reads (LSE, D) or stores (dQ, dK, dV)
+};
+#ifdef FA2_DEBUG
+__device__ __forceinline__ bool dbg_in_bounds(bool ok, int site) {
+    if (!ok) atomicCAS(&g_fa2_status, 0, FA2_ERR_BOUNDS | (site << 8));
+    return ok;
+}
+#define FA2_DBG_OK(cond, site) (::fa2::dbg_in_bounds((cond), (site)))
+#else
+#define FA2_DBG_OK(cond, site) (true)
+#endif
 
 struct Waiter {
     volatile int* abort_flag;
@@ -320,10 +350,11 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmQ, const CUtensorM
             if (load_q) {
                 const uint32_t dst = sbase + L::kQOff + t * L::kTileBytes;
                 ptx::mbar_arrive_expect_tx(bars.q_full(t), L::kTileBytes);
+                if (FA2_DBG_OK(item.q_row0 + t * kBM + kBM <= p.rows_q, kDbgQTile))
 #pragma unroll
-                for (int blk = 0; blk < D / 64; ++blk)
-                    ptx::tma_load_2d(dst + blk * L::kBlkBytes, tmQ, blk * 64, item.q_row0 + t * kBM,
-                                     bars.q_full(t));
+                    for (int blk = 0; blk < D / 64; ++blk)
+                        ptx::tma_load_2d(dst + blk * L::kBlkBytes, tmQ, blk * 64, item.q_row0 + t * kBM,
+                                         bars.q_full(t));
             }
             ++nq[t];
         }
@@ -343,9 +374,10 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmQ, const CUtensorM
             const CUtensorMap* tm = (k & 1) ? tmV : tmK;
             const int row = item.kv_row0 + (k >> 1) * kBN;
             ptx::mbar_arrive_expect_tx(bars.kv_full(s), L::kTileBytes);
+            if (FA2_DBG_OK(row + kBN <= p.rows_kv, kDbgKvTile))
 #pragma unroll
-            for (int blk = 0; blk < D / 64; ++blk)
-                ptx::tma_load_2d(dst + blk * L::kBlkBytes, tm, blk * 64, row, bars.kv_full(s));
+                for (int blk = 0; blk < D / 64; ++blk)
+                    ptx::tma_load_2d(dst + blk * L::kBlkBytes, tm, blk * 64, row, bars.kv_full(s));
             ++ring;
         }
     }
@@ -481,9 +513,11 @@ __device__ __forceinline__ void producer_gen(const CUtensorMap* tmQ, const CUten
             if (load_q) {
                 const uint32_t dst = sbase + L::kQOff + t * L::kTileBytes;
                 ptx::mbar_arrive_expect_tx(bars.q_full(t), L::kTileBytes);
+                if (FA2_DBG_OK(g.head < p.heads_q && g.q0 + t * kBM < p.nq, kDbgQTile))
 #pragma unroll
-                for (int blk = 0; blk < D / 64; ++blk)
-                    ptx::tma_load_3d(dst + blk * L::kBlkBytes, tmQ, blk * 64, g.q0 + t * kBM, g.head, bars.q_full(t));
+                    for (int blk = 0; blk < D / 64; ++blk)
+                        ptx::tma_load_3d(dst + blk * L::kBlkBytes, tmQ, blk * 64, g.q0 + t * kBM, g.head,
+                                         bars.q_full(t));
             }
             ++nq[t];
         }
@@ -494,9 +528,11 @@ __device__ __forceinline__ void producer_gen(const CUtensorMap* tmQ, const CUten
             const uint32_t dst = sbase + L::kRingOff + s * L::kTileBytes;
             const CUtensorMap* tm = (k & 1) ? tmV : tmK;
             ptx::mbar_arrive_expect_tx(bars.kv_full(s), L::kTileBytes);
+            if (FA2_DBG_OK(g.kvhead < p.heads_kv && (k >> 1) * kBN < p.nk, kDbgKvTile))
 #pragma unroll
-            for (int blk = 0; blk < D / 64; ++blk)
-                ptx::tma_load_3d(dst + blk * L::kBlkBytes, tm, blk * 64, (k >> 1) * kBN, g.kvhead, bars.kv_full(s));
+                for (int blk = 0; blk < D / 64; ++blk)
+                    ptx::tma_load_3d(dst + blk * L::kBlkBytes, tm, blk * 64, (k >> 1) * kBN, g.kvhead,
+                                     bars.kv_full(s));
             ++ring;
         }
     }
@@ -758,16 +794,24 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
 
 // ---------------------------------------------------------------- correction + epilogue
 
-template <int D, bool kBf16, bool kGen>
-__device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, uint8_t* smem, const Bars<D>& bars,
-                                                const Waiter& w) {
-    using L = Layout<D>;
-    constexpr int kChunk = 32;  // O is rescaled / stored 32 columns at a time
+// Shared by the 16-bit and the FP8 kernel (L, BarsT: their shared-memory
+// layout and barriers; kFp8: O is also multiplied by the item's V descale and
+// the LSE loses the 2^8 the FP8 softmax scales its weights by).
+template <class L, class BarsT, int D, bool kBf16, bool kGen, bool kFp8>
+__device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, uint8_t* smem, uint32_t sbase,
+                                                const BarsT& bars, const Waiter& w) {
+    constexpr int kChunk = 32;        // O is rescaled 32 columns at a time
+    constexpr int kHalves = D / 64;   // the epilogue stores 64 columns (128 bytes a row) at a time
     const int q = (threadIdx.x / 32) & 3;      // TMEM lane quarter
     const int lane = threadIdx.x & 31;
     const int row = 32 * q + lane;
     const uint32_t row_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
     const float* rowbuf = reinterpret_cast<const float*>(smem + L::kRowOff);  // alpha | m | l
+    // This warp's 32-row slice of the staging buffer (128 bytes a row). The
+    // 16-byte chunk c of row r sits at chunk c ^ (r mod 8), so that both the
+    // row-per-lane writes and the transposed reads hit every bank group
+    // equally (4 wavefronts per 512 bytes, the minimum).
+    const uint32_t wslice = sbase + L::kStageOff + static_cast<uint32_t>(q) * (32u * 128u);
 
     int n_s[2] = {0, 0};
     int n_items[2] = {0, 0};
@@ -775,7 +819,7 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
     for (int it = blockIdx.x; it < p.total_items && ok; it = next_item<kGen>(it)) {
         // row0: first row of tile 0 in the output view; q0: the same row's
         // index within its head (general mode, for the ragged-end check).
-        int n_tiles, nkv[2], row0, q0 = 0;
+        int n_tiles, nkv[2], row0, q0 = 0, head = 0, grp;
         if constexpr (kGen) {
             const ItemG g = make_item_gen(p, it);
             n_tiles = g.n_tiles;
@@ -783,12 +827,17 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
             nkv[1] = g.nkv[1];
             row0 = g.head * p.nq + g.q0;
             q0 = g.q0;
+            head = g.head;
+            grp = g.kvhead;
         } else {
             const Item item = make_item(p, it);
             n_tiles = item.n_tiles;
             nkv[0] = nkv[1] = p.n_kv_tiles;
             row0 = item.q_row0;
+            grp = it / p.pairs;         // the item's (batch, KV head)
         }
+        float out_scale = 1.0f;         // O = out_scale * O_acc / l
+        if constexpr (kFp8) out_scale = __ldg(p.v_descale + grp);
         const int nmax = max(nkv[0], n_tiles > 1 ? nkv[1] : 0);
         for (int j = 0; j < nmax && ok; ++j) {
             for (int t = 0; t < n_tiles; ++t) {
@@ -830,16 +879,17 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
                 ptx::mbar_arrive(bars.p_full(t));
             }
         }
-        // Epilogue for each tile of the item: O / l -> 16 bit, LSE. The next
-        // item's first PV overwrites O only after this warpgroup's next
-        // p_full arrival, which comes after these loads.
+        // Epilogue for each tile of the item: O / l -> 16 bit, stored in
+        // whole 128-byte lines through the warp's staging slice; LSE direct.
+        // The next item's first PV overwrites O only after this
+        // warpgroup's next p_full arrival, which comes after these loads.
         for (int t = 0; t < n_tiles && ok; ++t) {
             const int grow = row0 + t * kBM + row;
             // Rows past a ragged query end are computed but not stored.
             const bool valid = !kGen || q0 + t * kBM + row < p.nq;
             if (kGen && nkv[t] == 0) {
                 // No row of this tile may attend any key: O = 0, LSE = -inf.
-                if (valid) {
+                if (valid && FA2_DBG_OK(grow < p.rows_q, kDbgORow)) {
                     uint4* z = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + static_cast<size_t>(grow) * D);
 #pragma unroll
                     for (int v = 0; v < D / 8; ++v) z[v] = make_uint4(0, 0, 0, 0);
@@ -859,26 +909,69 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
             const float l = rowbuf[(4 + t) * kBM + row];
             if constexpr (kGen) ptx::mbar_arrive(bars.stats_free(t));   // m, l read: may be overwritten
             // l = 0 only for a row with no allowed key: O = 0, LSE = -inf.
-            const float inv_l = (!kGen || l > 0.0f) ? ptx::rcp_approx(l) : 0.0f;
+            const float inv_l = (!kGen || l > 0.0f) ? out_scale * ptx::rcp_approx(l) : 0.0f;
             const uint32_t colO = L::col_o(t);
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + static_cast<size_t>(grow) * D);
 #pragma unroll
-            for (int h = 0; h < D; h += kChunk) {
-                uint32_t o[kChunk];
-                ptx::tmem_ld32_at<0>(row_addr + colO + h, o);
-                ptx::tmem_wait_ld();
-                uint32_t hv[kChunk / 2];
+            for (int h = 0; h < kHalves; ++h) {
+                // 64 columns -> 32 packed pairs. At d = 128 each 32-column
+                // load is converted before the next (fewer live registers:
+                // no spills); at d = 64 both loads share one wait.
+                uint32_t hv[32];
+                if constexpr (D == 128) {
 #pragma unroll
-                for (int i = 0; i < kChunk / 2; ++i)
-                    hv[i] = ptx::pack2<kBf16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-                if (valid) {
+                    for (int part = 0; part < 2; ++part) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32_at<0>(row_addr + colO + 64 * h + 32 * part, o);
+                        ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int v = 0; v < kChunk / 8; ++v)
-                        dst[h / 8 + v] = make_uint4(hv[4 * v], hv[4 * v + 1], hv[4 * v + 2], hv[4 * v + 3]);
+                        for (int i = 0; i < 16; ++i)
+                            hv[16 * part + i] = ptx::pack2<kBf16>(__uint_as_float(o[2 * i]) * inv_l,
+                                                                  __uint_as_float(o[2 * i + 1]) * inv_l);
+                    }
+                } else {
+                    uint32_t o[64];
+                    ptx::tmem_ld32_at<0>(row_addr + colO, o);
+                    ptx::tmem_ld32_at<32>(row_addr + colO + 32, o);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        hv[i] = ptx::pack2<kBf16>(__uint_as_float(o[2 * i]) * inv_l,
+                                                  __uint_as_float(o[2 * i + 1]) * inv_l);
+                }
+                // Through the warp's staging slice: each lane writes its own
+                // row, then reads back so that eight lanes cover one row's
+                // 128 bytes and each store instruction writes four whole
+                // 128-byte lines of O.
+                __syncwarp();   // the previous half's reads of the slice are done
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    ptx::st_shared_v4(wslice + static_cast<uint32_t>(lane) * 128u +
+                                          ((static_cast<uint32_t>(c) ^ (lane & 7u)) << 4),
+                                      hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
+                __syncwarp();
+                // lane: row 4i + lane / 8 of the warp's 32 (step i), chunk lane % 8
+                const uint32_t rd = wslice + static_cast<uint32_t>(lane >> 3) * 128u +
+                                    (static_cast<uint32_t>((lane & 7) ^ (lane >> 3)) << 4);
+                uint4* gdst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
+                                                       static_cast<size_t>(row0 + t * kBM + 32 * q + (lane >> 3)) * D +
+                                                       64 * h) + (lane & 7);
+                const int rows_left = kGen ? p.nq - (q0 + t * kBM + 32 * q + (lane >> 3)) : 32;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    // row 4i + lane / 8: its chunk sits at (lane % 8) ^ (row % 8)
+                    // = (lane % 8) ^ (lane / 8) ^ (4 (i % 2)), i.e. the step
+                    // only flips bit 2 of the chunk on odd steps
+                    const uint4 v = ptx::ld_shared_v4((rd ^ ((i & 1) << 6)) + static_cast<uint32_t>(i) * 512u);
+                    if ((!kGen || 4 * i < rows_left) &&
+                        FA2_DBG_OK(row0 + t * kBM + 32 * q + (lane >> 3) + 4 * i < p.rows_q, kDbgORow))
+                        gdst[static_cast<size_t>(4 * i) * (D / 8)] = v;
                 }
             }
-            if (valid)
-                p.lse[grow] = (!kGen || l > 0.0f) ? (m + ptx::lg2_approx(l)) * 0.69314718055994530942f : -INFINITY;
+            if (!ok) break;
+            constexpr float kLog2Off = kFp8 ? 8.0f : 0.0f;
+            if (valid && FA2_DBG_OK(grow < p.rows_q, kDbgORow))
+                p.lse[grow] = (!kGen || l > 0.0f) ? (m + ptx::lg2_approx(l) - kLog2Off) * 0.69314718055994530942f
+                                                  : -INFINITY;
         }
         ptx::tc_fence_before();
     }
@@ -941,7 +1034,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         softmax_role<D, kBf16, kGen>(p, tmem, smem, bars, w, warp / 4);
     } else if (warp < kLoadWarp) {
         ptx::setmaxnreg_dec<kRegCorr>();
-        correction_role<D, kBf16, kGen>(p, tmem, smem, bars, w);
+        correction_role<L, Bars<D>, D, kBf16, kGen, false>(p, tmem, smem, sbase, bars, w);
     } else {
         ptx::setmaxnreg_dec<kRegOther>();
         if (warp == kLoadWarp) {

@@ -20,6 +20,7 @@ FA2_ERR_INVALID_ARG = 1
 FA2_ERR_UNSUPPORTED = 2
 FA2_ERR_CUDA = 3
 FA2_ERR_TIMEOUT = 4
+FA2_ERR_BOUNDS = 5   # debug builds only: a device-side bounds check failed
 
 # symbols declared in include/fa2.h
 EXPORTS = ("fa2_fwd", "fa2_fwd_gqa", "fa2_fwd_ex", "fa2_fwd_fp8", "fa2_fwd_fp8_ex", "fa2_bwd", "fa2_bwd_noalloc", "fa2_check_status",

@@ -626,8 +626,11 @@ def harmonic_mean_line(lines, tag, n_gpus):
     if not pts:
         return None
     hm = len(pts) / sum(1.0 / ln["value"] for ln in pts)
-    hk = len(pts) / sum(1.0 / ln["roofline"]["achieved"] for ln in pts)
-    peak = pts[0]["roofline"]["peak"]
+    # per-launch kernel TFLOP/s of each point (points left of the ridge
+    # report GB/s as `achieved` and keep their TFLOP/s under `tflops`)
+    rate = lambda r: r["tflops"] if r["bound"] == "hbm" else r["achieved"]
+    hk = len(pts) / sum(1.0 / rate(ln["roofline"]) for ln in pts)
+    peak, peak_src = load_peak()
     return {"metric": METRIC + "; harmonic mean over N in {512..16384}", "value": hm, "unit": UNIT,
             "n_gpus": n_gpus, "steps": pts[0]["steps"], "warmup": pts[0]["warmup"],
             "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -636,7 +639,7 @@ def harmonic_mean_line(lines, tag, n_gpus):
                 ln["config"]["workload"]: round(ln["value"], 1) for ln in pts},
                 "B*N": 16384, "H": 16, "d": 128},
             "roofline": {"bound": "tensor", "achieved": hk, "peak": peak, "unit": UNIT, "frac": hk / peak,
-                         "traffic": None, "peak_source": pts[0]["roofline"]["peak_source"],
+                         "traffic": None, "peak_source": peak_src,
                          "kernel": pts[0]["roofline"]["kernel"],
                          "note": "harmonic mean of the points' per-launch kernel rates"}}
 

@@ -65,7 +65,10 @@ typedef enum {
                                  32-bit coordinates, or a device that is not
                                  compute capability 10.3 */
     FA2_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
-    FA2_ERR_TIMEOUT = 4       /* the kernel's watchdog gave up on a wait */
+    FA2_ERR_TIMEOUT = 4,      /* the kernel's watchdog gave up on a wait */
+    FA2_ERR_BOUNDS = 5        /* debug builds only (libfa2_debug.so, compiled
+                                 with FA2_DEBUG): a device-side bounds check
+                                 failed and the access was skipped */
 } fa2_status;
 
 /*
@@ -232,6 +235,7 @@ fa2_status fa2_bwd_noalloc(const void* q, const void* k, const void* v, const vo
  * that `stream` belongs to (the current device is switched to it for the
  * read and restored afterwards). Returns FA2_ERR_TIMEOUT if a kernel since
  * the last check abandoned a wait (its outputs are then undefined),
+ * FA2_ERR_BOUNDS if (debug builds only) a device-side bounds check failed,
  * FA2_ERR_CUDA if the stream reported an error, FA2_OK otherwise.
  * There is one status word per device, shared by every stream and host
  * thread that uses the device: a timeout of a kernel on another stream is
@@ -261,7 +265,8 @@ int64_t fa2_set_wait_limit_ns(int64_t limit_ns);
  */
 int fa2_set_debug_flags(int flags);
 
-/* Library version string, e.g. "fa2-sm103a 0.1.0". */
+/* Library version string, e.g. "fa2-sm103a 0.2.0" ("... debug" for the
+ * FA2_DEBUG build, libfa2_debug.so). */
 const char* fa2_version(void);
 
 #ifdef __cplusplus

@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings(lib):
     names = {0: "FA2_OK", 1: "FA2_ERR_INVALID_ARG", 2: "FA2_ERR_UNSUPPORTED",
-             3: "FA2_ERR_CUDA", 4: "FA2_ERR_TIMEOUT"}
+             3: "FA2_ERR_CUDA", 4: "FA2_ERR_TIMEOUT", 5: "FA2_ERR_BOUNDS"}
     for code, name in names.items():
         assert fa2.status_string(code) == name
     assert fa2.status_string(99) == "FA2_ERR_UNKNOWN"
@@ -177,3 +177,16 @@ def test_binding_refuses_missing_library(tmp_path):
             fa2.load(str(tmp_path / "absent.so"))
     finally:
         fa2._lib = saved
+
+
+def test_debug_library_exports_the_same_symbols(lib):
+    """libfa2_debug.so (FA2_DEBUG: device-side bounds checks) is built beside
+    the release library, exports the same calls and says which it is."""
+    dbg = ctypes.CDLL(build.DEBUG_LIB)
+    for name in header_functions():
+        assert hasattr(dbg, name), name
+    dbg.fa2_version.restype = ctypes.c_char_p
+    assert dbg.fa2_version().decode().endswith("debug")
+    assert not fa2.fa2_version().endswith("debug")
+    dbg.fa2_status_string.restype = ctypes.c_char_p
+    assert dbg.fa2_status_string(5).decode() == "FA2_ERR_BOUNDS"

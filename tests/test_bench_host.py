@@ -129,15 +129,19 @@ def test_all_configs_cover_every_forward_configuration():
 
 
 def test_harmonic_mean_line():
-    def line(name, v, a):
-        return {"value": v, "steps": 10, "warmup": 3, "config": {"workload": name},
-                "roofline": {"achieved": a, "peak": 2000.0, "peak_source": "x", "kernel": "k"}}
-    lines = [line("sweep_N512_bf16", 1000.0, 1100.0), line("sweep_N1024_bf16", 2000.0, 2200.0),
+    def line(name, v, a, hbm=False):
+        roof = {"bound": "tensor", "achieved": a, "peak": 2000.0, "peak_source": "x", "kernel": "k"}
+        if hbm:   # left of the ridge: GB/s as achieved, TFLOP/s kept aside
+            roof.update({"bound": "hbm", "achieved": 3800.0, "unit": "GB/s", "tflops": a})
+        return {"value": v, "steps": 10, "warmup": 3, "config": {"workload": name}, "roofline": roof}
+    lines = [line("sweep_N512_bf16", 1000.0, 1100.0, hbm=True), line("sweep_N1024_bf16", 2000.0, 2200.0),
              line("sweep_N512_fp16", 5.0, 5.0), line("mha_B4_H16_N4096_d128_bf16", 7.0, 7.0)]
     hm = bench.harmonic_mean_line(lines, "bf16", 1)
     assert abs(hm["value"] - 2 / (1 / 1000 + 1 / 2000)) < 1e-9
     assert abs(hm["roofline"]["achieved"] - 2 / (1 / 1100 + 1 / 2200)) < 1e-9
-    assert abs(hm["roofline"]["frac"] - hm["roofline"]["achieved"] / 2000.0) < 1e-12
+    peak, _ = bench.load_peak()
+    assert abs(hm["roofline"]["frac"] - hm["roofline"]["achieved"] / peak) < 1e-12
+    assert hm["roofline"]["unit"] == "TFLOP/s"
     assert set(hm["config"]["points"]) == {"sweep_N512_bf16", "sweep_N1024_bf16"}
     assert bench.harmonic_mean_line(lines, "e4m3", 1) is None
 
