@@ -121,36 +121,6 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, 
                  : "memory");
 }
 
-// ------------------------------------------------------------------ cluster launch control
-
-// Asks the hardware to cancel the launch of a CTA of this grid that has not
-// started yet; the 16-byte response lands at `resp` (16-byte aligned shared
-// memory) and completes 16 transaction bytes on `bar`. After a response that
-// reports no cancellation, no further request may be issued.
-__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
-    asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
-                     resp),
-                 "r"(bar)
-                 : "memory");
-}
-
-// Decodes a response: the x index of the cancelled CTA (whose work the
-// caller now owns), or -1 if no CTA was cancelled.
-__device__ __forceinline__ int clc_cancelled_x(uint32_t resp) {
-    uint32_t valid, x;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b128 c;\n\t"
-        "ld.shared.b128 c, [%2];\n\t"
-        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, c;\n\t"
-        "selp.u32 %1, 1, 0, p;\n\t"
-        "mov.u32 %0, 0;\n\t"
-        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, c;\n\t}"
-        : "=r"(x), "=r"(valid)
-        : "r"(resp)
-        : "memory");
-    return valid ? static_cast<int>(x) : -1;
-}
-
 // ------------------------------------------------------------------ registers
 
 // Warpgroup-wide register reallocation: every warp of the warpgroup executes
