@@ -18,6 +18,7 @@ LIB = os.path.join(PKG, "libfa2.so")
 DEBUG_LIB = os.path.join(PKG, "libfa2_debug.so")
 SOURCES = [os.path.join(CSRC, "fa2_fwd_sm103.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "ptx_sm103.cuh"), os.path.join(CSRC, "fa2_fwd_sm103.cuh"), os.path.join(CSRC, "fa2_bwd_sm103.cuh"), os.path.join(CSRC, "fa2_fwd_fp8_sm103.cuh"),
+                     os.path.join(CSRC, "fa2_fwd_d64_sm103.cuh"),
                      os.path.join(INCLUDE, "fa2.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

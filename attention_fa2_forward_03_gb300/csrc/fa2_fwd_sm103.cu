@@ -19,6 +19,7 @@
 #include "fa2_bwd_sm103.cuh"
 #include "fa2_fwd_fp8_sm103.cuh"
 #include "fa2_fwd_sm103.cuh"
+#include "fa2_fwd_d64_sm103.cuh"
 
 // ==================================================================== host
 
@@ -34,8 +35,8 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 constexpr int kMaxDevices = 64;
 // Kernel slots: 16-bit forward 0-7, backward dK/dV 8-11, FP8 forward 12-13,
-// backward dQ 14-17.
-constexpr int kKernelSlots = 18;
+// backward dQ 14-17, d = 64 equal-length forward 18-19.
+constexpr int kKernelSlots = 20;
 // Per-device facts, read without a lock: every field is an atomic written
 // with release and read with acquire, and two threads that probe the same
 // device at once store the same values.
@@ -145,6 +146,17 @@ fa2_status launch(int dev, const CUtensorMap& mq, const CUtensorMap& mk, const C
     auto kern = fa2::fa2_fwd_kernel<D, kBf16, kGen>;
     const int slot = (D == 128 ? 0 : 2) + (kBf16 ? 0 : 1) + (kGen ? 4 : 0);
     const fa2_status st = set_smem(dev, slot, kern, kSmem);
+    if (st != FA2_OK) return st;
+    return launch_kernel(kern, grid, fa2::kThreads, kSmem, stream, mq, mk, mv, p);
+}
+
+// The d = 64 equal-length kernel (P in TMEM columns of its own).
+template <bool kBf16>
+fa2_status launch_d64(int dev, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                      const Params& p, dim3 grid, cudaStream_t stream) {
+    constexpr int kSmem = fa2::d64::Lay::kSmemBytes;
+    auto kern = fa2::fa2_fwd_d64_kernel<kBf16>;
+    const fa2_status st = set_smem(dev, kBf16 ? 18 : 19, kern, kSmem);
     if (st != FA2_OK) return st;
     return launch_kernel(kern, grid, fa2::kThreads, kSmem, stream, mq, mk, mv, p);
 }
@@ -346,8 +358,7 @@ fa2_status fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, flo
     if (d == 128)
         return bf ? launch<128, true>(dev, mq, mk, mv, p, grid, stream)
                   : launch<128, false>(dev, mq, mk, mv, p, grid, stream);
-    return bf ? launch<64, true>(dev, mq, mk, mv, p, grid, stream)
-              : launch<64, false>(dev, mq, mk, mv, p, grid, stream);
+    return bf ? launch_d64<true>(dev, mq, mk, mv, p, grid, stream) : launch_d64<false>(dev, mq, mk, mv, p, grid, stream);
 }
 
 fa2_status fa2_fwd_fp8(const void* q, const void* k, const void* v, const float* q_descale,

@@ -334,9 +334,11 @@ __device__ __forceinline__ int next_item(int it) {
 
 // ---------------------------------------------------------------- producer
 
-template <int D>
+// BarsT: any barrier set with this layout's q_full, q_empty, kv_full and
+// kv_empty (the d = 64 three-buffer kernel shares this producer).
+template <int D, class BarsT>
 __device__ __forceinline__ void producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
-                                         const Params& p, uint32_t sbase, const Bars<D>& bars, const Waiter& w) {
+                                         const Params& p, uint32_t sbase, const BarsT& bars, const Waiter& w) {
     using L = Layout<D>;
     constexpr int S = L::kStages;
     const bool load_q = (p.debug_flags & 1) == 0;
@@ -631,6 +633,20 @@ __device__ __forceinline__ void mma_issuer_gen(const Params& p, uint32_t sbase, 
     __syncwarp();
 }
 
+// Hands one row's rescale factor to the correction warpgroup (store, then
+// arrive) and returns it as read back from shared memory. The caller makes
+// its exponentials depend on the read-back: the arrive feeds nothing else in
+// this thread, so the compiler was free to schedule it after the whole
+// exponential loop, and did -- the correction warpgroup then started only
+// when this warpgroup had finished the step (measured with clock64 traces:
+// the factor became visible ~1200 cycles after S instead of ~560, and a
+// step took 11% longer). A volatile load is not moved above the arrive.
+__device__ __forceinline__ float publish_alpha(float* slot, float alpha, uint32_t bar) {
+    *slot = alpha;
+    ptx::mbar_arrive(bar);
+    return ptx::ld_volatile_shared_f32(ptx::smem_addr(slot));
+}
+
 // ---------------------------------------------------------------- softmax
 
 // 32-column TMEM load/store into slice [off, off+32) of a register array;
@@ -794,6 +810,39 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t tmem, uin
 
 // ---------------------------------------------------------------- correction + epilogue
 
+// Stores 32 rows x 64 columns of 16-bit O (hv: the calling lane's row as 32
+// packed pairs) through the warp's 4 KB staging slice: each lane writes its
+// own row, then the warp reads back so that eight lanes cover one row's 128
+// bytes and each store instruction writes four whole 128-byte lines. The 16-
+// byte chunk c of row r sits at chunk c ^ (r mod 8) in the slice, so both
+// the row-per-lane writes and the transposed reads hit every bank group
+// equally. first_row: the output row of the warp's first row in the [rows,
+// D] view; col0: the first column; rows_valid: how many of the 32 rows exist
+// (a ragged end); rows_total bounds the debug check.
+template <int D>
+__device__ __forceinline__ void store_o_rows(const uint32_t (&hv)[32], uint32_t wslice, int lane, void* out,
+                                             int first_row, int col0, int rows_valid, long long rows_total) {
+    __syncwarp();   // the previous call's reads of the slice are done
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        ptx::st_shared_v4(wslice + static_cast<uint32_t>(lane) * 128u + ((static_cast<uint32_t>(c) ^ (lane & 7u)) << 4),
+                          hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
+    __syncwarp();
+    // lane: row 4i + lane / 8 of the 32 (step i), chunk lane % 8
+    const int r0 = lane >> 3;
+    const uint32_t rd = wslice + static_cast<uint32_t>(r0) * 128u + (static_cast<uint32_t>((lane & 7) ^ r0) << 4);
+    uint4* gdst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + static_cast<size_t>(first_row + r0) * D +
+                                           col0) + (lane & 7);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        // row 4i + lane / 8: its chunk sits at (lane % 8) ^ (row % 8)
+        // = (lane % 8) ^ (lane / 8) ^ (4 (i % 2)): odd steps flip bit 2
+        const uint4 v = ptx::ld_shared_v4((rd ^ ((i & 1) << 6)) + static_cast<uint32_t>(i) * 512u);
+        if (4 * i + r0 < rows_valid && FA2_DBG_OK(first_row + r0 + 4 * i < rows_total, kDbgORow))
+            gdst[static_cast<size_t>(4 * i) * (D / 8)] = v;
+    }
+}
+
 // Shared by the 16-bit and the FP8 kernel (L, BarsT: their shared-memory
 // layout and barriers; kFp8: O is also multiplied by the item's V descale and
 // the LSE loses the 2^8 the FP8 softmax scales its weights by).
@@ -938,34 +987,8 @@ __device__ __forceinline__ void correction_role(const Params& p, uint32_t tmem, 
                         hv[i] = ptx::pack2<kBf16>(__uint_as_float(o[2 * i]) * inv_l,
                                                   __uint_as_float(o[2 * i + 1]) * inv_l);
                 }
-                // Through the warp's staging slice: each lane writes its own
-                // row, then reads back so that eight lanes cover one row's
-                // 128 bytes and each store instruction writes four whole
-                // 128-byte lines of O.
-                __syncwarp();   // the previous half's reads of the slice are done
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    ptx::st_shared_v4(wslice + static_cast<uint32_t>(lane) * 128u +
-                                          ((static_cast<uint32_t>(c) ^ (lane & 7u)) << 4),
-                                      hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
-                __syncwarp();
-                // lane: row 4i + lane / 8 of the warp's 32 (step i), chunk lane % 8
-                const uint32_t rd = wslice + static_cast<uint32_t>(lane >> 3) * 128u +
-                                    (static_cast<uint32_t>((lane & 7) ^ (lane >> 3)) << 4);
-                uint4* gdst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
-                                                       static_cast<size_t>(row0 + t * kBM + 32 * q + (lane >> 3)) * D +
-                                                       64 * h) + (lane & 7);
-                const int rows_left = kGen ? p.nq - (q0 + t * kBM + 32 * q + (lane >> 3)) : 32;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    // row 4i + lane / 8: its chunk sits at (lane % 8) ^ (row % 8)
-                    // = (lane % 8) ^ (lane / 8) ^ (4 (i % 2)), i.e. the step
-                    // only flips bit 2 of the chunk on odd steps
-                    const uint4 v = ptx::ld_shared_v4((rd ^ ((i & 1) << 6)) + static_cast<uint32_t>(i) * 512u);
-                    if ((!kGen || 4 * i < rows_left) &&
-                        FA2_DBG_OK(row0 + t * kBM + 32 * q + (lane >> 3) + 4 * i < p.rows_q, kDbgORow))
-                        gdst[static_cast<size_t>(4 * i) * (D / 8)] = v;
-                }
+                store_o_rows<D>(hv, wslice, lane, p.o, row0 + t * kBM + 32 * q, 64 * h,
+                                kGen ? p.nq - (q0 + t * kBM + 32 * q) : 32, p.rows_q);
             }
             if (!ok) break;
             constexpr float kLog2Off = kFp8 ? 8.0f : 0.0f;

@@ -75,6 +75,10 @@ SMALL = [
     (1, 1, 1, 2048, 128, gen.FP16, 1.0),
     (1, 2, 2, 512, 128, gen.BF16, 6.0),    # very sharp softmax
     (1, 8, 2, 256, 64, gen.FP16, 3.0),
+    # d = 64 runs four query tiles per item: items of 2, of 4 + 1, of 4 + 3
+    (2, 3, 3, 256, 64, gen.BF16, 1.0),
+    (1, 5, 1, 256, 64, gen.FP16, 1.0),
+    (1, 7, 7, 768, 64, gen.BF16, 3.0),
 ]
 
 
