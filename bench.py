@@ -61,7 +61,8 @@ L2_BYTES = 129 * 1024 * 1024
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 CSRC = os.path.join(ROOT, "attention_fa2_forward_03_gb300", "csrc")
 # Device code of each kernel (host planning code is not part of it)
-KERNEL_SOURCES = [os.path.join(CSRC, "fa2_fwd_sm103.cuh"), os.path.join(CSRC, "ptx_sm103.cuh")]
+KERNEL_SOURCES = [os.path.join(CSRC, "fa2_fwd_sm103.cuh"), os.path.join(CSRC, "fa2_fwd_d64_sm103.cuh"),
+                  os.path.join(CSRC, "ptx_sm103.cuh")]
 BWD_SOURCES = KERNEL_SOURCES + [os.path.join(CSRC, "fa2_bwd_sm103.cuh")]
 FP8_SOURCES = KERNEL_SOURCES + [os.path.join(CSRC, "fa2_fwd_fp8_sm103.cuh")]
 PASSES = ("fwd", "fwd_causal", "bwd", "bwd_causal")
@@ -477,6 +478,8 @@ class Step:
             self.kernel = "fa2_bwd (delta + dK/dV + dQ kernels)"
         elif self.fp8:
             self.kernel = "fa2_fwd_fp8_kernel" + ("<general>" if self.causal else "")
+        elif w.d == 64 and not self.causal:
+            self.kernel = f"fa2_fwd_d64_kernel<{'bf16' if w.dtype == gen.BF16 else 'fp16'}>"
         else:
             self.kernel = (f"fa2_fwd_kernel<{w.d},{'bf16' if w.dtype == gen.BF16 else 'fp16'}"
                            f"{',general' if self.causal else ''}>")
