@@ -226,21 +226,22 @@ def test_long_sequence_single_head(gpu_lib):
 
 # ------------------------------------------------------------------ watchdog
 
-def test_watchdog_reports_timeout_and_context_survives(gpu_lib):
+@pytest.mark.parametrize("d", [128, 64])   # d = 64: the kernel with two MMA warps
+def test_watchdog_reports_timeout_and_context_survives(gpu_lib, d):
     torch = _torch()
-    q, k, v = gen.make_qkv(39, 1, 1, 1, 256, 128, gen.BF16)
+    q, k, v = gen.make_qkv(39, 1, 1, 1, 256, d, gen.BF16)
     tq, tk, tv = (to_dev(x, gen.BF16) for x in (q, k, v))
     old_limit = gpu_lib.fa2_set_wait_limit_ns(20_000_000)  # 20 ms
     old_flags = gpu_lib.fa2_set_debug_flags(1)              # skip the query-tile loads
     try:
-        gpu_lib.fa2_fwd(tq, tk, tv, scale=128 ** -0.5)
+        gpu_lib.fa2_fwd(tq, tk, tv, scale=d ** -0.5)
         rc = gpu_lib.fa2_check_status(torch.cuda.current_stream().cuda_stream)
     finally:
         gpu_lib.fa2_set_debug_flags(old_flags)
         gpu_lib.fa2_set_wait_limit_ns(old_limit)
     assert rc == gpu_lib.FA2_ERR_TIMEOUT
     assert gpu_lib.fa2_check_status(0) == gpu_lib.FA2_OK  # the word was cleared
-    full_check(gpu_lib, q, k, v, gen.BF16, 128 ** -0.5, "after watchdog")
+    full_check(gpu_lib, q, k, v, gen.BF16, d ** -0.5, "after watchdog")
 
 
 def test_check_status_reads_the_streams_device_word(gpu_lib):
