@@ -97,6 +97,18 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmQ, const CUtensorM
     bool ok = true;
     for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
         const Item item = make_item(p, it);
+        auto load_kv = [&](int k) {
+            const int s = ring % S;
+            if (!(ok = w.wait(bars.kv_empty(s), ((ring / S) & 1) ^ 1, kSiteKvEmpty))) return;
+            ptx::mbar_arrive_expect_tx(bars.kv_full(s), kTile);
+            if (FA2_DBG_OK(item.kv_row0 + (k >> 1) * kBN + kBN <= p.rows_kv, kDbgKvTile))
+                ptx::tma_load_2d(sbase + Lay::kRingOff + s * kTile, (k & 1) ? tmV : tmK, 0,
+                                 item.kv_row0 + (k >> 1) * kBN, bars.kv_full(s));
+            ++ring;
+        };
+        // K_0, V_0 before the Q tiles (the 16-bit producer says why).
+        constexpr int kPre = 2;
+        for (int k = 0; k < kPre && ok; ++k) load_kv(k);
         for (int t = 0; t < item.n_tiles && ok; ++t) {
             if (!(ok = w.wait(bars.q_empty(t), (nq[t] & 1) ^ 1, kSiteQEmpty))) break;
             ptx::mbar_arrive_expect_tx(bars.q_full(t), kTile);
@@ -109,15 +121,7 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmQ, const CUtensorM
             const Item ni = make_item(p, nxt);
             for (int t = 0; t < ni.n_tiles; ++t) ptx::tma_prefetch_l2_2d(tmQ, 0, ni.q_row0 + t * kBM);
         }
-        for (int k = 0; k < 2 * p.n_kv_tiles && ok; ++k) {
-            const int s = ring % S;
-            if (!(ok = w.wait(bars.kv_empty(s), ((ring / S) & 1) ^ 1, kSiteKvEmpty))) break;
-            ptx::mbar_arrive_expect_tx(bars.kv_full(s), kTile);
-            if (FA2_DBG_OK(item.kv_row0 + (k >> 1) * kBN + kBN <= p.rows_kv, kDbgKvTile))
-                ptx::tma_load_2d(sbase + Lay::kRingOff + s * kTile, (k & 1) ? tmV : tmK, 0,
-                                 item.kv_row0 + (k >> 1) * kBN, bars.kv_full(s));
-            ++ring;
-        }
+        for (int k = kPre; k < 2 * p.n_kv_tiles && ok; ++k) load_kv(k);
     }
     if (!ok) {
         const int first = ring > S ? ring - S : 0;

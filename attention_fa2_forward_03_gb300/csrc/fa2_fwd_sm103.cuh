@@ -347,6 +347,26 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmQ, const CUtensorM
     bool ok = true;
     for (int it = blockIdx.x; it < p.total_items && ok; it += gridDim.x) {
         const Item item = make_item(p, it);
+        // Ring entry k of this item: K_{k/2} (k even) or V_{k/2} (k odd).
+        auto load_kv = [&](int k) {
+            const int s = ring % S;
+            if (!(ok = w.wait(bars.kv_empty(s), ((ring / S) & 1) ^ 1, kSiteKvEmpty))) return;
+            const uint32_t dst = sbase + L::kRingOff + s * L::kTileBytes;
+            const CUtensorMap* tm = (k & 1) ? tmV : tmK;
+            const int row = item.kv_row0 + (k >> 1) * kBN;
+            ptx::mbar_arrive_expect_tx(bars.kv_full(s), L::kTileBytes);
+            if (FA2_DBG_OK(row + kBN <= p.rows_kv, kDbgKvTile))
+#pragma unroll
+                for (int blk = 0; blk < D / 64; ++blk)
+                    ptx::tma_load_2d(dst + blk * L::kBlkBytes, tm, blk * 64, row, bars.kv_full(s));
+            ++ring;
+        };
+        // K_0 and V_0 first: their stages free up a step or more before the
+        // Q slots do (a Q slot is released by the item's last QK of that
+        // tile), and a copy takes thousands of cycles under load, so the
+        // next item's first QK would otherwise wait for K_0.
+        constexpr int kPre = 2;
+        for (int k = 0; k < kPre && ok; ++k) load_kv(k);
         for (int t = 0; t < item.n_tiles && ok; ++t) {
             if (!(ok = w.wait(bars.q_empty(t), (nq[t] & 1) ^ 1, kSiteQEmpty))) break;
             if (load_q) {
@@ -369,19 +389,7 @@ __device__ __forceinline__ void producer(const CUtensorMap* tmQ, const CUtensorM
                 for (int blk = 0; blk < D / 64; ++blk)
                     ptx::tma_prefetch_l2_2d(tmQ, blk * 64, ni.q_row0 + t * kBM);
         }
-        for (int k = 0; k < 2 * p.n_kv_tiles && ok; ++k) {
-            const int s = ring % S;
-            if (!(ok = w.wait(bars.kv_empty(s), ((ring / S) & 1) ^ 1, kSiteKvEmpty))) break;
-            const uint32_t dst = sbase + L::kRingOff + s * L::kTileBytes;
-            const CUtensorMap* tm = (k & 1) ? tmV : tmK;
-            const int row = item.kv_row0 + (k >> 1) * kBN;
-            ptx::mbar_arrive_expect_tx(bars.kv_full(s), L::kTileBytes);
-            if (FA2_DBG_OK(row + kBN <= p.rows_kv, kDbgKvTile))
-#pragma unroll
-                for (int blk = 0; blk < D / 64; ++blk)
-                    ptx::tma_load_2d(dst + blk * L::kBlkBytes, tm, blk * 64, row, bars.kv_full(s));
-            ++ring;
-        }
+        for (int k = kPre; k < 2 * p.n_kv_tiles && ok; ++k) load_kv(k);
     }
     if (!ok) {
         // Aborting: let every copy this CTA started land before it exits.
