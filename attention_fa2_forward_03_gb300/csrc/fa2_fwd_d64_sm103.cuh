@@ -20,23 +20,25 @@
 // take 384 of the 512 TMEM columns, which leaves room for each tile's P:
 //     TMEM: S_0 | S_1 | O_0 | O_1 | P_0 | P_1  (128, 128, 64, 64, 64, 64)
 // so a softmax warpgroup releases S as soon as it has loaded it (s_free),
-// the MMA warp computes the tile's next S during the rest of the softmax,
-// and the softmax goes from one step to the next without waiting for the
-// tensor core. P_t of step j is written only after P V of step j - 1 has
-// read P_t (pv_done), which the tensor core finished long before.
+// the tile's next S is computed during the rest of the softmax, and the
+// softmax goes from one step to the next without waiting for the tensor
+// core. P_t of step j is written only after P V of step j - 1 has read P_t
+// (pv_done), which the tensor core finished long before. Two warps issue
+// the MMAs, one every Q K^T and one every P V: the two streams touch
+// disjoint TMEM, so neither waits behind the other's barriers.
 //
 // Hand-offs per tile t (every barrier is at most one phase ahead of each
 // of its waiters; each line says why):
-//   s_full(t)   MMA -> softmax t      next S(t) is issued only after s_free
-//   s_free(t)   softmax t -> MMA      next load of S(t) waits for s_full
+//   s_full(t)   QK warp -> softmax t  next S(t) is issued only after s_free
+//   s_free(t)   softmax t -> QK warp  next load of S(t) waits for s_full
 //   alpha(t, c & 1)  softmax t -> correction, c = the tile's step count: a
 //               slot is rewritten two steps later, after the P store of the
 //               step between, which waits for P V of this step, which waits
 //               for the correction's p_full arrival of this step
-//   p_full(t)   softmax t + correction -> MMA (P V)
-//   pv_done(t)  MMA -> softmax t (before storing P) and correction (before
-//               rescaling O, and before the epilogue reads it); the next
-//               P V(t) needs both of their p_full arrivals
+//   p_full(t)   softmax t + correction -> PV warp
+//   pv_done(t)  PV warp -> softmax t (before storing P) and correction
+//               (before rescaling O, and before the epilogue reads it); the
+//               next P V(t) needs both of their p_full arrivals
 //   stats(t)    softmax t -> correction (m, l of the item's last step)
 #pragma once
 
