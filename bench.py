@@ -37,6 +37,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -69,14 +70,22 @@ PASSES = ("fwd", "fwd_causal", "bwd", "bwd_causal")
 REASON_FIELDS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
 
+def strip_comments(src: str) -> str:
+    """C++ source without comments and blank runs (string literals in these
+    files hold no comment markers), so that a comment edit keeps the hash."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def kernel_source_hash(which: str = "fwd") -> str:
-    """sha256[:16] of the device code a pass runs: "fwd" (16-bit forward,
-    also fwd_causal), "bwd*" or "fp8"."""
+    """sha256[:16] of the device code a pass runs, comments removed: "fwd"
+    (16-bit forward, also fwd_causal), "bwd*" or "fp8"."""
     h = hashlib.sha256()
     files = BWD_SOURCES if which.startswith("bwd") else FP8_SOURCES if which == "fp8" else KERNEL_SOURCES
     for f in files:
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
