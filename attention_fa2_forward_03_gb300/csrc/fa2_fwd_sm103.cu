@@ -12,6 +12,8 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <utility>
 
@@ -30,6 +32,25 @@ using fa2::Params;
 
 std::atomic<long long> g_wait_limit_ns{2000000000LL};
 std::atomic<int> g_debug_flags{0};
+
+// The planner's kernel table has one shape with a choice: d = 64 with equal
+// lengths runs fa2_fwd_d64_kernel (P in TMEM columns of its own, two MMA
+// warps; the default, measured faster) or, with this bit set, the 16-bit
+// kernel's d = 64 path (P written over S, one MMA warp).
+constexpr int kTileCfgD64Shared = 1;
+constexpr int kTileCfgMask = kTileCfgD64Shared;
+std::atomic<int> g_tile_cfg{-1};   // -1: FA2_TILE_CFG not read yet
+
+int tile_cfg() {
+    const int c = g_tile_cfg.load(std::memory_order_acquire);
+    if (c >= 0) return c;
+    int v = 0;
+    if (const char* e = std::getenv("FA2_TILE_CFG"))
+        if (std::strcmp(e, "d64=shared") == 0) v = kTileCfgD64Shared;
+    int expected = -1;
+    g_tile_cfg.compare_exchange_strong(expected, v, std::memory_order_acq_rel);
+    return g_tile_cfg.load(std::memory_order_acquire);
+}
 std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -358,6 +379,9 @@ fa2_status fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, flo
     if (d == 128)
         return bf ? launch<128, true>(dev, mq, mk, mv, p, grid, stream)
                   : launch<128, false>(dev, mq, mk, mv, p, grid, stream);
+    if (tile_cfg() & kTileCfgD64Shared)
+        return bf ? launch<64, true>(dev, mq, mk, mv, p, grid, stream)
+                  : launch<64, false>(dev, mq, mk, mv, p, grid, stream);
     return bf ? launch_d64<true>(dev, mq, mk, mv, p, grid, stream) : launch_d64<false>(dev, mq, mk, mv, p, grid, stream);
 }
 
@@ -631,6 +655,12 @@ int64_t fa2_set_wait_limit_ns(int64_t limit_ns) {
 }
 
 int fa2_set_debug_flags(int flags) { return g_debug_flags.exchange(flags); }
+
+int fa2_set_tile_config(int config) {
+    if (config < 0 || (config & ~kTileCfgMask) != 0) return -1;
+    (void)tile_cfg();   // the environment's value first, so the previous value is the one in effect
+    return g_tile_cfg.exchange(config, std::memory_order_acq_rel);
+}
 
 #ifdef FA2_DEBUG
 const char* fa2_version(void) { return "fa2-sm103a 0.2.0 debug"; }

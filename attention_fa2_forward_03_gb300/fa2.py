@@ -25,7 +25,7 @@ FA2_ERR_BOUNDS = 5   # debug builds only: a device-side bounds check failed
 # symbols declared in include/fa2.h
 EXPORTS = ("fa2_fwd", "fa2_fwd_gqa", "fa2_fwd_ex", "fa2_fwd_fp8", "fa2_fwd_fp8_ex", "fa2_bwd", "fa2_bwd_noalloc", "fa2_check_status",
            "fa2_status_string",
-           "fa2_set_wait_limit_ns", "fa2_set_debug_flags", "fa2_version")
+           "fa2_set_wait_limit_ns", "fa2_set_debug_flags", "fa2_set_tile_config", "fa2_version")
 
 _lib = None
 
@@ -68,6 +68,8 @@ def load(path: str = LIB_PATH):
     lib.fa2_set_wait_limit_ns.restype = ctypes.c_int64
     lib.fa2_set_debug_flags.argtypes = [i]
     lib.fa2_set_debug_flags.restype = i
+    lib.fa2_set_tile_config.argtypes = [i]
+    lib.fa2_set_tile_config.restype = i
     lib.fa2_version.argtypes = []
     lib.fa2_version.restype = ctypes.c_char_p
     _lib = lib
@@ -137,6 +139,16 @@ def fa2_set_wait_limit_ns(limit_ns: int) -> int:
 
 def fa2_set_debug_flags(flags: int) -> int:
     return load().fa2_set_debug_flags(int(flags))
+
+
+# bit 0 of fa2_set_tile_config: d = 64, equal lengths, on the 16-bit kernel's d = 64 path
+TILE_CFG_D64_SHARED = 1
+
+
+def fa2_set_tile_config(config: int) -> int:
+    """Planner choice for d = 64 with equal lengths (see include/fa2.h);
+    returns the previous value, -1 if `config` was rejected."""
+    return load().fa2_set_tile_config(int(config))
 
 
 def fa2_version() -> str:

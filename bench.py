@@ -487,7 +487,7 @@ class Step:
             self.kernel = "fa2_bwd (delta + dK/dV + dQ kernels)"
         elif self.fp8:
             self.kernel = "fa2_fwd_fp8_kernel" + ("<general>" if self.causal else "")
-        elif w.d == 64 and not self.causal:
+        elif w.d == 64 and not self.causal and os.environ.get("FA2_TILE_CFG") != "d64=shared":
             self.kernel = f"fa2_fwd_d64_kernel<{'bf16' if w.dtype == gen.BF16 else 'fp16'}>"
         else:
             self.kernel = (f"fa2_fwd_kernel<{w.d},{'bf16' if w.dtype == gen.BF16 else 'fp16'}"

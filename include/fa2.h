@@ -265,6 +265,20 @@ int64_t fa2_set_wait_limit_ns(int64_t limit_ns);
  */
 int fa2_set_debug_flags(int flags);
 
+/*
+ * The planner's kernel choice where two kernels compute the same result
+ * (process-wide, for calls made after it returns). Bit 0 (value 1): d = 64
+ * with equal lengths runs the 16-bit kernel's d = 64 path (P written over S,
+ * one MMA-issuing warp) instead of the default d = 64 kernel (P in TMEM
+ * columns of its own, separate warps for Q K^T and P V), which measured
+ * faster. Results differ only by rounding order and are within the same
+ * tolerance. The first call to the library reads the initial value from the
+ * environment: FA2_TILE_CFG=d64=shared sets bit 0, anything else or no
+ * variable gives 0. Returns the previous value, or -1 (nothing changed) if
+ * config is negative or has a bit other than bit 0 set.
+ */
+int fa2_set_tile_config(int config);
+
 /* Library version string, e.g. "fa2-sm103a 0.2.0" ("... debug" for the
  * FA2_DEBUG build, libfa2_debug.so). */
 const char* fa2_version(void);

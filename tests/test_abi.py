@@ -169,6 +169,34 @@ def test_wait_limit_and_debug_flags_round_trip(lib):
     assert fa2.fa2_set_debug_flags(old) == 1
 
 
+def test_tile_config_round_trip(lib):
+    prev = fa2.fa2_set_tile_config(fa2.TILE_CFG_D64_SHARED)
+    assert prev in (0, fa2.TILE_CFG_D64_SHARED)
+    assert fa2.fa2_set_tile_config(prev) == fa2.TILE_CFG_D64_SHARED
+    assert fa2.fa2_set_tile_config(2) == -1          # unknown bit: rejected, unchanged
+    assert fa2.fa2_set_tile_config(-1) == -1
+    assert fa2.fa2_set_tile_config(prev) == prev
+
+
+def test_tile_config_read_from_environment(tmp_path):
+    """A fresh process picks FA2_TILE_CFG up on its first call."""
+    import os
+    import subprocess
+    import sys
+
+    code = ("from attention_fa2_forward_03_gb300 import fa2; "
+            "print(fa2.fa2_set_tile_config(0))")
+    for env_value, want in (("d64=shared", "1"), ("d64=split", "0"), (None, "0")):
+        env = dict(os.environ)
+        env.pop("FA2_TILE_CFG", None)
+        if env_value is not None:
+            env["FA2_TILE_CFG"] = env_value
+        out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                             cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))), timeout=120)
+        assert out.returncode == 0, out.stderr
+        assert out.stdout.strip().splitlines()[-1] == want
+
+
 def test_binding_refuses_missing_library(tmp_path):
     saved = fa2._lib
     fa2._lib = None

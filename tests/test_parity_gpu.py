@@ -88,6 +88,24 @@ def test_small_shapes_every_element(gpu_lib, B, Hq, Hkv, N, d, dtype, amp):
     full_check(gpu_lib, q, k, v, dtype, 1 / math.sqrt(d), f"B{B} Hq{Hq} Hkv{Hkv} N{N} d{d}")
 
 
+# ------------------------------------------------------------------ the planner's other d = 64 kernel
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,dtype,amp", [
+    (1, 2, 2, 384, gen.BF16, 1.0),     # one item of three tiles
+    (1, 8, 2, 256, gen.FP16, 3.0),
+    (2, 3, 3, 1024, gen.BF16, 3.0),    # the d = 64 workload's input scale
+])
+def test_d64_shared_kernel_every_element(gpu_lib, B, Hq, Hkv, N, dtype, amp):
+    """d = 64 with equal lengths on the 16-bit kernel's d = 64 path (P over S),
+    selected through the planner hook instead of the default d = 64 kernel."""
+    q, k, v = gen.make_qkv(4000 + N + Hq, B, Hq, Hkv, N, 64, dtype, amp)
+    old = gpu_lib.fa2_set_tile_config(gpu_lib.TILE_CFG_D64_SHARED)
+    try:
+        full_check(gpu_lib, q, k, v, dtype, 1 / 8, f"shared d64 B{B} Hq{Hq} Hkv{Hkv} N{N}")
+    finally:
+        gpu_lib.fa2_set_tile_config(old)
+
+
 # ------------------------------------------------------------------ degenerate and adversarial inputs
 
 @pytest.mark.parametrize("d", [64, 128])
