@@ -663,9 +663,9 @@ int fa2_set_tile_config(int config) {
 }
 
 #ifdef FA2_DEBUG
-const char* fa2_version(void) { return "fa2-sm103a 0.2.0 debug"; }
+const char* fa2_version(void) { return "fa2-sm103a 0.3.0 debug"; }
 #else
-const char* fa2_version(void) { return "fa2-sm103a 0.2.0"; }
+const char* fa2_version(void) { return "fa2-sm103a 0.3.0"; }
 #endif
 
 }  // extern "C"

@@ -279,7 +279,7 @@ int fa2_set_debug_flags(int flags);
  */
 int fa2_set_tile_config(int config);
 
-/* Library version string, e.g. "fa2-sm103a 0.2.0" ("... debug" for the
+/* Library version string, e.g. "fa2-sm103a 0.3.0" ("... debug" for the
  * FA2_DEBUG build, libfa2_debug.so). */
 const char* fa2_version(void);
 
