@@ -17,12 +17,14 @@
 //
 // How: the 16-bit kernel's persistent, warp-specialised pipeline (two query
 // tiles per item, softmax warpgroups 0-1, correction warpgroup 2, TMA
-// producer warp 12, MMA warp 13) with two changes. Both GEMMs run on 8-bit
-// operands, so the P V product needs V with keys contiguous (K-major): warps
-// 14-15, idle in the 16-bit kernel, transpose each V tile in shared memory
-// into a double-buffered V^T tile (the in-kernel pre-processing); the MMA
-// waits on V^T instead of V. And P is packed four per TMEM column.
-// Head dimension 128 (one 128-byte swizzle row per tile row).
+// producer warp 12, MMA warp 13) with both GEMMs on 8-bit operands and P
+// packed four per TMEM column. The P V product reads V where TMA put it,
+// dims contiguous, as an MN-major B operand: tcgen05 takes 8-bit operands in
+// either major order, so V needs no transposition (the Hopper kernel of the
+// FA3-for-inference page transposes V in shared memory because its 8-bit
+// wgmma takes K-major operands only). Head dimension 128 (one 128-byte
+// swizzle row per tile row, so the MN-major V tile is a single swizzle atom
+// wide).
 //
 // Two modes, as in the 16-bit kernel: equal lengths N % 128 == 0 without a
 // mask (kGen = false: query-head packing, 2-D tensor maps), and the general
@@ -40,20 +42,18 @@ namespace fp8 {
 
 constexpr int kD = 128;              // head dimension = bytes per tile row
 constexpr int kTile = kBM * kD;      // 16 KB: one Q, K, V or V^T tile
-constexpr int kStages = 8;           // K/V ring; K_j in even stages, V_j in odd ones
-constexpr int kXposeWarp0 = 14;      // warps 14, 15
+constexpr int kStages = 8;           // K/V ring (K_j, V_j, K_{j+1}, ...)
 
 struct Lay {
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = kNQ * kTile;
-    static constexpr int kVtOff = kRingOff + kStages * kTile;
     // Epilogue staging: 128 rows x 64 bf16 columns (the 16-bit kernel's form)
-    static constexpr int kStageOff = kVtOff + 2 * kTile;
+    static constexpr int kStageOff = kRingOff + kStages * kTile;
     static constexpr int kStageBytes = kBM * 128;
     static constexpr int kBarOff = kStageOff + kStageBytes;
     // q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] alpha[2] stats[2]
-    // p_full[2] o_full[2] mma_done vt_full[2] vt_empty[2] stats_free[2]
-    static constexpr int kNumBars = 2 * kStages + 21;
+    // p_full[2] o_full[2] mma_done stats_free[2]
+    static constexpr int kNumBars = 2 * kStages + 17;
     static constexpr int kRowOff = kBarOff + kNumBars * 8;  // alpha[2][128], m[2][128], l[2][128]
     static constexpr int kMiscOff = kRowOff + 3 * kNQ * kBM * 4;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
@@ -61,7 +61,6 @@ struct Lay {
     static __device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
     static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + kD * t; }
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-    static_assert(kStages % 2 == 0, "K and V must keep their stage parity");
 };
 
 struct BarsF8 {
@@ -77,12 +76,8 @@ struct BarsF8 {
     __device__ uint32_t p_full(int t) const { return base + 8 * (10 + 2 * S + t); }
     __device__ uint32_t o_full(int t) const { return base + 8 * (12 + 2 * S + t); }
     __device__ uint32_t mma_done() const { return base + 8 * (14 + 2 * S); }
-    __device__ uint32_t vt_full(int b) const { return base + 8 * (15 + 2 * S + b); }
-    __device__ uint32_t vt_empty(int b) const { return base + 8 * (17 + 2 * S + b); }
-    __device__ uint32_t stats_free(int t) const { return base + 8 * (19 + 2 * S + t); }
+    __device__ uint32_t stats_free(int t) const { return base + 8 * (15 + 2 * S + t); }
 };
-
-enum WaitSiteF8 : int { kSiteVtFull = 11, kSiteVtEmpty = 12 };
 
 // (batch, KV head) group of a work item: the index of its descales.
 __device__ __forceinline__ int item_group(const Params& p, int item) { return item / p.pairs; }
@@ -169,113 +164,25 @@ __device__ __forceinline__ void producer_gen(const CUtensorMap* tmQ, const CUten
     }
 }
 
-// ---------------------------------------------------------------- V transpose
-
-// Warps 14-15 turn each V tile (keys x dims, dims contiguous, 128-byte
-// swizzle as TMA wrote it) into V^T (dims x keys, keys contiguous, the same
-// swizzle), the K-major B operand of O += P V. A 128-byte swizzled row r
-// keeps its 16-byte chunk c at chunk position c ^ (r % 8).
-//
-// Work split: a unit is 4 keys x 16 dims; lane (qi = lane / 8, j = lane % 8)
-// of warp w takes, in round u, key block br = j (keys 16 br + 4 qi + 0..3) and
-// dim block bc = (j + 2u + w) % 8, so 2 warps x 4 rounds cover all 8 dim
-// blocks of every (br, qi). Each unit is four 16-byte loads (conflict-free:
-// the 8 lanes of a load phase share qi and hold 8 different bc), sixteen
-// 4x4 byte transposes' worth of byte permutes, and sixteen 4-byte stores
-// (conflict-free: the 32 lanes hold 32 different (br, qi), so 32 banks).
-__device__ __forceinline__ void transpose_tile(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int xid) {
-    const int lane = xid & 31;
-    const int w = xid >> 5;
-    const int j = lane & 7;
-    const int qi = lane >> 3;
-    const int br = j;
-#pragma unroll 1   // one unit's 16 words live at a time: the warp runs on 56 registers
-    for (int u = 0; u < 4; ++u) {
-        const int bc = (j + 2 * u + w) & 7;
-        uint32_t x[4][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = 16 * br + 4 * qi + i;
-            const uint4 v = *reinterpret_cast<const uint4*>(src + r * 128 + ((bc ^ (r & 7)) << 4));
-            x[i][0] = v.x;
-            x[i][1] = v.y;
-            x[i][2] = v.z;
-            x[i][3] = v.w;
-        }
-#pragma unroll
-        for (int wq = 0; wq < 4; ++wq) {
-            // x[i][wq] holds dims 16bc + 4wq + 0..3 of key 16br + 4qi + i;
-            // y[b] gathers dim 16bc + 4wq + b of the four keys.
-            const uint32_t t0 = __byte_perm(x[0][wq], x[1][wq], 0x5140);
-            const uint32_t t1 = __byte_perm(x[0][wq], x[1][wq], 0x7362);
-            const uint32_t t2 = __byte_perm(x[2][wq], x[3][wq], 0x5140);
-            const uint32_t t3 = __byte_perm(x[2][wq], x[3][wq], 0x7362);
-            const uint32_t y[4] = {__byte_perm(t0, t2, 0x5410), __byte_perm(t0, t2, 0x7632),
-                                   __byte_perm(t1, t3, 0x5410), __byte_perm(t1, t3, 0x7632)};
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int c = 16 * bc + 4 * wq + b;
-                *reinterpret_cast<uint32_t*>(dst + c * 128 + ((br ^ (c & 7)) << 4) + 4 * qi) = y[b];
-            }
-        }
-    }
-}
-
-template <bool kGen>
-__device__ __forceinline__ void xpose_role(const Params& p, uint8_t* smem, const BarsF8& bars, const Waiter& w) {
-    constexpr int S = kStages;
-    const int xid = threadIdx.x - kXposeWarp0 * 32;
-    const int lane = xid & 31;
-    int ring = 0;   // K/V ring items (same sequence as the producer's)
-    int nv = 0;     // V tiles transposed
-    bool ok = true;
-    for (int it = blockIdx.x; it < p.total_items && ok; it = next_item<kGen>(it)) {
-        int nkv = p.n_kv_tiles;   // KV tiles the item loads
-        if constexpr (kGen) {
-            const ItemG g = make_item_gen(p, it);
-            nkv = max(g.nkv[0], g.nkv[1]);
-        }
-        for (int jt = 0; jt < nkv; ++jt, ++nv) {
-            ++ring;                      // K_jt: not ours
-            const int r = ring++;        // V_jt
-            const int s = r % S;
-            const int b = nv & 1;
-            ok = w.wait(bars.kv_full(s), (r / S) & 1, kSiteKvFull);
-            if (ok) ok = w.wait(bars.vt_empty(b), ((nv >> 1) & 1) ^ 1, kSiteVtEmpty);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
-            transpose_tile(smem + Lay::kRingOff + s * kTile, smem + Lay::kVtOff + b * kTile, xid);
-            // Make this thread's generic-proxy stores visible to the tensor
-            // core (async proxy) before the warp's arrival publishes them.
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                ptx::mbar_arrive(bars.vt_full(b));
-                ptx::mbar_arrive(bars.kv_empty(s));
-            }
-        }
-    }
-}
-
 // ---------------------------------------------------------------- MMA issuer
 
 __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint32_t tmem, const BarsF8& bars,
                                            const Waiter& w) {
     constexpr int S = kStages;
-    // e4m3 x e4m3 -> f32; both operands K-major (V is transposed in smem)
+    // e4m3 x e4m3 -> f32; Q and K K-major, V MN-major
     constexpr uint32_t kIdS = ptx::idesc_f16(0u, 0, 0, kBM, kBN);
-    constexpr uint32_t kIdO = ptx::idesc_f16(0u, 0, 0, kBM, kD);
+    constexpr uint32_t kIdO = ptx::idesc_f16(0u, 0, 1, kBM, kD);
     auto stage_addr = [&](int r) { return sbase + Lay::kRingOff + (r % S) * kTile; };
     auto issue_qk = [&](int t, uint32_t kaddr) {
         const uint64_t qd = ptx::desc_sw128(sbase + Lay::kQOff + t * kTile, 16, 1024);
         const uint64_t kd = ptx::desc_sw128(kaddr, 16, 1024);
         ptx::mma_ss_kloop4_f8(tmem + Lay::col_s(t), qd, kd, kIdS, 0u);
     };
-    auto issue_pv = [&](int t, int vb, bool acc) {
-        const uint64_t vd = ptx::desc_sw128(sbase + Lay::kVtOff + vb * kTile, 16, 1024);
-        ptx::mma_ts_kloop4_f8(tmem + Lay::col_o(t), tmem + Lay::col_s(t), vd, kIdO, acc ? 1u : 0u);
+    // V MN-major: one 128-byte swizzle atom across the 128 dims (the leading
+    // offset is never stepped over), 1024 B between groups of 8 keys.
+    auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
+        const uint64_t vd = ptx::desc_sw128(vaddr, kTile, 1024);
+        ptx::mma_ts_kloop4_f8_mn(tmem + Lay::col_o(t), tmem + Lay::col_s(t), vd, kIdO, acc ? 1u : 0u);
     };
     auto wait_u = [&](uint32_t bar, uint32_t parity, int site) {
         return __shfl_sync(0xffffffffu, w.wait(bar, parity, site) ? 1 : 0, 0) != 0;
@@ -284,7 +191,6 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint
 
     const int nkv = p.n_kv_tiles;
     int ring = 0;
-    int nv = 0;                   // V^T tiles consumed
     int nq[2] = {0, 0};
     int np[2] = {0, 0};
     bool ok = true;
@@ -303,22 +209,20 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint
         ++ring;
         for (int j = 0; j < nkv; ++j) {
             const bool more = j + 1 < nkv;
-            ++ring;                       // V_j: released by the transposer
-            const int vb = nv & 1;
+            const int v_ring = ring++;
             if (more) k_ring = ring++;
-            // V^T_j, K_{j+1} and P(0, j) are waited for together.
-            const uint32_t wb[3] = {bars.vt_full(vb), more ? bars.kv_full(k_ring % S) : bars.vt_full(vb), bars.p_full(0)};
-            const uint32_t wp[3] = {static_cast<uint32_t>((nv >> 1) & 1),
-                                    static_cast<uint32_t>(more ? (k_ring / S) & 1 : (nv >> 1) & 1),
+            // V_j, K_{j+1} and P(0, j) are waited for together.
+            const int kr = more ? k_ring : v_ring;
+            const uint32_t wb[3] = {bars.kv_full(v_ring % S), bars.kv_full(kr % S), bars.p_full(0)};
+            const uint32_t wp[3] = {static_cast<uint32_t>((v_ring / S) & 1), static_cast<uint32_t>((kr / S) & 1),
                                     static_cast<uint32_t>(np[0] & 1)};
-            if (!(ok = __shfl_sync(0xffffffffu, w.wait_all<3>(wb, wp, kSiteVtFull) ? 1 : 0, 0) != 0)) break;
-            ++nv;
+            if (!(ok = __shfl_sync(0xffffffffu, w.wait_all<3>(wb, wp, kSiteKvFull) ? 1 : 0, 0) != 0)) break;
             for (int t = 0; t < nt; ++t) {
                 if (t > 0 && !(ok = wait_u(bars.p_full(t), np[t] & 1, kSitePFull))) break;
                 ++np[t];
                 ptx::tc_fence_after();
-                issue_pv(t, vb, j > 0);
-                if (t == nt - 1) ptx::tc_commit_elect(bars.vt_empty(vb));
+                issue_pv(t, stage_addr(v_ring), j > 0);
+                if (t == nt - 1) ptx::tc_commit_elect(bars.kv_empty(v_ring % S));
                 if (more) {
                     issue_qk(t, stage_addr(k_ring));
                     ptx::tc_commit_elect(bars.s_full(t));
@@ -339,22 +243,24 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t sbase, uint
 
 // General mode: mma_issuer's order with a KV tile count per query tile (as
 // the 16-bit kernel's general issuer): at KV tile j only tiles with
-// j < nkv[t] take part; V^T_j's buffer and K_{j+1}'s stage are released
-// after their last user.
+// j < nkv[t] take part; V_j's and K_{j+1}'s stages are released after their
+// last user.
 __device__ __forceinline__ void mma_issuer_gen(const Params& p, uint32_t sbase, uint32_t tmem, const BarsF8& bars,
                                                const Waiter& w) {
     constexpr int S = kStages;
     constexpr uint32_t kIdS = ptx::idesc_f16(0u, 0, 0, kBM, kBN);
-    constexpr uint32_t kIdO = ptx::idesc_f16(0u, 0, 0, kBM, kD);
+    constexpr uint32_t kIdO = ptx::idesc_f16(0u, 0, 1, kBM, kD);
     auto stage_addr = [&](int r) { return sbase + Lay::kRingOff + (r % S) * kTile; };
     auto issue_qk = [&](int t, uint32_t kaddr) {
         const uint64_t qd = ptx::desc_sw128(sbase + Lay::kQOff + t * kTile, 16, 1024);
         const uint64_t kd = ptx::desc_sw128(kaddr, 16, 1024);
         ptx::mma_ss_kloop4_f8(tmem + Lay::col_s(t), qd, kd, kIdS, 0u);
     };
-    auto issue_pv = [&](int t, int vb, bool acc) {
-        const uint64_t vd = ptx::desc_sw128(sbase + Lay::kVtOff + vb * kTile, 16, 1024);
-        ptx::mma_ts_kloop4_f8(tmem + Lay::col_o(t), tmem + Lay::col_s(t), vd, kIdO, acc ? 1u : 0u);
+    // V MN-major: one 128-byte swizzle atom across the 128 dims (the leading
+    // offset is never stepped over), 1024 B between groups of 8 keys.
+    auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
+        const uint64_t vd = ptx::desc_sw128(vaddr, kTile, 1024);
+        ptx::mma_ts_kloop4_f8_mn(tmem + Lay::col_o(t), tmem + Lay::col_s(t), vd, kIdO, acc ? 1u : 0u);
     };
     auto wait_u = [&](uint32_t bar, uint32_t parity, int site) {
         return __shfl_sync(0xffffffffu, w.wait(bar, parity, site) ? 1 : 0, 0) != 0;
@@ -362,7 +268,6 @@ __device__ __forceinline__ void mma_issuer_gen(const Params& p, uint32_t sbase, 
     auto wait_ring = [&](int r) { return wait_u(bars.kv_full(r % S), (r / S) & 1, kSiteKvFull); };
 
     int ring = 0;
-    int nv = 0;
     int nq[2] = {0, 0};
     int np[2] = {0, 0};
     bool ok = true;
@@ -385,26 +290,24 @@ __device__ __forceinline__ void mma_issuer_gen(const Params& p, uint32_t sbase, 
         ++ring;
         for (int j = 0; j < nmax; ++j) {
             const bool more = j + 1 < nmax;
-            ++ring;                       // V_j: released by the transposer
-            const int vb = nv & 1;
+            const int v_ring = ring++;
             if (more) k_ring = ring++;
-            // V^T_j, K_{j+1} and P of the first tile taking part, together.
+            // V_j, K_{j+1} and P of the first tile taking part, together.
             const int t0 = j < g.nkv[0] ? 0 : 1;
-            const uint32_t wb[3] = {bars.vt_full(vb), more ? bars.kv_full(k_ring % S) : bars.vt_full(vb), bars.p_full(t0)};
-            const uint32_t wp[3] = {static_cast<uint32_t>((nv >> 1) & 1),
-                                    static_cast<uint32_t>(more ? (k_ring / S) & 1 : (nv >> 1) & 1),
+            const int kr = more ? k_ring : v_ring;
+            const uint32_t wb[3] = {bars.kv_full(v_ring % S), bars.kv_full(kr % S), bars.p_full(t0)};
+            const uint32_t wp[3] = {static_cast<uint32_t>((v_ring / S) & 1), static_cast<uint32_t>((kr / S) & 1),
                                     static_cast<uint32_t>(np[t0] & 1)};
-            if (!(ok = __shfl_sync(0xffffffffu, w.wait_all<3>(wb, wp, kSiteVtFull) ? 1 : 0, 0) != 0)) break;
-            ++nv;
-            const int last_v = j < g.nkv[1] ? 1 : 0;                 // last tile reading V^T_j
+            if (!(ok = __shfl_sync(0xffffffffu, w.wait_all<3>(wb, wp, kSiteKvFull) ? 1 : 0, 0) != 0)) break;
+            const int last_v = j < g.nkv[1] ? 1 : 0;                 // last tile reading V_j
             const int last_k = (more && j + 1 < g.nkv[1]) ? 1 : 0;   // last tile reading K_{j+1}
             for (int t = 0; t < 2; ++t) {
                 if (j >= g.nkv[t]) continue;
                 if (t != t0 && !(ok = wait_u(bars.p_full(t), np[t] & 1, kSitePFull))) break;
                 ++np[t];
                 ptx::tc_fence_after();
-                issue_pv(t, vb, j > 0);
-                if (t == last_v) ptx::tc_commit_elect(bars.vt_empty(vb));
+                issue_pv(t, stage_addr(v_ring), j > 0);
+                if (t == last_v) ptx::tc_commit_elect(bars.kv_empty(v_ring % S));
                 if (j + 1 < g.nkv[t]) {
                     issue_qk(t, stage_addr(k_ring));
                     ptx::tc_commit_elect(bars.s_full(t));
@@ -599,14 +502,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bars.stats_free(t), kBM);   // the epilogue's threads have read m, l
             ptx::mbar_init(bars.p_full(t), 2 * kBM);
             ptx::mbar_init(bars.o_full(t), 1);
-            ptx::mbar_init(bars.vt_full(t), 2);    // one arrival per transposer warp
-            ptx::mbar_init(bars.vt_empty(t), 1);   // tcgen05.commit after the P V MMAs
         }
         for (int s = 0; s < fp8::kStages; ++s) {
             ptx::mbar_init(bars.kv_full(s), 1);
-            // K stages are released by the MMA warp's commit, V stages by the
-            // two transposer warps
-            ptx::mbar_init(bars.kv_empty(s), (s & 1) ? 2 : 1);
+            ptx::mbar_init(bars.kv_empty(s), 1);   // the MMA warp's commit
         }
         ptx::mbar_init(bars.mma_done(), 1);
         *abort_flag = 0;
@@ -648,8 +547,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fp8::mma_issuer_gen(p, sbase, tmem, bars, w);
             else
                 fp8::mma_issuer(p, sbase, tmem, bars, w);
-        } else {
-            fp8::xpose_role<kGen>(p, smem, bars, w);
         }
     }
 

@@ -561,11 +561,11 @@ __device__ __forceinline__ void mma_ss_kloop4_f8(uint32_t d_tmem, uint64_t adesc
         : "memory");
 }
 
-// O (+)= P B^T with P (e4m3, four per 32-bit column) read from TMEM and B
-// K-major in shared memory: 4 MMAs of K = 32; A advances 8 columns and B 32
-// bytes per step.
-__device__ __forceinline__ void mma_ts_kloop4_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                                 uint32_t acc) {
+// O (+)= P V with P (e4m3, four per 32-bit column) read from TMEM and V
+// MN-major in shared memory (rows of 128 one-byte values, 128-byte swizzle):
+// 4 MMAs of K = 32; A advances 8 columns and B 32 rows (4096 B) per step.
+__device__ __forceinline__ void mma_ts_kloop4_f8_mn(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                    uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred e, p0, pt;\n\t.reg .b32 blo, bhi, t0, t1;\n\t.reg .b64 b;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
@@ -573,11 +573,11 @@ __device__ __forceinline__ void mma_ts_kloop4_f8(uint32_t d_tmem, uint32_t a_tme
         "setp.eq.b32 pt, %4, %4;\n\t"
         "mov.b64 {blo, bhi}, %2;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p0;\n\t"
-        "add.u32 t0, %1, 8;\n\tadd.u32 t1, blo, 2;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "add.u32 t0, %1, 8;\n\tadd.u32 t1, blo, 256;\n\tmov.b64 b, {t1, bhi};\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [t0], b, %3, pt;\n\t"
-        "add.u32 t0, %1, 16;\n\tadd.u32 t1, blo, 4;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "add.u32 t0, %1, 16;\n\tadd.u32 t1, blo, 512;\n\tmov.b64 b, {t1, bhi};\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [t0], b, %3, pt;\n\t"
-        "add.u32 t0, %1, 24;\n\tadd.u32 t1, blo, 6;\n\tmov.b64 b, {t1, bhi};\n\t"
+        "add.u32 t0, %1, 24;\n\tadd.u32 t1, blo, 768;\n\tmov.b64 b, {t1, bhi};\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [t0], b, %3, pt;\n\t"
         "}" ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc)
         : "memory");
