@@ -6,7 +6,7 @@ a degree-3 polynomial with constant term 1 for 2^f, and an integer add of n into
 the exponent field. This test reads the polynomial coefficients out of the
 header, replays the same float32 operation sequence with numpy, and checks it
 against 2^x in float64: relative error <= 1.1e-4 over [-125, 0], exactly 1 at
-x = 0, and the clamp below -125.
+x = 0, exact powers of two at the integers, and the clamp below -125.
 """
 import os
 import re
@@ -57,6 +57,8 @@ def test_relative_error_bound_and_exact_one():
     ref = 2.0 ** x.astype(np.float64)
     assert np.max(np.abs(y / ref - 1.0)) <= 1.1e-4
     assert emulate(np.array([0.0], f32), c)[0] == 1.0
+    n = np.arange(-125, 1).astype(f32)
+    assert np.array_equal(emulate(n, c).astype(np.float64), 2.0 ** n.astype(np.float64))
 
 
 def test_clamp_keeps_tiny_results_normal_and_positive():

@@ -82,6 +82,33 @@ def test_fp8_matches_oracle(gpu_lib, B, Hq, Hkv, N, amp):
     assert_fp8_parity(o, lse, q, k, v, qd, kd, vd, scale, what=f"B{B} Hq{Hq} Hkv{Hkv} N{N} x{amp}")
 
 
+@pytest.mark.parametrize("log2_step,causal", [(0.5, False), (1.0, False), (3.0, False), (1.0, True)])
+def test_fp8_running_max_grows_in_steps(gpu_lib, log2_step, causal):
+    """Row maxima growing by about 0.5 (1, 3) log2 units per KV tile: every
+    tile's weights are rounded to e4m3 against a new running max and O is
+    rescaled, also in the general (causal) mode; the step is checked on the
+    decoded inputs."""
+    B, Hq, Hkv, N, d = 1, 2, 2, 1280, 128
+    rng = np.random.default_rng(int(log2_step * 100))
+    scale = d ** -0.5
+    qf = 0.5 + 0.02 * rng.standard_normal((B, Hq, N, d))
+    tile = (np.arange(N) // 128).astype(np.float64)
+    kf = (tile * log2_step / np.log2(np.e) / (scale * 0.5 * d))[None, None, :, None] + 0.02 * rng.standard_normal((B, Hkv, N, d))
+    vf = rng.standard_normal((B, Hkv, N, d))
+    ones = np.ones(B * Hkv, dtype=np.float32)
+    q, k, v = gen.e4m3_encode(qf), gen.e4m3_encode(kf), gen.e4m3_encode(vf)
+    dec = lambda c: np.where(c & 0x80, -1.0, 1.0) * gen._E4M3[np.minimum(c & 0x7F, 126)]
+    s = dec(q[0, 0]) @ dec(k[0, 0]).T * scale * np.log2(np.e)
+    steps = np.diff(s.reshape(N, N // 128, 128).max(axis=2), axis=1)
+    assert abs(float(np.median(steps)) - log2_step) < 0.25 * log2_step + 0.1, float(np.median(steps))
+    if causal:
+        o, lse = run_fp8_ex(gpu_lib, q, k, v, ones, ones, ones, scale, True)
+    else:
+        o, lse = run_fp8(gpu_lib, q, k, v, ones, ones, ones, scale)
+    assert_fp8_parity(o, lse, q, k, v, ones, ones, ones, scale, what=f"running max +{log2_step} a tile",
+                      causal=causal)
+
+
 def test_fp8_descales_are_applied(gpu_lib):
     # A descale changes only its own group, by its own factor: a power of two
     # on v's descale scales that group's O exactly and leaves its LSE alone.

@@ -79,6 +79,24 @@ def test_general_every_element(gpu_lib, B, Hq, Hkv, Nq, Nk, d, dtype, causal, am
     assert_parity(o, lse, o_ref, lse_ref, dtype, f"B{B} Hq{Hq} Hkv{Hkv} Nq{Nq} Nk{Nk} d{d} causal{causal}")
 
 
+@pytest.mark.parametrize("log2_step", [4.0, 12.0])
+def test_causal_running_max_grows_in_steps(gpu_lib, log2_step):
+    """Causal and ragged (N = 1000), row maxima growing by about 4 (12) log2
+    units per KV tile: the general mode rescales O on every tile, with
+    masked keys in the diagonal tiles."""
+    N, d = 1000, 128
+    rng = np.random.default_rng(int(log2_step))
+    scale = d ** -0.5
+    qv = np.full((1, 2, N, d), 0.5) + 0.02 * rng.standard_normal((1, 2, N, d))
+    tile = (np.arange(N) // 128).astype(np.float64)
+    kv = (tile * log2_step / np.log2(np.e) / (scale * 0.5 * d))[None, None, :, None] + 0.02 * rng.standard_normal((1, 2, N, d))
+    q, k = gen.round_to_16bit(qv, gen.BF16), gen.round_to_16bit(kv, gen.BF16)
+    v = gen.round_to_16bit(rng.standard_normal((1, 2, N, d)), gen.BF16)
+    o, lse = run_ex(gpu_lib, q, k, v, gen.BF16, scale, True)
+    o_ref, lse_ref = oracle.attention_ex(q, k, v, scale, gen.BF16, causal=True)
+    assert_parity(o, lse, o_ref, lse_ref, gen.BF16, f"causal running max +{log2_step} a tile")
+
+
 def test_causal_zero_queries_give_prefix_means(gpu_lib):
     Nq = Nk = 384
     _, k, v = inputs(3100, 1, 2, 2, Nq, Nk, 128, gen.BF16)

@@ -142,6 +142,28 @@ def test_running_max_moves_every_tile(gpu_lib, increasing):
     full_check(gpu_lib, q, k, v, gen.BF16, d ** -0.5, f"monotone max increasing={increasing}")
 
 
+@pytest.mark.parametrize("log2_step,dtype", [(4.0, gen.BF16), (12.0, gen.FP16), (7.5, gen.BF16)])
+def test_running_max_grows_in_steps(gpu_lib, log2_step, dtype):
+    """Scores whose row max grows by about 4 (12, 7.5) log2 units per KV
+    tile: a rescale of O on every tile by a factor of 2^-4 (2^-12, 2^-7.5),
+    with the weights of the earlier tiles fading; the step is checked on the
+    inputs."""
+    N, d = 1536, 128
+    rng = np.random.default_rng(int(log2_step * 10))
+    qv = np.full((1, 2, N, d), 0.5) + 0.02 * rng.standard_normal((1, 2, N, d))
+    tile = (np.arange(N) // 128).astype(np.float64)
+    scale = d ** -0.5
+    # s = scale * q.k: a per-tile offset of log2_step / log2(e) natural units
+    kv = (tile * log2_step / np.log2(np.e) / (scale * 0.5 * d))[None, None, :, None] + 0.02 * rng.standard_normal((1, 2, N, d))
+    q, k = gen.round_to_16bit(qv, dtype), gen.round_to_16bit(kv, dtype)
+    v = gen.round_to_16bit(rng.standard_normal((1, 2, N, d)), dtype)
+    s = gen.bits_to_float32(q, dtype)[0, 0].astype(np.float64) @ gen.bits_to_float32(k, dtype)[0, 0].astype(np.float64).T
+    tile_max = (s * scale * np.log2(np.e)).reshape(N, N // 128, 128).max(axis=2)
+    steps = np.diff(tile_max, axis=1)
+    assert abs(float(np.median(steps)) - log2_step) < 0.5, float(np.median(steps))
+    full_check(gpu_lib, q, k, v, dtype, scale, f"running max +{log2_step} log2 units a tile")
+
+
 def test_one_dominant_key_per_row(gpu_lib):
     N, d = 512, 64
     rng = np.random.default_rng(6)
