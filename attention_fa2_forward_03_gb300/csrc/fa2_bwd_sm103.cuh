@@ -10,7 +10,7 @@
 //     dQ = scale dS K.
 // Three kernels, all on one stream, none using atomics:
 //   fa2_bwd_delta_kernel  D for every query row (memory bound)
-//   fa2_bwd_dkdv_kernel   one CTA per 128-key tile: S^T = K Q^T and
+//   fa2_bwd_dkdv_kernel   persistent, one 128-key tile at a time: S^T = K Q^T and
 //                         dP^T = V dO^T (keys in TMEM lanes), P^T and dS^T
 //                         formed by the elementwise warps and written back
 //                         to TMEM as 16-bit, then dV += P^T dO and
@@ -136,11 +136,11 @@ __device__ __forceinline__ void store_acc_row(uint32_t row_addr, uint32_t col, f
 // ---------------------------------------------------------------- dK, dV
 
 
-// dK/dV kernel layout: K and V once, then separate rings for the query
-// tiles (3 stages: Q(n) is read by S^T(n), issued as early as mid-step n-1,
-// and by dK(n) at the end of step n) and the upstream-gradient tiles (2
-// stages: dO(n) is read by dP^T(n) and dV(n) only). LSE and D are read by
-// the elementwise warps from global memory, one step ahead.
+// dK/dV kernel layout: K and V of the current key tile, then separate rings
+// for the query tiles (3 stages: Q(n) is read by S^T(n), issued as early as
+// mid-step n-1, and by dK(n) at the end of step n) and the upstream-gradient
+// tiles (2 stages: dO(n) is read by dP^T(n) and dV(n) only). LSE and D are
+// read by the elementwise warps from global memory, one step ahead.
 template <int D>
 struct DkdvLayout {
     static constexpr int kBlkBytes = 128 * 128;
@@ -150,8 +150,9 @@ struct DkdvLayout {
     static constexpr int kQOff = 2 * kTileBytes;
     static constexpr int kDoOff = kQOff + kQStages * kTileBytes;
     static constexpr int kBarOff = kDoOff + kDoStages * kTileBytes;
-    // fixed_full, q_full[3], q_empty[3], do_full[2], do_empty[2], s_full, dp_full, p_full, ds_full, acc_full
-    static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDoStages + 5;
+    // fixed_full, q_full[3], q_empty[3], do_full[2], do_empty[2], s_full, dp_full, p_full, ds_full, acc_full,
+    // fixed_empty
+    static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDoStages + 6;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -171,8 +172,43 @@ struct DkdvBars {
     __device__ uint32_t p_full() const { return base + 8 * (3 + 2 * QS + 2 * DS); }
     __device__ uint32_t ds_full() const { return base + 8 * (4 + 2 * QS + 2 * DS); }
     __device__ uint32_t acc_full() const { return base + 8 * (5 + 2 * QS + 2 * DS); }
+    __device__ uint32_t fixed_empty() const { return base + 8 * (6 + 2 * QS + 2 * DS); }
 };
 
+// The key tiles of a persistent dK/dV CTA. Without the mask every key tile
+// costs the same (all query tiles of its KV head's group), so CTA c takes
+// tiles c, c + grid, c + 2 grid, ... in (KV head, key tile) order: the CTAs
+// running at one time share few KV heads, whose Q and dO stay in L2. With the
+// causal mask key tile kt costs n_tiles - kt query steps, so tiles are taken
+// in pairs (m, n_tiles - 1 - m) of equal total cost n_tiles + 1, pair index
+// u = c, c + grid, ...; the middle tile of an odd count is a pair alone.
+// Returns 0 past the last tile, 1 for a tile (kt, kvh), 2 for the empty second
+// half of a lone middle tile (skipped by every role alike).
+__device__ __forceinline__ int dkdv_tile(const Params& p, int slot, int& kt, int& kvh) {
+    if (!p.causal) {
+        const long long t = blockIdx.x + static_cast<long long>(slot) * gridDim.x;
+        if (t >= static_cast<long long>(p.n_tiles) * p.heads_kv) return 0;
+        kvh = static_cast<int>(t / p.n_tiles);
+        kt = static_cast<int>(t % p.n_tiles);
+        return 1;
+    }
+    const int half = (p.n_tiles + 1) / 2;
+    const long long u = blockIdx.x + static_cast<long long>(slot >> 1) * gridDim.x;
+    if (u >= static_cast<long long>(half) * p.heads_kv) return 0;
+    kvh = static_cast<int>(u / half);
+    const int m = static_cast<int>(u % half);
+    kt = (slot & 1) ? p.n_tiles - 1 - m : m;
+    return ((slot & 1) && kt == m) ? 2 : 1;
+}
+
+// Persistent: one CTA per SM walks its key tiles (dkdv_tile). Per key tile
+// the roles run as before; across tiles the K/V buffer is reloaded once the
+// previous tile's last S^T and dP^T have read it (fixed_empty), the
+// step-indexed barriers and the Q/dO rings keep counting, and the next tile's
+// first products (S^T, dP^T) run on the tensor core while the elementwise
+// warps store the previous tile's dK and dV. The first dV of a tile, which
+// overwrites the accumulator, waits for that tile's first P^T, which the
+// elementwise warps publish only after their accumulator loads.
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa2_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -189,15 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
-    const int kt = blockIdx.x;                 // key tile
-    const int kvh = blockIdx.y;                // b * Hkv + kv head
-    const int b = kvh / (p.hq / p.group);
-    const int hk = kvh - b * (p.hq / p.group);
-    const int first = p.causal ? kt : 0;       // first query tile that sees this key tile
-    const int steps = p.group * (p.n_tiles - first);
+    const int heads_per_batch = p.hq / p.group;   // KV heads per batch
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(bars.fixed_full(), 1);
+        ptx::mbar_init(bars.fixed_empty(), 1);
         for (int s = 0; s < QS; ++s) {
             ptx::mbar_init(bars.q_full(s), 1);
             ptx::mbar_init(bars.q_empty(s), 1);
@@ -223,56 +255,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Waiter w{abort_flag, p.wait_limit_ns};
-    // Query head of step n's tile: the group's query heads in turn, tiles
-    // first .. n_tiles - 1 of each. Tensor maps are [heads, N, d]: a tile never
-    // crosses heads and rows past N read as zero.
-    auto q_head = [&](int g) { return b * p.hq + hk * p.group + g; };
+    // Ring stage of global step n (steps count across this CTA's tiles).
     auto q_addr = [&](int n) { return sbase + L::kQOff + (n % QS) * L::kTileBytes; };
     auto do_addr = [&](int n) { return sbase + L::kDoOff + (n % DS) * L::kTileBytes; };
+    // Per key tile: its query steps run over the group's query heads in
+    // turn, query tiles first .. n_tiles - 1 of each (tensor maps are
+    // [heads, N, d]: a tile never crosses heads, rows past N read as zero).
+    auto first_of = [&](int kt) { return p.causal ? kt : 0; };
+    auto steps_of = [&](int kt) { return p.group * (p.n_tiles - first_of(kt)); };
+    auto q_head = [&](int kvh, int g) {
+        const int b = kvh / heads_per_batch;
+        return b * p.hq + (kvh - b * heads_per_batch) * p.group + g;
+    };
 
     if (warp == kLoadWarp) {
         if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(bars.fixed_full(), 2 * L::kTileBytes);
-#pragma unroll
-            for (int blk = 0; blk < D / 64; ++blk) {
-                if (!FA2_DBG_OK(kvh < p.heads_kv && kt * 128 < p.n, kDbgKvTile)) break;
-                ptx::tma_load_3d(sbase + L::kFixedOff + blk * L::kBlkBytes, &tmK, blk * 64, kt * 128, kvh,
-                                 bars.fixed_full());
-                ptx::tma_load_3d(sbase + L::kFixedOff + L::kTileBytes + blk * L::kBlkBytes, &tmV, blk * 64, kt * 128,
-                                 kvh, bars.fixed_full());
-            }
-            int nq = 0, nd = 0;   // Q and dO tiles issued
-            int g = 0, i = first;
+            int nq = 0, nd = 0, nf = 0;   // Q, dO and K/V tiles issued
             bool ok = true;
-            for (int n = 0; n < steps && ok; ++n) {
-                const int qh = q_head(g);
-                if (!(ok = w.wait(bars.q_empty(n % QS), ((n / QS) & 1) ^ 1, kSiteKvEmpty))) break;
-                ptx::mbar_arrive_expect_tx(bars.q_full(n % QS), L::kTileBytes);
-                if (FA2_DBG_OK(qh < p.heads_q && i * 128 < p.n, kDbgQTile))
+            int kt, kvh;
+            for (int slot = 0, r; ok && (r = dkdv_tile(p, slot, kt, kvh)) != 0; ++slot) {
+                if (r == 2) continue;
+                // K and V of this tile, once the previous tile's last S^T and dP^T have read theirs
+                if (!(ok = w.wait(bars.fixed_empty(), (nf & 1) ^ 1, kSiteKvEmpty))) break;
+                ptx::mbar_arrive_expect_tx(bars.fixed_full(), 2 * L::kTileBytes);
 #pragma unroll
-                    for (int blk = 0; blk < D / 64; ++blk)
-                        ptx::tma_load_3d(q_addr(n) + blk * L::kBlkBytes, &tmQ, blk * 64, i * 128, qh,
-                                         bars.q_full(n % QS));
-                ++nq;
-                if (!(ok = w.wait(bars.do_empty(n % DS), ((n / DS) & 1) ^ 1, kSiteKvEmpty))) break;
-                ptx::mbar_arrive_expect_tx(bars.do_full(n % DS), L::kTileBytes);
-                if (FA2_DBG_OK(qh < p.heads_q && i * 128 < p.n, kDbgQTile))
+                for (int blk = 0; blk < D / 64; ++blk) {
+                    if (!FA2_DBG_OK(kvh < p.heads_kv && kt * 128 < p.n, kDbgKvTile)) break;
+                    ptx::tma_load_3d(sbase + L::kFixedOff + blk * L::kBlkBytes, &tmK, blk * 64, kt * 128, kvh,
+                                     bars.fixed_full());
+                    ptx::tma_load_3d(sbase + L::kFixedOff + L::kTileBytes + blk * L::kBlkBytes, &tmV, blk * 64,
+                                     kt * 128, kvh, bars.fixed_full());
+                }
+                ++nf;
+                const int first = first_of(kt), steps = steps_of(kt);
+                int g = 0, i = first;
+                for (int n = 0; n < steps && ok; ++n) {
+                    const int qh = q_head(kvh, g);
+                    if (!(ok = w.wait(bars.q_empty(nq % QS), ((nq / QS) & 1) ^ 1, kSiteKvEmpty))) break;
+                    ptx::mbar_arrive_expect_tx(bars.q_full(nq % QS), L::kTileBytes);
+                    if (FA2_DBG_OK(qh < p.heads_q && i * 128 < p.n, kDbgQTile))
 #pragma unroll
-                    for (int blk = 0; blk < D / 64; ++blk)
-                        ptx::tma_load_3d(do_addr(n) + blk * L::kBlkBytes, &tmDO, blk * 64, i * 128, qh,
-                                         bars.do_full(n % DS));
-                ++nd;
-                if (++i == p.n_tiles) {
-                    i = first;
-                    ++g;
+                        for (int blk = 0; blk < D / 64; ++blk)
+                            ptx::tma_load_3d(q_addr(nq) + blk * L::kBlkBytes, &tmQ, blk * 64, i * 128, qh,
+                                             bars.q_full(nq % QS));
+                    ++nq;
+                    if (!(ok = w.wait(bars.do_empty(nd % DS), ((nd / DS) & 1) ^ 1, kSiteKvEmpty))) break;
+                    ptx::mbar_arrive_expect_tx(bars.do_full(nd % DS), L::kTileBytes);
+                    if (FA2_DBG_OK(qh < p.heads_q && i * 128 < p.n, kDbgQTile))
+#pragma unroll
+                        for (int blk = 0; blk < D / 64; ++blk)
+                            ptx::tma_load_3d(do_addr(nd) + blk * L::kBlkBytes, &tmDO, blk * 64, i * 128, qh,
+                                             bars.do_full(nd % DS));
+                    ++nd;
+                    if (++i == p.n_tiles) {
+                        i = first;
+                        ++g;
+                    }
                 }
             }
             if (!ok) {
                 // let every copy this CTA started land before it exits
-                for (int r = nq > QS ? nq - QS : 0; r < nq; ++r) w.drain(bars.q_full(r % QS), (r / QS) & 1);
-                for (int r = nd > DS ? nd - DS : 0; r < nd; ++r) w.drain(bars.do_full(r % DS), (r / DS) & 1);
+                for (int r2 = nq > QS ? nq - QS : 0; r2 < nq; ++r2) w.drain(bars.q_full(r2 % QS), (r2 / QS) & 1);
+                for (int r2 = nd > DS ? nd - DS : 0; r2 < nd; ++r2) w.drain(bars.do_full(r2 % DS), (r2 / DS) & 1);
             }
-            w.drain(bars.fixed_full(), 0);
+            if (nf > 0) w.drain(bars.fixed_full(), (nf - 1) & 1);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -282,67 +328,83 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto wait_u = [&](uint32_t bar, uint32_t parity, int site) {
             return __shfl_sync(0xffffffffu, w.wait(bar, parity, site) ? 1 : 0, 0) != 0;
         };
-        bool ok = wait_u(bars.fixed_full(), 0, kSiteQFull);
         const uint64_t kdesc = ptx::desc_sw128(sbase + L::kFixedOff, 16, 1024);
         const uint64_t vdesc = ptx::desc_sw128(sbase + L::kFixedOff + L::kTileBytes, 16, 1024);
-        auto issue_s = [&](int n) {   // S^T of step n, once Q(n) has landed
+        auto issue_s = [&](int n) {   // S^T of global step n, once Q(n) has landed
             qk_kloop<D>(tmem + L::kColS, kdesc, ptx::desc_sw128(q_addr(n), 16, 1024), kIdT);
             ptx::tc_commit_elect(bars.s_full());
         };
-        int s_issued = 0;   // steps whose S^T has been issued
-        if (steps > 0 && (ok = ok && wait_u(bars.q_full(0), 0, kSiteKvFull))) {
-            ptx::tc_fence_after();
-            issue_s(0);
-            s_issued = 1;
-        }
-        bool do_seen = false;   // dO(n) observed landed while waiting for dS^T(n-1)
-        for (int n = 0; n < steps && ok; ++n) {
-            // dP^T = V dO(n)^T
-            if (!do_seen && !(ok = wait_u(bars.do_full(n % DS), (n / DS) & 1, kSiteKvFull))) break;
-            ptx::tc_fence_after();
-            qk_kloop<D>(tmem + L::kColDP, vdesc, ptx::desc_sw128(do_addr(n), 16, 1024), kIdT);
-            ptx::tc_commit_elect(bars.dp_full());
-            // dV += P^T dO as soon as P^T is in TMEM (16-bit over the S
-            // columns; dO as the MN-major B operand); dO(n) is then free
-            if (!(ok = wait_u(bars.p_full(), n & 1, kSitePFull))) break;
-            ptx::tc_fence_after();
-            ptx::mma_ts_kloop8_split(tmem + L::kColAcc0, tmem + L::kColS,
-                                     ptx::desc_sw128(do_addr(n), L::kBlkBytes, 1024), kIdA, n > 0 ? 1u : 0u);
-            ptx::tc_commit_elect(bars.do_empty(n % DS));
-            // S^T of the next step if Q(n+1) is here (it overwrites P^T(n)
-            // only after dV has read it: in order), so the elementwise warps
-            // go from dS^T(n) straight to P^T(n+1)
-            if (s_issued == n + 1 && n + 1 < steps) {
-                const uint32_t bar = bars.q_full((n + 1) % QS);
-                const uint32_t par = ((n + 1) / QS) & 1;
-                if (__shfl_sync(0xffffffffu, ptx::mbar_test_wait(bar, par) ? 1 : 0, 0)) {
+        int nb = 0;     // global steps of the tiles before this one
+        int nf = 0;     // tiles started
+        bool ok = true;
+        int kt, kvh;
+        for (int slot = 0, r; ok && (r = dkdv_tile(p, slot, kt, kvh)) != 0; ++slot) {
+            if (r == 2) continue;
+            const int steps = steps_of(kt);
+            ok = wait_u(bars.fixed_full(), nf & 1, kSiteQFull);
+            ++nf;
+            if (ok) ok = wait_u(bars.q_full(nb % QS), (nb / QS) & 1, kSiteKvFull);
+            if (ok) {
+                ptx::tc_fence_after();
+                issue_s(nb);
+            }
+            int s_issued = 1;       // steps of this tile whose S^T has been issued
+            bool do_seen = false;   // dO(n) observed landed while waiting for dS^T(n-1)
+            for (int n = 0; n < steps && ok; ++n) {
+                const int ng = nb + n;
+                // dP^T = V dO(n)^T
+                if (!do_seen && !(ok = wait_u(bars.do_full(ng % DS), (ng / DS) & 1, kSiteKvFull))) break;
+                ptx::tc_fence_after();
+                qk_kloop<D>(tmem + L::kColDP, vdesc, ptx::desc_sw128(do_addr(ng), 16, 1024), kIdT);
+                ptx::tc_commit_elect(bars.dp_full());
+                // the tile's K and V are read for the last time by now-issued products
+                if (n + 1 == steps) ptx::tc_commit_elect(bars.fixed_empty());
+                // dV += P^T dO as soon as P^T is in TMEM (16-bit over the S
+                // columns; dO as the MN-major B operand); dO(n) is then free
+                if (!(ok = wait_u(bars.p_full(), ng & 1, kSitePFull))) break;
+                ptx::tc_fence_after();
+                ptx::mma_ts_kloop8_split(tmem + L::kColAcc0, tmem + L::kColS,
+                                         ptx::desc_sw128(do_addr(ng), L::kBlkBytes, 1024), kIdA, n > 0 ? 1u : 0u);
+                ptx::tc_commit_elect(bars.do_empty(ng % DS));
+                // S^T of the next step if Q(n+1) is here (it overwrites P^T(n)
+                // only after dV has read it: in order), so the elementwise warps
+                // go from dS^T(n) straight to P^T(n+1)
+                if (s_issued == n + 1 && n + 1 < steps) {
+                    const uint32_t bar = bars.q_full((ng + 1) % QS);
+                    const uint32_t par = ((ng + 1) / QS) & 1;
+                    if (__shfl_sync(0xffffffffu, ptx::mbar_test_wait(bar, par) ? 1 : 0, 0)) {
+                        ptx::tc_fence_after();
+                        issue_s(ng + 1);
+                        ++s_issued;
+                    }
+                }
+                // dK += dS^T Q once dS^T is; Q(n) is then free. The wait also
+                // tests whether dO(n+1) has landed, so that the next step's
+                // dP^T needs no separate wait.
+                do_seen = n + 1 >= steps;
+                ok = __shfl_sync(0xffffffffu,
+                                 w.wait_and_test(bars.ds_full(), ng & 1, kSitePFull, bars.do_full((ng + 1) % DS),
+                                                 ((ng + 1) / DS) & 1, do_seen) ? 1 : 0, 0) != 0;
+                do_seen = __all_sync(0xffffffffu, do_seen);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                ptx::mma_ts_kloop8_split(tmem + L::kColAcc1, tmem + L::kColDP,
+                                         ptx::desc_sw128(q_addr(ng), L::kBlkBytes, 1024), kIdA, n > 0 ? 1u : 0u);
+                ptx::tc_commit_elect(bars.q_empty(ng % QS));
+                if (s_issued == n + 1 && n + 1 < steps) {
+                    if (!(ok = wait_u(bars.q_full((ng + 1) % QS), ((ng + 1) / QS) & 1, kSiteKvFull))) break;
                     ptx::tc_fence_after();
-                    issue_s(n + 1);
+                    issue_s(ng + 1);
                     ++s_issued;
                 }
             }
-            // dK += dS^T Q once dS^T is; Q(n) is then free. The wait also
-            // tests whether dO(n+1) has landed, so that the next step's
-            // dP^T needs no separate wait.
-            do_seen = n + 1 >= steps;
-            ok = __shfl_sync(0xffffffffu,
-                             w.wait_and_test(bars.ds_full(), n & 1, kSitePFull, bars.do_full((n + 1) % DS),
-                                             ((n + 1) / DS) & 1, do_seen) ? 1 : 0, 0) != 0;
-            do_seen = __all_sync(0xffffffffu, do_seen);
-            if (!ok) break;
-            ptx::tc_fence_after();
-            ptx::mma_ts_kloop8_split(tmem + L::kColAcc1, tmem + L::kColDP, ptx::desc_sw128(q_addr(n), L::kBlkBytes, 1024),
-                                     kIdA, n > 0 ? 1u : 0u);
-            ptx::tc_commit_elect(bars.q_empty(n % QS));
-            if (s_issued == n + 1 && n + 1 < steps) {
-                if (!(ok = wait_u(bars.q_full((n + 1) % QS), ((n + 1) / QS) & 1, kSiteKvFull))) break;
-                ptx::tc_fence_after();
-                issue_s(n + 1);
-                ++s_issued;
-            }
+            // dK and dV of this tile are complete once every product above is
+            // (committed on an abort too: the drain below waits for it)
+            ptx::tc_commit_elect(bars.acc_full());
+            nb += steps;
         }
-        ptx::tc_commit_elect(bars.acc_full());
-        w.drain(bars.acc_full(), 0);
+        // every product must finish before the CTA frees its TMEM
+        if (nf > 0) w.drain(bars.acc_full(), (nf - 1) & 1);
         __syncwarp();
     } else {
         // elementwise: thread = key row of the tile = TMEM lane; columns
@@ -357,94 +419,106 @@ __global__ void __launch_bounds__(kThreads, 1)
         // step ahead); the loops take them by shuffle. A query past N (a
         // ragged last tile) gets -LSE = -inf and D = 0: its P^T and dS^T
         // columns are exactly 0.
-        int g = 0, qi = first;
         float nl_nx[2] = {0.0f, 0.0f}, d_nx[2] = {0.0f, 0.0f};
-        auto fetch = [&](int gg, int ii) {
-            const long long base = static_cast<long long>(q_head(gg)) * p.n;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int q = ii * 128 + c0 + 32 * h + lane;
-                const bool in = q < p.n && FA2_DBG_OK(base + q < p.rows_q, kDbgBwdRow);
-                nl_nx[h] = in ? -__ldg(p.lse + base + q) * kLog2e : -INFINITY;
-                d_nx[h] = in ? __ldg(p.delta + base + q) : 0.0f;
-            }
-        };
-        if (steps > 0) fetch(g, qi);
+        int nb = 0;   // global steps of the tiles before this one
+        int nf = 0;   // tiles done
         bool ok = true;
-        for (int n = 0; n < steps; ++n) {
-            const float l2v[2] = {nl_nx[0], nl_nx[1]};
-            const float dv2[2] = {d_nx[0], d_nx[1]};
-            const bool diag = p.causal && qi == kt;  // query q may see key k only if q >= k
-            if (++qi == p.n_tiles) {
-                qi = first;
-                ++g;
-            }
-            if (n + 1 < steps) fetch(g, qi);
-            ok = w.wait(bars.s_full(), n & 1, kSiteSFull);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            // P phase: P^T = exp2(S^T c - LSE log2 e) -> 16-bit over S^T
-            float pf[64];
-            {
-                uint32_t sv[64];
-                ptx::tmem_ld32_at<0>(row_addr + L::kColS + c0, sv);
-                ptx::tmem_ld32_at<32>(row_addr + L::kColS + c0 + 32, sv);
-                ptx::tmem_wait_ld();
+        int kt, kvh;
+        for (int slot = 0, r; ok && (r = dkdv_tile(p, slot, kt, kvh)) != 0; ++slot) {
+            if (r == 2) continue;
+            const int first = first_of(kt), steps = steps_of(kt);
+            auto fetch = [&](int gg, int ii) {
+                const long long base = static_cast<long long>(q_head(kvh, gg)) * p.n;
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    const float nl = __shfl_sync(0xffffffffu, l2v[j / 32], j % 32);
-                    pf[j] = ptx::ex2_approx(fmaf(__uint_as_float(sv[j]), c, nl));
+                for (int h = 0; h < 2; ++h) {
+                    const int q = ii * 128 + c0 + 32 * h + lane;
+                    const bool in = q < p.n && FA2_DBG_OK(base + q < p.rows_q, kDbgBwdRow);
+                    nl_nx[h] = in ? -__ldg(p.lse + base + q) * kLog2e : -INFINITY;
+                    d_nx[h] = in ? __ldg(p.delta + base + q) : 0.0f;
                 }
-            }
-            if (diag) {
+            };
+            int g = 0, qi = first;
+            fetch(g, qi);
+            for (int n = 0; n < steps; ++n) {
+                const int ng = nb + n;
+                const float l2v[2] = {nl_nx[0], nl_nx[1]};
+                const float dv2[2] = {d_nx[0], d_nx[1]};
+                const bool diag = p.causal && qi == kt;  // query q may see key k only if q >= k
+                if (++qi == p.n_tiles) {
+                    qi = first;
+                    ++g;
+                }
+                if (n + 1 < steps) fetch(g, qi);
+                ok = w.wait(bars.s_full(), ng & 1, kSiteSFull);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                // P phase: P^T = exp2(S^T c - LSE log2 e) -> 16-bit over S^T
+                float pf[64];
+                {
+                    uint32_t sv[64];
+                    ptx::tmem_ld32_at<0>(row_addr + L::kColS + c0, sv);
+                    ptx::tmem_ld32_at<32>(row_addr + L::kColS + c0 + 32, sv);
+                    ptx::tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 64; ++j) pf[j] = c0 + j < row ? 0.0f : pf[j];
-            }
+                    for (int j = 0; j < 64; ++j) {
+                        const float nl = __shfl_sync(0xffffffffu, l2v[j / 32], j % 32);
+                        pf[j] = ptx::ex2_approx(fmaf(__uint_as_float(sv[j]), c, nl));
+                    }
+                }
+                if (diag) {
 #pragma unroll
-            for (int cc = 0; cc < 64; cc += 32) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int x = 0; x < 16; ++x) pk[x] = ptx::pack2<kBf16>(pf[cc + 2 * x], pf[cc + 2 * x + 1]);
-                ptx::tmem_st16(row_addr + L::kColS + c0 + cc / 2, pk);
-            }
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bars.p_full());
-            // dS phase: dS^T = P^T o (dP^T - D) -> 16-bit over dP^T
-            ok = w.wait(bars.dp_full(), n & 1, kSiteSFull);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            {
-                uint32_t dp[64];
-                ptx::tmem_ld32_at<0>(row_addr + L::kColDP + c0, dp);
-                ptx::tmem_ld32_at<32>(row_addr + L::kColDP + c0 + 32, dp);
-                ptx::tmem_wait_ld();
+                    for (int j = 0; j < 64; ++j) pf[j] = c0 + j < row ? 0.0f : pf[j];
+                }
 #pragma unroll
                 for (int cc = 0; cc < 64; cc += 32) {
-                    uint32_t dk[16];
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) {
-                        const int j = cc + 2 * x;
-                        const float d0 = __shfl_sync(0xffffffffu, dv2[cc / 32], 2 * x);
-                        const float d1 = __shfl_sync(0xffffffffu, dv2[cc / 32], 2 * x + 1);
-                        dk[x] = ptx::pack2<kBf16>(pf[j] * (__uint_as_float(dp[j]) - d0),
-                                                  pf[j + 1] * (__uint_as_float(dp[j + 1]) - d1));
-                    }
-                    ptx::tmem_st16(row_addr + L::kColDP + c0 + cc / 2, dk);
+                    for (int x = 0; x < 16; ++x) pk[x] = ptx::pack2<kBf16>(pf[cc + 2 * x], pf[cc + 2 * x + 1]);
+                    ptx::tmem_st16(row_addr + L::kColS + c0 + cc / 2, pk);
                 }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bars.p_full());
+                // dS phase: dS^T = P^T o (dP^T - D) -> 16-bit over dP^T
+                ok = w.wait(bars.dp_full(), ng & 1, kSiteSFull);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                {
+                    uint32_t dp[64];
+                    ptx::tmem_ld32_at<0>(row_addr + L::kColDP + c0, dp);
+                    ptx::tmem_ld32_at<32>(row_addr + L::kColDP + c0 + 32, dp);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int cc = 0; cc < 64; cc += 32) {
+                        uint32_t dk[16];
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) {
+                            const int j = cc + 2 * x;
+                            const float d0 = __shfl_sync(0xffffffffu, dv2[cc / 32], 2 * x);
+                            const float d1 = __shfl_sync(0xffffffffu, dv2[cc / 32], 2 * x + 1);
+                            dk[x] = ptx::pack2<kBf16>(pf[j] * (__uint_as_float(dp[j]) - d0),
+                                                      pf[j + 1] * (__uint_as_float(dp[j + 1]) - d1));
+                        }
+                        ptx::tmem_st16(row_addr + L::kColDP + c0 + cc / 2, dk);
+                    }
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bars.ds_full());
             }
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bars.ds_full());
-        }
-        if (ok) ok = w.wait(bars.acc_full(), 0, kSiteOFull);
-        if (__all_sync(0xffffffffu, ok)) {
+            if (!ok) break;
+            ok = w.wait(bars.acc_full(), nf & 1, kSiteOFull);
+            ++nf;
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
             ptx::tc_fence_after();
             // key rows past N (a ragged last tile) are not stored
             const long long grow = static_cast<long long>(kvh) * p.n + kt * 128 + row;
@@ -453,6 +527,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 store_acc_row<D, kBf16>(row_addr, L::kColAcc0, 1.0f, p.dv, grow, p.rows_kv, 0, D, valid);
             else
                 store_acc_row<D, kBf16>(row_addr, L::kColAcc1, p.scale, p.dk, grow, p.rows_kv, 0, D, valid);
+            // the accumulator loads are complete (store_acc_row waits for
+            // each); order them before the next tile's P^T arrival, which
+            // lets the first dV of that tile overwrite the accumulator
+            ptx::tc_fence_before();
+            nb += steps;
         }
     }
 
