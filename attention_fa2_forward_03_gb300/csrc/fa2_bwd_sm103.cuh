@@ -17,7 +17,7 @@
 //                         dK += dS^T Q as MMAs with A from TMEM; dK and dV
 //                         accumulate over every query tile (and every query
 //                         head of a KV head) in TMEM
-//   fa2_bwd_dq_kernel     one CTA per 128-query tile: S = Q K^T,
+//   fa2_bwd_dq_kernel     persistent, one 128-query tile at a time: S = Q K^T,
 //                         dP = dO V^T, dS in TMEM, dQ += dS K
 // Warps 0-7 elementwise (warp w: TMEM lanes 32 (w % 4) .. + 31, one row per
 // thread, columns 64 (w / 4) .. + 63 of the tile, so two warps per scheduler
@@ -194,33 +194,34 @@ struct DkdvBars {
     __device__ uint32_t fixed_empty() const { return base + 8 * (6 + 2 * QS + 2 * DS); }
 };
 
-// The key tiles of a persistent dK/dV CTA. Without the mask every key tile
-// costs the same (all query tiles of its KV head's group), so CTA c takes
-// tiles c, c + grid, c + 2 grid, ... in (KV head, key tile) order: the CTAs
-// running at one time share few KV heads, whose Q and dO stay in L2. With the
-// causal mask key tile kt costs n_tiles - kt query steps, so tiles are taken
-// in pairs (m, n_tiles - 1 - m) of equal total cost n_tiles + 1, pair index
-// u = c, c + grid, ...; the middle tile of an odd count is a pair alone.
-// Returns 0 past the last tile, 1 for a tile (kt, kvh), 2 for the empty second
-// half of a lone middle tile (skipped by every role alike).
-__device__ __forceinline__ int dkdv_tile(const Params& p, int slot, int& kt, int& kvh) {
-    if (!p.causal) {
+// The 128-row tiles of a persistent backward CTA (key tiles for dK/dV, query
+// tiles for dQ), `heads` heads of n_tiles tiles each. Without the mask every
+// tile costs the same (n_tiles steps per head of work), so CTA c takes tiles
+// c, c + grid, c + 2 grid, ... in (head, tile) order: the CTAs running at one
+// time share few heads, whose operands stay in L2. With the causal mask tile
+// m costs n_tiles - m (dK/dV) or m + 1 (dQ) steps, so tiles are taken in pairs
+// (m, n_tiles - 1 - m) of equal total cost n_tiles + 1, pair index u = c,
+// c + grid, ...; the middle tile of an odd count is a pair alone. Returns 0
+// past the last tile, 1 for a tile (tile, head), 2 for the empty second half
+// of a lone middle tile (skipped by every role alike).
+__device__ __forceinline__ int bwd_tile(int causal, int n_tiles, int heads, int slot, int& tile, int& head) {
+    if (!causal) {
         const long long t = blockIdx.x + static_cast<long long>(slot) * gridDim.x;
-        if (t >= static_cast<long long>(p.n_tiles) * p.heads_kv) return 0;
-        kvh = static_cast<int>(t / p.n_tiles);
-        kt = static_cast<int>(t % p.n_tiles);
+        if (t >= static_cast<long long>(n_tiles) * heads) return 0;
+        head = static_cast<int>(t / n_tiles);
+        tile = static_cast<int>(t % n_tiles);
         return 1;
     }
-    const int half = (p.n_tiles + 1) / 2;
+    const int half = (n_tiles + 1) / 2;
     const long long u = blockIdx.x + static_cast<long long>(slot >> 1) * gridDim.x;
-    if (u >= static_cast<long long>(half) * p.heads_kv) return 0;
-    kvh = static_cast<int>(u / half);
+    if (u >= static_cast<long long>(half) * heads) return 0;
+    head = static_cast<int>(u / half);
     const int m = static_cast<int>(u % half);
-    kt = (slot & 1) ? p.n_tiles - 1 - m : m;
-    return ((slot & 1) && kt == m) ? 2 : 1;
+    tile = (slot & 1) ? n_tiles - 1 - m : m;
+    return ((slot & 1) && tile == m) ? 2 : 1;
 }
 
-// Persistent: one CTA per SM walks its key tiles (dkdv_tile). Per key tile
+// Persistent: one CTA per SM walks its key tiles (bwd_tile). Per key tile
 // the roles run as before; across tiles the K/V buffer is reloaded once the
 // previous tile's last S^T and dP^T have read it (fixed_empty), the
 // step-indexed barriers and the Q/dO rings keep counting, and the next tile's
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int nq = 0, nd = 0, nf = 0;   // Q, dO and K/V tiles issued
             bool ok = true;
             int kt, kvh;
-            for (int slot = 0, r; ok && (r = dkdv_tile(p, slot, kt, kvh)) != 0; ++slot) {
+            for (int slot = 0, r; ok && (r = bwd_tile(p.causal, p.n_tiles, p.heads_kv, slot, kt, kvh)) != 0; ++slot) {
                 if (r == 2) continue;
                 // K and V of this tile, once the previous tile's last S^T and dP^T have read theirs
                 if (!(ok = w.wait(bars.fixed_empty(), (nf & 1) ^ 1, kSiteKvEmpty))) break;
@@ -357,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int nf = 0;     // tiles started
         bool ok = true;
         int kt, kvh;
-        for (int slot = 0, r; ok && (r = dkdv_tile(p, slot, kt, kvh)) != 0; ++slot) {
+        for (int slot = 0, r; ok && (r = bwd_tile(p.causal, p.n_tiles, p.heads_kv, slot, kt, kvh)) != 0; ++slot) {
             if (r == 2) continue;
             const int steps = steps_of(kt);
             ok = wait_u(bars.fixed_full(), nf & 1, kSiteQFull);
@@ -443,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int nf = 0;   // tiles done
         bool ok = true;
         int kt, kvh;
-        for (int slot = 0, r; ok && (r = dkdv_tile(p, slot, kt, kvh)) != 0; ++slot) {
+        for (int slot = 0, r; ok && (r = bwd_tile(p.causal, p.n_tiles, p.heads_kv, slot, kt, kvh)) != 0; ++slot) {
             if (r == 2) continue;
             const int first = first_of(kt), steps = steps_of(kt);
             auto fetch = [&](int gg, int ii) {
@@ -564,9 +565,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- dQ
 
-// dQ kernel layout: Q and dO once, then separate rings for the key tiles
-// (3 stages: K(j) is read by S(j), issued as early as mid-step j-1, and by
-// dQ(j)) and the value tiles (2 stages: V(j) is read by dP(j) only).
+// dQ kernel layout: Q and dO of the current query tile, then separate rings
+// for the key tiles (3 stages: K(j) is read by S(j), issued as early as
+// mid-step j-1, and by dQ(j)) and the value tiles (2 stages: V(j) is read by
+// dP(j) only).
 template <int D>
 struct DqLayout {
     static constexpr int kBlkBytes = 128 * 128;
@@ -576,8 +578,9 @@ struct DqLayout {
     static constexpr int kKOff = 2 * kTileBytes;
     static constexpr int kVOff = kKOff + kKStages * kTileBytes;
     static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-    // fixed_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], dp_full, ds_full, acc_full
-    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 5;
+    // fixed_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], dp_full, ds_full, acc_full,
+    // fixed_empty
+    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 6;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -597,8 +600,15 @@ struct DqBars {
     __device__ uint32_t dp_full() const { return base + 8 * (3 + 2 * KS + 2 * VS); }
     __device__ uint32_t ds_full() const { return base + 8 * (4 + 2 * KS + 2 * VS); }
     __device__ uint32_t acc_full() const { return base + 8 * (5 + 2 * KS + 2 * VS); }
+    __device__ uint32_t fixed_empty() const { return base + 8 * (6 + 2 * KS + 2 * VS); }
 };
 
+// Persistent like the dK/dV kernel: one CTA per SM walks its query tiles
+// (bwd_tile over the B * H_q query heads). Q and dO of the next tile load
+// once the current tile's last S and dP have read the buffer; the step
+// barriers (S double-buffered by global step parity) and the K/V rings count
+// across tiles; the next tile's first dQ, which overwrites the accumulator,
+// waits for its first dS, published after the previous tile's dQ loads.
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa2_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -615,15 +625,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
-    const int qt = blockIdx.x;                 // query tile
-    const int qh = blockIdx.y;                 // b * Hq + query head
-    const int b = qh / p.hq;
-    const int hkv = (qh - b * p.hq) / p.group;
-    const int kvh = b * (p.hq / p.group) + hkv;
-    const int steps = p.causal ? qt + 1 : p.n_tiles;
+    // KV head of query head qh (b * Hq + query head)
+    auto kvh_of = [&](int qh) {
+        const int b = qh / p.hq;
+        return b * (p.hq / p.group) + (qh - b * p.hq) / p.group;
+    };
+    auto steps_of = [&](int qt) { return p.causal ? qt + 1 : p.n_tiles; };
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(bars.fixed_full(), 1);
+        ptx::mbar_init(bars.fixed_empty(), 1);
         for (int s = 0; s < KS; ++s) {
             ptx::mbar_init(bars.k_full(s), 1);
             ptx::mbar_init(bars.k_empty(s), 1);
@@ -649,45 +660,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Waiter w{abort_flag, p.wait_limit_ns};
+    // Ring stage of global step n (steps count across this CTA's tiles).
     auto k_addr = [&](int n) { return sbase + L::kKOff + (n % KS) * L::kTileBytes; };
     auto v_addr = [&](int n) { return sbase + L::kVOff + (n % VS) * L::kTileBytes; };
 
     if (warp == kLoadWarp) {
         if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(bars.fixed_full(), 2 * L::kTileBytes);
-#pragma unroll
-            for (int blk = 0; blk < D / 64; ++blk) {
-                if (!FA2_DBG_OK(qh < p.heads_q && qt * 128 < p.n, kDbgQTile)) break;
-                ptx::tma_load_3d(sbase + L::kFixedOff + blk * L::kBlkBytes, &tmQ, blk * 64, qt * 128, qh,
-                                 bars.fixed_full());
-                ptx::tma_load_3d(sbase + L::kFixedOff + L::kTileBytes + blk * L::kBlkBytes, &tmDO, blk * 64, qt * 128,
-                                 qh, bars.fixed_full());
-            }
-            int nk = 0, nv = 0;
+            int nk = 0, nv = 0, nf = 0;   // K, V and Q/dO tiles issued
             bool ok = true;
-            for (int n = 0; n < steps && ok; ++n) {
-                if (!(ok = w.wait(bars.k_empty(n % KS), ((n / KS) & 1) ^ 1, kSiteKvEmpty))) break;
-                ptx::mbar_arrive_expect_tx(bars.k_full(n % KS), L::kTileBytes);
-                if (FA2_DBG_OK(kvh < p.heads_kv && n * 128 < p.n, kDbgKvTile))
+            int qt, qh;
+            for (int slot = 0, r; ok && (r = bwd_tile(p.causal, p.n_tiles, p.heads_q, slot, qt, qh)) != 0; ++slot) {
+                if (r == 2) continue;
+                // Q and dO of this tile, once the previous tile's last S and dP have read theirs
+                if (!(ok = w.wait(bars.fixed_empty(), (nf & 1) ^ 1, kSiteKvEmpty))) break;
+                ptx::mbar_arrive_expect_tx(bars.fixed_full(), 2 * L::kTileBytes);
 #pragma unroll
-                    for (int blk = 0; blk < D / 64; ++blk)
-                        ptx::tma_load_3d(k_addr(n) + blk * L::kBlkBytes, &tmK, blk * 64, n * 128, kvh,
-                                         bars.k_full(n % KS));
-                ++nk;
-                if (!(ok = w.wait(bars.v_empty(n % VS), ((n / VS) & 1) ^ 1, kSiteKvEmpty))) break;
-                ptx::mbar_arrive_expect_tx(bars.v_full(n % VS), L::kTileBytes);
-                if (FA2_DBG_OK(kvh < p.heads_kv && n * 128 < p.n, kDbgKvTile))
+                for (int blk = 0; blk < D / 64; ++blk) {
+                    if (!FA2_DBG_OK(qh < p.heads_q && qt * 128 < p.n, kDbgQTile)) break;
+                    ptx::tma_load_3d(sbase + L::kFixedOff + blk * L::kBlkBytes, &tmQ, blk * 64, qt * 128, qh,
+                                     bars.fixed_full());
+                    ptx::tma_load_3d(sbase + L::kFixedOff + L::kTileBytes + blk * L::kBlkBytes, &tmDO, blk * 64,
+                                     qt * 128, qh, bars.fixed_full());
+                }
+                ++nf;
+                const int kvh = kvh_of(qh), steps = steps_of(qt);
+                for (int n = 0; n < steps && ok; ++n) {
+                    if (!(ok = w.wait(bars.k_empty(nk % KS), ((nk / KS) & 1) ^ 1, kSiteKvEmpty))) break;
+                    ptx::mbar_arrive_expect_tx(bars.k_full(nk % KS), L::kTileBytes);
+                    if (FA2_DBG_OK(kvh < p.heads_kv && n * 128 < p.n, kDbgKvTile))
 #pragma unroll
-                    for (int blk = 0; blk < D / 64; ++blk)
-                        ptx::tma_load_3d(v_addr(n) + blk * L::kBlkBytes, &tmV, blk * 64, n * 128, kvh,
-                                         bars.v_full(n % VS));
-                ++nv;
+                        for (int blk = 0; blk < D / 64; ++blk)
+                            ptx::tma_load_3d(k_addr(nk) + blk * L::kBlkBytes, &tmK, blk * 64, n * 128, kvh,
+                                             bars.k_full(nk % KS));
+                    ++nk;
+                    if (!(ok = w.wait(bars.v_empty(nv % VS), ((nv / VS) & 1) ^ 1, kSiteKvEmpty))) break;
+                    ptx::mbar_arrive_expect_tx(bars.v_full(nv % VS), L::kTileBytes);
+                    if (FA2_DBG_OK(kvh < p.heads_kv && n * 128 < p.n, kDbgKvTile))
+#pragma unroll
+                        for (int blk = 0; blk < D / 64; ++blk)
+                            ptx::tma_load_3d(v_addr(nv) + blk * L::kBlkBytes, &tmV, blk * 64, n * 128, kvh,
+                                             bars.v_full(nv % VS));
+                    ++nv;
+                }
             }
             if (!ok) {
-                for (int r = nk > KS ? nk - KS : 0; r < nk; ++r) w.drain(bars.k_full(r % KS), (r / KS) & 1);
-                for (int r = nv > VS ? nv - VS : 0; r < nv; ++r) w.drain(bars.v_full(r % VS), (r / VS) & 1);
+                for (int r2 = nk > KS ? nk - KS : 0; r2 < nk; ++r2) w.drain(bars.k_full(r2 % KS), (r2 / KS) & 1);
+                for (int r2 = nv > VS ? nv - VS : 0; r2 < nv; ++r2) w.drain(bars.v_full(r2 % VS), (r2 / VS) & 1);
             }
-            w.drain(bars.fixed_full(), 0);
+            if (nf > 0) w.drain(bars.fixed_full(), (nf - 1) & 1);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -697,61 +717,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto wait_u = [&](uint32_t bar, uint32_t parity, int site) {
             return __shfl_sync(0xffffffffu, w.wait(bar, parity, site) ? 1 : 0, 0) != 0;
         };
-        bool ok = wait_u(bars.fixed_full(), 0, kSiteQFull);
         const uint64_t qdesc = ptx::desc_sw128(sbase + L::kFixedOff, 16, 1024);
         const uint64_t dodesc = ptx::desc_sw128(sbase + L::kFixedOff + L::kTileBytes, 16, 1024);
-        // S of key tile n into buffer n % 2, once K(n) has landed
+        // S of global step n into buffer n % 2, once K(n) has landed
         auto issue_s = [&](int n) {
             qk_kloop<D>(tmem + L::kColS0 + 128u * (n & 1), qdesc, ptx::desc_sw128(k_addr(n), 16, 1024), kIdS);
             ptx::tc_commit_elect(bars.s_full(n & 1));
         };
-        int s_issued = 0;   // key tiles whose S has been issued
-        if (steps > 0 && (ok = ok && wait_u(bars.k_full(0), 0, kSiteKvFull))) {
-            ptx::tc_fence_after();
-            issue_s(0);
-            s_issued = 1;
-        }
-        bool v_seen = false;   // V(n) observed landed while waiting for dS(n-1)
-        for (int n = 0; n < steps && ok; ++n) {
-            // dP = dO V(n)^T; V(n) is then free
-            if (!v_seen && !(ok = wait_u(bars.v_full(n % VS), (n / VS) & 1, kSiteKvFull))) break;
-            ptx::tc_fence_after();
-            qk_kloop<D>(tmem + L::kColDP, dodesc, ptx::desc_sw128(v_addr(n), 16, 1024), kIdS);
-            ptx::tc_commit_elect(bars.dp_full());
-            ptx::tc_commit_elect(bars.v_empty(n % VS));
-            // S of the next key tile now if K(n+1) is here, so it is ready
-            // when the elementwise warps finish this tile
-            if (s_issued == n + 1 && n + 1 < steps) {
-                const uint32_t bar = bars.k_full((n + 1) % KS);
-                const uint32_t par = ((n + 1) / KS) & 1;
-                if (__shfl_sync(0xffffffffu, ptx::mbar_test_wait(bar, par) ? 1 : 0, 0)) {
+        int nb = 0;     // global steps of the tiles before this one
+        int nf = 0;     // tiles started
+        bool ok = true;
+        int qt, qh;
+        for (int slot = 0, r; ok && (r = bwd_tile(p.causal, p.n_tiles, p.heads_q, slot, qt, qh)) != 0; ++slot) {
+            if (r == 2) continue;
+            const int steps = steps_of(qt);
+            ok = wait_u(bars.fixed_full(), nf & 1, kSiteQFull);
+            ++nf;
+            if (ok) ok = wait_u(bars.k_full(nb % KS), (nb / KS) & 1, kSiteKvFull);
+            if (ok) {
+                ptx::tc_fence_after();
+                issue_s(nb);
+            }
+            int s_issued = 1;      // steps of this tile whose S has been issued
+            bool v_seen = false;   // V(n) observed landed while waiting for dS(n-1)
+            for (int n = 0; n < steps && ok; ++n) {
+                const int ng = nb + n;
+                // dP = dO V(n)^T; V(n) is then free
+                if (!v_seen && !(ok = wait_u(bars.v_full(ng % VS), (ng / VS) & 1, kSiteKvFull))) break;
+                ptx::tc_fence_after();
+                qk_kloop<D>(tmem + L::kColDP, dodesc, ptx::desc_sw128(v_addr(ng), 16, 1024), kIdS);
+                ptx::tc_commit_elect(bars.dp_full());
+                ptx::tc_commit_elect(bars.v_empty(ng % VS));
+                // the tile's Q and dO are read for the last time by now-issued products
+                if (n + 1 == steps) ptx::tc_commit_elect(bars.fixed_empty());
+                // S of the next key tile now if K(n+1) is here, so it is ready
+                // when the elementwise warps finish this tile
+                if (s_issued == n + 1 && n + 1 < steps) {
+                    const uint32_t bar = bars.k_full((ng + 1) % KS);
+                    const uint32_t par = ((ng + 1) / KS) & 1;
+                    if (__shfl_sync(0xffffffffu, ptx::mbar_test_wait(bar, par) ? 1 : 0, 0)) {
+                        ptx::tc_fence_after();
+                        issue_s(ng + 1);
+                        ++s_issued;
+                    }
+                }
+                // dQ += dS K once dS is in TMEM (16-bit over the dP columns; K as
+                // the MN-major B operand); K(n) is then free. The wait also tests
+                // whether V(n+1) has landed (see the dK/dV kernel).
+                v_seen = n + 1 >= steps;
+                ok = __shfl_sync(0xffffffffu,
+                                 w.wait_and_test(bars.ds_full(), ng & 1, kSitePFull, bars.v_full((ng + 1) % VS),
+                                                 ((ng + 1) / VS) & 1, v_seen) ? 1 : 0, 0) != 0;
+                v_seen = __all_sync(0xffffffffu, v_seen);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                ptx::mma_ts_kloop8_split(tmem + L::kColAcc, tmem + L::kColDP,
+                                         ptx::desc_sw128(k_addr(ng), L::kBlkBytes, 1024), kIdQ, n > 0 ? 1u : 0u);
+                ptx::tc_commit_elect(bars.k_empty(ng % KS));
+                if (s_issued == n + 1 && n + 1 < steps) {
+                    if (!(ok = wait_u(bars.k_full((ng + 1) % KS), ((ng + 1) / KS) & 1, kSiteKvFull))) break;
                     ptx::tc_fence_after();
-                    issue_s(n + 1);
+                    issue_s(ng + 1);
                     ++s_issued;
                 }
             }
-            // dQ += dS K once dS is in TMEM (16-bit over the dP columns; K as
-            // the MN-major B operand); K(n) is then free. The wait also tests
-            // whether V(n+1) has landed (see the dK/dV kernel).
-            v_seen = n + 1 >= steps;
-            ok = __shfl_sync(0xffffffffu,
-                             w.wait_and_test(bars.ds_full(), n & 1, kSitePFull, bars.v_full((n + 1) % VS),
-                                             ((n + 1) / VS) & 1, v_seen) ? 1 : 0, 0) != 0;
-            v_seen = __all_sync(0xffffffffu, v_seen);
-            if (!ok) break;
-            ptx::tc_fence_after();
-            ptx::mma_ts_kloop8_split(tmem + L::kColAcc, tmem + L::kColDP, ptx::desc_sw128(k_addr(n), L::kBlkBytes, 1024),
-                                     kIdQ, n > 0 ? 1u : 0u);
-            ptx::tc_commit_elect(bars.k_empty(n % KS));
-            if (s_issued == n + 1 && n + 1 < steps) {
-                if (!(ok = wait_u(bars.k_full((n + 1) % KS), ((n + 1) / KS) & 1, kSiteKvFull))) break;
-                ptx::tc_fence_after();
-                issue_s(n + 1);
-                ++s_issued;
-            }
+            // dQ of this tile is complete once every product above is
+            // (committed on an abort too: the drain below waits for it)
+            ptx::tc_commit_elect(bars.acc_full());
+            nb += steps;
         }
-        ptx::tc_commit_elect(bars.acc_full());
-        w.drain(bars.acc_full(), 0);
+        // every product must finish before the CTA frees its TMEM
+        if (nf > 0) w.drain(bars.acc_full(), (nf - 1) & 1);
         __syncwarp();
     } else {
         // elementwise: thread = query row of the tile = TMEM lane; columns
@@ -760,75 +796,91 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c0 = 64 * (warp >> 2);
         const uint32_t row_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
         const float c = p.scale_log2;
-        // A query row past N (a ragged last tile) gets LSE = +inf and D = 0:
-        // its P and dS are exactly 0 and it is not stored.
-        const bool row_valid = qt * 128 + row < p.n;
-        const long long grow = static_cast<long long>(qh) * p.n + qt * 128 + row;
-        const bool in = row_valid && FA2_DBG_OK(grow < p.rows_q, kDbgBwdRow);
-        const float lse2 = in ? p.lse[grow] * 1.4426950408889634f : INFINITY;
-        const float dl = in ? p.delta[grow] : 0.0f;
         const int key_end = p.n - (p.n_tiles - 1) * 128;   // keys of the last key tile (1..128)
+        int nb = 0;   // global steps of the tiles before this one
+        int nf = 0;   // tiles done
         bool ok = true;
-        for (int n = 0; n < steps; ++n) {
-            ok = w.wait(bars.s_full(n & 1), (n >> 1) & 1, kSiteSFull);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            const bool diag = p.causal && n == qt;  // key k visible to query q only if k <= q
-            // P phase: P = exp2(S c - LSE log2 e), kept in registers
-            const uint32_t colS = L::kColS0 + 128u * (n & 1);
-            float pf[64];
-            {
-                uint32_t sv[64];
-                ptx::tmem_ld32_at<0>(row_addr + colS + c0, sv);
-                ptx::tmem_ld32_at<32>(row_addr + colS + c0 + 32, sv);
-                ptx::tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 64; ++j) pf[j] = ptx::ex2_approx(fmaf(__uint_as_float(sv[j]), c, -lse2));
-            }
-            if (diag) {
-#pragma unroll
-                for (int j = 0; j < 64; ++j) pf[j] = c0 + j > row ? 0.0f : pf[j];
-            }
-            if (n == p.n_tiles - 1 && key_end < 128) {   // keys past N (zero-filled K) get no weight
-#pragma unroll
-                for (int j = 0; j < 64; ++j) pf[j] = c0 + j >= key_end ? 0.0f : pf[j];
-            }
-            // dS phase: dS = P o (dP - D) -> 16-bit over dP
-            ok = w.wait(bars.dp_full(), n & 1, kSiteSFull);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            {
-                uint32_t dp[64];
-                ptx::tmem_ld32_at<0>(row_addr + L::kColDP + c0, dp);
-                ptx::tmem_ld32_at<32>(row_addr + L::kColDP + c0 + 32, dp);
-                ptx::tmem_wait_ld();
-#pragma unroll
-                for (int cc = 0; cc < 64; cc += 32) {
-                    uint32_t dk[16];
-#pragma unroll
-                    for (int x = 0; x < 16; ++x) {
-                        const int j = cc + 2 * x;
-                        dk[x] = ptx::pack2<kBf16>(pf[j] * (__uint_as_float(dp[j]) - dl),
-                                                  pf[j + 1] * (__uint_as_float(dp[j + 1]) - dl));
-                    }
-                    ptx::tmem_st16(row_addr + L::kColDP + c0 + cc / 2, dk);
+        int qt, qh;
+        for (int slot = 0, r; ok && (r = bwd_tile(p.causal, p.n_tiles, p.heads_q, slot, qt, qh)) != 0; ++slot) {
+            if (r == 2) continue;
+            const int steps = steps_of(qt);
+            // A query row past N (a ragged last tile) gets LSE = +inf and D = 0:
+            // its P and dS are exactly 0 and it is not stored.
+            const bool row_valid = qt * 128 + row < p.n;
+            const long long grow = static_cast<long long>(qh) * p.n + qt * 128 + row;
+            const bool in = row_valid && FA2_DBG_OK(grow < p.rows_q, kDbgBwdRow);
+            const float lse2 = in ? p.lse[grow] * 1.4426950408889634f : INFINITY;
+            const float dl = in ? p.delta[grow] : 0.0f;
+            for (int n = 0; n < steps; ++n) {
+                const int ng = nb + n;
+                ok = w.wait(bars.s_full(ng & 1), (ng >> 1) & 1, kSiteSFull);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
                 }
+                ptx::tc_fence_after();
+                const bool diag = p.causal && n == qt;  // key k visible to query q only if k <= q
+                // P phase: P = exp2(S c - LSE log2 e), kept in registers
+                const uint32_t colS = L::kColS0 + 128u * (ng & 1);
+                float pf[64];
+                {
+                    uint32_t sv[64];
+                    ptx::tmem_ld32_at<0>(row_addr + colS + c0, sv);
+                    ptx::tmem_ld32_at<32>(row_addr + colS + c0 + 32, sv);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) pf[j] = ptx::ex2_approx(fmaf(__uint_as_float(sv[j]), c, -lse2));
+                }
+                if (diag) {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) pf[j] = c0 + j > row ? 0.0f : pf[j];
+                }
+                if (n == p.n_tiles - 1 && key_end < 128) {   // keys past N (zero-filled K) get no weight
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) pf[j] = c0 + j >= key_end ? 0.0f : pf[j];
+                }
+                // dS phase: dS = P o (dP - D) -> 16-bit over dP
+                ok = w.wait(bars.dp_full(), ng & 1, kSiteSFull);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                {
+                    uint32_t dp[64];
+                    ptx::tmem_ld32_at<0>(row_addr + L::kColDP + c0, dp);
+                    ptx::tmem_ld32_at<32>(row_addr + L::kColDP + c0 + 32, dp);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int cc = 0; cc < 64; cc += 32) {
+                        uint32_t dk[16];
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) {
+                            const int j = cc + 2 * x;
+                            dk[x] = ptx::pack2<kBf16>(pf[j] * (__uint_as_float(dp[j]) - dl),
+                                                      pf[j + 1] * (__uint_as_float(dp[j + 1]) - dl));
+                        }
+                        ptx::tmem_st16(row_addr + L::kColDP + c0 + cc / 2, dk);
+                    }
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bars.ds_full());
             }
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bars.ds_full());
-        }
-        if (ok) ok = w.wait(bars.acc_full(), 0, kSiteOFull);
-        if (__all_sync(0xffffffffu, ok)) {
+            if (!ok) break;
+            ok = w.wait(bars.acc_full(), nf & 1, kSiteOFull);
+            ++nf;
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
             ptx::tc_fence_after();
             store_acc_row<D, kBf16>(row_addr, L::kColAcc, p.scale, p.dq, grow, p.rows_q, c0 * D / 128,
                                     (c0 + 64) * D / 128, row_valid);
+            // the accumulator loads are complete; order them before the next
+            // tile's first dS arrival, which lets its first dQ overwrite them
+            ptx::tc_fence_before();
+            nb += steps;
         }
     }
 

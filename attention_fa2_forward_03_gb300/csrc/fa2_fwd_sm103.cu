@@ -538,11 +538,12 @@ fa2_status bwd_launch(int dev, const void* q, const void* k, const void* v, cons
     p.rows_kv = static_cast<long long>(B) * H_kv * N;
     const bool bf = dtype == FA2_BF16;
     const dim3 gdelta(static_cast<unsigned>((rows_q + 15) / 16));
-    // dK/dV: persistent, one CTA per SM over the key tiles (pairs of key
-    // tiles of equal total cost under the causal mask)
+    // dK/dV and dQ: persistent, one CTA per SM over the key (query) tiles,
+    // in pairs of equal total cost under the causal mask
     const long long kv_units = static_cast<long long>(causal ? (p.n_tiles + 1) / 2 : p.n_tiles) * B * H_kv;
     const dim3 gkv(static_cast<unsigned>(std::min<long long>(kv_units, sm_count(dev))));
-    const dim3 gq(static_cast<unsigned>(p.n_tiles), static_cast<unsigned>(B * H_q));
+    const long long q_units = static_cast<long long>(causal ? (p.n_tiles + 1) / 2 : p.n_tiles) * B * H_q;
+    const dim3 gq(static_cast<unsigned>(std::min<long long>(q_units, sm_count(dev))));
 
     auto run = [&](auto delta_k, auto dkdv_k, auto dq_k, int smem_kv, int smem_q, int slot) -> fa2_status {
         fa2_status s = set_smem(dev, slot, dkdv_k, smem_kv);
