@@ -10,22 +10,23 @@
 //     dQ = scale dS K.
 // Three kernels, all on one stream, none using atomics:
 //   fa2_bwd_delta_kernel  D for every query row (memory bound)
-//   fa2_bwd_dkdv_kernel   persistent, one 128-key tile at a time: S^T = K Q^T and
-//                         dP^T = V dO^T (keys in TMEM lanes), P^T and dS^T
+//   fa2_bwd_dkdv_kernel   persistent, one 128-key tile at a time:
+//                         S^T = K Q^T and dP^T = V dO^T (keys in TMEM
+//                         lanes), P^T and dS^T
 //                         formed by the elementwise warps and written back
 //                         to TMEM as 16-bit, then dV += P^T dO and
 //                         dK += dS^T Q as MMAs with A from TMEM; dK and dV
 //                         accumulate over every query tile (and every query
 //                         head of a KV head) in TMEM
-//   fa2_bwd_dq_kernel     persistent, one 128-query tile at a time: S = Q K^T,
-//                         dP = dO V^T, dS in TMEM, dQ += dS K
+//   fa2_bwd_dq_kernel     persistent, one 128-query tile at a time:
+//                         S = Q K^T, dP = dO V^T, dS in TMEM, dQ += dS K
 // Warps 0-7 elementwise (warp w: TMEM lanes 32 (w % 4) .. + 31, one row per
 // thread, columns 64 (w / 4) .. + 63 of the tile, so two warps per scheduler
 // hide each other's latency), warp 8 TMA producer, warp 9 TMEM allocator and
 // MMA issuer. Each half's 16-bit results (P^T, dS^T, dS) are packed into the
 // first 32 of its own 64 fp32 columns -- never into the other warp's, which
-// may not have been read yet -- and the MMAs read A in those two halves. TMEM: S | dP | two d-column accumulators
-// (dK/dV), S0 | S1 | dP | dQ (dQ).
+// may not have been read yet -- and the MMAs read A in those two halves.
+// TMEM: S | dP | two d-column accumulators (dK/dV), S0 | S1 | dP | dQ (dQ).
 //
 // Overlap. The elementwise step of a tile runs in two phases with their own
 // barriers: P as soon as S is in TMEM (while the tensor core computes dP),
