@@ -114,6 +114,11 @@ CASES = [
     (1, 4, 2, 300, 64, gen.FP16, True),
     (1, 1, 1, 1, 128, gen.BF16, False),     # a single row
     (1, 2, 2, 1000, 128, gen.BF16, True),
+    # more tiles than the 152 SMs: the persistent CTAs take several tiles each
+    # (160 key / query tiles); causal with 5 tiles a head: pairs (0, 4),
+    # (1, 3) and the middle tile alone, 192 units
+    (1, 40, 40, 512, 64, gen.BF16, False),
+    (1, 64, 64, 640, 64, gen.FP16, True),
 ]
 
 
