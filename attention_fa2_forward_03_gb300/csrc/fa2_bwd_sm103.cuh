@@ -55,6 +55,7 @@ struct Params {
     void* dk;             // [B*Hkv*N, D]
     void* dv;             // [B*Hkv*N, D]
     long long wait_limit_ns;
+    int debug_flags;      // watchdog test hook: bit 0 skips the dK/dV kernel's query-tile loads
     int n;                // N: rows per head (any positive length)
     int n_tiles;          // ceil(N / 128)
     int hq, group;        // Hq, Hq / Hkv
@@ -292,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kLoadWarp) {
         if (lane == 0) {
             int nq = 0, nd = 0, nf = 0;   // Q, dO and K/V tiles issued
+            const bool load_q = (p.debug_flags & 1) == 0;
             bool ok = true;
             int kt, kvh;
             for (int slot = 0, r; ok && (r = bwd_tile(p.causal, p.n_tiles, p.heads_kv, slot, kt, kvh)) != 0; ++slot) {
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int qh = q_head(kvh, g);
                     if (!(ok = w.wait(bars.q_empty(nq % QS), ((nq / QS) & 1) ^ 1, kSiteKvEmpty))) break;
                     ptx::mbar_arrive_expect_tx(bars.q_full(nq % QS), L::kTileBytes);
-                    if (FA2_DBG_OK(qh < p.heads_q && i * 128 < p.n, kDbgQTile))
+                    if (load_q && FA2_DBG_OK(qh < p.heads_q && i * 128 < p.n, kDbgQTile))
 #pragma unroll
                         for (int blk = 0; blk < D / 64; ++blk)
                             ptx::tma_load_3d(q_addr(nq) + blk * L::kBlkBytes, &tmQ, blk * 64, i * 128, qh,

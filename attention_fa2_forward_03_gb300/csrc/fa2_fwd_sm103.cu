@@ -525,6 +525,7 @@ fa2_status bwd_launch(int dev, const void* q, const void* k, const void* v, cons
     p.dk = dk;
     p.dv = dv;
     p.wait_limit_ns = g_wait_limit_ns.load();
+    p.debug_flags = g_debug_flags.load();
     p.n = N;
     p.n_tiles = (N + fa2::kBM - 1) / fa2::kBM;
     p.hq = H_q;

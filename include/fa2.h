@@ -257,8 +257,9 @@ const char* fa2_status_string(fa2_status status);
 int64_t fa2_set_wait_limit_ns(int64_t limit_ns);
 
 /*
- * Test hook for the watchdog. With flags = 1 the next kernels skip the load
- * of their query tiles, so their waits run out and the status word reports
+ * Test hook for the watchdog. With flags = 1 the next 16-bit forward kernels
+ * and the backward's dK/dV kernel skip the load of their query tiles, so
+ * their waits run out and the status word reports
  * FA2_ERR_TIMEOUT; the kernel still frees its tensor memory, waits for its
  * own copies and returns normally. 0 (the default) restores normal
  * operation. Returns the previous flags.

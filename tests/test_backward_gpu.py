@@ -137,6 +137,36 @@ def test_backward_matches_oracle(gpu_lib, B, Hq, Hkv, N, d, dtype, causal):
     print("worst error / bound (dq, dk, dv):", res)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_watchdog_reports_timeout_and_context_survives(gpu_lib, causal):
+    """The dK/dV kernel with its query-tile loads skipped (test hook): its
+    bounded waits run out, the status word reports FA2_ERR_TIMEOUT, every
+    persistent CTA returns, and the next backward on the same context is
+    correct."""
+    import torch
+
+    B, Hq, Hkv, N, d, dtype = 1, 2, 2, 384, 128, gen.BF16
+    q, k, v = gen.make_qkv(4200, B, Hq, Hkv, N, d, dtype)
+    do, _, _ = gen.make_qkv(4201, B, Hq, Hkv, N, d, dtype)
+    scale = 1 / math.sqrt(d)
+    tq, tk, tv, tdo = (to_dev(x, dtype) for x in (q, k, v, do))
+    o, lse = gpu_lib.fa2_fwd_ex(tq, tk, tv, scale=scale, causal=causal)
+    assert gpu_lib.fa2_check_status(torch.cuda.current_stream().cuda_stream) == gpu_lib.FA2_OK
+    old_limit = gpu_lib.fa2_set_wait_limit_ns(20_000_000)  # 20 ms
+    old_flags = gpu_lib.fa2_set_debug_flags(1)
+    try:
+        gpu_lib.fa2_bwd(tq, tk, tv, o, lse, tdo, scale=scale, causal=causal)
+        rc = gpu_lib.fa2_check_status(torch.cuda.current_stream().cuda_stream)
+    finally:
+        gpu_lib.fa2_set_debug_flags(old_flags)
+        gpu_lib.fa2_set_wait_limit_ns(old_limit)
+    assert rc == gpu_lib.FA2_ERR_TIMEOUT
+    assert gpu_lib.fa2_check_status(0) == gpu_lib.FA2_OK  # the word was cleared
+    dq, dk, dv = gpu_lib.fa2_bwd(tq, tk, tv, o, lse, tdo, scale=scale, causal=causal)
+    assert gpu_lib.fa2_check_status(torch.cuda.current_stream().cuda_stream) == gpu_lib.FA2_OK
+    check_all(*(g.float().cpu().numpy() for g in (dq, dk, dv)), q, k, v, do, scale, dtype, causal, "after watchdog")
+
+
 def test_backward_zero_upstream_gradient(gpu_lib):
     import torch
 
